@@ -1,0 +1,240 @@
+"""fp64 CPU oracle for routing attention -- TEST INFRASTRUCTURE ONLY.
+
+This module is the plain, slow reference the CUDA library is checked against.
+Only the test suite, the package smoke check and the benchmark's CPU-baseline
+leg may import it; the library itself never calls it and has no CPU fallback.
+It shares no code with the CUDA path: it reads the same seeded inputs and
+restates the method step by step in float64, one numpy library primitive
+(matmul, sort, exp) per step, without blocking, fusion or reordering.
+
+Method: "Efficient Content-Based Sparse Attention with Routing Transformers"
+(Roy, Saffar, Vaswani, Grangier).  The pages available state the method only
+in summary form (paperlayer.ai source-linked summary, §3 and §4; arXiv
+abstract).  Where they leave a step open the plainest reading is taken and
+named in the docstring of the step ("reading: ...").
+
+Steps (per batch b and head h, with Q shared as K):
+  a1 normalise   r_t = (x_t - mean x_t) / ||x_t - mean x_t||       (0 if norm 0)
+  a2 score       S[c, t] = <r_t, mu_c>;  a_t = first argmax_c S[c, t]
+  a3 select      T_c = the w tokens with largest S[c, .], ties -> lower t
+  a4 sort        idx[c] = T_c in ascending position order
+  a5 attention   inside each cluster: softmax(scale * Q_c K_c^T + causal mask) V_c
+  a6 scatter     O[t] = mean of t's per-cluster outputs; 0 if t is in no cluster
+  a7 update      mu_c <- normalise(decay * mu_c + (1 - decay) * mean of the r_t
+                 with a_t = c, over every sequence of the batch); unchanged if none
+
+Parity status: every function below is pinned by tests in
+``tests/test_oracle_pins.py`` (closed forms, invariants, brute force, library
+routines); none is "parity unpinned".
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "normalise_rows",
+    "centroid_scores",
+    "kmeans_assign",
+    "top_w_per_centroid",
+    "cluster_attention",
+    "scatter_average",
+    "membership_counts",
+    "routing_attention_head",
+    "routing_attention",
+    "centroid_ema",
+]
+
+
+def normalise_rows(x: np.ndarray) -> np.ndarray:
+    """a1: project each row onto the unit sphere.
+
+    Source: §4 "Routing attention with clustering" (unit-normalised queries and
+    keys make nearest-centroid routing a maximum-inner-product search).
+    Reading: "layer-normalised onto the unit sphere" = subtract the row mean
+    (layer norm without affine; its variance scaling does not change the
+    direction), then divide by the Euclidean norm.  A row whose centred norm is
+    exactly 0 maps to the zero vector.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    u = x - x.mean(axis=-1, keepdims=True)
+    nrm = np.sqrt((u * u).sum(axis=-1, keepdims=True))
+    safe = np.where(nrm > 0.0, nrm, 1.0)
+    return np.where(nrm > 0.0, u / safe, 0.0)
+
+
+def centroid_scores(r: np.ndarray, mu: np.ndarray) -> np.ndarray:
+    """a2: S[c, t] = <r_t, mu_c> for r [n, d] and mu [k, d]; returns [k, n].
+
+    Source: §4 "Routing attention with clustering": routing compares every
+    token with every centroid, O(nkd).  Reading: the nearest centroid is the
+    one with the largest inner product (centroids are kept at unit norm, so
+    this equals the smallest Euclidean distance).
+    """
+    r = np.asarray(r, dtype=np.float64)
+    mu = np.asarray(mu, dtype=np.float64)
+    return mu @ r.T
+
+
+def kmeans_assign(S: np.ndarray) -> np.ndarray:
+    """a2: a_t = the centroid with the largest score; ties go to the lower index.
+
+    Source: §4 (nearest-centroid routing of the online k-means).  np.argmax
+    returns the first maximum, which is the lower-index tie rule.
+    """
+    return np.argmax(np.asarray(S), axis=0).astype(np.int64)
+
+
+def top_w_per_centroid(S: np.ndarray, w: int) -> np.ndarray:
+    """a3 + a4: for every centroid the w tokens with the largest score, ties
+    to the lower position, listed in ascending position order.  Returns [k, w].
+
+    Source: §4 "Routing attention with clustering": balanced clusters, each
+    query compares with about n/k keys, via a top-k assignment of cost
+    O(n log n).  Reading: each centroid takes its own top-w tokens (so a token
+    may sit in several clusters or in none), and the chosen tokens are put back
+    in position order so the causal mask inside a cluster is the plain lower
+    triangle.
+    """
+    S = np.asarray(S)
+    k, n = S.shape
+    if not (1 <= w <= n):
+        raise ValueError("need 1 <= w <= n")
+    pos = np.arange(n)
+    out = np.empty((k, w), dtype=np.int64)
+    for c in range(k):
+        # primary key: score descending; secondary: position ascending
+        order = np.lexsort((pos, -S[c]))
+        out[c] = np.sort(order[:w])
+    return out
+
+
+def cluster_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, members: np.ndarray,
+                      causal: bool, scale: float, return_probs: bool = False):
+    """a5: dense softmax attention restricted to one cluster.
+
+    q, k, v: [n, d] rows of one (batch, head); members: ascending positions of
+    the cluster.  Returns Y [w, d] (and P [w, w] if asked).
+
+    Source: §3 "Self-Attentive Auto-regressive Sequence Modeling" (an n-by-n
+    attention matrix from queries and keys, rows normalised with softmax,
+    output = attention times values; autoregressive queries see only earlier
+    positions) and §4 (only query-key pairs of the same cluster are
+    considered).  Readings: the attention uses the raw Q, K, V rows (the
+    normalised vectors serve routing only); a position attends to itself; the
+    causal mask compares original positions, i.e. key p_j is visible to query
+    p_i iff p_j <= p_i.
+    """
+    members = np.asarray(members)
+    qc = np.asarray(q, dtype=np.float64)[members]
+    kc = np.asarray(k, dtype=np.float64)[members]
+    vc = np.asarray(v, dtype=np.float64)[members]
+    logits = scale * (qc @ kc.T)
+    if causal:
+        visible = members[None, :] <= members[:, None]
+        logits = np.where(visible, logits, -np.inf)
+    row_max = logits.max(axis=1, keepdims=True)
+    e = np.exp(logits - row_max)
+    P = e / e.sum(axis=1, keepdims=True)
+    Y = P @ vc
+    if return_probs:
+        return Y, P
+    return Y
+
+
+def membership_counts(idx: np.ndarray, n: int) -> np.ndarray:
+    """m_t = number of clusters whose member list contains position t."""
+    return np.bincount(np.asarray(idx).reshape(-1), minlength=n)[:n]
+
+
+def scatter_average(Y: np.ndarray, idx: np.ndarray, n: int) -> np.ndarray:
+    """a6: put every cluster's outputs back at their positions.
+
+    Y [k, w, d], idx [k, w].  Reading: a position chosen by several clusters
+    gets the plain arithmetic mean of its outputs; a position chosen by none
+    gets a zero row (the pages leave the combination open).
+    """
+    Y = np.asarray(Y, dtype=np.float64)
+    idx = np.asarray(idx)
+    d = Y.shape[-1]
+    acc = np.zeros((n, d), dtype=np.float64)
+    np.add.at(acc, idx.reshape(-1), Y.reshape(-1, d))
+    m = membership_counts(idx, n)
+    out = np.zeros((n, d), dtype=np.float64)
+    hit = m > 0
+    out[hit] = acc[hit] / m[hit, None]
+    return out
+
+
+def routing_attention_head(q, k, v, mu, w: int, causal: bool = True, scale=None,
+                           idx=None):
+    """a1..a6 for one (batch, head): returns dict(O, idx, assign, S).
+
+    Routing uses the normalised shared query/key rows; ``idx`` may be given to
+    evaluate a5..a6 on externally chosen clusters (e.g. another
+    implementation's index lists).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    n, d = q.shape
+    if scale is None or scale <= 0:
+        scale = 1.0 / np.sqrt(d)
+    r = normalise_rows(q)
+    S = centroid_scores(r, mu)
+    a = kmeans_assign(S)
+    if idx is None:
+        idx = top_w_per_centroid(S, w)
+    idx = np.asarray(idx)
+    Y = np.stack([cluster_attention(q, k, v, idx[c], causal, scale)
+                  for c in range(idx.shape[0])])
+    O = scatter_average(Y, idx, n)
+    return {"O": O, "idx": idx, "assign": a, "S": S}
+
+
+def routing_attention(q, k, v, mu, w: int, causal: bool = True, scale=None):
+    """a1..a6 over [B, H, n, d] inputs with centroids [H, k, d] shared across
+    the batch (§4: centroids are shared across sequences)."""
+    q = np.asarray(q, dtype=np.float64)
+    B, H, n, d = q.shape
+    kc = mu.shape[1]
+    O = np.zeros((B, H, n, d))
+    idx = np.zeros((B, H, kc, w), dtype=np.int64)
+    assign = np.zeros((B, H, n), dtype=np.int64)
+    for b in range(B):
+        for h in range(H):
+            res = routing_attention_head(q[b, h], k[b, h], v[b, h], mu[h], w, causal, scale)
+            O[b, h], idx[b, h], assign[b, h] = res["O"], res["idx"], res["assign"]
+    return O, idx, assign
+
+
+def centroid_ema(qk: np.ndarray, assign: np.ndarray, mu: np.ndarray, decay: float) -> np.ndarray:
+    """a7: one online spherical k-means step for every head's centroids.
+
+    qk [B, H, n, d] (raw rows; normalised here exactly as in a1),
+    assign [B, H, n], mu [H, k, d].  Returns the updated centroids (float64).
+
+    Source: §2 "Attention with Content-Based Sparsity" (centroids learned with
+    mini-batch spherical k-means), §4 (centroids shared across sequences,
+    learned online), §6 "Local vs Global" (spherical k-means over the global
+    token set).  Readings: each token counts toward its argmax centroid only;
+    the batch mean over every sequence of the head is blended in with weight
+    (1 - decay); the result is put back on the unit sphere; a centroid with no
+    assigned token is left exactly as it was.
+    """
+    qk = np.asarray(qk, dtype=np.float64)
+    B, H, n, d = qk.shape
+    mu = np.asarray(mu, dtype=np.float64)
+    out = mu.copy()
+    r = normalise_rows(qk)
+    for h in range(H):
+        rh = r[:, h].reshape(B * n, d)
+        ah = np.asarray(assign)[:, h].reshape(B * n)
+        for c in range(mu.shape[1]):
+            sel = ah == c
+            cnt = int(sel.sum())
+            if cnt == 0:
+                continue
+            mean = rh[sel].sum(axis=0) / cnt
+            blended = decay * mu[h, c] + (1.0 - decay) * mean
+            nrm = np.sqrt((blended * blended).sum())
+            out[h, c] = blended / nrm if nrm > 0 else blended
+    return out

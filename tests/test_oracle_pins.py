@@ -1,0 +1,350 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Nothing here re-types an oracle formula: every expected value is a closed
+form worked by hand (tests/golden), a textbook routine (torch's
+scaled_dot_product_attention in float64 for full causal attention), brute
+force over all subsets, or an invariant of the method.  The mutation tests at
+the bottom plant plausible mistakes in the oracle (on the CPU) and check that
+some pin fails for each.
+"""
+
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.routing_oracle as orc
+from tests.conftest import eval_tree
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def _sdpa(q, k, v, causal, scale):
+    t = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float64))[None, None]
+    out = torch.nn.functional.scaled_dot_product_attention(
+        t(q), t(k), t(v), is_causal=causal, scale=scale)
+    return out[0, 0].numpy()
+
+
+def _zero_mean_orthonormal(d, m, rng):
+    """m orthonormal vectors in the zero-mean subspace of R^d."""
+    a = rng.standard_normal((d, m))
+    a -= a.mean(axis=0, keepdims=True)
+    qmat, _ = np.linalg.qr(a)
+    return qmat.T  # [m, d]
+
+
+# ---------------------------------------------------------------------------
+# pin checks (each raises AssertionError on a mismatch)
+# ---------------------------------------------------------------------------
+
+def check_golden(g):
+    q = np.array(g["q"], dtype=np.float64)
+    v = np.array(g["v"], dtype=np.float64)
+    mu = np.array(eval_tree(g["centroids"]))
+    scale = eval_tree(g["scale"])
+    ex = g["expected"]
+    res = orc.routing_attention_head(q, q, v, mu, g["w"], causal=True, scale=scale)
+    np.testing.assert_allclose(res["S"], np.array(eval_tree(ex["S"])), atol=1e-12)
+    assert res["assign"].tolist() == ex["assign"]
+    assert res["idx"].tolist() == ex["idx"]
+    assert orc.membership_counts(res["idx"], g["n"]).tolist() == ex["membership"]
+    np.testing.assert_allclose(res["O"], np.array(ex["O_causal"], dtype=float), atol=1e-12)
+    res_nc = orc.routing_attention_head(q, q, v, mu, g["w"], causal=False, scale=scale)
+    np.testing.assert_allclose(res_nc["O"], np.array(ex["O_noncausal"], dtype=float), atol=1e-12)
+    a = np.array(ex["assign"])[None, None]
+    qq = q[None, None]
+    np.testing.assert_allclose(orc.centroid_ema(qq, a, mu[None], 0.0)[0],
+                               np.array(eval_tree(ex["centroids_decay0"])), atol=1e-12)
+    np.testing.assert_allclose(orc.centroid_ema(qq, a, mu[None], 0.5)[0],
+                               np.array(eval_tree(ex["centroids_decay_half"])), atol=1e-12)
+    np.testing.assert_allclose(orc.centroid_ema(qq, a, mu[None], 1.0)[0], mu, atol=1e-15)
+
+
+def check_normalise_closed_form():
+    rng = np.random.default_rng(11)
+    for d in (4, 64, 128):
+        basis = _zero_mean_orthonormal(d, 1, rng)[0]
+        for offset, s in ((0.0, 1.0), (3.5, 0.25), (-2.0, 7.0)):
+            x = offset + s * basis
+            np.testing.assert_allclose(orc.normalise_rows(x[None])[0], basis, atol=1e-12)
+            np.testing.assert_allclose(orc.normalise_rows(-x[None])[0], -basis, atol=1e-12)
+        const = np.full((1, d), 1.25)
+        assert np.array_equal(orc.normalise_rows(const), np.zeros((1, d)))
+
+
+def check_scores_cosine():
+    rng = np.random.default_rng(12)
+    d = 16
+    e = _zero_mean_orthonormal(d, 3, rng)
+    thetas = np.array([0.0, 0.3, 1.1, 2.0, math.pi])
+    x = 5.0 + 2.0 * (np.cos(thetas)[:, None] * e[0] + np.sin(thetas)[:, None] * e[1])
+    mu = np.stack([e[0], e[1], e[2]])
+    S = orc.centroid_scores(orc.normalise_rows(x), mu)
+    assert S.shape == (3, len(thetas))
+    np.testing.assert_allclose(S[0], np.cos(thetas), atol=1e-12)
+    np.testing.assert_allclose(S[1], np.sin(thetas), atol=1e-12)
+    np.testing.assert_allclose(S[2], 0.0, atol=1e-12)
+
+
+def check_assign_ties():
+    S = np.array([[0.5, 0.2, 0.9], [0.5, 0.7, 0.9], [0.1, 0.7, 0.9]])
+    assert orc.kmeans_assign(S).tolist() == [0, 1, 0]
+
+
+def check_top_w_exhaustive():
+    rng = np.random.default_rng(13)
+    for trial in range(60):
+        n = int(rng.integers(1, 9))
+        k = int(rng.integers(1, 4))
+        S = rng.integers(0, 3, size=(k, n)).astype(float) / 2.0  # many ties
+        for w in range(1, n + 1):
+            got = orc.top_w_per_centroid(S, w)
+            for c in range(k):
+                valid = []
+                for T in itertools.combinations(range(n), w):
+                    Ts = set(T)
+                    ok = all((S[c, i] > S[c, j]) or (S[c, i] == S[c, j] and i < j)
+                             for i in Ts for j in range(n) if j not in Ts)
+                    if ok:
+                        valid.append(list(T))
+                assert len(valid) == 1
+                assert got[c].tolist() == valid[0]
+
+
+def check_top_w_invariants():
+    rng = np.random.default_rng(14)
+    for n, k, w in ((50, 5, 10), (37, 3, 37), (64, 8, 1), (100, 7, 13)):
+        S = rng.standard_normal((k, n))
+        idx = orc.top_w_per_centroid(S, w)
+        assert idx.shape == (k, w)
+        for c in range(k):
+            assert np.all(np.diff(idx[c]) > 0)
+            assert idx[c].min() >= 0 and idx[c].max() < n
+        assert orc.membership_counts(idx, n).sum() == k * w
+
+
+def check_full_attention_k1():
+    rng = np.random.default_rng(15)
+    for n, d, causal in ((33, 8, True), (64, 16, True), (20, 4, False)):
+        q = rng.standard_normal((n, d))
+        v = rng.standard_normal((n, d))
+        mu = orc.normalise_rows(rng.standard_normal((1, d)))
+        scale = 1.0 / math.sqrt(d)
+        res = orc.routing_attention_head(q, q, v, mu, n, causal=causal, scale=scale)
+        assert res["idx"].tolist() == [list(range(n))]
+        np.testing.assert_allclose(res["O"], _sdpa(q, q, v, causal, scale), atol=1e-12)
+        # default scale is 1/sqrt(d)
+        res2 = orc.routing_attention_head(q, q, v, mu, n, causal=causal)
+        np.testing.assert_allclose(res2["O"], res["O"], atol=0)
+
+
+def check_k_copies_average():
+    rng = np.random.default_rng(16)
+    n, d, kc = 40, 8, 3
+    q = rng.standard_normal((n, d))
+    v = rng.standard_normal((n, d))
+    mu = np.repeat(orc.normalise_rows(rng.standard_normal((1, d))), kc, axis=0)
+    res = orc.routing_attention_head(q, q, v, mu, n, causal=True)
+    assert orc.membership_counts(res["idx"], n).tolist() == [kc] * n
+    np.testing.assert_allclose(res["O"], _sdpa(q, q, v, True, 1 / math.sqrt(d)), atol=1e-12)
+
+
+def check_rows_sum_to_one():
+    rng = np.random.default_rng(17)
+    n, d = 30, 8
+    q = rng.standard_normal((n, d)) * 3
+    members = np.sort(rng.choice(n, size=12, replace=False))
+    for causal in (True, False):
+        _, P = orc.cluster_attention(q, q, rng.standard_normal((n, d)), members, causal,
+                                     0.4, return_probs=True)
+        np.testing.assert_allclose(P.sum(axis=1), 1.0, atol=1e-12)
+        assert np.all(P >= 0)
+        if causal:
+            assert np.all(np.triu(P, 1) == 0.0)
+            assert np.all(np.diag(P) > 0)
+
+
+def check_v_ones_and_coverage():
+    rng = np.random.default_rng(18)
+    n, d, kc, w = 50, 8, 4, 9
+    q = rng.standard_normal((n, d))
+    mu = orc.normalise_rows(rng.standard_normal((kc, d)))
+    res = orc.routing_attention_head(q, q, np.ones((n, d)), mu, w)
+    m = orc.membership_counts(res["idx"], n)
+    assert (m == 0).any() and (m > 0).any()
+    np.testing.assert_allclose(res["O"], np.broadcast_to(np.where(m[:, None] > 0, 1.0, 0.0), (n, d)), atol=1e-12)
+    assert np.all(res["O"][m == 0] == 0.0)
+
+
+def check_w1_and_first_slot():
+    rng = np.random.default_rng(19)
+    n, d, kc = 30, 8, 5
+    q = rng.standard_normal((n, d))
+    v = rng.standard_normal((n, d))
+    mu = orc.normalise_rows(rng.standard_normal((kc, d)))
+    res = orc.routing_attention_head(q, q, v, mu, 1)
+    m = orc.membership_counts(res["idx"], n)
+    sel = m > 0
+    np.testing.assert_allclose(res["O"][sel], v[sel], atol=1e-12)
+    idx = orc.top_w_per_centroid(orc.centroid_scores(orc.normalise_rows(q), mu), 7)
+    for c in range(kc):
+        Y = orc.cluster_attention(q, q, v, idx[c], True, 0.3)
+        np.testing.assert_allclose(Y[0], v[idx[c][0]], atol=1e-12)
+
+
+def check_ema_special_cases():
+    rng = np.random.default_rng(20)
+    d, kc = 8, 3
+    e = _zero_mean_orthonormal(d, 3, rng)
+    mu = np.stack([e[0], e[1], e[2]])
+    # two sequences of one head: tokens of centroid 0 are +-rotations around e0
+    # in the (e0, e1) plane (mean direction e0); centroid 2 gets no token.
+    ang = 0.4
+    t_plus = math.cos(ang) * e[0] + math.sin(ang) * e[1]
+    t_minus = math.cos(ang) * e[0] - math.sin(ang) * e[1]
+    x = np.zeros((2, 1, 3, d))
+    x[0, 0, 0] = 3 + 2 * t_plus
+    x[1, 0, 0] = -1 + 5 * t_minus
+    x[0, 0, 1] = 2 * e[1]
+    x[1, 0, 1] = 4 * e[1]
+    x[0, 0, 2] = 7 * t_plus
+    x[1, 0, 2] = 0.5 * t_minus
+    a = np.array([[[0, 1, 0]], [[0, 1, 0]]])
+    out0 = orc.centroid_ema(x, a, mu[None], 0.0)[0]
+    np.testing.assert_allclose(out0[0], e[0], atol=1e-12)   # mean of +-ang rotations
+    np.testing.assert_allclose(out0[1], e[1], atol=1e-12)
+    assert np.array_equal(out0[2], mu[2])                    # empty: untouched
+    # decay d: unit-norm blend of mu0 = e0 and mean = cos(ang) e0 -> still e0
+    np.testing.assert_allclose(orc.centroid_ema(x, a, mu[None], 0.999)[0][0], e[0], atol=1e-12)
+    # a centroid between two directions: mu = e2, mean = e0 at decay 1/2 ->
+    # (e2/2 + cos(ang) e0 / 2) normalised
+    mu2 = np.stack([e[2], e[1], e[0]])
+    got = orc.centroid_ema(x, a, mu2[None], 0.5)[0][0]
+    want = (e[2] + math.cos(ang) * e[0]) / math.sqrt(1 + math.cos(ang) ** 2)
+    np.testing.assert_allclose(got, want, atol=1e-12)
+    np.testing.assert_allclose(orc.centroid_ema(x, a, mu[None], 1.0)[0], mu, atol=1e-15)
+    out = orc.centroid_ema(x, a, rng.standard_normal((1, kc, d)), 0.3)[0]
+    np.testing.assert_allclose(np.linalg.norm(out[:2], axis=1), 1.0, atol=1e-12)
+
+
+ALL_CHECKS = [
+    check_normalise_closed_form, check_scores_cosine, check_assign_ties,
+    check_top_w_exhaustive, check_top_w_invariants, check_full_attention_k1,
+    check_k_copies_average, check_rows_sum_to_one, check_v_ones_and_coverage,
+    check_w1_and_first_slot, check_ema_special_cases,
+]
+
+
+def test_golden_hand_worked(hand_worked):
+    check_golden(hand_worked)
+
+
+@pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda f: f.__name__)
+def test_pin(check):
+    check()
+
+
+def test_batched_entry_matches_heads():
+    rng = np.random.default_rng(21)
+    B, H, n, d, kc, w = 2, 2, 24, 8, 3, 6
+    q = rng.standard_normal((B, H, n, d))
+    v = rng.standard_normal((B, H, n, d))
+    mu = orc.normalise_rows(rng.standard_normal((H, kc, d)))
+    O, idx, a = orc.routing_attention(q, q, v, mu, w)
+    for b in range(B):
+        for h in range(H):
+            r = orc.routing_attention_head(q[b, h], q[b, h], v[b, h], mu[h], w)
+            assert np.array_equal(O[b, h], r["O"]) and np.array_equal(idx[b, h], r["idx"])
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: each must trip at least one pin
+# ---------------------------------------------------------------------------
+
+def _fails(checks, hand_worked):
+    for chk in checks:
+        try:
+            chk(hand_worked) if chk is check_golden else chk()
+        except AssertionError:
+            return True
+    return False
+
+
+def _mut_no_centering(x):
+    x = np.asarray(x, dtype=np.float64)
+    nrm = np.sqrt((x * x).sum(axis=-1, keepdims=True))
+    return np.where(nrm > 0, x / np.where(nrm > 0, nrm, 1), 0.0)
+
+
+def _mut_mask_flipped(q, k, v, members, causal, scale, return_probs=False):
+    members = np.asarray(members)
+    qc, kc, vc = (np.asarray(a, dtype=np.float64)[members] for a in (q, k, v))
+    logits = scale * qc @ kc.T
+    if causal:
+        logits = np.where(members[None, :] >= members[:, None], logits, -np.inf)
+    e = np.exp(logits - logits.max(axis=1, keepdims=True))
+    P = e / e.sum(axis=1, keepdims=True)
+    return (P @ vc, P) if return_probs else P @ vc
+
+
+def _mut_no_scale(q, k, v, members, causal, scale, return_probs=False):
+    return _ORIG_ATT(q, k, v, members, causal, 1.0, return_probs)
+
+
+def _mut_ties_high(S, w):
+    S = np.asarray(S)
+    k, n = S.shape
+    out = np.empty((k, w), dtype=np.int64)
+    for c in range(k):
+        order = np.lexsort((-np.arange(n), -S[c]))
+        out[c] = np.sort(order[:w])
+    return out
+
+
+def _mut_sum_scatter(Y, idx, n):
+    Y = np.asarray(Y, dtype=np.float64)
+    acc = np.zeros((n, Y.shape[-1]))
+    np.add.at(acc, np.asarray(idx).reshape(-1), Y.reshape(-1, Y.shape[-1]))
+    return acc
+
+
+def _mut_ema_swapped(qk, assign, mu, decay):
+    return _ORIG_EMA(qk, assign, mu, 1.0 - decay)
+
+
+def _mut_argmax_last(S):
+    S = np.asarray(S)
+    return (S.shape[0] - 1 - np.argmax(S[::-1], axis=0)).astype(np.int64)
+
+
+def _mut_scores_transposed(r, mu):
+    return np.asarray(r, dtype=np.float64) @ np.asarray(mu, dtype=np.float64).T
+
+
+_ORIG_ATT = orc.cluster_attention
+_ORIG_EMA = orc.centroid_ema
+
+MUTANTS = [
+    ("normalise_rows", _mut_no_centering),
+    ("cluster_attention", _mut_mask_flipped),
+    ("cluster_attention", _mut_no_scale),
+    ("top_w_per_centroid", _mut_ties_high),
+    ("scatter_average", _mut_sum_scatter),
+    ("centroid_ema", _mut_ema_swapped),
+    ("kmeans_assign", _mut_argmax_last),
+    ("centroid_scores", _mut_scores_transposed),
+]
+
+
+@pytest.mark.parametrize("name,mutant", MUTANTS, ids=[f"{a}:{b.__name__}" for a, b in MUTANTS])
+def test_planted_mistake_is_caught(monkeypatch, hand_worked, name, mutant):
+    monkeypatch.setattr(orc, name, mutant)
+    caught = False
+    try:
+        caught = _fails([check_golden] + ALL_CHECKS, hand_worked)
+    except Exception:
+        caught = True  # a shape error is also a caught mistake
+    assert caught, f"no pin catches the planted mistake in {name}"
