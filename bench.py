@@ -1,0 +1,445 @@
+"""Routing-attention benchmark (one JSON line on stdout, rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload c3] [--no-graph]
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+routing (normalise, score, argmax, top-w per centroid, position sort),
+in-cluster causal attention, the averaging scatter and the centroid update.
+The default workload is the n=8192, H=8, d=128 configuration
+(mix128_bf16_b1h8_n8192_d128_k128_w64).
+
+ours:       CUDA library; device time with CUDA events per step, L2 flushed
+            (256 MiB write) before every timed step; e2e = the same step with
+            pinned-host inputs copied in and the output copied out inside the
+            timed region; per-kernel times from the library's launch hook.
+reference:  the fp64 CPU oracle on the host cores, each step a bounded sample
+            (one head of the batch) scaled to the same tokens/s metric.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "routed-attention tokens/s and TFLOPS (% bf16 peak) at n=8192, H=8, d=128, 1 B300"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    sm_max_mhz=d.get("sm_max_mhz", 2032.0), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0,
+                sm_max_mhz=2032.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per launch, by kernel kind (bytes moved that the method
+# must move, or flops it must do); see the design doc for the derivations.
+# ---------------------------------------------------------------------------
+
+def kernel_work(name, wl):
+    s = 2 if wl.dtype == "bf16" else 4
+    BH, n, d, k, w = wl.B * wl.H, wl.n, wl.d, wl.k, wl.w
+    if name in ("score_simt", "score_tc"):
+        byts = BH * n * d * s + BH * k * n * 4 + BH * n * 4 * 2
+        return dict(bytes=byts, flops=2.0 * BH * n * k * d)
+    if name == "select_topw":
+        return dict(bytes=BH * k * n * 4 + BH * k * w * 4 * 2, flops=0.0)
+    if name in ("attention_simt", "attention_tc"):
+        # gathered Q(=K) and V rows, per-slot output rows, index lists
+        byts = 2 * BH * k * w * d * s + BH * k * w * d * s + BH * k * w * 4
+        return dict(bytes=byts, flops=4.0 * BH * k * w * w * d)
+    if name == "scatter_average":
+        return dict(bytes=BH * n * 4 + BH * n * d * s, flops=0.0)
+    if name == "ema_bucket":
+        return dict(bytes=BH * n * 4 * 2, flops=0.0)
+    if name == "ema_update":
+        return dict(bytes=BH * n * d * s + wl.H * k * d * 8, flops=3.0 * BH * n * d)
+    return dict(bytes=0, flops=0.0)
+
+
+def alu_peak_tflops(sm_mhz):
+    # fp32 FMA: 148 SMs x 128 lanes x 2 flop per cycle
+    return 148 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+KERNEL_BOUND = {
+    "score_simt": "alu", "attention_simt": "alu", "score_tc": "hbm", "attention_tc": "hbm",
+    "select_topw": "hbm", "scatter_average": "hbm", "ema_bucket": "hbm", "ema_update": "hbm",
+}
+
+KERNEL_SOURCES = {
+    "score_simt": "k_score_simt.cu", "score_tc": "k_score_tc.cu", "select_topw": "k_select.cu",
+    "attention_simt": "k_attention_simt.cu", "attention_tc": "k_attention_tc.cu",
+    "scatter_average": "k_scatter.cu", "ema_bucket": "k_ema.cu", "ema_update": "k_ema.cu",
+}
+
+
+def kernel_source_hash(name):
+    p = os.path.join(ROOT, "content_sparse_attention_shared_b300", "csrc", KERNEL_SOURCES.get(name, ""))
+    if not os.path.isfile(p):
+        return None
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def traffic_for(name, wl_name):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of that kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    e = rec.get(name)
+    if not e or e.get("source_sha") != kernel_source_hash(name):
+        return None
+    if e.get("workload") != wl_name:
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in rows:
+            for key, nm in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                            ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def oracle_head_seconds(wl, head, reps=1):
+    """Time the oracle's full step (a1..a7) on one head of the batch."""
+    import numpy as np
+    from threadpoolctl import threadpool_limits
+
+    import oracle.routing_oracle as orc
+
+    q64 = wl.q_f32().astype(np.float64)[:, head:head + 1]
+    v64 = wl.v_f32().astype(np.float64)[:, head:head + 1]
+    mu = wl.centroids[head:head + 1]
+    best = float("inf")
+    with threadpool_limits(limits=1):
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            _, _, a = orc.routing_attention(q64, q64, v64, mu, wl.w, causal=True)
+            if wl.ema:
+                orc.centroid_ema(q64, a, mu, wl.decay)
+            best = min(best, time.perf_counter() - t0)
+    return best
+
+
+def cpu_baseline(wl, target_s=10.0, max_reps=5):
+    """Whole steps (every head) of the oracle, repeated until ~target_s of CPU
+    work; best step time."""
+    best, spent, reps = float("inf"), 0.0, 0
+    while reps < max_reps and (spent < target_s or reps == 0):
+        t = sum(oracle_head_seconds(wl, h) for h in range(wl.H))
+        best = min(best, t)
+        spent += t
+        reps += 1
+    return {"value": wl.tokens / best, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} full step(s) of {wl.name} (forward + centroid update, all "
+                      f"{wl.H} heads), fp64 numpy on 1 thread; best step {best:.2f} s"}
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    for i in range(args.warmup):
+        oracle_head_seconds(wl, i % wl.H)
+    times = []
+    for i in range(args.steps):
+        times.append(oracle_head_seconds(wl, i % wl.H) * wl.H)
+    step_s = statistics.mean(times)
+    value = wl.tokens / step_s
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "n": wl.n, "d": wl.d, "k": wl.k,
+                       "w": wl.w, "step": "forward + centroid update"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"each step: one head of {wl.name} through the fp64 "
+                                       f"oracle on 1 thread, x {wl.H} heads"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, wl):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import content_sparse_attention_shared_b300 as rt
+    from content_sparse_attention_shared_b300 import build as rt_build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rt_build.build()
+    rt.load_library()
+
+    if wl.dtype == "f32":
+        q_h = torch.from_numpy(wl.q)
+        v_h = torch.from_numpy(wl.v)
+    else:
+        q_h = torch.from_numpy(wl.q.view(np.int16)).view(torch.bfloat16)
+        v_h = torch.from_numpy(wl.v.view(np.int16)).view(torch.bfloat16)
+    q_h, v_h = q_h.pin_memory(), v_h.pin_memory()
+    mu0 = torch.from_numpy(wl.centroids).to(dev)
+    q = q_h.to(dev)
+    v = v_h.to(dev)
+    mu = mu0.clone()
+    out = torch.empty_like(v)
+    idx = torch.empty((wl.B, wl.H, wl.k, wl.w), dtype=torch.int32, device=dev)
+    assign = torch.empty((wl.B, wl.H, wl.n), dtype=torch.int32, device=dev)
+    ws = rt.Workspace.for_shape(wl.B, wl.H, wl.n, wl.d, wl.k, wl.w, q.dtype, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(qq, vv):
+        rt.rt_routing_attention(qq, qq, vv, mu, wl.w, causal=True, out=out, idx_out=idx,
+                                assign_out=assign, workspace=ws, stream=stream)
+        if wl.ema:
+            rt.rt_centroid_ema(qq, assign, mu, wl.decay, workspace=ws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step(q, v)
+    torch.cuda.synchronize()
+    ws.check()
+    launches_per_step = None
+
+    # ---- device-timed region --------------------------------------------
+    n_launch_before = rt.rt_launch_count()
+    step(q, v)
+    torch.cuda.synchronize()
+    launches_per_step = rt.rt_launch_count() - n_launch_before
+    prof_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(launches_per_step * args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    rt.rt_profile_set(prof_pairs)
+    l0 = rt.rt_launch_count()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step(q, v)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    gpu_launches = rt.rt_launch_count() - l0
+    rt.rt_profile_set([])
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    t_ms = statistics.mean(step_ms)
+    if world > 1:
+        tt = torch.tensor([t_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_ms = float(tt.item())
+        dist.barrier()
+    ws.check()
+
+    # per-kernel times over the timed region
+    per_kind = {}
+    for i, (a, b) in enumerate(prof_pairs):
+        name = rt.rt_profile_kernel_name(i)
+        per_kind.setdefault(name, []).append(a.elapsed_time(b))
+    kern = {k2: {"launches": len(v2), "avg_us": 1e3 * statistics.mean(v2),
+                 "total_ms": sum(v2)} for k2, v2 in per_kind.items()}
+    total_kernel_ms = sum(x["total_ms"] for x in kern.values())
+    for x in kern.values():
+        x["share"] = x["total_ms"] / total_kernel_ms if total_kernel_ms else None
+
+    # ---- end-to-end through the public API with host buffers -------------
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        q.copy_(q_h, non_blocking=True)
+        v.copy_(v_h, non_blocking=True)
+        step(q, v)
+        out_h.copy_(out, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks = _peaks()
+    clocks = clk.summary()
+    tokens = wl.tokens * world
+    value = tokens / (t_ms * 1e-3)
+    tflops = wl.nominal_flops() * world / (t_ms * 1e-3) / 1e12
+
+    # dominant kernel roofline
+    dom = max(kern.items(), key=lambda kv: kv[1]["total_ms"])
+    dname, dstat = dom
+    work = kernel_work(dname, wl)
+    bound = KERNEL_BOUND.get(dname, "hbm")
+    avg_s = dstat["avg_us"] * 1e-6
+    if bound == "hbm":
+        achieved = work["bytes"] / avg_s / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    elif bound == "tensor":
+        achieved = work["flops"] / avg_s / 1e12
+        peak = peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+    else:
+        achieved = work["flops"] / avg_s / 1e12
+        peak = alu_peak_tflops(peaks["sm_max_mhz"])
+        unit = "TFLOP/s"
+    traffic = traffic_for(dname, wl.name)
+    roof = {"kernel": dname, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic,
+            "peak_source": (peaks["source"] if bound != "alu"
+                            else "derived: 148 SMs x 128 fp32 lanes x 2 flop x max SM clock"),
+            "algorithmic_per_launch": work["bytes"] if bound == "hbm" else work["flops"]}
+    for name, x in kern.items():
+        wk = kernel_work(name, wl)
+        x["hbm_gbs"] = wk["bytes"] / (x["avg_us"] * 1e-6) / 1e9 if x["avg_us"] else None
+        x["hbm_frac"] = x["hbm_gbs"] / peaks["hbm_gbs"] if x["hbm_gbs"] else None
+
+    h2d = (q_h.numel() * q_h.element_size() + v_h.numel() * v_h.element_size())
+    d2h = out_h.numel() * out_h.element_size()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "n": wl.n, "d": wl.d, "k": wl.k,
+                   "w": wl.w, "causal": True, "step": "forward + centroid update" if wl.ema
+                   else "forward", "l2": "flushed before every timed step (256 MiB write)",
+                   "graph": False},
+        "tflops": tflops, "tflops_frac_bf16": tflops / peaks["bf16_tflops"],
+        "roofline": roof,
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": gpu_launches, "launches_per_step": launches_per_step,
+        "clocks": clocks, "kernels": kern,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c3", help="c1..c5 (default: the n=8192 configuration)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from workloads import make_workload
+    wl = make_workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,19 @@
+"""B300-native routing attention (Routing Transformer, shared-QK).
+
+The compute lives in ``librouting_attention.so`` (hand-written sm_103a CUDA,
+C ABI in ``include/routing_attention.h``); this package is its thin binding.
+"""
+
+from ._binding import (  # noqa: F401
+    LIB_PATH,
+    RoutingAttentionError,
+    Workspace,
+    load_library,
+    rt_centroid_ema,
+    rt_launch_count,
+    rt_profile_kernel_name,
+    rt_profile_set,
+    rt_route_assign,
+    rt_routing_attention,
+    rt_workspace_bytes,
+)

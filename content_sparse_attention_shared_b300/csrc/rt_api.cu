@@ -1,0 +1,283 @@
+// C-ABI layer: argument validation, workspace carving and the launch order of
+// the routing-attention pass.  No allocation, no synchronisation and no host
+// copies happen in the compute entry points.
+#include <atomic>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "rt_internal.cuh"
+
+namespace rt {
+
+// ---------------------------------------------------------------------------
+// launch counting and the per-launch timing hook
+// ---------------------------------------------------------------------------
+static std::atomic<long long> g_launches{0};
+static std::mutex g_prof_mu;
+static std::vector<cudaEvent_t> g_prof_events;
+static std::vector<int> g_prof_kinds;
+static int g_prof_pairs = 0;
+static int g_prof_next = 0;
+static thread_local int t_prof_slot = -1;
+
+void launch_begin(int kind, cudaStream_t s) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  t_prof_slot = -1;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (g_prof_next < g_prof_pairs) {
+    t_prof_slot = g_prof_next++;
+    g_prof_kinds[t_prof_slot] = kind;
+    cudaEventRecord(g_prof_events[2 * t_prof_slot], s);
+  }
+}
+
+void launch_end(int kind, cudaStream_t s) {
+  (void)kind;
+  if (t_prof_slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (t_prof_slot < g_prof_pairs) cudaEventRecord(g_prof_events[2 * t_prof_slot + 1], s);
+  t_prof_slot = -1;
+}
+
+// ---------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------
+static inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct FwdLayout {
+  size_t err, S, mcount, idx, assign, yslot, total;
+};
+
+static FwdLayout fwd_layout(int B, int H, int n, int d, int k, int w) {
+  const size_t BH = (size_t)B * H;
+  FwdLayout L;
+  size_t off = 0;
+  L.err = off; off += 256;
+  L.S = off; off += align256(BH * k * n * sizeof(float));
+  L.mcount = off; off += align256(BH * n * sizeof(int32_t));
+  L.idx = off; off += align256(BH * k * w * sizeof(int32_t));
+  L.assign = off; off += align256(BH * n * sizeof(int32_t));
+  L.yslot = off; off += align256(BH * k * w * d * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+static size_t ema_total(int B, int H, int n, int k) { return 256 + ema_workspace_bytes(B, H, n, k); }
+
+}  // namespace rt
+
+using namespace rt;
+
+// ---------------------------------------------------------------------------
+// error reporting
+// ---------------------------------------------------------------------------
+static thread_local char t_err[512];
+
+static rt_status fail(rt_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+static rt_status ok() {
+  t_err[0] = '\0';
+  return RT_OK;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static rt_status check_shape(rt_dtype dt, int B, int H, int n, int d, int k, int w) {
+  if (dt != RT_F32 && dt != RT_BF16) return fail(RT_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  if (B < 1 || H < 1 || n < 1 || k < 1 || w < 1)
+    return fail(RT_ERR_INVALID_ARG, "sizes must be positive (B=%d H=%d n=%d k=%d w=%d)", B, H, n, k, w);
+  if (w > n) return fail(RT_ERR_INVALID_ARG, "w=%d exceeds n=%d", w, n);
+  if (d != 64 && d != 128) return fail(RT_ERR_UNSUPPORTED, "head dimension d=%d (supported: 64, 128)", d);
+  const double bhkn = (double)B * H * k * n;
+  const double bhkwd = (double)B * H * k * w * d;
+  if (bhkn > 4.0e9 || bhkwd > 1.6e10 || (double)B * H * n * d > 1.6e10)
+    return fail(RT_ERR_UNSUPPORTED, "problem too large for one call");
+  if ((double)B * n > 12.0e6) return fail(RT_ERR_UNSUPPORTED, "B*n above 12M rows per head");
+  return RT_OK;
+}
+
+static rt_status from_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return RT_OK;
+  return fail(RT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+extern "C" {
+
+const char* rt_status_string(rt_status s) {
+  switch (s) {
+    case RT_OK: return "RT_OK";
+    case RT_ERR_INVALID_ARG: return "RT_ERR_INVALID_ARG";
+    case RT_ERR_UNSUPPORTED: return "RT_ERR_UNSUPPORTED";
+    case RT_ERR_WORKSPACE: return "RT_ERR_WORKSPACE";
+    case RT_ERR_CUDA: return "RT_ERR_CUDA";
+    case RT_ERR_TIMEOUT: return "RT_ERR_TIMEOUT";
+  }
+  return "RT_ERR_UNKNOWN";
+}
+
+const char* rt_last_error_detail(void) { return t_err; }
+
+int64_t rt_launch_count(void) { return (int64_t)g_launches.load(); }
+
+rt_status rt_profile_set(void* const* events, int n_pairs) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (n_pairs < 0 || (n_pairs > 0 && events == nullptr))
+    return fail(RT_ERR_INVALID_ARG, "bad profile event array");
+  g_prof_events.assign(2 * (size_t)n_pairs, nullptr);
+  for (int i = 0; i < 2 * n_pairs; ++i) g_prof_events[i] = static_cast<cudaEvent_t>(events[i]);
+  g_prof_kinds.assign(n_pairs, -1);
+  g_prof_pairs = n_pairs;
+  g_prof_next = 0;
+  return ok();
+}
+
+int rt_profile_kernel_id(int i) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (i < 0 || i >= g_prof_next) return -1;
+  return g_prof_kinds[i];
+}
+
+const char* rt_kernel_name(int id) {
+  static const char* names[K_NUM_KINDS] = {
+      "score_simt", "score_tc", "select_topw", "attention_simt", "attention_tc",
+      "scatter_average", "ema_bucket", "ema_update", "centroid_prep"};
+  if (id < 0 || id >= K_NUM_KINDS) return "unknown";
+  return names[id];
+}
+
+size_t rt_workspace_bytes(int B, int H, int n, int d, int k, int w, rt_dtype dt) {
+  if (check_shape(dt, B, H, n, d, k, w) != RT_OK) return 0;
+  const size_t a = fwd_layout(B, H, n, d, k, w).total;
+  const size_t b = ema_total(B, H, n, k);
+  return a > b ? a : b;
+}
+
+rt_status rt_route_assign(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                          const float* centroids, int k, int w, int32_t* idx, int32_t* assign,
+                          float* scores, void* workspace, size_t workspace_bytes, void* stream) {
+  rt_status st = check_shape(dt, B, H, n, d, k, w);
+  if (st != RT_OK) return st;
+  if (!qk || !centroids || !idx) return fail(RT_ERR_INVALID_ARG, "null qk/centroids/idx");
+  if (!aligned16(qk) || !aligned16(centroids) || !aligned16(idx) ||
+      (assign && !aligned16(assign)) || (scores && !aligned16(scores)))
+    return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  const FwdLayout L = fwd_layout(B, H, n, d, k, w);
+  if (!workspace || workspace_bytes < L.total)
+    return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, L.total);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  float* S = scores ? scores : reinterpret_cast<float*>(ws + L.S);
+  st = from_cuda(launch_score_simt(qk, dt, BH, H, n, d, centroids, k, S, assign, nullptr, s),
+                 "score kernel");
+  if (st != RT_OK) return st;
+  st = from_cuda(launch_select(S, BH, n, k, w, idx, nullptr, s), "select kernel");
+  if (st != RT_OK) return st;
+  return ok();
+}
+
+rt_status rt_routing_attention(const void* q, const void* kp, const void* v, rt_dtype dt, int B,
+                               int H, int n, int d, const float* centroids, int kc, int w,
+                               int causal, float scale, void* out, int32_t* idx_out,
+                               int32_t* assign_out, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  rt_status st = check_shape(dt, B, H, n, d, kc, w);
+  if (st != RT_OK) return st;
+  if (!q || !kp || !v || !centroids || !out) return fail(RT_ERR_INVALID_ARG, "null tensor pointer");
+  if (kp != q) return fail(RT_ERR_UNSUPPORTED, "separate keys: only shared QK (k == q) is routed");
+  if (causal != 0 && causal != 1) return fail(RT_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!std::isfinite(scale)) return fail(RT_ERR_INVALID_ARG, "scale is not finite");
+  if (!aligned16(q) || !aligned16(v) || !aligned16(centroids) || !aligned16(out) ||
+      (idx_out && !aligned16(idx_out)) || (assign_out && !aligned16(assign_out)))
+    return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  const FwdLayout L = fwd_layout(B, H, n, d, kc, w);
+  if (!workspace || workspace_bytes < L.total)
+    return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, L.total);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (scale <= 0.0f) scale = 1.0f / sqrtf((float)d);
+
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  float* S = reinterpret_cast<float*>(ws + L.S);
+  int32_t* mcount = reinterpret_cast<int32_t*>(ws + L.mcount);
+  int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + L.idx);
+  float* yslot = reinterpret_cast<float*>(ws + L.yslot);
+
+  st = from_cuda(launch_score_simt(q, dt, BH, H, n, d, centroids, kc, S, assign_out, mcount, s),
+                 "score kernel");
+  if (st != RT_OK) return st;
+  st = from_cuda(launch_select(S, BH, n, kc, w, idx, mcount, s), "select kernel");
+  if (st != RT_OK) return st;
+  st = from_cuda(launch_attention_simt(q, kp, v, dt, BH, n, d, kc, w, causal, scale, idx, mcount,
+                                       out, yslot, s),
+                 "attention kernel");
+  if (st != RT_OK) return st;
+  st = from_cuda(launch_scatter(dt, BH, n, d, kc, w, idx, mcount, yslot, out, s), "scatter kernel");
+  if (st != RT_OK) return st;
+  return ok();
+}
+
+rt_status rt_centroid_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                          const int32_t* assign, float* centroids, int k, float decay,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  rt_status st = check_shape(dt, B, H, n, d, k, 1);
+  if (st != RT_OK) return st;
+  if (!qk || !assign || !centroids) return fail(RT_ERR_INVALID_ARG, "null qk/assign/centroids");
+  if (!(decay >= 0.0f && decay <= 1.0f)) return fail(RT_ERR_INVALID_ARG, "decay must be in [0, 1]");
+  if (!aligned16(qk) || !aligned16(assign) || !aligned16(centroids))
+    return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (k > 4096) return fail(RT_ERR_UNSUPPORTED, "k above 4096 for the centroid update");
+  const size_t need = ema_total(B, H, n, k);
+  if (!workspace || workspace_bytes < need)
+    return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = from_cuda(launch_ema(qk, dt, B, H, n, d, assign, centroids, k, decay, ws + 256, s),
+                 "centroid update kernels");
+  if (st != RT_OK) return st;
+  return ok();
+}
+
+rt_status rt_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < 256) return fail(RT_ERR_WORKSPACE, "no workspace");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  return from_cuda(cudaMemsetAsync(workspace, 0, 256, static_cast<cudaStream_t>(stream)),
+                   "clearing the device status word") == RT_OK ? ok() : RT_ERR_CUDA;
+}
+
+rt_status rt_check_device_status(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < 256) return fail(RT_ERR_WORKSPACE, "no workspace");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return from_cuda(e, "reading the device status word");
+  if (word != DEV_OK) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyAsync(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (word == DEV_TIMEOUT) return fail(RT_ERR_TIMEOUT, "a device-side wait ran out (code %u)", word);
+    return fail(RT_ERR_CUDA, "device status word %u", word);
+  }
+  return ok();
+}
+
+}  // extern "C"

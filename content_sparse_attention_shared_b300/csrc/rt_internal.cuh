@@ -1,0 +1,106 @@
+// Internal declarations shared by the kernels and the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/routing_attention.h"
+
+namespace rt {
+
+// ---------------------------------------------------------------------------
+// kernel kinds (for launch counting and the per-launch timing hook)
+// ---------------------------------------------------------------------------
+enum KernelId {
+  K_SCORE_SIMT = 0,
+  K_SCORE_TC = 1,
+  K_SELECT = 2,
+  K_ATTN_SIMT = 3,
+  K_ATTN_TC = 4,
+  K_SCATTER = 5,
+  K_EMA_BUCKET = 6,
+  K_EMA_UPDATE = 7,
+  K_CENTROID_PREP = 8,
+  K_NUM_KINDS = 9
+};
+
+// Called by every launcher around its launch.
+void launch_begin(int kind, cudaStream_t s);
+void launch_end(int kind, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// device error word (first bytes of every workspace)
+// ---------------------------------------------------------------------------
+enum DeviceError : unsigned int {
+  DEV_OK = 0,
+  DEV_TIMEOUT = 1,
+};
+
+// ---------------------------------------------------------------------------
+// small device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Order-preserving map of an fp32 score to an unsigned key (larger score,
+// larger key).  -0 is folded onto +0 so that equal scores give equal keys.
+__device__ __forceinline__ uint32_t score_key(float f) {
+  if (f == 0.0f) f = 0.0f;
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------
+// launchers (one per kernel family); all asynchronous on `s`
+// ---------------------------------------------------------------------------
+
+// normalise + score + argmax.  S: [BH,k,n] fp32 (may be null), a: [BH,n]
+// (may be null), mcount: [BH,n] zeroed here when non-null.
+cudaError_t launch_score_simt(const void* qk, rt_dtype dt, int BH, int H, int n, int d,
+                              const float* mu, int k, float* S, int32_t* a,
+                              int32_t* mcount, cudaStream_t s);
+
+// top-w per centroid in ascending position order; counts memberships into
+// mcount (atomic integer increments; may be null).
+cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* idx,
+                          int32_t* mcount, cudaStream_t s);
+
+// in-cluster attention.  Rows of positions with mcount == 1 go straight to
+// `out`; rows of positions in several clusters go to yslot [BH,k,w,d] fp32.
+cudaError_t launch_attention_simt(const void* q, const void* kk, const void* v, rt_dtype dt,
+                                  int BH, int n, int d, int k, int w, int causal,
+                                  float scale, const int32_t* idx, const int32_t* mcount,
+                                  void* out, float* yslot, cudaStream_t s);
+
+// zero rows (mcount == 0) and the mean over clusters (mcount >= 2).
+cudaError_t launch_scatter(rt_dtype dt, int BH, int n, int d, int k, int w,
+                           const int32_t* idx, const int32_t* mcount, const float* yslot,
+                           void* out, cudaStream_t s);
+
+// centroid update: bucket the rows by centroid per tile, then a segmented
+// sum per (head, centroid) and the blend/renormalise.
+size_t ema_workspace_bytes(int B, int H, int n, int k);
+cudaError_t launch_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                       const int32_t* assign, float* mu, int k, float decay,
+                       void* ws, cudaStream_t s);
+
+}  // namespace rt

@@ -1,0 +1,163 @@
+/*
+ * routing_attention.h -- C ABI of the B300 (sm_103a) routing-attention library.
+ *
+ * Method: "Efficient Content-Based Sparse Attention with Routing Transformers"
+ * (Roy, Saffar, Vaswani, Grangier; TACL 2021).  The pages describing it
+ * (paperlayer.ai summary §4 "Efficient Content-Dependent Sparse Attention",
+ * "Routing attention with clustering") fix the operation: queries and keys
+ * are put on the unit sphere, routed to the nearest of k shared centroids
+ * learned by online spherical k-means, and attention is computed only
+ * between query/key pairs routed to the same cluster, with balanced clusters
+ * of about n/k members.  The steps the pages leave open are read as follows
+ * and implemented exactly so:
+ *   - "unit-normalised" = subtract the row mean, divide by the Euclidean norm
+ *     (a row with zero centred norm maps to the zero vector);
+ *   - each centroid takes its own top-w tokens by score, ties to the lower
+ *     position, and lists them in ascending position order;
+ *   - attention inside a cluster uses the raw Q, K, V rows, scale 1/sqrt(d)
+ *     unless given, causal on original positions (a token sees itself);
+ *   - a token in several clusters receives the mean of its outputs, a token in
+ *     none receives a zero row;
+ *   - the centroid update blends the mean of the normalised rows assigned to
+ *     each centroid (argmax assignment, over the whole batch) into the
+ *     centroid with weight (1 - decay), then renormalises; a centroid with no
+ *     assigned row is left unchanged.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous,
+ *     16-byte aligned, innermost dimension fastest.  Shapes are given in the
+ *     argument comments ([B,H,n,d] means index ((b*H + h)*n + t)*d + j).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     Calls are asynchronous on that stream; the library never synchronises,
+ *     never allocates device memory and never copies to the host inside the
+ *     compute entry points.  All scratch lives in the caller's `workspace`
+ *     of at least rt_workspace_bytes(...) bytes (256-byte aligned).
+ *   - Errors found on the host (bad arguments, too-small workspace, a CUDA
+ *     launch error) are returned immediately; nothing is launched then.
+ *     A device-side error (a bounded wait that ran out) is recorded in the
+ *     workspace and reported by rt_check_device_status().
+ *   - Supported: d in {64, 128}; 1 <= w <= n; k >= 1; causal in {0, 1};
+ *     dtype RT_F32 or RT_BF16 (Q, K, V and the output share it; centroids
+ *     are always fp32).  Other values return RT_ERR_UNSUPPORTED or
+ *     RT_ERR_INVALID_ARG.  There is no CPU fallback.
+ */
+#ifndef ROUTING_ATTENTION_H
+#define ROUTING_ATTENTION_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rt_status {
+  RT_OK = 0,
+  RT_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer     */
+  RT_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement    */
+  RT_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required     */
+  RT_ERR_CUDA = 4,         /* a CUDA call or kernel launch failed            */
+  RT_ERR_TIMEOUT = 5       /* a device-side bounded wait ran out             */
+} rt_status;
+
+typedef enum rt_dtype { RT_F32 = 0, RT_BF16 = 1 } rt_dtype;
+
+/* Bytes of device workspace the three compute calls need for this shape
+ * (the maximum over them, so one buffer serves all).  Returns 0 for an
+ * invalid shape. */
+size_t rt_workspace_bytes(int B, int H, int n, int d, int k, int w, rt_dtype dt);
+
+/* Routing only (steps: normalise, score, argmax, top-w per centroid, sort).
+ * Source: §4 "Routing attention with clustering" (nearest-centroid routing
+ * of unit-normalised shared queries/keys; balanced clusters via a top-k
+ * assignment).
+ *   qk        [B,H,n,d]  shared query/key rows (dtype dt)
+ *   centroids [H,k,d]    fp32 centroids (read only)
+ *   idx       [B,H,k,w]  out: the w positions chosen by each centroid,
+ *                        strictly ascending
+ *   assign    [B,H,n]    out, may be NULL: argmax centroid of every row
+ *                        (ties to the lower centroid)
+ *   scores    [B,H,k,n]  out, may be NULL: the fp32 scores <r_t, mu_c>
+ */
+rt_status rt_route_assign(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                          const float* centroids, int k, int w,
+                          int32_t* idx, int32_t* assign, float* scores,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Full routing-attention forward pass: routing as above, dense softmax
+ * attention inside every w-by-w cluster block (causal on original positions
+ * when causal=1), and the averaging scatter back to positions.
+ * Source: §3 "Self-Attentive Auto-regressive Sequence Modeling" (softmax
+ * attention, causal masking) and §4 (same-cluster query/key pairs only).
+ *   q, k, v   [B,H,n,d]  dtype dt; shared QK: k must equal q (the same
+ *                        pointer), otherwise RT_ERR_UNSUPPORTED
+ *   centroids [H,kc,d]   fp32 (read only; the update is rt_centroid_ema)
+ *   scale     logit scale; <= 0 selects 1/sqrt(d)
+ *   out       [B,H,n,d]  dtype dt; every row is written (zero rows for
+ *                        positions no centroid chose)
+ *   idx_out   [B,H,kc,w] out, may be NULL
+ *   assign_out[B,H,n]    out, may be NULL (argmax centroid per row, the
+ *                        input rt_centroid_ema expects)
+ */
+rt_status rt_routing_attention(const void* q, const void* k, const void* v, rt_dtype dt,
+                               int B, int H, int n, int d,
+                               const float* centroids, int kc, int w,
+                               int causal, float scale,
+                               void* out, int32_t* idx_out, int32_t* assign_out,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* One online spherical k-means step on the centroids, in place.
+ * Source: §2 "Attention with Content-Based Sparsity" (centroids learned by
+ * mini-batch spherical k-means), §4 (centroids shared across sequences,
+ * learned online).  For every head h and centroid c:
+ *   N = #{(b,t): assign[b,h,t] == c};  if N > 0:
+ *   mu_c <- normalise(decay * mu_c + (1 - decay) * (1/N) * sum r_t)
+ * with r_t the normalised row of qk; otherwise mu_c is left bit-exact.
+ *   qk        [B,H,n,d]  dtype dt
+ *   assign    [B,H,n]    int32 in [0, k)
+ *   centroids [H,k,d]    fp32, updated in place
+ *   decay     in [0, 1]
+ * The reduction is a counting sort by centroid followed by a segmented sum in
+ * a fixed order: results are deterministic. */
+rt_status rt_centroid_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                          const int32_t* assign, float* centroids, int k, float decay,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Clears the device status word at the start of a new workspace (an async
+ * memset of its first 256 bytes on `stream`).  Call once after allocating a
+ * workspace; the compute calls only ever set the word. */
+rt_status rt_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, reads the device error word kept in `workspace`,
+ * clears it, and returns RT_OK, RT_ERR_TIMEOUT or RT_ERR_CUDA.  Not for use
+ * inside stream capture. */
+rt_status rt_check_device_status(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* rt_status_string(rt_status s);
+
+/* Detail of the last error returned on the calling host thread (static
+ * thread-local buffer; empty string if none). */
+const char* rt_last_error_detail(void);
+
+/* Number of kernels this library has launched since it was loaded (all
+ * threads).  Used by benchmarks to count launches in a timed region. */
+int64_t rt_launch_count(void);
+
+/* Per-launch timing hook for benchmarks.  While set, the i-th kernel the
+ * library launches after this call (i < n_pairs) records events[2i] just
+ * before and events[2i+1] just after itself on its stream.  `events` are
+ * cudaEvent_t handles created by the caller with timing enabled; the array
+ * is copied.  rt_profile_set(NULL, 0) switches the hook off. */
+rt_status rt_profile_set(void* const* events, int n_pairs);
+
+/* Kernel-kind id of the i-th launch recorded since rt_profile_set (or -1),
+ * and the name of a kernel kind. */
+int rt_profile_kernel_id(int i);
+const char* rt_kernel_name(int id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROUTING_ATTENTION_H */

@@ -1,0 +1,230 @@
+"""GPU-vs-oracle parity through the C ABI (needs a B300).
+
+Every case draws seeded inputs, runs the CUDA library, and compares with the
+fp64 oracle element by element (tolerances in tests/parity_helpers.py).  The
+five measured configurations run at their full sizes, in the same launch
+configuration the benchmark times; the sweep adds ragged and degenerate
+shapes (n=1, odd w, w=1, w=n, k*w != n, non-causal, several sequences).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.routing_oracle as orc
+from tests import parity_helpers as ph
+from workloads import CONFIG_ORDER, make_random, make_workload
+
+pytestmark = pytest.mark.gpu
+
+rt = pytest.importorskip("content_sparse_attention_shared_b300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from content_sparse_attention_shared_b300 import build
+    build.build()
+
+
+def run_gpu(wl, causal=True, scale=0.0):
+    q, v, mu = ph.to_device(wl)
+    B, H, n, d, k, w = wl.B, wl.H, wl.n, wl.d, wl.k, wl.w
+    ws = rt.Workspace.for_shape(B, H, n, d, k, w, q.dtype)
+    idx = torch.empty((B, H, k, w), dtype=torch.int32, device="cuda")
+    a = torch.empty((B, H, n), dtype=torch.int32, device="cuda")
+    out = rt.rt_routing_attention(q, q, v, mu, w, causal=causal, scale=scale, idx_out=idx,
+                                  assign_out=a, workspace=ws)
+    idx2, a2, S = rt.rt_route_assign(q, mu, w, want_scores=True, workspace=ws)
+    torch.cuda.synchronize()
+    ws.check()
+    return dict(q=q, v=v, mu=mu, ws=ws, out=out, idx=idx.cpu().numpy(), a=a.cpu().numpy(),
+                idx2=idx2.cpu().numpy(), a2=a2.cpu().numpy(), S=S.cpu().numpy())
+
+
+def check_forward(wl, res, causal=True, scale=None):
+    q64 = wl.q_f32().astype(np.float64)
+    v64 = wl.v_f32().astype(np.float64)
+    if scale is None or scale <= 0:
+        scale = 1.0 / math.sqrt(wl.d)
+    out = ph.out_to_f64(res["out"])
+    assert np.array_equal(res["idx"], res["idx2"]), "route_assign and the forward disagree"
+    assert np.array_equal(res["a"], res["a2"])
+    worst = 0.0
+    for b in range(wl.B):
+        for h in range(wl.H):
+            S64 = ph.oracle_scores(q64[b, h], wl.centroids[h])
+            gS = res["S"][b, h]
+            assert np.max(np.abs(gS - S64)) < ph.TOL_SCORE
+            ph.check_self_consistent(res["idx"][b, h], res["a"][b, h], gS, wl.w)
+            ph.check_index_lists(res["idx"][b, h], S64, wl.w, wl.n)
+            ph.check_assign(res["a"][b, h], S64)
+            want = ph.oracle_output_on(q64[b, h], v64[b, h], res["idx"][b, h], causal, scale)
+            err = np.max(np.abs(out[b, h] - want))
+            worst = max(worst, err)
+            m = orc.membership_counts(res["idx"][b, h], wl.n)
+            assert np.all(out[b, h][m == 0] == 0.0), "uncovered rows must be exactly zero"
+    assert worst <= ph.TOL_OUT[wl.dtype], f"max abs error {worst:.3g}"
+    return worst
+
+
+def check_ema(wl, res, decay):
+    mu_gpu = res["mu"].clone()
+    a_t = torch.from_numpy(res["a"]).cuda()
+    rt.rt_centroid_ema(res["q"], a_t, mu_gpu, decay, workspace=res["ws"])
+    torch.cuda.synchronize()
+    want = orc.centroid_ema(wl.q_f32().astype(np.float64), res["a"], wl.centroids, decay)
+    got = mu_gpu.cpu().numpy().astype(np.float64)
+    err = np.max(np.abs(got - want))
+    assert err <= ph.TOL_EMA, f"centroid update error {err:.3g}"
+    # centroids nobody chose stay bit-exact
+    for h in range(wl.H):
+        counts = np.bincount(res["a"][:, h].reshape(-1), minlength=wl.k)
+        for c in np.nonzero(counts == 0)[0]:
+            assert np.array_equal(got[h, c], wl.centroids[h, c].astype(np.float64))
+
+
+# ---------------------------------------------------------------------------
+# the five measured configurations, full size
+# ---------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def cfg_results():
+    return {}
+
+
+@pytest.mark.parametrize("cid", CONFIG_ORDER)
+def test_config_full_size(cid, cfg_results):
+    wl = make_workload(cid)
+    res = run_gpu(wl)
+    check_forward(wl, res)
+    check_ema(wl, res, wl.decay)
+    check_ema(wl, res, 0.0)
+
+
+def test_hand_worked_example(hand_worked):
+    from tests.conftest import eval_tree
+    g = hand_worked
+    for dt in (torch.float32, torch.bfloat16):
+        # d=4 is below the supported head dimension: embed in d=64 with zeros
+        # appended (zero-mean rows stay zero-mean; dot products unchanged).
+        d = 64
+        q = np.zeros((1, 1, 4, d)); q[0, 0, :, :4] = g["q"]
+        v = np.zeros((1, 1, 4, d)); v[0, 0, :, :4] = g["v"]
+        mu = np.zeros((1, 2, d)); mu[0, :, :4] = eval_tree(g["centroids"])
+        qt = torch.tensor(q, dtype=dt, device="cuda")
+        vt = torch.tensor(v, dtype=dt, device="cuda")
+        mt = torch.tensor(mu, dtype=torch.float32, device="cuda")
+        idx = torch.empty((1, 1, 2, 2), dtype=torch.int32, device="cuda")
+        a = torch.empty((1, 1, 4), dtype=torch.int32, device="cuda")
+        scale = eval_tree(g["scale"])
+        for causal, key in ((True, "O_causal"), (False, "O_noncausal")):
+            out = rt.rt_routing_attention(qt, qt, vt, mt, 2, causal=causal, scale=scale,
+                                          idx_out=idx, assign_out=a)
+            torch.cuda.synchronize()
+            assert idx.cpu().numpy()[0, 0].tolist() == g["expected"]["idx"]
+            assert a.cpu().numpy()[0, 0].tolist() == g["expected"]["assign"]
+            got = out.float().cpu().numpy()[0, 0, :, :4]
+            tol = 1e-5 if dt == torch.float32 else 2e-2
+            np.testing.assert_allclose(got, np.array(g["expected"][key], float), atol=tol)
+            assert np.all(out.float().cpu().numpy()[0, 0, :, 4:] == 0)
+        for decay, key in ((0.0, "centroids_decay0"), (0.5, "centroids_decay_half")):
+            m2 = mt.clone()
+            rt.rt_centroid_ema(qt, a, m2, decay)
+            torch.cuda.synchronize()
+            np.testing.assert_allclose(m2.cpu().numpy()[0, :, :4],
+                                       np.array(eval_tree(g["expected"][key])), atol=1e-6)
+
+
+# ---------------------------------------------------------------------------
+# shape sweep: ragged, degenerate and extreme cases
+# ---------------------------------------------------------------------------
+
+SWEEP = [
+    # B, H, n, d, k, w, dtype, causal
+    (1, 1, 1, 64, 1, 1, "bf16", True),
+    (1, 1, 7, 64, 3, 5, "f32", True),
+    (1, 2, 100, 64, 7, 13, "bf16", True),
+    (2, 1, 300, 128, 5, 61, "bf16", True),
+    (1, 1, 300, 128, 1, 300, "bf16", True),     # one cluster = full causal attention
+    (1, 1, 257, 64, 4, 257, "f32", True),       # every centroid takes everything
+    (1, 3, 515, 64, 9, 1, "bf16", True),        # w = 1
+    (2, 2, 640, 128, 10, 64, "f32", False),     # non-causal
+    (1, 1, 1000, 64, 33, 97, "bf16", True),     # k*w != n, odd w
+    (3, 2, 777, 128, 24, 129, "bf16", True),    # w just above a tile
+    (1, 1, 2048, 128, 300, 16, "bf16", True),   # k > 256
+]
+
+
+@pytest.mark.parametrize("case", SWEEP, ids=lambda c: "b{}h{}n{}d{}k{}w{}{}{}".format(
+    c[0], c[1], c[2], c[3], c[4], c[5], c[6], "" if c[7] else "nc"))
+def test_sweep(case):
+    B, H, n, d, k, w, dt, causal = case
+    wl = make_random(B, H, n, d, k, w, dtype=dt, seed=n + k + w,
+                     centroid_init="tokens" if k <= n else "random")
+    res = run_gpu(wl, causal=causal)
+    check_forward(wl, res, causal=causal)
+    check_ema(wl, res, 0.3)
+
+
+def test_full_attention_matches_sdpa():
+    wl = make_random(1, 2, 512, 64, 1, 512, dtype="f32", seed=5)
+    res = run_gpu(wl)
+    q = res["q"].double()
+    ref = torch.nn.functional.scaled_dot_product_attention(q, q, res["v"].double(), is_causal=True)
+    assert torch.max(torch.abs(res["out"].double() - ref)).item() < 1e-4
+
+
+def test_degenerate_ties():
+    # constant rows normalise to zero: every score is 0, so every centroid
+    # takes the first w positions and every row goes to centroid 0.
+    B, H, n, d, k, w = 1, 2, 200, 64, 5, 37
+    q = torch.full((B, H, n, d), 0.75, dtype=torch.bfloat16, device="cuda")
+    v = torch.randn((B, H, n, d), device="cuda").to(torch.bfloat16)
+    mu = torch.nn.functional.normalize(torch.randn(H, k, d, device="cuda"), dim=-1)
+    idx = torch.empty((B, H, k, w), dtype=torch.int32, device="cuda")
+    a = torch.empty((B, H, n), dtype=torch.int32, device="cuda")
+    out = rt.rt_routing_attention(q, q, v, mu, w, idx_out=idx, assign_out=a)
+    torch.cuda.synchronize()
+    assert torch.equal(idx.cpu(), torch.arange(w, dtype=torch.int32).expand(B, H, k, w))
+    assert int(a.abs().sum()) == 0
+    assert torch.all(out[:, :, w:] == 0)
+
+
+def test_value_ones_property_full_size():
+    wl = make_workload("c3")
+    q, v, mu = ph.to_device(wl)
+    ones = torch.ones_like(v)
+    idx = torch.empty((wl.B, wl.H, wl.k, wl.w), dtype=torch.int32, device="cuda")
+    out = rt.rt_routing_attention(q, q, ones, mu, wl.w, idx_out=idx)
+    torch.cuda.synchronize()
+    m = torch.zeros((wl.B * wl.H, wl.n), dtype=torch.int32, device="cuda")
+    flat = idx.view(wl.B * wl.H, -1).long()
+    m.scatter_add_(1, flat, torch.ones_like(flat, dtype=torch.int32))
+    want = (m > 0).to(out.dtype).view(wl.B, wl.H, wl.n, 1).expand_as(out)
+    assert torch.max(torch.abs(out.float() - want.float())).item() < 1e-2
+
+
+def test_deterministic_repeat():
+    wl = make_workload("c2")
+    q, v, mu = ph.to_device(wl)
+    ws = rt.Workspace.for_shape(wl.B, wl.H, wl.n, wl.d, wl.k, wl.w)
+    o1 = rt.rt_routing_attention(q, q, v, mu, wl.w, workspace=ws).clone()
+    o2 = rt.rt_routing_attention(q, q, v, mu, wl.w, workspace=ws).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+
+
+def test_bad_arguments_raise_on_gpu():
+    q = torch.zeros((1, 1, 64, 96), dtype=torch.bfloat16, device="cuda")
+    mu = torch.zeros((1, 4, 96), device="cuda")
+    with pytest.raises(rt.RoutingAttentionError):
+        rt.rt_routing_attention(q, q, q, mu, 16)
+    q = torch.zeros((1, 1, 64, 64), dtype=torch.bfloat16, device="cuda")
+    k2 = q.clone()
+    mu = torch.zeros((1, 4, 64), device="cuda")
+    with pytest.raises(rt.RoutingAttentionError):
+        rt.rt_routing_attention(q, k2, q, mu, 16)
