@@ -187,7 +187,6 @@ class ClockSampler:
 def oracle_head_seconds(wl, head, reps=1):
     """Time the oracle's full step (a1..a7) on one head of the batch."""
     import numpy as np
-    from threadpoolctl import threadpool_limits
 
     import oracle.routing_oracle as orc
 
@@ -195,28 +194,37 @@ def oracle_head_seconds(wl, head, reps=1):
     v64 = wl.v_f32().astype(np.float64)[:, head:head + 1]
     mu = wl.centroids[head:head + 1]
     best = float("inf")
-    with threadpool_limits(limits=1):
-        for _ in range(reps):
-            t0 = time.perf_counter()
-            _, _, a = orc.routing_attention(q64, q64, v64, mu, wl.w, causal=True)
-            if wl.ema:
-                orc.centroid_ema(q64, a, mu, wl.decay)
-            best = min(best, time.perf_counter() - t0)
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        _, _, a = orc.routing_attention(q64, q64, v64, mu, wl.w, causal=True)
+        if wl.ema:
+            orc.centroid_ema(q64, a, mu, wl.decay)
+        best = min(best, time.perf_counter() - t0)
     return best
 
 
-def cpu_baseline(wl, target_s=10.0, max_reps=5):
-    """Whole steps (every head) of the oracle, repeated until ~target_s of CPU
-    work; best step time."""
-    best, spent, reps = float("inf"), 0.0, 0
-    while reps < max_reps and (spent < target_s or reps == 0):
-        t = sum(oracle_head_seconds(wl, h) for h in range(wl.H))
-        best = min(best, t)
-        spent += t
-        reps += 1
-    return {"value": wl.tokens / best, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{reps} full step(s) of {wl.name} (forward + centroid update, all "
-                      f"{wl.H} heads), fp64 numpy on 1 thread; best step {best:.2f} s"}
+ONE_THREAD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+
+
+def cpu_baseline(wl_id, wl):
+    """The oracle as it stands, timed in a child process pinned to one BLAS
+    thread: every head of one step once (the reference arm, H steps)."""
+    env = dict(os.environ, **ONE_THREAD_ENV)
+    env.pop("RANK", None), env.pop("WORLD_SIZE", None), env.pop("LOCAL_RANK", None)
+    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", wl_id,
+           "--steps", str(wl.H), "--warmup", "0"]
+    res = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
+    line = None
+    for ln in res.stdout.splitlines():
+        if ln.startswith("{"):
+            line = json.loads(ln)
+    if res.returncode != 0 or line is None:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": "oracle run failed: " + res.stderr.strip()[-200:]}
+    return {"value": line["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"one step of {wl.name} (forward + centroid update), each of the "
+                      f"{wl.H} heads once, fp64 numpy oracle on 1 thread; mean head time "
+                      f"x {wl.H} heads = {line['ms_per_step'] / 1e3:.2f} s per step"}
 
 
 def run_reference(args, wl):
@@ -317,6 +325,7 @@ def run_ours(args, wl):
             ev[i][1].record(stream)
         torch.cuda.synchronize()
     gpu_launches = rt.rt_launch_count() - l0
+    prof_names = [rt.rt_profile_kernel_name(i) for i in range(len(prof_pairs))]
     rt.rt_profile_set([])
     step_ms = [a.elapsed_time(b) for a, b in ev]
     t_ms = statistics.mean(step_ms)
@@ -330,7 +339,7 @@ def run_ours(args, wl):
     # per-kernel times over the timed region
     per_kind = {}
     for i, (a, b) in enumerate(prof_pairs):
-        name = rt.rt_profile_kernel_name(i)
+        name = prof_names[i]
         per_kind.setdefault(name, []).append(a.elapsed_time(b))
     kern = {k2: {"launches": len(v2), "avg_us": 1e3 * statistics.mean(v2),
                  "total_ms": sum(v2)} for k2, v2 in per_kind.items()}
@@ -418,7 +427,7 @@ def run_ours(args, wl):
         "clocks": clocks, "kernels": kern,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl)
+        line["cpu_baseline"] = cpu_baseline(args.workload, wl)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -433,6 +442,8 @@ def main():
     ap.add_argument("--workload", default="c3", help="c1..c5 (default: the n=8192 configuration)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.impl == "reference":
+        os.environ.update(ONE_THREAD_ENV)  # before numpy is imported
     from workloads import make_workload
     wl = make_workload(args.workload)
     if args.impl == "reference":

@@ -198,7 +198,12 @@ def rt_profile_set(events) -> None:
     lib = load_library()
     flat = []
     for a, b in events:
+        for e in (a, b):
+            if not e.cuda_event:  # torch creates the handle on first record
+                e.record()
         flat += [a.cuda_event, b.cuda_event]
+    if events:
+        torch.cuda.synchronize()
     arr = (ctypes.c_void_p * max(1, len(flat)))(*flat)
     _check(lib.rt_profile_set(arr, len(events)))
 

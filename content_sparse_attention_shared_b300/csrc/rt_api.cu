@@ -32,7 +32,10 @@ void launch_begin(int kind, cudaStream_t s) {
   if (g_prof_next < g_prof_pairs) {
     t_prof_slot = g_prof_next++;
     g_prof_kinds[t_prof_slot] = kind;
-    cudaEventRecord(g_prof_events[2 * t_prof_slot], s);
+    if (cudaEventRecord(g_prof_events[2 * t_prof_slot], s) != cudaSuccess) {
+      cudaGetLastError();  // a bad timing event must not fail the launch
+      g_prof_kinds[t_prof_slot] = -1;
+    }
   }
 }
 
@@ -40,7 +43,8 @@ void launch_end(int kind, cudaStream_t s) {
   (void)kind;
   if (t_prof_slot < 0) return;
   std::lock_guard<std::mutex> lk(g_prof_mu);
-  if (t_prof_slot < g_prof_pairs) cudaEventRecord(g_prof_events[2 * t_prof_slot + 1], s);
+  if (t_prof_slot < g_prof_pairs && cudaEventRecord(g_prof_events[2 * t_prof_slot + 1], s) != cudaSuccess)
+    cudaGetLastError();
   t_prof_slot = -1;
 }
 
