@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     rt_profile_kernel_name,
     rt_profile_set,
     rt_route_assign,
+    rt_route_assign_noalloc,
     rt_routing_attention,
     rt_workspace_bytes,
 )

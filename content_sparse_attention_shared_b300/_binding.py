@@ -30,6 +30,8 @@ SIGNATURES = {
                                       _vp]),
     "rt_centroid_ema": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_int,
                                  _c_float, _vp, _c_size, _vp]),
+    "rt_route_assign_noalloc": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int,
+                                         _c_int, _vp, _vp, _vp]),
     "rt_workspace_init": (_c_int, [_vp, _c_size, _vp]),
     "rt_check_device_status": (_c_int, [_vp, _c_size, _vp]),
     "rt_status_string": (ctypes.c_char_p, [_c_int]),
@@ -211,3 +213,14 @@ def rt_profile_set(events) -> None:
 def rt_profile_kernel_name(i: int) -> str:
     lib = load_library()
     return lib.rt_kernel_name(lib.rt_profile_kernel_id(i)).decode()
+
+
+def rt_route_assign_noalloc(qk: torch.Tensor, centroids: torch.Tensor, w: int, idx: torch.Tensor,
+                            assign: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Routing with the library's fixed scratch array; outputs are caller-owned
+    (no allocation on either side of the call)."""
+    B, H, n, d = qk.shape
+    k = centroids.shape[1]
+    _check(load_library().rt_route_assign_noalloc(
+        _ptr(qk), _dtype_code(qk), B, H, n, d, _ptr(centroids), k, w, _ptr(idx), _ptr(assign),
+        _stream(stream)))

@@ -285,3 +285,16 @@ rt_status rt_check_device_status(void* workspace, size_t workspace_bytes, void* 
 }
 
 }  // extern "C"
+
+namespace rt {
+
+rt_status record_error(rt_status s, const char* msg) {
+  if (s == RT_OK) return ok();
+  return fail(s, "%s", msg);
+}
+
+rt_status validate_shape(rt_dtype dt, int B, int H, int n, int d, int k, int w) {
+  return check_shape(dt, B, H, n, d, k, w);
+}
+
+}  // namespace rt

@@ -26,6 +26,11 @@ enum KernelId {
   K_NUM_KINDS = 9
 };
 
+// Error detail for the calling host thread (rt_last_error_detail) and the
+// shape checks shared by the entry points.
+rt_status record_error(rt_status s, const char* msg);
+rt_status validate_shape(rt_dtype dt, int B, int H, int n, int d, int k, int w);
+
 // Called by every launcher around its launch.
 void launch_begin(int kind, cudaStream_t s);
 void launch_end(int kind, cudaStream_t s);

@@ -128,6 +128,31 @@ rt_status rt_centroid_ema(const void* qk, rt_dtype dt, int B, int H, int n, int 
  * workspace; the compute calls only ever set the word. */
 rt_status rt_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
+/* Routing for callers that cannot allocate device memory.  The paper has no
+ * counterpart to this call: it exists for callers that cannot call cudaMalloc
+ * (or any allocating routine) where they route -- code running inside a host
+ * framework whose device allocator it does not own, or a program that fixes
+ * its device footprint at start-up -- and so cannot provide the workspace
+ * rt_route_assign needs for its score matrix.
+ *
+ * Same computation and outputs as rt_route_assign (no `scores` output), with
+ * the fp32 score scratch [B,H,k,n] taken from a fixed array in device memory
+ * that the library owns: at most RT_NOALLOC_MAX_SCORES elements (32 MiB),
+ * held on every GPU that loads the library until the process exits.  Larger
+ * B*H*k*n returns RT_ERR_UNSUPPORTED before anything is launched.
+ *   - allocates nothing: no cudaMalloc/cudaFree, no allocating library call;
+ *   - the first call on a device (with that device current) looks up the
+ *     array's device address once; make that first call before any stream
+ *     capture;
+ *   - every call shares the one array, so calls that overlap on the GPU
+ *     (other streams, other host threads) race; serialise them.
+ *   qk [B,H,n,d] dtype dt, centroids [H,k,d] fp32, idx [B,H,k,w] out,
+ *   assign [B,H,n] out or NULL, stream as elsewhere. */
+#define RT_NOALLOC_MAX_SCORES (8u * 1024u * 1024u)
+rt_status rt_route_assign_noalloc(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                                  const float* centroids, int k, int w,
+                                  int32_t* idx, int32_t* assign, void* stream);
+
 /* Synchronises `stream`, reads the device error word kept in `workspace`,
  * clears it, and returns RT_OK, RT_ERR_TIMEOUT or RT_ERR_CUDA.  Not for use
  * inside stream capture. */
