@@ -227,9 +227,16 @@ rt_status rt_routing_attention(const void* q, const void* kp, const void* v, rt_
   if (st != RT_OK) return st;
   st = from_cuda(launch_select(S, BH, n, kc, w, idx, mcount, s), "select kernel");
   if (st != RT_OK) return st;
-  st = from_cuda(launch_attention_simt(q, kp, v, dt, BH, n, d, kc, w, causal, scale, idx, mcount,
-                                       out, yslot, s),
-                 "attention kernel");
+  unsigned int* err = reinterpret_cast<unsigned int*>(ws + L.err);
+  if (attention_tc_supported(dt, d, w)) {
+    st = from_cuda(launch_attention_tc(q, v, BH, n, d, kc, w, causal, scale, idx, mcount, out,
+                                       yslot, err, s),
+                   "attention kernel");
+  } else {
+    st = from_cuda(launch_attention_simt(q, kp, v, dt, BH, n, d, kc, w, causal, scale, idx,
+                                         mcount, out, yslot, s),
+                   "attention kernel");
+  }
   if (st != RT_OK) return st;
   st = from_cuda(launch_scatter(dt, BH, n, d, kc, w, idx, mcount, yslot, out, s), "scatter kernel");
   if (st != RT_OK) return st;

@@ -96,6 +96,13 @@ cudaError_t launch_attention_simt(const void* q, const void* kk, const void* v, 
                                   float scale, const int32_t* idx, const int32_t* mcount,
                                   void* out, float* yslot, cudaStream_t s);
 
+// the same on tcgen05 tensor cores (bf16 only); err: device error word.
+bool attention_tc_supported(rt_dtype dt, int d, int w);
+cudaError_t launch_attention_tc(const void* q, const void* v, int BH, int n, int d, int k, int w,
+                                int causal, float scale, const int32_t* idx,
+                                const int32_t* mcount, void* out, float* yslot,
+                                unsigned int* err, cudaStream_t s);
+
 // zero rows (mcount == 0) and the mean over clusters (mcount >= 2).
 cudaError_t launch_scatter(rt_dtype dt, int BH, int n, int d, int k, int w,
                            const int32_t* idx, const int32_t* mcount, const float* yslot,
