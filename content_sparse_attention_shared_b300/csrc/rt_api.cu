@@ -54,7 +54,7 @@ void launch_end(int kind, cudaStream_t s) {
 static inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct FwdLayout {
-  size_t err, S, mcount, idx, assign, yslot, total;
+  size_t err, S, mcount, slots, idx, assign, yslot, total;
 };
 
 static FwdLayout fwd_layout(int B, int H, int n, int d, int k, int w) {
@@ -64,6 +64,7 @@ static FwdLayout fwd_layout(int B, int H, int n, int d, int k, int w) {
   L.err = off; off += 256;
   L.S = off; off += align256(BH * k * n * sizeof(float));
   L.mcount = off; off += align256(BH * n * sizeof(int32_t));
+  L.slots = off; off += align256(BH * n * SLOTS_PER_ROW * sizeof(int32_t));
   L.idx = off; off += align256(BH * k * w * sizeof(int32_t));
   L.assign = off; off += align256(BH * n * sizeof(int32_t));
   L.yslot = off; off += align256(BH * k * w * d * sizeof(float));
@@ -185,10 +186,11 @@ rt_status rt_route_assign(const void* qk, rt_dtype dt, int B, int H, int n, int 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int BH = B * H;
   float* S = scores ? scores : reinterpret_cast<float*>(ws + L.S);
-  st = from_cuda(launch_score_simt(qk, dt, BH, H, n, d, centroids, k, S, assign, nullptr, s),
+  unsigned int* err = reinterpret_cast<unsigned int*>(ws + L.err);
+  st = from_cuda(launch_score(qk, dt, B, H, n, d, centroids, k, S, assign, nullptr, err, s),
                  "score kernel");
   if (st != RT_OK) return st;
-  st = from_cuda(launch_select(S, BH, n, k, w, idx, nullptr, s), "select kernel");
+  st = from_cuda(launch_select(S, BH, n, k, w, idx, nullptr, nullptr, s), "select kernel");
   if (st != RT_OK) return st;
   return ok();
 }
@@ -222,12 +224,13 @@ rt_status rt_routing_attention(const void* q, const void* kp, const void* v, rt_
   int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + L.idx);
   float* yslot = reinterpret_cast<float*>(ws + L.yslot);
 
-  st = from_cuda(launch_score_simt(q, dt, BH, H, n, d, centroids, kc, S, assign_out, mcount, s),
+  unsigned int* err = reinterpret_cast<unsigned int*>(ws + L.err);
+  st = from_cuda(launch_score(q, dt, B, H, n, d, centroids, kc, S, assign_out, mcount, err, s),
                  "score kernel");
   if (st != RT_OK) return st;
-  st = from_cuda(launch_select(S, BH, n, kc, w, idx, mcount, s), "select kernel");
+  int32_t* slots = reinterpret_cast<int32_t*>(ws + L.slots);
+  st = from_cuda(launch_select(S, BH, n, kc, w, idx, mcount, slots, s), "select kernel");
   if (st != RT_OK) return st;
-  unsigned int* err = reinterpret_cast<unsigned int*>(ws + L.err);
   if (attention_tc_supported(dt, d, w)) {
     st = from_cuda(launch_attention_tc(q, v, BH, n, d, kc, w, causal, scale, idx, mcount, out,
                                        yslot, err, s),
@@ -238,7 +241,8 @@ rt_status rt_routing_attention(const void* q, const void* kp, const void* v, rt_
                    "attention kernel");
   }
   if (st != RT_OK) return st;
-  st = from_cuda(launch_scatter(dt, BH, n, d, kc, w, idx, mcount, yslot, out, s), "scatter kernel");
+  st = from_cuda(launch_scatter(dt, BH, n, d, kc, w, idx, mcount, slots, yslot, out, s),
+                 "scatter kernel");
   if (st != RT_OK) return st;
   return ok();
 }

@@ -84,10 +84,21 @@ cudaError_t launch_score_simt(const void* qk, rt_dtype dt, int BH, int H, int n,
                               const float* mu, int k, float* S, int32_t* a,
                               int32_t* mcount, cudaStream_t s);
 
+// dispatcher: tcgen05 scoring for bf16 with k <= 256 (fp32-accurate via a
+// three-plane split of the centroids), the SIMT kernel otherwise.  err: device
+// error word (may be null).
+bool score_tc_supported(rt_dtype dt, int d, int k);
+cudaError_t launch_score(const void* qk, rt_dtype dt, int B, int H, int n, int d, const float* mu,
+                         int k, float* S, int32_t* a, int32_t* mcount, unsigned int* err,
+                         cudaStream_t s);
+
 // top-w per centroid in ascending position order; counts memberships into
-// mcount (atomic integer increments; may be null).
+// mcount (atomic integer increments; may be null) and records up to
+// SLOTS_PER_ROW global slot ids (c*w + slot) per position in `slots`
+// [BH, n, SLOTS_PER_ROW] (may be null; entry order is arbitrary).
+constexpr int SLOTS_PER_ROW = 4;
 cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* idx,
-                          int32_t* mcount, cudaStream_t s);
+                          int32_t* mcount, int32_t* slots, cudaStream_t s);
 
 // in-cluster attention.  Rows of positions with mcount == 1 go straight to
 // `out`; rows of positions in several clusters go to yslot [BH,k,w,d] fp32.
@@ -105,8 +116,8 @@ cudaError_t launch_attention_tc(const void* q, const void* v, int BH, int n, int
 
 // zero rows (mcount == 0) and the mean over clusters (mcount >= 2).
 cudaError_t launch_scatter(rt_dtype dt, int BH, int n, int d, int k, int w,
-                           const int32_t* idx, const int32_t* mcount, const float* yslot,
-                           void* out, cudaStream_t s);
+                           const int32_t* idx, const int32_t* mcount, const int32_t* slots,
+                           const float* yslot, void* out, cudaStream_t s);
 
 // centroid update: bucket the rows by centroid per tile, then a segmented
 // sum per (head, centroid) and the blend/renormalise.

@@ -156,6 +156,9 @@ SWEEP = [
     (1, 1, 1000, 64, 33, 97, "bf16", True),     # k*w != n, odd w
     (3, 2, 777, 128, 24, 129, "bf16", True),    # w just above a tile
     (1, 1, 2048, 128, 300, 16, "bf16", True),   # k > 256
+    (1, 1, 600, 64, 2, 300, "bf16", False),     # several key blocks, non-causal
+    (1, 2, 1024, 128, 8, 128, "bf16", False),   # one cluster per tile, non-causal
+    (2, 1, 1500, 64, 5, 384, "bf16", True),     # three key blocks, causal
 ]
 
 
@@ -178,10 +181,13 @@ def test_full_attention_matches_sdpa():
     assert torch.max(torch.abs(res["out"].double() - ref)).item() < 1e-4
 
 
-def test_degenerate_ties():
+@pytest.mark.parametrize("n,w", [(200, 37), (5000, 300)])
+def test_degenerate_ties(n, w):
     # constant rows normalise to zero: every score is 0, so every centroid
-    # takes the first w positions and every row goes to centroid 0.
-    B, H, n, d, k, w = 1, 2, 200, 64, 5, 37
+    # takes the first w positions and every row goes to centroid 0.  With
+    # n = 5000 the equal scores overflow the candidate buffer of the select
+    # kernel and its exact radix path runs.
+    B, H, d, k = 1, 2, 64, 5
     q = torch.full((B, H, n, d), 0.75, dtype=torch.bfloat16, device="cuda")
     v = torch.randn((B, H, n, d), device="cuda").to(torch.bfloat16)
     mu = torch.nn.functional.normalize(torch.randn(H, k, d, device="cuda"), dim=-1)
