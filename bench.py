@@ -122,62 +122,118 @@ def traffic_for(name, wl_name):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
+    """Samples SM clock, power and clock-event reasons while the timed region
+    runs: NVML from a polling thread (every ~2 ms, so even a region of a few
+    tens of milliseconds gets samples), else ``nvidia-smi -lms``.  Read-only:
+    nothing about the GPU's settings is changed."""
+
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index):
+    def __init__(self, device_index, pci_bus_id=None):
         self.dev = device_index
+        self.pci = pci_bus_id
+        self.rows = []
+        self.source = None
+        self._stop = None
+        self._thread = None
         self.proc = None
         self.path = None
+        self.nvml_error = None
+
+    def _nvml_handle(self):
+        import pynvml
+        pynvml.nvmlInit()
+        if self.pci:
+            try:
+                return pynvml, pynvml.nvmlDeviceGetHandleByPciBusId(self.pci)
+            except pynvml.NVMLError:
+                pass
+        return pynvml, pynvml.nvmlDeviceGetHandleByIndex(self.dev)
+
+    def _poll(self, nv, h):
+        bits = {"hw_slowdown": nv.nvmlClocksEventReasonHwSlowdown,
+                "hw_thermal_slowdown": nv.nvmlClocksEventReasonHwThermalSlowdown,
+                "sw_thermal_slowdown": nv.nvmlClocksEventReasonSwThermalSlowdown,
+                "sw_power_cap": nv.nvmlClocksEventReasonSwPowerCap}
+        smax = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+        while not self._stop.is_set():
+            try:
+                sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
+                pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
+                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+            except nv.NVMLError:
+                break
+            self.rows.append(dict(sm=float(sm), smax=float(smax), power=pw,
+                                  reasons=[k for k, b in bits.items() if rs & b]))
+            time.sleep(0.002)
 
     def __enter__(self):
+        import threading
+        try:
+            nv, h = self._nvml_handle()
+            self._stop = threading.Event()
+            self._thread = threading.Thread(target=self._poll, args=(nv, h), daemon=True)
+            self._thread.start()
+            self.source = "nvml"
+            return self
+        except Exception as e:  # no NVML: fall back to nvidia-smi
+            self._thread = None
+            self.nvml_error = f"{type(e).__name__}: {e}"[:120]
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi"
         except (OSError, FileNotFoundError):
             self.proc = None
         time.sleep(0.3)
         return self
 
     def __exit__(self, *a):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+            self._read_smi()
 
-    def summary(self):
-        if self.proc is None or not self.path:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
+    def _read_smi(self):
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
-                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+                names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                         "sw_power_cap")
+                self.rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                      power=float(parts[3]),
+                                      reasons=[nm for nm, v in zip(names, parts[5:9])
+                                               if v.lower() == "active"]))
             except ValueError:
                 continue
         os.unlink(self.path)
+
+    def summary(self):
+        rows = self.rows
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "source": self.source}
         loaded = [r for r in rows if r["power"] > 200.0] or rows
-        reasons = set()
-        for r in rows:
-            for key, nm in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
-                            ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
-                if r[key].lower() == "active":
-                    reasons.add(nm)
+        reasons = sorted({nm for r in rows for nm in r["reasons"]})
         return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
-                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
-                "samples": len(rows), "samples_under_load": len(loaded)}
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r["power"] for r in rows), "source": self.source,
+                **({"nvml_error": self.nvml_error} if self.nvml_error else {})}
 
 
 # ---------------------------------------------------------------------------
@@ -317,7 +373,12 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     rt.rt_profile_set(prof_pairs)
     l0 = rt.rt_launch_count()
-    with ClockSampler(local) as clk:
+    props = torch.cuda.get_device_properties(dev)
+    pci = None
+    if hasattr(props, "pci_bus_id"):
+        pci = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                     getattr(props, "pci_device_id", 0))
+    with ClockSampler(local, pci) as clk:
         for i in range(args.steps):
             flush.zero_()
             ev[i][0].record(stream)
