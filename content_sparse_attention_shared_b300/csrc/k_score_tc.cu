@@ -18,13 +18,15 @@
 //
 // Persistent, warp-specialised CTA per (slice of tiles, head): the head's
 // centroid planes are built once in shared memory (no-swizzle K-major core
-// matrices); warp 0 streams 128-row tiles of Q with TMA (a 2-D tensor map,
-// 8-element x 128-row boxes that land directly in the core-matrix layout),
-// warp 1 issues the MMAs into one of two TMEM accumulators, warps 2-5 run
-// the epilogue (row statistics from the L2-resident row, scores written
-// centroid-major [BH,k,n] with coalesced stores, argmax) while the next tile
-// is loaded and multiplied.  Every mbarrier wait is bounded; a wait that runs
-// out sets the device error word and the CTA stops.
+// matrices, written 16 bytes per thread, conflict-free); warp 0 streams
+// 128-row tiles of Q with TMA (2-D tensor map, 64-element x 128-row boxes,
+// 128-byte swizzle) into a ring of stages, warp 1 issues the MMAs into one of
+// two TMEM accumulators, and two epilogue warpgroups (warps 2-5 and 6-9)
+// take alternate tiles: each reads its rows' statistics (mean, centred norm)
+// from the staged tile in shared memory while the MMA runs, then the scores
+// from TMEM, writes them centroid-major [BH,k,n] with coalesced stores and
+// takes the argmax.  Every mbarrier wait is bounded; a wait that runs out
+// sets the device error word and the CTA stops.
 #include <cuda.h>
 
 #include <mutex>
@@ -37,9 +39,10 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 constexpr int ROWS = 128;
-constexpr int THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int THREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 two epilogue groups
 constexpr uint64_t WAIT_LIMIT_NS = 200ull * 1000 * 1000;
 constexpr int MAX_SMEM = 232448;  // 227 KiB opt-in per block
+constexpr int BOX_K = 64;         // elements per 128-byte swizzled row
 
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar) {
@@ -54,6 +57,10 @@ __device__ __forceinline__ void set_timeout(unsigned int* err) {
   if (err != nullptr) atomicExch(err, (unsigned)DEV_TIMEOUT);
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
 struct ScoreCfg {
   int D, kpad, acc_cols, stages;
   size_t a_bytes, plane_bytes, smem;
@@ -65,22 +72,27 @@ inline int pow2_at_least(int x) {
   return p;
 }
 
+__device__ __forceinline__ uint32_t pack2_bf16(bf16 a, bf16 b) {
+  return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+}
+
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
-score_tc_kernel(const __grid_constant__ CUtensorMap qmap, const bf16* __restrict__ q, int B,
-                int H, int n, const float* __restrict__ mu, int k, int kpad, int acc_cols,
-                int stages, int ctas_per_head, float* __restrict__ S, int32_t* __restrict__ assign,
+score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
+                const float* __restrict__ mu, int k, int kpad, int acc_cols, int stages,
+                int ctas_per_head, float* __restrict__ S, int32_t* __restrict__ assign,
                 int32_t* __restrict__ mcount, unsigned int* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   constexpr int A_BYTES = ROWS * D * 2;
+  constexpr int KB = D / BOX_K;  // swizzled 128-byte column blocks per row
   const int plane_bytes = kpad * D * 2;
-  uint8_t* As = sm;                                  // stages x [128 x D] K-major
+  uint8_t* As = sm;                                  // stages x [KB][128 rows x 128 B] SW128
   uint8_t* Bs = As + (size_t)stages * A_BYTES;       // 3 planes x [kpad x D] K-major
   float* sumu = reinterpret_cast<float*>(Bs + 3 * (size_t)plane_bytes);  // [kpad]
 
-  __shared__ uint64_t full_bar[2], empty_bar[2], accf_bar[2], acce_bar[2];
+  __shared__ uint64_t full_bar[4], empty_bar[4], accf_bar[2], acce_bar[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int stop_flag;
 
@@ -90,45 +102,57 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, const bf16* __restrict
   const int ntiles = B * tiles_per_bh;  // tiles of this head (all sequences)
 
   // ---- centroid planes for head h (all threads) ---------------------------
-  // warp per centroid row, each lane D/32 consecutive elements; the loads of
-  // several rows are issued before any is used, so the set-up costs a few L2
-  // round trips instead of one per element.  Row sums use a fixed order.
+  // item (c, jc): 8 consecutive features of centroid c, split into three bf16
+  // planes and written as one 16-byte chunk per plane at jc*kpad*16 + c*16.
   {
-    constexpr int PER = D / 32;
-    constexpr int ROWS_IN_FLIGHT = 8;
     const float* mu_h = mu + (size_t)h * k * D;
-    for (int c0 = warp * ROWS_IN_FLIGHT; c0 < kpad; c0 += (THREADS / 32) * ROWS_IN_FLIGHT) {
-      float vals[ROWS_IN_FLIGHT][PER];
+    const int items = kpad * (D / 8);
+    for (int it = tid; it < items; it += THREADS) {
+      const int c = it % kpad, jc = it / kpad;
+      float m[8];
+      if (c < k) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(mu_h + (size_t)c * D + jc * 8));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(mu_h + (size_t)c * D + jc * 8 + 4));
+        m[0] = a.x; m[1] = a.y; m[2] = a.z; m[3] = a.w;
+        m[4] = b.x; m[5] = b.y; m[6] = b.z; m[7] = b.w;
+      } else {
 #pragma unroll
-      for (int rr = 0; rr < ROWS_IN_FLIGHT; ++rr) {
-        const int c = c0 + rr;
-#pragma unroll
-        for (int e = 0; e < PER; ++e)
-          vals[rr][e] = (c < k) ? __ldg(mu_h + (size_t)c * D + lane * PER + e) : 0.0f;
+        for (int e = 0; e < 8; ++e) m[e] = 0.0f;
       }
+      uint32_t ph[4], pm[4], pl[4];
 #pragma unroll
-      for (int rr = 0; rr < ROWS_IN_FLIGHT; ++rr) {
-        const int c = c0 + rr;
-        if (c >= kpad) break;
-        float rowsum = 0.0f;
+      for (int e = 0; e < 8; e += 2) {
+        bf16 hi[2], md[2], lo[2];
 #pragma unroll
-        for (int e = 0; e < PER; ++e) {
-          const int j = lane * PER + e;
-          const float m = vals[rr][e];
-          rowsum += m;
-          const bf16 hi = __float2bfloat16_rn(m);
-          const float r1 = m - __bfloat162float(hi);
-          const bf16 md = __float2bfloat16_rn(r1);
-          const float r2 = r1 - __bfloat162float(md);
-          const bf16 lo = __float2bfloat16_rn(r2);
-          const size_t off = (size_t)(j >> 3) * (kpad * 16) + c * 16 + (j & 7) * 2;
-          *reinterpret_cast<bf16*>(Bs + off) = hi;
-          *reinterpret_cast<bf16*>(Bs + plane_bytes + off) = md;
-          *reinterpret_cast<bf16*>(Bs + 2 * (size_t)plane_bytes + off) = lo;
+        for (int u = 0; u < 2; ++u) {
+          hi[u] = __float2bfloat16_rn(m[e + u]);
+          const float r1 = m[e + u] - __bfloat162float(hi[u]);
+          md[u] = __float2bfloat16_rn(r1);
+          const float r2 = r1 - __bfloat162float(md[u]);
+          lo[u] = __float2bfloat16_rn(r2);
         }
-        rowsum = warp_sum(rowsum);
-        if (lane == 0) sumu[c] = rowsum;
+        ph[e / 2] = pack2_bf16(hi[0], hi[1]);
+        pm[e / 2] = pack2_bf16(md[0], md[1]);
+        pl[e / 2] = pack2_bf16(lo[0], lo[1]);
       }
+      const size_t off = (size_t)jc * (kpad * 16) + (size_t)c * 16;
+      *reinterpret_cast<uint4*>(Bs + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+      *reinterpret_cast<uint4*>(Bs + plane_bytes + off) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
+      *reinterpret_cast<uint4*>(Bs + 2 * (size_t)plane_bytes + off) =
+          make_uint4(pl[0], pl[1], pl[2], pl[3]);
+    }
+    // row sums of the fp32 centroids, fixed order
+    for (int c = tid; c < kpad; c += THREADS) {
+      float rs = 0.0f;
+      if (c < k) {
+        const float4* row = reinterpret_cast<const float4*>(mu_h + (size_t)c * D);
+#pragma unroll 4
+        for (int j = 0; j < D / 4; ++j) {
+          const float4 v = __ldg(row + j);
+          rs += v.x; rs += v.y; rs += v.z; rs += v.w;
+        }
+      }
+      sumu[c] = rs;
     }
   }
   if (warp == 1) {
@@ -136,9 +160,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, const bf16* __restrict
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < stages; ++i) {
       tc::mbar_init(&full_bar[i], 1);
-      tc::mbar_init(&empty_bar[i], 1);
+      tc::mbar_init(&empty_bar[i], 4);  // the 4 warps of the epilogue group that read the tile
+    }
+    for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&accf_bar[i], 1);
       tc::mbar_init(&acce_bar[i], 4);
     }
@@ -170,8 +196,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, const bf16* __restrict
         tc::mbar_arrive_expect_tx(&full_bar[s], A_BYTES);
         uint8_t* dst = As + (size_t)s * A_BYTES;
 #pragma unroll
-        for (int kc = 0; kc < D / 8; ++kc)
-          tma_load_2d(dst + kc * 2048, &qmap, kc * 8, row0, &full_bar[s]);
+        for (int kb = 0; kb < KB; ++kb)
+          tma_load_2d(dst + kb * (ROWS * 128), &qmap, kb * BOX_K, row0, &full_bar[s]);
       }
     }
   } else if (warp == 1) {
@@ -200,64 +226,37 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, const bf16* __restrict
           const uint32_t b0 = tc::smem_u32(Bs + (size_t)p * plane_bytes);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t ad = tc::smem_desc_noswizzle(a0 + ks * 4096, 2048, 128);
+            const uint32_t a_addr = a0 + (ks / 4) * (ROWS * 128) + (ks % 4) * 32;
+            const uint64_t ad = tc::smem_desc_sw128(a_addr, 1024);
             const uint64_t bd = tc::smem_desc_noswizzle(b0 + ks * 2 * lbo_b, lbo_b, 128);
             tc::mma_f16_ss(d_tmem, ad, bd, idesc, first_mma ? 0u : 1u);
             first_mma = 0;
           }
         }
-        tc::mma_commit(&empty_bar[s]);
         tc::mma_commit(&accf_bar[ab]);
       }
     }
   } else {
-    // ===================== epilogue (warps 2..5) ============================
-    const int row = 32 * (warp & 3) + lane;  // TMEM lane this thread reads
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    int i = 0;
-    for (int tile = first; tile < ntiles; tile += stride, ++i) {
-      const int ab = i & 1;
+    // ===================== epilogue groups (warps 2-5, 6-9) ==================
+    const int grp = (warp - 2) >> 2;         // takes tiles i with i % 2 == grp
+    const int quad = warp & 3;               // TMEM lane quadrant this warp may read
+    const int row = 32 * quad + lane;        // tile row == TMEM lane
+    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+    int i = grp;
+    for (int tile = first + grp * stride; tile < ntiles; tile += 2 * stride, i += 2) {
+      const int s = i % stages;
+      const uint32_t use = (uint32_t)(i / stages);
       const uint32_t ause = (uint32_t)(i >> 1);
       const int b = tile / tiles_per_bh, tb = tile - b * tiles_per_bh;
       const int bh = b * H + h;
       const int t = tb * ROWS + row;
       const bool valid = t < n;
-      // row statistics from the (L2-resident) row: mean, centred norm
-      float mean = 0.0f, inv = 0.0f;
-      bool zero_row = true;
-      if (valid) {
-        const uint4* src = reinterpret_cast<const uint4*>(q + ((size_t)bh * n + t) * D);
-        uint4 v[D / 8];
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) v[c] = __ldg(src + c);
-        float s = 0.0f;
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const uint32_t w4[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&w4[e]);
-            s += __low2float(p2);
-            s += __high2float(p2);
-          }
-        }
-        mean = s / (float)D;
-        float ss = 0.0f;
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const uint32_t w4[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&w4[e]);
-            const float a = __low2float(p2) - mean, bq = __high2float(p2) - mean;
-            ss = fmaf(a, a, ss);
-            ss = fmaf(bq, bq, ss);
-          }
-        }
-        zero_row = !(ss > 0.0f);
-        inv = zero_row ? 0.0f : 1.0f / sqrtf(ss);
-      }
-      bool ok = tc::mbar_wait_bounded(&accf_bar[ab], ause & 1u, WAIT_LIMIT_NS) &&
+      // Wait for this tile's MMA; the tile's TMA phase is then complete too
+      // (the MMA waited for it) and cannot advance before this group releases
+      // the stage, so the full-barrier wait below returns at once and only
+      // orders the staged bytes for this thread.
+      bool ok = tc::mbar_wait_bounded(&accf_bar[grp], ause & 1u, WAIT_LIMIT_NS) &&
+                tc::mbar_wait_bounded(&full_bar[s], use & 1u, WAIT_LIMIT_NS) &&
                 !*(volatile int*)&stop_flag;
       ok = __all_sync(0xffffffffu, ok);  // warp-uniform: tcgen05.ld below is collective
       if (!ok) {
@@ -266,29 +265,78 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, const bf16* __restrict
         break;
       }
       tc::tc_fence_after_sync();
+      // row statistics from the staged tile: mean and centred norm
+      float mean = 0.0f, inv = 0.0f;
+      bool zero_row = true;
+      {
+        // two passes over the row in shared memory (sum, then centred squares)
+        const uint8_t* arow = As + (size_t)s * A_BYTES + row * 128;
+        float sx = 0.0f;
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(arow + kb * (ROWS * 128) +
+                                                            ((j ^ (row & 7)) << 4));
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&w4[e]);
+              sx += __low2float(p2);
+              sx += __high2float(p2);
+            }
+          }
+        }
+        mean = sx / (float)D;
+        float sxx = 0.0f;
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(arow + kb * (ROWS * 128) +
+                                                            ((j ^ (row & 7)) << 4));
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&w4[e]);
+              const float a = __low2float(p2) - mean, bq = __high2float(p2) - mean;
+              sxx = fmaf(a, a, sxx);
+              sxx = fmaf(bq, bq, sxx);
+            }
+          }
+        }
+        zero_row = !(sxx > 0.0f);
+        inv = zero_row ? 0.0f : 1.0f / sqrtf(sxx);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);  // stage free: MMA done, rows read
       float best = -INFINITY;
       int best_c = 0;
       float* srow = S + (size_t)bh * k * n + t;
-      for (int c0 = 0; c0 < kpad; c0 += 16) {
-        uint32_t r[16];
-        tc::tmem_ld16(tmem + ab * acc_cols + lane_base + c0, r);
+      const uint32_t tacc = tmem + grp * acc_cols + lane_base;
+      for (int c0 = 0; c0 < kpad; c0 += 32) {
+        uint32_t r[2][16];
+        tc::tmem_ld16(tacc + c0, r[0]);
+        if (c0 + 16 < kpad) tc::tmem_ld16(tacc + c0 + 16, r[1]);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int c = c0 + j;
-          const float dot = __uint_as_float(r[j]);
-          const float sc = zero_row ? 0.0f : (dot - mean * sumu[c]) * inv;
-          if (valid && c < k) {
-            if (S != nullptr) srow[(size_t)c * n] = sc;
-            if (sc > best) { best = sc; best_c = c; }
+        for (int hh = 0; hh < 2; ++hh) {
+          if (c0 + 16 * hh >= kpad) break;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int c = c0 + 16 * hh + j;
+            const float dot = __uint_as_float(r[hh][j]);
+            const float sc = zero_row ? 0.0f : (dot - mean * sumu[c]) * inv;
+            if (valid && c < k) {
+              if (S != nullptr) srow[(size_t)c * n] = sc;
+              if (sc > best) { best = sc; best_c = c; }
+            }
           }
         }
       }
       tc::tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0)
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(&acce_bar[ab]))
-                     : "memory");
+      if (lane == 0) mbar_arrive(&acce_bar[grp]);
       if (valid) {
         if (assign != nullptr) assign[(size_t)bh * n + t] = best_c;
         if (mcount != nullptr) mcount[(size_t)bh * n + t] = 0;
@@ -323,6 +371,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Shared-memory plan: 1 KiB alignment slack, A stages (1024-byte aligned
+// swizzle atoms), the three centroid planes, the centroid row sums; as many
+// A stages (up to 4) as fit beside the planes.  Static shared memory (the
+// barriers) takes well under 256 bytes.
 bool plan(int d, int k, ScoreCfg& c) {
   c.D = d;
   c.kpad = (k + 15) / 16 * 16;
@@ -331,9 +383,13 @@ bool plan(int d, int k, ScoreCfg& c) {
   c.a_bytes = (size_t)ROWS * d * 2;
   c.plane_bytes = (size_t)c.kpad * d * 2;
   const size_t fixed = 1024 + 3 * c.plane_bytes + (size_t)c.kpad * 4;
-  c.stages = (fixed + 2 * c.a_bytes + 512 <= (size_t)MAX_SMEM) ? 2 : 1;
+  const size_t budget = (size_t)MAX_SMEM - 256;
+  c.stages = 0;
+  for (int st = 4; st >= 1; --st)
+    if (fixed + st * c.a_bytes <= budget) { c.stages = st; break; }
+  if (c.stages == 0) return false;
   c.smem = fixed + c.stages * c.a_bytes;
-  return c.smem + 512 <= (size_t)MAX_SMEM;
+  return true;
 }
 
 template <int D>
@@ -345,10 +401,10 @@ cudaError_t launch_t(const ScoreCfg& c, const void* qk, int B, int H, int n, con
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)B * H * n};
   const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  const cuuint32_t box[2] = {8, (cuuint32_t)ROWS};
+  const cuuint32_t box[2] = {(cuuint32_t)BOX_K, (cuuint32_t)ROWS};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qk), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   auto kern = score_tc_kernel<D>;
@@ -359,9 +415,8 @@ cudaError_t launch_t(const ScoreCfg& c, const void* qk, int B, int H, int n, con
   if (cph < 1) cph = 1;
   if (cph > tiles_per_head) cph = tiles_per_head;
   launch_begin(K_SCORE_TC, s);
-  kern<<<dim3(cph, H), THREADS, c.smem, s>>>(map, static_cast<const bf16*>(qk), B, H, n, mu, k,
-                                             c.kpad, c.acc_cols, c.stages, cph, S, a, mcount,
-                                             err);
+  kern<<<dim3(cph, H), THREADS, c.smem, s>>>(map, B, H, n, mu, k, c.kpad, c.acc_cols, c.stages,
+                                             cph, S, a, mcount, err);
   e = cudaGetLastError();
   launch_end(K_SCORE_TC, s);
   return e;

@@ -6,38 +6,44 @@
 // keeps the w positions with the largest score; equal scores go to the lower
 // position; the kept positions are listed in ascending order.
 //
-// One CTA per (batch*head, centroid), in three steps over the row of n
-// scores:
-//   1. one read of the row: every score gets a bin of a 2048-bin linear
-//      partition of [-1, 1] (a non-decreasing function of the score, so all
-//      scores of a higher bin are strictly larger); the bin index is staged in
-//      shared memory (u16) and counted in a shared histogram;
-//   2. the bin b* holding the w-th largest score is found by a descending scan
-//      of the histogram; its members (the candidates, typically a handful) are
-//      collected and ranked exactly by (score desc, position asc) -- a
-//      candidate is kept iff its rank is below the number still needed;
-//   3. an ordered compaction walks the positions in order and keeps bin > b*
-//      plus the kept candidates; a block prefix sum gives each kept position
-//      its output slot, so the list comes out sorted without a sort.
+// One CTA of 256 threads per (batch*head, centroid) row of n scores, with a
+// handful of block barriers in total (the cost of this kernel is latency, not
+// bytes: the row is read once, usually from L2 right after the score kernel
+// wrote it):
+//   1. one vectorised read of the row: every score gets a bin of a 2048-bin
+//      linear partition of [-1, 1] (non-decreasing in the score, so every
+//      score of a higher bin is strictly larger); bins are staged in shared
+//      memory (u16) and counted in a shared histogram;
+//   2. a block-wide scan of the histogram from the top bin down finds the bin
+//      b* holding the w-th largest score and how many of its members are
+//      still needed;
+//   3. the members of b* (the candidates, typically a few) are ranked
+//      exactly by (score desc, position asc); the kept ones are re-binned
+//      above every other bin;
+//   4. ordered compaction: warp j owns a contiguous segment of positions,
+//      counts its kept positions with ballots, one barrier gives every warp
+//      its output offset, and a second ballot pass writes the positions in
+//      order -- the list comes out sorted without a sort.
 // Membership counts are incremented here with integer atomics (the totals are
 // order independent), and the first SLOTS_PER_ROW (cluster, slot) entries of
 // every position are recorded for the scatter.
-// Rows whose boundary bin holds too many candidates (many equal scores), or
-// that do not fit in shared memory, use an exact 32-bit most-significant-digit
-// radix select over order-preserving keys instead.
+// Rows whose boundary bin holds more than CAND_CAP candidates (many equal
+// scores), or too long to stage in shared memory, use an exact 32-bit
+// most-significant-digit radix select over order-preserving keys instead.
 #include "rt_internal.cuh"
 
 namespace rt {
 namespace {
 
-constexpr int THREADS = 512;
+constexpr int THREADS = 256;
 constexpr int WARPS = THREADS / 32;
 constexpr int NBINS = 2048;
-constexpr int CAND_CAP = 2048;
-constexpr int MAX_STAGED_BINS = 80 * 1024;  // u16 bins staged in shared memory
+constexpr int BINS_PER_THREAD = NBINS / THREADS;
+constexpr int CAND_CAP = 1024;
+constexpr int MAX_STAGED_BINS = 96 * 1024;  // u16 bins staged in shared memory
 
 __device__ __forceinline__ int score_bin(float s) {
-  // non-decreasing in s; [-1, 1] -> [0, 2047]
+  // non-decreasing in s; [-1, 1] -> [0, 2047] (NaN -> 0)
   float f = (s + 1.0f) * 1024.0f;
   f = fminf(fmaxf(f, 0.0f), (float)(NBINS - 1));
   return (int)f;
@@ -58,35 +64,31 @@ struct SelectOut {
   }
 };
 
-// Ordered compaction: keep(t) is evaluated for t = 0, 1, ... in chunks of
-// THREADS; one barrier per chunk (double-buffered warp totals).
-template <typename Keep>
-__device__ __forceinline__ void ordered_compact(int n, int w, int* wsum /* [2][WARPS] */,
-                                                const SelectOut& so, Keep keep) {
+// Exclusive block-wide prefix of one int per thread (and the total).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* wsum /* [WARPS] */, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int out_base = 0, buf = 0;
-  for (int t0 = 0; t0 < n && out_base < w; t0 += THREADS, buf ^= 1) {
-    const int t = t0 + threadIdx.x;
-    const bool sel = (t < n) && keep(t);
-    const unsigned b = __ballot_sync(0xffffffffu, sel);
-    if (lane == 0) wsum[buf * WARPS + warp] = __popc(b);
-    __syncthreads();
-    int pre = 0, tot = 0;
+  int incl = v;
 #pragma unroll
-    for (int i = 0; i < WARPS; ++i) {
-      const int x = wsum[buf * WARPS + i];
-      pre += (i < warp) ? x : 0;
-      tot += x;
-    }
-    if (sel) {
-      const int o = out_base + pre + __popc(b & ((1u << lane) - 1u));
-      if (o < w) so.emit(o, t);
-    }
-    out_base += tot;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
   }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  total = 0;
+#pragma unroll
+  for (int i = 0; i < WARPS; ++i) {
+    const int x = wsum[i];
+    before += (i < warp) ? x : 0;
+    total += x;
+  }
+  __syncthreads();  // wsum may be reused by the caller
+  return before + incl - v;
 }
 
-// Exact fallback: 32-bit MSD radix select on order-preserving keys.
+// Exact fallback: 32-bit MSD radix select on order-preserving keys, reading
+// the row from global memory (L2).  Slow but general.
 __device__ void radix_select_row(const float* __restrict__ row, int n, int w, const SelectOut& so,
                                  unsigned* hist /* >= 256 */, int* wsum /* [4][WARPS] */) {
   __shared__ unsigned s_digit;
@@ -176,19 +178,18 @@ __device__ void radix_select_row(const float* __restrict__ row, int n, int w, co
 __global__ void __launch_bounds__(THREADS)
 select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __restrict__ idx,
                    int32_t* __restrict__ mcount, int32_t* __restrict__ slots, int staged) {
-  extern __shared__ uint16_t sbin[];  // [n] when staged
+  extern __shared__ __align__(16) uint16_t sbin[];  // [n] when staged
   __shared__ unsigned hist[NBINS];
   __shared__ int cand_t[CAND_CAP];
   __shared__ float cand_s[CAND_CAP];
   __shared__ int wsum[4 * WARPS];
   __shared__ int s_bstar, s_need, s_ncand;
-  __shared__ unsigned keep_bits[CAND_CAP / 32];
 
   const int c = blockIdx.x;
   const int bh = blockIdx.y;
   const float* row = S + ((size_t)bh * k + c) * n;
   const SelectOut so{idx + ((size_t)bh * k + c) * w, mcount, slots, bh, c, n, w};
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   if (!staged) {
     radix_select_row(row, n, w, so, hist, wsum);
@@ -198,36 +199,73 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
   for (int b = tid; b < NBINS; b += THREADS) hist[b] = 0u;
   if (tid == 0) s_ncand = 0;
   __syncthreads();
-  // 1. bins + histogram (one read of the row)
-  for (int t = tid; t < n; t += THREADS) {
-    const int b = score_bin(__ldg(row + t));
-    sbin[t] = (uint16_t)b;
-    atomicAdd(&hist[b], 1u);
+
+  // 1. bins + histogram: one vectorised read of the row
+  const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
+  const int n4 = vec ? (n >> 2) : 0;
+  {
+    const float4* row4 = reinterpret_cast<const float4*>(row);
+    int i = tid;
+    for (; i + 3 * THREADS < n4; i += 4 * THREADS) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldg(row4 + i + u * THREADS);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int b0 = score_bin(v[u].x), b1 = score_bin(v[u].y);
+        const int b2 = score_bin(v[u].z), b3 = score_bin(v[u].w);
+        uint2 packed;
+        packed.x = (uint32_t)b0 | ((uint32_t)b1 << 16);
+        packed.y = (uint32_t)b2 | ((uint32_t)b3 << 16);
+        *reinterpret_cast<uint2*>(sbin + 4 * (i + u * THREADS)) = packed;
+        atomicAdd(&hist[b0], 1u);
+        atomicAdd(&hist[b1], 1u);
+        atomicAdd(&hist[b2], 1u);
+        atomicAdd(&hist[b3], 1u);
+      }
+    }
+    for (; i < n4; i += THREADS) {
+      const float4 v = __ldg(row4 + i);
+      const int b0 = score_bin(v.x), b1 = score_bin(v.y);
+      const int b2 = score_bin(v.z), b3 = score_bin(v.w);
+      uint2 packed;
+      packed.x = (uint32_t)b0 | ((uint32_t)b1 << 16);
+      packed.y = (uint32_t)b2 | ((uint32_t)b3 << 16);
+      *reinterpret_cast<uint2*>(sbin + 4 * i) = packed;
+      atomicAdd(&hist[b0], 1u);
+      atomicAdd(&hist[b1], 1u);
+      atomicAdd(&hist[b2], 1u);
+      atomicAdd(&hist[b3], 1u);
+    }
+    for (int t = 4 * n4 + tid; t < n; t += THREADS) {
+      const int b = score_bin(__ldg(row + t));
+      sbin[t] = (uint16_t)b;
+      atomicAdd(&hist[b], 1u);
+    }
   }
   __syncthreads();
-  // 2a. boundary bin: the descending cumulative count reaches w inside b*
-  if (tid < 32) {
-    constexpr int PER = NBINS / 32;  // bins per lane, lane 0 = highest bins
-    unsigned lsum = 0;
-    for (int q = 0; q < PER; ++q) lsum += hist[NBINS - 1 - PER * lane - q];
-    unsigned incl = lsum;
+
+  // 2. boundary bin: thread i owns bins [top - 8i - 7, top - 8i] (descending)
+  {
+    const int hi_bin = NBINS - 1 - BINS_PER_THREAD * tid;
+    unsigned hb[BINS_PER_THREAD];
+    int lsum = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+    for (int q = 0; q < BINS_PER_THREAD; ++q) {
+      hb[q] = hist[hi_bin - q];
+      lsum += (int)hb[q];
     }
-    const unsigned excl = incl - lsum;
-    if (excl < (unsigned)w && (unsigned)w <= incl) {
-      unsigned cum = excl;
-      for (int q = 0; q < PER; ++q) {
-        const int b = NBINS - 1 - PER * lane - q;
-        const unsigned hb = hist[b];
-        if (cum + hb >= (unsigned)w) {
-          s_bstar = b;
-          s_need = w - (int)cum;
-          break;
+    int total;
+    const int excl = block_exclusive_scan(lsum, wsum, total);
+    if (excl < w && w <= excl + lsum) {
+      int cum = excl;
+#pragma unroll
+      for (int q = 0; q < BINS_PER_THREAD; ++q) {
+        if (cum < w && cum + (int)hb[q] >= w) {
+          s_bstar = hi_bin - q;
+          s_need = w - cum;
         }
-        cum += hb;
+        cum += (int)hb[q];
       }
     }
   }
@@ -235,43 +273,76 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
   const int bstar = s_bstar, need = s_need;
   const int ncand_total = (int)hist[bstar];
   if (ncand_total > CAND_CAP) {  // many equal or near-equal scores: exact radix path
+    __syncthreads();             // every thread has read hist[b*] before it is reused
     radix_select_row(row, n, w, so, hist, wsum);
     return;
   }
-  // 2b. collect the candidates (order irrelevant) and rank them exactly
-  for (int t0 = 0; t0 < n; t0 += THREADS) {
-    const int t = t0 + tid;
-    const bool is_c = (t < n) && sbin[t] == bstar;
-    const unsigned bm = __ballot_sync(0xffffffffu, is_c);
-    int base = 0;
-    if (lane == 0 && bm) base = atomicAdd(&s_ncand, __popc(bm));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (is_c) {
-      const int slot = base + __popc(bm & ((1u << lane) - 1u));
-      cand_t[slot] = t;
-      cand_s[slot] = __ldg(row + t);
+
+  // 3. candidates (members of b*): keep all of them if all are needed, else
+  //    rank them exactly by (score desc, position asc)
+  if (need < ncand_total) {
+    for (int t0 = 0; t0 < n; t0 += THREADS) {
+      const int t = t0 + tid;
+      const bool is_c = (t < n) && sbin[t] == bstar;
+      const unsigned bm = __ballot_sync(0xffffffffu, is_c);
+      if (bm == 0u) continue;
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&s_ncand, __popc(bm));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (is_c) {
+        const int slot = base + __popc(bm & ((1u << lane) - 1u));
+        cand_t[slot] = t;
+        cand_s[slot] = __ldg(row + t);
+      }
     }
-  }
-  for (int i = tid; i < CAND_CAP / 32; i += THREADS) keep_bits[i] = 0u;
-  __syncthreads();
-  const int nc = s_ncand;
-  for (int i = tid; i < nc; i += THREADS) {
-    const float si = cand_s[i];
-    const int ti = cand_t[i];
-    int rank = 0;
-    for (int j = 0; j < nc; ++j) {
-      const float sj = cand_s[j];
-      rank += (sj > si) || (sj == si && cand_t[j] < ti);
+    __syncthreads();
+    const int nc = s_ncand;
+    int keep_t[CAND_CAP / THREADS];
+    int nkeep = 0;
+    for (int i = tid; i < nc; i += THREADS) {
+      const float si = cand_s[i];
+      const int ti = cand_t[i];
+      int rank = 0;
+      for (int j = 0; j < nc; ++j) {
+        const float sj = cand_s[j];
+        rank += (sj > si) || (sj == si && cand_t[j] < ti);
+      }
+      keep_t[nkeep++] = (rank < need) ? ti : -1;
     }
-    if (rank < need) atomicOr(&keep_bits[i >> 5], 1u << (i & 31));
+    __syncthreads();  // every candidate read its bin before any is rewritten
+    for (int q = 0; q < nkeep; ++q)
+      if (keep_t[q] >= 0) sbin[keep_t[q]] = (uint16_t)NBINS;
+  } else {
+    // every member of b* is kept: lower the cut instead of re-binning
   }
   __syncthreads();
-  // kept candidates get bin value NBINS (> every b*)
-  for (int i = tid; i < nc; i += THREADS)
-    if (keep_bits[i >> 5] & (1u << (i & 31))) sbin[cand_t[i]] = (uint16_t)NBINS;
+  const int cut = (need < ncand_total) ? bstar : bstar - 1;  // keep bin > cut
+
+  // 4. ordered compaction over per-warp contiguous segments
+  const int seg = ((n + WARPS * 32 - 1) / (WARPS * 32)) * 32;
+  const int s0 = warp * seg;
+  const int s1 = min(n, s0 + seg);
+  int cnt = 0;
+  for (int t0 = s0; t0 < s1; t0 += 32) {
+    const int t = t0 + lane;
+    const bool sel = (t < s1) && (int)sbin[t] > cut;
+    cnt += __popc(__ballot_sync(0xffffffffu, sel));
+  }
+  if (lane == 0) wsum[warp] = cnt;
   __syncthreads();
-  // 3. ordered compaction: bin > b*
-  ordered_compact(n, w, wsum, so, [&](int t) { return (int)sbin[t] > bstar; });
+  int base = 0;
+#pragma unroll
+  for (int i = 0; i < WARPS; ++i) base += (i < warp) ? wsum[i] : 0;
+  for (int t0 = s0; t0 < s1 && base < w; t0 += 32) {
+    const int t = t0 + lane;
+    const bool sel = (t < s1) && (int)sbin[t] > cut;
+    const unsigned bm = __ballot_sync(0xffffffffu, sel);
+    if (sel) {
+      const int o = base + __popc(bm & ((1u << lane) - 1u));
+      if (o < w) so.emit(o, t);
+    }
+    base += __popc(bm);
+  }
 }
 
 }  // namespace
@@ -280,7 +351,7 @@ cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* 
                           int32_t* mcount, int32_t* slots, cudaStream_t s) {
   dim3 grid(k, BH);
   const int staged = n <= MAX_STAGED_BINS ? 1 : 0;
-  const size_t smem = staged ? (size_t)n * sizeof(uint16_t) : 0;
+  const size_t smem = staged ? ((size_t)n * sizeof(uint16_t) + 15) / 16 * 16 : 0;
   cudaError_t e = cudaFuncSetAttribute(select_topw_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        MAX_STAGED_BINS * (int)sizeof(uint16_t));

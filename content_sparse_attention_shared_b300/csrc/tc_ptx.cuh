@@ -126,6 +126,22 @@ __device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t
   return d;
 }
 
+// Shared-memory matrix descriptor for the K-major 128-byte-swizzled layout
+// that a TMA load with CU_TENSOR_MAP_SWIZZLE_128B writes: rows of 128 bytes,
+// 8-row atoms of 1024 bytes (the atom must start 1024-byte aligned), the
+// 16-byte chunks of row r XOR-permuted by (r % 8).  sbo: byte distance between
+// 8-row groups; the leading offset is unused for this layout.  A K step inside
+// the 128-byte row is taken by advancing the start address.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                       // leading offset (unused), 16 bytes
+  d |= (uint64_t)((sbo & 0x3FFFFu) >> 4) << 32;
+  d |= (uint64_t)1 << 46;                       // descriptor version for the sm_100 family
+  d |= (uint64_t)2 << 61;                       // layout type: 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor for kind::f16 with fp32 accumulation.
 //   ab_bf16: operands are bf16 (else fp16); a_mn / b_mn: operand is MN-major.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool ab_bf16, bool a_mn,
