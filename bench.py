@@ -142,39 +142,62 @@ class ClockSampler:
         self.path = None
         self.nvml_error = None
 
-    def _nvml_handle(self):
-        import pynvml
-        pynvml.nvmlInit()
-        if self.pci:
-            try:
-                return pynvml, pynvml.nvmlDeviceGetHandleByPciBusId(self.pci)
-            except pynvml.NVMLError:
-                pass
-        return pynvml, pynvml.nvmlDeviceGetHandleByIndex(self.dev)
+    class _Nvml:
+        """Minimal read-only NVML access through ctypes (libnvidia-ml ships with
+        the driver; no Python package needed)."""
+        CLOCK_SM = 1
+        REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40}
 
-    def _poll(self, nv, h):
-        bits = {"hw_slowdown": nv.nvmlClocksEventReasonHwSlowdown,
-                "hw_thermal_slowdown": nv.nvmlClocksEventReasonHwThermalSlowdown,
-                "sw_thermal_slowdown": nv.nvmlClocksEventReasonSwThermalSlowdown,
-                "sw_power_cap": nv.nvmlClocksEventReasonSwPowerCap}
-        smax = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+        def __init__(self, index, pci):
+            import ctypes
+            self.ct = ctypes
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            self.h = ctypes.c_void_p()
+            rc = 1
+            if pci:
+                rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci.encode(), ctypes.byref(self.h))
+            if rc != 0:
+                rc = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index),
+                                                            ctypes.byref(self.h))
+            if rc != 0:
+                raise RuntimeError(f"no NVML handle (rc {rc})")
+            fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            self.reasons_fn = fn or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+        def _u32(self, fn, *args):
+            v = self.ct.c_uint()
+            if fn(self.h, *args, self.ct.byref(v)) != 0:
+                raise RuntimeError("NVML query failed")
+            return v.value
+
+        def sample(self):
+            sm = self._u32(self.lib.nvmlDeviceGetClockInfo, self.CLOCK_SM)
+            smax = self._u32(self.lib.nvmlDeviceGetMaxClockInfo, self.CLOCK_SM)
+            pw = self._u32(self.lib.nvmlDeviceGetPowerUsage) / 1000.0
+            r = self.ct.c_ulonglong()
+            if self.reasons_fn(self.h, self.ct.byref(r)) != 0:
+                raise RuntimeError("NVML query failed")
+            return dict(sm=float(sm), smax=float(smax), power=pw,
+                        reasons=[k for k, b in self.REASONS.items() if r.value & b])
+
+    def _poll(self, nv):
         while not self._stop.is_set():
             try:
-                sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
-                pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
-                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
-            except nv.NVMLError:
+                self.rows.append(nv.sample())
+            except RuntimeError:
                 break
-            self.rows.append(dict(sm=float(sm), smax=float(smax), power=pw,
-                                  reasons=[k for k, b in bits.items() if rs & b]))
             time.sleep(0.002)
 
     def __enter__(self):
         import threading
         try:
-            nv, h = self._nvml_handle()
+            nv = self._Nvml(self.dev, self.pci)
+            nv.sample()
             self._stop = threading.Event()
-            self._thread = threading.Thread(target=self._poll, args=(nv, h), daemon=True)
+            self._thread = threading.Thread(target=self._poll, args=(nv,), daemon=True)
             self._thread.start()
             self.source = "nvml"
             return self

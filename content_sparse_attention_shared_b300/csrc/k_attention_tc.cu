@@ -21,9 +21,14 @@
 // Each of the 128 threads owns one row: it reads its S row from TMEM,
 // applies the mask and the softmax in registers, writes its P row (bf16) to
 // shared memory in the MMA operand layout, and after O = P V reads its O row
-// back.  Rows are gathered from HBM by position with 16-byte cp.async straight
-// into the no-swizzle core-matrix layouts (Q/K: K-major; V: MN-major).  The
-// MMA completions are waited on with a bounded mbarrier wait; a wait that runs
+// back.  Only the 16-column chunks that hold a valid key for some row of the
+// warp are read and exponentiated; the other chunks of P are written as
+// zeros.  P reuses the shared memory of the key operand once S = Q K^T is
+// done, and O reuses S's TMEM columns, so a packed CTA needs 64 KiB of shared
+// memory and 128 TMEM columns (three CTAs per SM at d = 128, four at d = 64).
+// Rows are gathered from HBM by position with 16-byte cp.async straight into
+// the no-swizzle core-matrix layouts (Q/K: K-major; V: MN-major).  The MMA
+// completions are waited on with a bounded mbarrier wait; a wait that runs
 // out sets the device error word and the CTA gives up its tile.
 #include "rt_internal.cuh"
 #include "tc_ptx.cuh"
@@ -95,29 +100,41 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Shared-memory plan (bytes, after 1 KiB alignment slack).
+//   packed: [Q then P: max(Q, P)] [V]
+//   multi:  [Q] [K then P: max(K, P)] [V]
 template <int D, bool MULTI>
-__global__ void __launch_bounds__(THREADS, MULTI ? 1 : 2)
+struct AttnSmem {
+  static constexpr int QB = ROWS * D * 2;
+  static constexpr int PB = ROWS * ROWS * 2;
+  static constexpr int XB = QB > PB ? QB : PB;
+  static constexpr int Q_OFF = 0;
+  static constexpr int KP_OFF = MULTI ? QB : 0;      // K (multi) / P region
+  static constexpr int V_OFF = MULTI ? QB + XB : XB;
+  static constexpr int BYTES = V_OFF + QB;
+};
+
+template <int D, bool MULTI>
+__global__ void __launch_bounds__(THREADS, MULTI ? 2 : 3)
 attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int n, int k, int w,
                     int g, int tiles_per_bh, int R, int causal, float scale_log2,
                     const int32_t* __restrict__ idx, const int32_t* __restrict__ mcount,
                     bf16* __restrict__ out, float* __restrict__ yslot,
                     unsigned int* __restrict__ err) {
+  using L = AttnSmem<D, MULTI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  constexpr int QB = ROWS * D * 2;
-  uint8_t* Qs = sm;                 // K-major [128 x D]
-  uint8_t* Vs = Qs + QB;            // MN-major [128 keys x D]
-  uint8_t* Ps = Vs + QB;            // K-major [128 x 128 keys]
-  uint8_t* Ks = Ps + ROWS * ROWS * 2;  // MULTI only: K-major [128 keys x D]
+  uint8_t* Qs = sm + L::Q_OFF;   // K-major [128 x D]
+  uint8_t* KPs = sm + L::KP_OFF; // K-major keys (multi) / P [128 x 128 keys]
+  uint8_t* Vs = sm + L::V_OFF;   // MN-major [128 keys x D]
 
   __shared__ uint64_t bar_s, bar_o;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int qpos[ROWS];
   __shared__ int kpos[ROWS];
-  __shared__ int vpos[ROWS];
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile = blockIdx.x;
   const int bh = tile / tiles_per_bh;
   const int lt = tile % tiles_per_bh;
@@ -126,7 +143,7 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
   const bf16* v_bh = v + (size_t)bh * n * D;
 
   // ---- row mapping (thread tid owns tile row tid) ------------------------
-  int cluster, slot, row_lo, row_hi;  // row_lo/hi: valid key columns of this row
+  int cluster, slot, row_lo, row_hi;  // row_lo/hi: key columns of this row's cluster
   bool row_valid;
   int nkb = 1, rt = 0;
   if (!MULTI) {
@@ -147,22 +164,23 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
   }
   int my_pos = -1;
   if (row_valid) {
-    my_pos = idx_bh[(size_t)cluster * w + slot];
+    my_pos = __ldg(idx_bh + (size_t)cluster * w + slot);
     if ((unsigned)my_pos >= (unsigned)n) { my_pos = -1; row_valid = false; }  // defensive
   }
+  // membership count of this row's position, loaded now, used by the epilogue
+  const int my_m = row_valid ? __ldg(mcount + (size_t)bh * n + my_pos) : 0;
   qpos[tid] = my_pos;
-  if (!MULTI) vpos[tid] = my_pos;
   __syncthreads();
 
   gather_kmajor<D>(Qs, q_bh, qpos);
   cp_async_commit();
   if (!MULTI) {
-    gather_mnmajor<D>(Vs, v_bh, vpos);
+    gather_mnmajor<D>(Vs, v_bh, qpos);
     cp_async_commit();
   }
 
   if (warp == 0) {
-    tc::tmem_alloc(&tmem_base_sh, 256);
+    tc::tmem_alloc(&tmem_base_sh, 128);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
@@ -174,9 +192,7 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
   __syncthreads();
   tc::tc_fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-  const uint32_t t_s = tmem + lane_base;        // S: columns [0, 128)
-  const uint32_t t_o = tmem + lane_base + 128;  // O: columns [128, 128 + D)
+  const uint32_t t_row = tmem + ((uint32_t)(32 * warp) << 16);  // S, later O: columns [0, 128)
 
   constexpr uint32_t IDESC_S = tc::idesc_f16(ROWS, ROWS, true, false, false);
   constexpr uint32_t IDESC_O = tc::idesc_f16(ROWS, D, true, false, true);
@@ -196,18 +212,17 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
       const int ks = kb * ROWS + tid;
       int p = -1;
       if (ks < w) {
-        p = idx_bh[(size_t)cluster * w + ks];
+        p = __ldg(idx_bh + (size_t)cluster * w + ks);
         if ((unsigned)p >= (unsigned)n) p = -1;
       }
       __syncthreads();  // previous block's buffers are free (all reads done)
       kpos[tid] = p;
-      vpos[tid] = p;
       __syncthreads();
       if (kb != rt) {
-        gather_kmajor<D>(Ks, q_bh, kpos);
-        Kop = Ks;
+        gather_kmajor<D>(KPs, q_bh, kpos);
+        Kop = KPs;
       }
-      gather_mnmajor<D>(Vs, v_bh, vpos);
+      gather_mnmajor<D>(Vs, v_bh, kpos);
       cp_async_commit();
       cp_async_wait_all();
     } else {
@@ -232,69 +247,79 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
     __syncwarp();
     if (!tc::mbar_wait_bounded(&bar_s, phase, WAIT_LIMIT_NS)) {
       failed = true;
-      if ((tid & 31) == 0) atomicExch(err, (unsigned)DEV_TIMEOUT);
+      if (lane == 0) atomicExch(err, (unsigned)DEV_TIMEOUT);
     }
     failed = __syncthreads_or(failed);
     if (failed) break;
     tc::tc_fence_after_sync();
 
     // ---- softmax on this thread's row -----------------------------------
-    // valid key column j: inside [row_lo, row_hi) (packed: own cluster),
-    // key slot < w, and causal: key slot <= own slot.
-    const int kslot0 = MULTI ? kb * ROWS : 0;
-    int jmax = ROWS;  // exclusive upper bound on valid key columns
-    int jmin = 0;
+    // valid key columns [jmin, jmax): inside the row's cluster block
+    // (packed), key slot < w, and causal: key slot <= own slot.
+    int jmin, jmax;
     if (!MULTI) {
       jmin = row_lo;
       jmax = causal ? tid + 1 : row_hi;
     } else {
+      const int kslot0 = kb * ROWS;
+      jmin = 0;
       jmax = min(ROWS, w - kslot0);
       if (causal) jmax = min(jmax, slot - kslot0 + 1);
     }
-    if (!row_valid) { jmin = 0; jmax = 0; }
+    if (!row_valid || jmax <= jmin) { jmin = ROWS; jmax = 0; }
+    // chunks of 16 columns that hold a valid column for some row of the warp
+    const int wlo = __reduce_min_sync(0xffffffffu, jmin);
+    const int whi = __reduce_max_sync(0xffffffffu, jmax);
+    const int ch_lo = (whi > wlo) ? (wlo >> 4) : 0;
+    const int ch_hi = (whi > wlo) ? ((whi + 15) >> 4) : 0;
 
-    // tcgen05.ld is warp-collective: every thread loads every chunk.
+    // tcgen05.ld is warp-collective: the chunk range is warp-uniform.
     float mrow = -INFINITY;
-#pragma unroll 1
-    for (int c0 = 0; c0 < ROWS; c0 += 16) {
+    for (int ch = ch_lo; ch < ch_hi; ++ch) {
       uint32_t r[16];
-      tc::tmem_ld16(t_s + c0, r);
+      tc::tmem_ld16(t_row + ch * 16, r);
       tc::tmem_ld_wait();
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const int col = c0 + j;
+        const int col = ch * 16 + j;
         if (col >= jmin && col < jmax) mrow = fmaxf(mrow, __uint_as_float(r[j]));
       }
     }
     const float m_new = fmaxf(m_run, mrow);
     const float mscaled = (m_new == -INFINITY) ? 0.0f : m_new * scale_log2;
     float lsum = 0.0f;
+    // P overwrites the key operand (packed: Q; multi: the K block or, on the
+    // diagonal block, the otherwise unused K buffer): S = Q K^T is complete.
+    uint8_t* Ps = KPs;
     const uint32_t prow = tc::smem_u32(Ps) + (tid >> 3) * 2048 + (tid & 7) * 16;
 #pragma unroll 1
-    for (int c0 = 0; c0 < ROWS; c0 += 16) {
-      uint32_t r[16];
-      tc::tmem_ld16(t_s + c0, r);
-      tc::tmem_ld_wait();
-      float p[16];
+    for (int ch = 0; ch < ROWS / 16; ++ch) {
+      uint32_t pk[8];
+      if (ch >= ch_lo && ch < ch_hi) {
+        uint32_t r[16];
+        tc::tmem_ld16(t_row + ch * 16, r);
+        tc::tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int col = c0 + j;
-        const bool ok = col >= jmin && col < jmax;
-        const float e = ok ? exp2f(__uint_as_float(r[j]) * scale_log2 - mscaled) : 0.0f;
-        const bf16 b = __float2bfloat16_rn(e);
-        p[j] = __bfloat162float(b);
-        lsum += p[j];
+        for (int j = 0; j < 16; j += 2) {
+          const int col = ch * 16 + j;
+          const bool ok0 = col >= jmin && col < jmax;
+          const bool ok1 = col + 1 >= jmin && col + 1 < jmax;
+          const float e0 = ok0 ? exp2f(__uint_as_float(r[j]) * scale_log2 - mscaled) : 0.0f;
+          const float e1 = ok1 ? exp2f(__uint_as_float(r[j + 1]) * scale_log2 - mscaled) : 0.0f;
+          const uint32_t pp = pack_bf16(e0, e1);
+          pk[j >> 1] = pp;
+          lsum += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xffff0000u);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pk[j] = 0u;
       }
-      // two 16-byte chunks (keys c0..c0+7, c0+8..c0+15)
+      // two 16-byte chunks (keys 16ch..16ch+7, 16ch+8..16ch+15)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t a0 = pack_bf16(p[8 * h + 0], p[8 * h + 1]);
-        const uint32_t a1 = pack_bf16(p[8 * h + 2], p[8 * h + 3]);
-        const uint32_t a2 = pack_bf16(p[8 * h + 4], p[8 * h + 5]);
-        const uint32_t a3 = pack_bf16(p[8 * h + 6], p[8 * h + 7]);
-        const uint32_t addr = prow + ((c0 >> 3) + h) * 128;
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a0), "r"(a1),
-                     "r"(a2), "r"(a3)
+        const uint32_t addr = prow + (2 * ch + h) * 128;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * h]),
+                     "r"(pk[4 * h + 1]), "r"(pk[4 * h + 2]), "r"(pk[4 * h + 3])
                      : "memory");
       }
     }
@@ -308,21 +333,21 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
     __syncthreads();
     tc::tc_fence_after_sync();
 
-    // ---- O_blk = P V ----------------------------------------------------
+    // ---- O_blk = P V (into S's columns) ---------------------------------
     if (tid == 0) {
       const uint32_t pa = tc::smem_u32(Ps), va = tc::smem_u32(Vs);
 #pragma unroll
       for (int s = 0; s < ROWS / 16; ++s) {
         const uint64_t ad = tc::smem_desc_noswizzle(pa + s * 256, 128, 2048);
         const uint64_t bd = tc::smem_desc_noswizzle(va + s * 256, 128, 2048);
-        tc::mma_f16_ss(tmem + 128, ad, bd, IDESC_O, s > 0 ? 1u : 0u);
+        tc::mma_f16_ss(tmem, ad, bd, IDESC_O, s > 0 ? 1u : 0u);
       }
       tc::mma_commit(&bar_o);
     }
     __syncwarp();
     if (!tc::mbar_wait_bounded(&bar_o, phase, WAIT_LIMIT_NS)) {
       failed = true;
-      if ((tid & 31) == 0) atomicExch(err, (unsigned)DEV_TIMEOUT);
+      if (lane == 0) atomicExch(err, (unsigned)DEV_TIMEOUT);
     }
     failed = __syncthreads_or(failed);
     if (failed) break;
@@ -333,18 +358,19 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 16) {
         uint32_t r[16];
-        tc::tmem_ld16(t_o + c0, r);
+        tc::tmem_ld16(t_row + c0, r);
         tc::tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) o_acc[c0 + j] = o_acc[c0 + j] * alpha + __uint_as_float(r[j]);
       }
+      tc::tc_fence_before_sync();  // O read before the next block's S overwrites it
     }
   }
 
   // ---- epilogue: this thread's output row --------------------------------
   if (!failed) {
     const int t = my_pos;
-    const bool single = row_valid && mcount[(size_t)bh * n + t] == 1;
+    const bool single = row_valid && my_m == 1;
     const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 16) {
@@ -354,7 +380,7 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
         for (int j = 0; j < 16; ++j) o[j] = o_acc[c0 + j] * inv_l;
       } else {
         uint32_t r[16];
-        tc::tmem_ld16(t_o + c0, r);  // warp-collective: every thread loads
+        tc::tmem_ld16(t_row + c0, r);  // warp-collective: every thread loads
         tc::tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(r[j]) * inv_l;
@@ -380,7 +406,7 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
 
   tc::tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+  if (warp == 0) tc::tmem_dealloc(tmem, 128);
 }
 
 template <int D, bool MULTI>
@@ -395,8 +421,7 @@ cudaError_t launch_t(const void* q, const void* v, int BH, int n, int k, int w, 
     R = (w + ROWS - 1) / ROWS;
     tiles_per_bh = k * R;
   }
-  const size_t smem = 1024 + 2 * (size_t)ROWS * D * 2 + (size_t)ROWS * ROWS * 2 +
-                      (MULTI ? (size_t)ROWS * D * 2 : 0);
+  const size_t smem = 1024 + (size_t)AttnSmem<D, MULTI>::BYTES;
   auto kern = attention_tc_kernel<D, MULTI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -81,11 +81,16 @@ ema_bucket_kernel(const int32_t* __restrict__ assign, int B, int H, int n, int k
     tot[c] = run;
   }
   __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int c = 0; c < k; ++c) {
-      start[c] = run;
-      run += tot[c];
+  {
+    // exclusive prefix of the tile totals over centroids (bucket starts)
+    __shared__ int wsum[WARPS1];
+    int carry = 0;
+    for (int c0 = 0; c0 < k; c0 += TE) {
+      const int c = c0 + tid;
+      int total;
+      const int ex = block_exclusive_scan<TE>(c < k ? tot[c] : 0, wsum, total);
+      if (c < k) start[c] = carry + ex;
+      carry += total;
     }
   }
   __syncthreads();
@@ -99,84 +104,135 @@ ema_bucket_kernel(const int32_t* __restrict__ assign, int B, int H, int n, int k
   }
 }
 
+// 8 consecutive features of a row as fp32
+__device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[8]) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = __uint_as_float(w4[e] << 16);
+    x[2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+  }
+}
+
+// Sum over the CH consecutive lanes that hold one row (CH a power of two).
+template <int CH>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = CH / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// One CTA per (centroid, head).  The centroid's rows (bucket entries of every
+// tile, in tile order, so in position order) are first listed in shared
+// memory, one lookup per row by one thread; then CH threads share each row,
+// every thread reading one 16-byte chunk of 8 features: the row's mean and
+// centred norm come from shuffles inside the group and the thread adds its
+// 8 normalised features into registers.  Row slots are summed in a fixed
+// order at the end, so the result is deterministic.
 template <typename T, int D>
 __global__ void __launch_bounds__(THREADS2)
 ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
                   const int32_t* __restrict__ counts, const int32_t* __restrict__ starts,
                   const int32_t* __restrict__ perm, float* __restrict__ mu, float decay) {
+  constexpr int CH = D / 8;          // threads per row
+  constexpr int RS = THREADS2 / CH;  // rows in flight per pass over the list
+  constexpr int LIST = 1024;         // rows listed per round
   extern __shared__ int32_t offs[];  // [Tn + 1]
-  __shared__ int part[THREADS2];
-  __shared__ float red[WARPS2][D];
+  __shared__ int rowlist[LIST];
+  __shared__ float red[RS][D];
   __shared__ float nrm_part[WARPS2];
   const int c = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t* cnt = counts + ((size_t)h * k + c) * Tn;
   const int32_t* st = starts + ((size_t)h * k + c) * Tn;
+  const long long rows_total = (long long)B * n;
 
-  // exclusive prefix of the per-tile counts: contiguous chunk per thread
-  const int per = (Tn + THREADS2 - 1) / THREADS2;
-  const int lo = tid * per, hi = min(Tn, lo + per);
-  int local = 0;
-  for (int i = lo; i < hi; ++i) local += cnt[i];
-  part[tid] = local;
-  __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int i = 0; i < THREADS2; ++i) {
-      const int x = part[i];
-      part[i] = run;
-      run += x;
-    }
-    offs[Tn] = run;
-  }
-  __syncthreads();
+  // exclusive prefix of the per-tile counts over the tiles
   {
-    int run = part[tid];
-    for (int i = lo; i < hi; ++i) {
-      offs[i] = run;
-      run += cnt[i];
+    __shared__ int wsum[WARPS2];
+    int carry = 0;
+    for (int i0 = 0; i0 < Tn; i0 += THREADS2) {
+      const int i = i0 + tid;
+      int total;
+      const int ex = block_exclusive_scan<THREADS2>(i < Tn ? __ldg(cnt + i) : 0, wsum, total);
+      if (i < Tn) offs[i] = carry + ex;
+      carry += total;
     }
+    if (tid == 0) offs[Tn] = carry;
   }
   __syncthreads();
   const int N = offs[Tn];
   if (N == 0) return;  // no assigned row: centroid unchanged
 
-  float acc[D / 32];
+  const int ch = tid % CH, rs = tid / CH;
+  float acc[8];
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) acc[i] = 0.0f;
-  for (int f = warp; f < N; f += WARPS2) {
-    // tile holding flattened entry f: last tl with offs[tl] <= f
-    int a0 = 0, a1 = Tn - 1;
-    while (a0 < a1) {
-      const int mid = (a0 + a1 + 1) >> 1;
-      if (offs[mid] <= f) a0 = mid; else a1 = mid - 1;
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+
+  for (int f0 = 0; f0 < N; f0 += LIST) {
+    const int nl = min(LIST, N - f0);
+    __syncthreads();  // the previous round's list is consumed
+    for (int i = tid; i < nl; i += THREADS2) {
+      const int f = f0 + i;
+      // tile holding flattened entry f: last tl with offs[tl] <= f
+      int a0 = 0, a1 = Tn - 1;
+      while (a0 < a1) {
+        const int mid = (a0 + a1 + 1) >> 1;
+        if (offs[mid] <= f) a0 = mid; else a1 = mid - 1;
+      }
+      const int p = __ldg(st + a0) + (f - offs[a0]);
+      int g = -1;
+      if (p >= 0 && p < TE) g = __ldg(perm + (size_t)h * Tn * TE + (size_t)a0 * TE + p);
+      if (g < 0 || (long long)g >= rows_total) g = -1;  // defensive
+      rowlist[i] = g;
     }
-    const int tl = a0;
-    const int p = st[tl] + (f - offs[tl]);
-    const int g = perm[(size_t)h * Tn * TE + (size_t)tl * TE + p];
-    if (g < 0 || (long long)g >= (long long)B * n) continue;  // defensive
-    const int b = g / n, t = g % n;
-    const T* row = qk + (((size_t)b * H + h) * n + t) * D;
-    float x[D / 32];
-    float s = 0.0f;
+    __syncthreads();
+    // uniform trip count: the shuffles below involve every lane of the warp
+    for (int base = 0; base < nl; base += 2 * RS) {
+      float x[2][8];
+      int gg[2];
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) { x[i] = to_f32(row[lane + 32 * i]); s += x[i]; }
-    const float mean = warp_sum(s) / (float)D;
-    float ss = 0.0f;
+      for (int u = 0; u < 2; ++u) {
+        const int i = base + rs + u * RS;
+        gg[u] = (i < nl) ? rowlist[i] : -1;
+        if (gg[u] >= 0) {
+          const int b = gg[u] / n, t = gg[u] - (gg[u] / n) * n;
+          load8(qk + (((size_t)b * H + h) * n + t) * D + ch * 8, x[u]);
+        } else {
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) { x[i] -= mean; ss = fmaf(x[i], x[i], ss); }
-    ss = warp_sum(ss);
-    const float inv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
+          for (int j = 0; j < 8; ++j) x[u][j] = 0.0f;
+        }
+      }
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) acc[i] += x[i] * inv;
+      for (int u = 0; u < 2; ++u) {
+        float sx = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sx += x[u][j];
+        const float mean = group_sum<CH>(sx) / (float)D;
+        float ss = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { x[u][j] -= mean; ss = fmaf(x[u][j], x[u][j], ss); }
+        ss = group_sum<CH>(ss);
+        const float inv = (gg[u] >= 0 && ss > 0.0f) ? 1.0f / sqrtf(ss) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = fmaf(x[u][j], inv, acc[j]);
+      }
+    }
   }
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) red[warp][lane + 32 * i] = acc[i];
+  for (int j = 0; j < 8; ++j) red[rs][ch * 8 + j] = acc[j];
   __syncthreads();
   float vj = 0.0f;
   if (tid < D) {
     float sum = 0.0f;
-    for (int wv = 0; wv < WARPS2; ++wv) sum += red[wv][tid];
+    for (int r = 0; r < RS; ++r) sum += red[r][tid];
     const float mean_j = sum / (float)N;
     const float old = mu[((size_t)h * k + c) * D + tid];
     vj = decay * old + (1.0f - decay) * mean_j;

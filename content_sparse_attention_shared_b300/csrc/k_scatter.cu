@@ -7,14 +7,16 @@
 // for a position no cluster chose.
 //
 // Positions chosen by exactly one cluster were written by the attention
-// epilogue already.  A warp takes 32 consecutive positions, reads their
-// membership counts with one coalesced load, and then serves the positions
-// that need work one after the other: a zero row, or the mean of the slot
-// rows.  The slots of a position come from the (cluster, slot) list the
-// select kernel recorded (up to SLOTS_PER_ROW entries), put in ascending
-// order; a position in more clusters than that finds its slots by binary
-// search in every cluster's ascending member list.  Either way the rows are
-// summed in ascending cluster order, so the result is deterministic.
+// epilogue already.  One thread per (position, 8-feature chunk): it reads the
+// position's membership count and, for a position in m = 0 clusters, writes
+// zeros; for 2 <= m <= SLOTS_PER_ROW it reads the (cluster, slot) ids the
+// select kernel recorded, sorts them (a fixed 8-input network), and sums its
+// chunk of the m slot rows in ascending cluster order -- the m row loads are
+// independent, so they are all in flight at once.  A position in more
+// clusters than that (only with many near-identical centroids) is served by
+// the whole warp: every lane binary-searches a different cluster's ascending
+// member list, and the rows found are summed in ascending cluster order.
+// Either way the result is deterministic.
 #include "rt_internal.cuh"
 
 namespace rt {
@@ -55,86 +57,145 @@ __device__ __forceinline__ void add_row(float (&acc)[PER], const float* src) {
   }
 }
 
+__device__ __forceinline__ void cswap(int& a, int& b) {
+  const int lo = min(a, b), hi = max(a, b);
+  a = lo;
+  b = hi;
+}
+
+// ascending sort of 8 ints (Batcher odd-even merge network, 19 exchanges)
+__device__ __forceinline__ void sort8(int (&v)[8]) {
+  cswap(v[0], v[1]); cswap(v[2], v[3]); cswap(v[4], v[5]); cswap(v[6], v[7]);
+  cswap(v[0], v[2]); cswap(v[1], v[3]); cswap(v[4], v[6]); cswap(v[5], v[7]);
+  cswap(v[1], v[2]); cswap(v[5], v[6]);
+  cswap(v[0], v[4]); cswap(v[1], v[5]); cswap(v[2], v[6]); cswap(v[3], v[7]);
+  cswap(v[2], v[4]); cswap(v[3], v[5]);
+  cswap(v[1], v[2]); cswap(v[3], v[4]); cswap(v[5], v[6]);
+}
+static_assert(SLOTS_PER_ROW == 8, "sort8 covers the recorded slot list");
+
+template <typename T>
+__device__ __forceinline__ void store8(T* dst, const float (&v)[8]) {
+  if constexpr (sizeof(T) == 2) {
+    uint4 u;
+    __nv_bfloat162 p;
+    p = __floats2bfloat162_rn(v[0], v[1]); u.x = *reinterpret_cast<uint32_t*>(&p);
+    p = __floats2bfloat162_rn(v[2], v[3]); u.y = *reinterpret_cast<uint32_t*>(&p);
+    p = __floats2bfloat162_rn(v[4], v[5]); u.z = *reinterpret_cast<uint32_t*>(&p);
+    p = __floats2bfloat162_rn(v[6], v[7]); u.w = *reinterpret_cast<uint32_t*>(&p);
+    *reinterpret_cast<uint4*>(dst) = u;
+  } else {
+    reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(THREADS)
 scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ idx,
                const int32_t* __restrict__ mcount, const int32_t* __restrict__ slots,
                const float* __restrict__ yslot, T* __restrict__ out) {
-  constexpr int PER = D / 32;  // contiguous features per lane
-  const long long warp_global = ((long long)blockIdx.x * THREADS + threadIdx.x) >> 5;
+  constexpr int CH = D / 8;    // 8-feature chunks per row
+  constexpr int PER = D / 32;  // contiguous features per lane on the warp-wide path
+  const long long g = (long long)blockIdx.x * THREADS + threadIdx.x;
+  const long long r = g / CH;  // row index bh * n + t
+  const int ch = (int)(g - r * CH);
   const int lane = threadIdx.x & 31;
-  const long long g0 = warp_global * 32;
-  if (g0 >= BHn) return;
-  const long long g = g0 + lane;
-  const int m = (g < BHn) ? mcount[g] : 1;
-  unsigned todo = __ballot_sync(0xffffffffu, m != 1);
-  while (todo) {
-    const int src = __ffs(todo) - 1;
-    todo &= todo - 1;
-    const long long gt = g0 + src;  // row index bh * n + t
+  const bool active = r < BHn;
+  const int m = active ? __ldg(mcount + r) : 1;
+
+  // rare: positions in more than SLOTS_PER_ROW clusters, one warp pass each
+  unsigned slow = __ballot_sync(0xffffffffu, active && ch == 0 && m > SLOTS_PER_ROW);
+  while (slow) {
+    const int src = __ffs(slow) - 1;
+    slow &= slow - 1;
+    const long long gt = __shfl_sync(0xffffffffu, r, src);
     const int mm = __shfl_sync(0xffffffffu, m, src);
-    T* orow = out + gt * D + lane * PER;
-    float acc[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = 0.0f;
-    if (mm == 0) {
-      store_row<T, PER>(orow, acc);
-      continue;
-    }
     const long long bh = gt / n;
     const int t = (int)(gt - bh * n);
     const float* ybase = yslot + (size_t)bh * k * w * D;
-    if (slots != nullptr && mm <= SLOTS_PER_ROW) {
-      const int sid = lane < mm ? slots[gt * SLOTS_PER_ROW + lane] : 0x7fffffff;
-      // rank of this lane's slot id among the first mm lanes (ids are distinct)
-      int rank = 0;
+    const int32_t* base = idx + (size_t)bh * k * w;
+    float acc[PER];
 #pragma unroll
-      for (int j = 0; j < SLOTS_PER_ROW; ++j) {
-        const int other = __shfl_sync(0xffffffffu, sid, j);
-        if (j < mm && other < sid) ++rank;
-      }
-      for (int r = 0; r < mm; ++r) {
-        const unsigned who = __ballot_sync(0xffffffffu, lane < mm && rank == r);
-        const int sl = __shfl_sync(0xffffffffu, sid, __ffs(who) - 1);
-        add_row<PER>(acc, ybase + (size_t)sl * D + lane * PER);
-      }
-    } else {
-      const int32_t* base = idx + (size_t)bh * k * w;
-      for (int c0 = 0; c0 < k; c0 += 32) {
-        const int c = c0 + lane;
-        int slot = -1;
-        if (c < k) {
-          const int32_t* list = base + (size_t)c * w;
-          int lo = 0, hi = w - 1;
-          while (lo <= hi) {
-            const int mid = (lo + hi) >> 1;
-            const int v = list[mid];
-            if (v == t) { slot = mid; break; }
-            if (v < t) lo = mid + 1; else hi = mid - 1;
-          }
+    for (int i = 0; i < PER; ++i) acc[i] = 0.0f;
+    for (int c0 = 0; c0 < k; c0 += 32) {
+      const int c = c0 + lane;
+      int slot = -1;
+      if (c < k) {
+        const int32_t* list = base + (size_t)c * w;
+        int lo = 0, hi = w - 1;
+        while (lo <= hi) {
+          const int mid = (lo + hi) >> 1;
+          const int v = __ldg(list + mid);
+          if (v == t) { slot = mid; break; }
+          if (v < t) lo = mid + 1; else hi = mid - 1;
         }
-        unsigned found = __ballot_sync(0xffffffffu, slot >= 0);
-        while (found) {
-          const int fl = __ffs(found) - 1;
-          found &= found - 1;
-          const int s = __shfl_sync(0xffffffffu, slot, fl);
-          add_row<PER>(acc, ybase + ((size_t)(c0 + fl) * w + s) * D + lane * PER);
-        }
+      }
+      unsigned found = __ballot_sync(0xffffffffu, slot >= 0);
+      while (found) {
+        const int fl = __ffs(found) - 1;
+        found &= found - 1;
+        const int sl = __shfl_sync(0xffffffffu, slot, fl);
+        add_row<PER>(acc, ybase + ((size_t)(c0 + fl) * w + sl) * D + lane * PER);
       }
     }
     const float fm = (float)mm;
+    float o[PER];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = acc[i] / fm;
-    store_row<T, PER>(orow, acc);
+    for (int i = 0; i < PER; ++i) o[i] = acc[i] / fm;
+    store_row<T, PER>(out + gt * D + lane * PER, o);
   }
+
+  if (!active || m == 1 || m > SLOTS_PER_ROW) return;
+  T* dst = out + r * D + ch * 8;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  if (m == 0) {
+    store8<T>(dst, acc);
+    return;
+  }
+  int ids[8];
+  {
+    const int4* sp = reinterpret_cast<const int4*>(slots + r * SLOTS_PER_ROW);
+    const int4 a = __ldg(sp), b = __ldg(sp + 1);
+    ids[0] = a.x; ids[1] = a.y; ids[2] = a.z; ids[3] = a.w;
+    ids[4] = b.x; ids[5] = b.y; ids[6] = b.z; ids[7] = b.w;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (i >= m) ids[i] = 0x7fffffff;
+  sort8(ids);
+  const long long bh = r / n;
+  const float* ybase = yslot + (size_t)bh * k * w * D + ch * 8;
+  float4 y[8][2];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (i < m) {
+      const float4* p = reinterpret_cast<const float4*>(ybase + (size_t)ids[i] * D);
+      y[i][0] = __ldg(p);
+      y[i][1] = __ldg(p + 1);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (i < m) {
+      acc[0] += y[i][0].x; acc[1] += y[i][0].y; acc[2] += y[i][0].z; acc[3] += y[i][0].w;
+      acc[4] += y[i][1].x; acc[5] += y[i][1].y; acc[6] += y[i][1].z; acc[7] += y[i][1].w;
+    }
+  }
+  const float fm = (float)m;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = acc[i] / fm;
+  store8<T>(dst, acc);
 }
 
 template <typename T, int D>
 cudaError_t launch_t(int BH, int n, int k, int w, const int32_t* idx, const int32_t* mcount,
                      const int32_t* slots, const float* yslot, void* out, cudaStream_t s) {
   const long long rows = (long long)BH * n;
-  const long long warps = (rows + 31) / 32;
-  const long long blocks = (warps * 32 + THREADS - 1) / THREADS;
+  const long long threads = rows * (D / 8);
+  const long long blocks = (threads + THREADS - 1) / THREADS;
   launch_begin(K_SCATTER, s);
   scatter_kernel<T, D><<<(unsigned)blocks, THREADS, 0, s>>>(rows, n, k, w, idx, mcount, slots,
                                                             yslot, static_cast<T*>(out));

@@ -101,64 +101,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
   const int tiles_per_bh = (n + ROWS - 1) / ROWS;
   const int ntiles = B * tiles_per_bh;  // tiles of this head (all sequences)
 
-  // ---- centroid planes for head h (all threads) ---------------------------
-  // item (c, jc): 8 consecutive features of centroid c, split into three bf16
-  // planes and written as one 16-byte chunk per plane at jc*kpad*16 + c*16.
-  {
-    const float* mu_h = mu + (size_t)h * k * D;
-    const int items = kpad * (D / 8);
-    for (int it = tid; it < items; it += THREADS) {
-      const int c = it % kpad, jc = it / kpad;
-      float m[8];
-      if (c < k) {
-        const float4 a = __ldg(reinterpret_cast<const float4*>(mu_h + (size_t)c * D + jc * 8));
-        const float4 b = __ldg(reinterpret_cast<const float4*>(mu_h + (size_t)c * D + jc * 8 + 4));
-        m[0] = a.x; m[1] = a.y; m[2] = a.z; m[3] = a.w;
-        m[4] = b.x; m[5] = b.y; m[6] = b.z; m[7] = b.w;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) m[e] = 0.0f;
-      }
-      uint32_t ph[4], pm[4], pl[4];
-#pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        bf16 hi[2], md[2], lo[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          hi[u] = __float2bfloat16_rn(m[e + u]);
-          const float r1 = m[e + u] - __bfloat162float(hi[u]);
-          md[u] = __float2bfloat16_rn(r1);
-          const float r2 = r1 - __bfloat162float(md[u]);
-          lo[u] = __float2bfloat16_rn(r2);
-        }
-        ph[e / 2] = pack2_bf16(hi[0], hi[1]);
-        pm[e / 2] = pack2_bf16(md[0], md[1]);
-        pl[e / 2] = pack2_bf16(lo[0], lo[1]);
-      }
-      const size_t off = (size_t)jc * (kpad * 16) + (size_t)c * 16;
-      *reinterpret_cast<uint4*>(Bs + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-      *reinterpret_cast<uint4*>(Bs + plane_bytes + off) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
-      *reinterpret_cast<uint4*>(Bs + 2 * (size_t)plane_bytes + off) =
-          make_uint4(pl[0], pl[1], pl[2], pl[3]);
-    }
-    // row sums of the fp32 centroids, fixed order
-    for (int c = tid; c < kpad; c += THREADS) {
-      float rs = 0.0f;
-      if (c < k) {
-        const float4* row = reinterpret_cast<const float4*>(mu_h + (size_t)c * D);
-#pragma unroll 4
-        for (int j = 0; j < D / 4; ++j) {
-          const float4 v = __ldg(row + j);
-          rs += v.x; rs += v.y; rs += v.z; rs += v.w;
-        }
-      }
-      sumu[c] = rs;
-    }
-  }
-  if (warp == 1) {
-    tc::tmem_alloc(&tmem_base_sh, 2 * acc_cols);
-    tc::tmem_relinquish();
-  }
+  // ---- barriers first, so the first Q tiles stream in during the set-up ---
+  const int first = blockIdx.x, stride = ctas_per_head;
   if (tid == 0) {
     for (int i = 0; i < stages; ++i) {
       tc::mbar_init(&full_bar[i], 1);
@@ -170,6 +114,99 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
     }
     stop_flag = 0;
     tc::fence_mbar_init();
+    // the first `stages` tiles need no free slot: issue them now
+    int i = 0;
+    for (int tile = first; tile < ntiles && i < stages; tile += stride, ++i) {
+      const int b = tile / tiles_per_bh, tb = tile - b * tiles_per_bh;
+      const int row0 = (b * H + h) * n + tb * ROWS;
+      tc::mbar_arrive_expect_tx(&full_bar[i], A_BYTES);
+#pragma unroll
+      for (int kb = 0; kb < KB; ++kb)
+        tma_load_2d(As + (size_t)i * A_BYTES + kb * (ROWS * 128), &qmap, kb * BOX_K, row0,
+                    &full_bar[i]);
+    }
+  }
+
+  // ---- centroid planes for head h (all threads) ---------------------------
+  // item (c, jc): 8 consecutive features of centroid c, split into three bf16
+  // planes and written as one 16-byte chunk per plane at jc*kpad*16 + c*16
+  // (consecutive threads take consecutive c: conflict-free).  Four items per
+  // thread are loaded before any is converted.
+  {
+    const float* mu_h = mu + (size_t)h * k * D;
+    const int items = kpad * (D / 8);
+    constexpr int U = 4;
+    for (int it0 = tid; it0 < items; it0 += U * THREADS) {
+      float m[U][8];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int it = it0 + u * THREADS;
+        const int c = it % kpad, jc = it / kpad;
+        if (it < items && c < k) {
+          const float4* src = reinterpret_cast<const float4*>(mu_h + (size_t)c * D + jc * 8);
+          const float4 a = __ldg(src), b = __ldg(src + 1);
+          m[u][0] = a.x; m[u][1] = a.y; m[u][2] = a.z; m[u][3] = a.w;
+          m[u][4] = b.x; m[u][5] = b.y; m[u][6] = b.z; m[u][7] = b.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m[u][e] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int it = it0 + u * THREADS;
+        if (it >= items) break;
+        const int c = it % kpad, jc = it / kpad;
+        uint32_t ph[4], pm[4], pl[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          bf16 hi[2], md[2], lo[2];
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            hi[v] = __float2bfloat16_rn(m[u][e + v]);
+            const float r1 = m[u][e + v] - __bfloat162float(hi[v]);
+            md[v] = __float2bfloat16_rn(r1);
+            const float r2 = r1 - __bfloat162float(md[v]);
+            lo[v] = __float2bfloat16_rn(r2);
+          }
+          ph[e / 2] = pack2_bf16(hi[0], hi[1]);
+          pm[e / 2] = pack2_bf16(md[0], md[1]);
+          pl[e / 2] = pack2_bf16(lo[0], lo[1]);
+        }
+        const size_t off = (size_t)jc * (kpad * 16) + (size_t)c * 16;
+        *reinterpret_cast<uint4*>(Bs + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+        *reinterpret_cast<uint4*>(Bs + plane_bytes + off) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
+        *reinterpret_cast<uint4*>(Bs + 2 * (size_t)plane_bytes + off) =
+            make_uint4(pl[0], pl[1], pl[2], pl[3]);
+      }
+    }
+    // row sums of the fp32 centroids: one warp per row (fixed shuffle
+    // order), eight rows in flight per warp
+    constexpr int NW = THREADS / 32;
+    constexpr int RU = 8;
+    for (int c0 = warp; c0 < kpad; c0 += NW * RU) {
+      float v[RU];
+#pragma unroll
+      for (int u = 0; u < RU; ++u) {
+        const int c = c0 + u * NW;
+        v[u] = 0.0f;
+        if (c < k) {
+          const float* row = mu_h + (size_t)c * D + lane * (D / 32);
+#pragma unroll
+          for (int e = 0; e < D / 32; ++e) v[u] += __ldg(row + e);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < RU; ++u) {
+        const float rs = warp_sum(v[u]);
+        const int c = c0 + u * NW;
+        if (lane == 0 && c < kpad) sumu[c] = rs;
+      }
+    }
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&tmem_base_sh, 2 * acc_cols);
+    tc::tmem_relinquish();
   }
   tc::fence_proxy_async_smem();  // planes written by threads, read by the MMA
   tc::tc_fence_before_sync();
@@ -177,12 +214,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
   tc::tc_fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
 
-  const int first = blockIdx.x, stride = ctas_per_head;
   if (warp == 0) {
     // ===================== TMA producer =====================================
     if (lane == 0) {
-      int i = 0;
-      for (int tile = first; tile < ntiles; tile += stride, ++i) {
+      int i = stages;  // tiles 0 .. stages-1 were issued before the set-up
+      for (int tile = first + stages * stride; tile < ntiles; tile += stride, ++i) {
         const int s = i % stages;
         const uint32_t use = (uint32_t)(i / stages);
         if (!tc::mbar_wait_bounded(&empty_bar[s], (use & 1u) ^ 1u, WAIT_LIMIT_NS) ||
@@ -312,7 +348,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
       if (lane == 0) mbar_arrive(&empty_bar[s]);  // stage free: MMA done, rows read
       float best = -INFINITY;
       int best_c = 0;
-      float* srow = S + (size_t)bh * k * n + t;
+      const float nmean = -mean;
+      float* sp = (S != nullptr && valid) ? S + (size_t)bh * k * n + t : nullptr;
       const uint32_t tacc = tmem + grp * acc_cols + lane_base;
       for (int c0 = 0; c0 < kpad; c0 += 32) {
         uint32_t r[2][16];
@@ -321,15 +358,38 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
         tc::tmem_ld_wait();
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          if (c0 + 16 * hh >= kpad) break;
+          const int cb = c0 + 16 * hh;
+          if (cb >= kpad) break;
+          float sc[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int c = c0 + 16 * hh + j;
-            const float dot = __uint_as_float(r[hh][j]);
-            const float sc = zero_row ? 0.0f : (dot - mean * sumu[c]) * inv;
-            if (valid && c < k) {
-              if (S != nullptr) srow[(size_t)c * n] = sc;
-              if (sc > best) { best = sc; best_c = c; }
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const float4 su = *reinterpret_cast<const float4*>(sumu + cb + 4 * q4);
+            sc[4 * q4 + 0] = fmaf(nmean, su.x, __uint_as_float(r[hh][4 * q4 + 0])) * inv;
+            sc[4 * q4 + 1] = fmaf(nmean, su.y, __uint_as_float(r[hh][4 * q4 + 1])) * inv;
+            sc[4 * q4 + 2] = fmaf(nmean, su.z, __uint_as_float(r[hh][4 * q4 + 2])) * inv;
+            sc[4 * q4 + 3] = fmaf(nmean, su.w, __uint_as_float(r[hh][4 * q4 + 3])) * inv;
+          }
+          if (zero_row) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sc[j] = 0.0f;
+          }
+          if (cb + 16 <= k) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (sc[j] > best) { best = sc[j]; best_c = cb + j; }
+            }
+            if (sp != nullptr) {
+              float* p = sp + (size_t)cb * n;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) { *p = sc[j]; p += n; }
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (cb + j < k) {
+                if (sc[j] > best) { best = sc[j]; best_c = cb + j; }
+                if (sp != nullptr) sp[(size_t)(cb + j) * n] = sc[j];
+              }
             }
           }
         }

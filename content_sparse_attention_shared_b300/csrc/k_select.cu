@@ -17,13 +17,13 @@
 //   2. a block-wide scan of the histogram from the top bin down finds the bin
 //      b* holding the w-th largest score and how many of its members are
 //      still needed;
-//   3. the members of b* (the candidates, typically a few) are ranked
-//      exactly by (score desc, position asc); the kept ones are re-binned
-//      above every other bin;
-//   4. ordered compaction: warp j owns a contiguous segment of positions,
-//      counts its kept positions with ballots, one barrier gives every warp
-//      its output offset, and a second ballot pass writes the positions in
-//      order -- the list comes out sorted without a sort.
+//   3. one pass over the staged bins records, per 32-position chunk, the
+//      mask of positions above b* and the mask of members of b* (the
+//      candidates, typically a few); the candidates are ranked exactly by
+//      (score desc, position asc) and the first `need` join the kept mask;
+//   4. ordered emission: a block-wide scan over the chunks' kept counts gives
+//      every chunk its first output slot, so the list comes out sorted by
+//      position without a sort.
 // Membership counts are incremented here with integer atomics (the totals are
 // order independent), and the first SLOTS_PER_ROW (cluster, slot) entries of
 // every position are recorded for the scatter.
@@ -40,7 +40,7 @@ constexpr int WARPS = THREADS / 32;
 constexpr int NBINS = 2048;
 constexpr int BINS_PER_THREAD = NBINS / THREADS;
 constexpr int CAND_CAP = 1024;
-constexpr int MAX_STAGED_BINS = 96 * 1024;  // u16 bins staged in shared memory
+constexpr int MAX_STAGED_BINS = 80 * 1024;  // u16 bins staged in shared memory
 
 __device__ __forceinline__ int score_bin(float s) {
   // non-decreasing in s; [-1, 1] -> [0, 2047] (NaN -> 0)
@@ -63,29 +63,6 @@ struct SelectOut {
     }
   }
 };
-
-// Exclusive block-wide prefix of one int per thread (and the total).
-__device__ __forceinline__ int block_exclusive_scan(int v, int* wsum /* [WARPS] */, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  int before = 0;
-  total = 0;
-#pragma unroll
-  for (int i = 0; i < WARPS; ++i) {
-    const int x = wsum[i];
-    before += (i < warp) ? x : 0;
-    total += x;
-  }
-  __syncthreads();  // wsum may be reused by the caller
-  return before + incl - v;
-}
 
 // Exact fallback: 32-bit MSD radix select on order-preserving keys, reading
 // the row from global memory (L2).  Slow but general.
@@ -256,7 +233,7 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
       lsum += (int)hb[q];
     }
     int total;
-    const int excl = block_exclusive_scan(lsum, wsum, total);
+    const int excl = block_exclusive_scan<THREADS>(lsum, wsum, total);
     if (excl < w && w <= excl + lsum) {
       int cum = excl;
 #pragma unroll
@@ -278,27 +255,40 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
     return;
   }
 
-  // 3. candidates (members of b*): keep all of them if all are needed, else
-  //    rank them exactly by (score desc, position asc)
-  if (need < ncand_total) {
-    for (int t0 = 0; t0 < n; t0 += THREADS) {
-      const int t = t0 + tid;
-      const bool is_c = (t < n) && sbin[t] == bstar;
-      const unsigned bm = __ballot_sync(0xffffffffu, is_c);
-      if (bm == 0u) continue;
-      int base = 0;
-      if (lane == 0) base = atomicAdd(&s_ncand, __popc(bm));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (is_c) {
-        const int slot = base + __popc(bm & ((1u << lane) - 1u));
+  // 3. one pass over the staged bins: per 32-position chunk q, the mask of
+  //    positions in a bin above b* (kept) and of members of b* (candidates)
+  const int nq = (n + 31) >> 5;
+  uint32_t* hmask = reinterpret_cast<uint32_t*>(sbin + ((n + 7) & ~7));  // [nq]
+  uint32_t* emask = hmask + nq;                                          // [nq]
+  for (int q = warp; q < nq; q += WARPS) {
+    const int t = q * 32 + lane;
+    const int bv = (t < n) ? (int)sbin[t] : -1;
+    const unsigned hi = __ballot_sync(0xffffffffu, bv > bstar);
+    const unsigned eq = __ballot_sync(0xffffffffu, bv == bstar);
+    if (lane == 0) {
+      hmask[q] = hi;
+      emask[q] = eq;
+    }
+  }
+  __syncthreads();
+  if (need == ncand_total) {
+    // every member of b* is kept
+    for (int q = tid; q < nq; q += THREADS) hmask[q] |= emask[q];
+  } else {
+    // rank the members of b* exactly by (score desc, position asc)
+    for (int q = tid; q < nq; q += THREADS) {
+      unsigned em = emask[q];
+      while (em) {
+        const int b = __ffs(em) - 1;
+        em &= em - 1;
+        const int slot = atomicAdd(&s_ncand, 1);
+        const int t = q * 32 + b;
         cand_t[slot] = t;
         cand_s[slot] = __ldg(row + t);
       }
     }
     __syncthreads();
     const int nc = s_ncand;
-    int keep_t[CAND_CAP / THREADS];
-    int nkeep = 0;
     for (int i = tid; i < nc; i += THREADS) {
       const float si = cand_s[i];
       const int ti = cand_t[i];
@@ -307,41 +297,28 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
         const float sj = cand_s[j];
         rank += (sj > si) || (sj == si && cand_t[j] < ti);
       }
-      keep_t[nkeep++] = (rank < need) ? ti : -1;
+      if (rank < need) atomicOr(&hmask[ti >> 5], 1u << (ti & 31));
     }
-    __syncthreads();  // every candidate read its bin before any is rewritten
-    for (int q = 0; q < nkeep; ++q)
-      if (keep_t[q] >= 0) sbin[keep_t[q]] = (uint16_t)NBINS;
-  } else {
-    // every member of b* is kept: lower the cut instead of re-binning
   }
   __syncthreads();
-  const int cut = (need < ncand_total) ? bstar : bstar - 1;  // keep bin > cut
 
-  // 4. ordered compaction over per-warp contiguous segments
-  const int seg = ((n + WARPS * 32 - 1) / (WARPS * 32)) * 32;
-  const int s0 = warp * seg;
-  const int s1 = min(n, s0 + seg);
-  int cnt = 0;
-  for (int t0 = s0; t0 < s1; t0 += 32) {
-    const int t = t0 + lane;
-    const bool sel = (t < s1) && (int)sbin[t] > cut;
-    cnt += __popc(__ballot_sync(0xffffffffu, sel));
-  }
-  if (lane == 0) wsum[warp] = cnt;
-  __syncthreads();
-  int base = 0;
-#pragma unroll
-  for (int i = 0; i < WARPS; ++i) base += (i < warp) ? wsum[i] : 0;
-  for (int t0 = s0; t0 < s1 && base < w; t0 += 32) {
-    const int t = t0 + lane;
-    const bool sel = (t < s1) && (int)sbin[t] > cut;
-    const unsigned bm = __ballot_sync(0xffffffffu, sel);
-    if (sel) {
-      const int o = base + __popc(bm & ((1u << lane) - 1u));
-      if (o < w) so.emit(o, t);
+  // 4. ordered emission: chunk q's kept positions go to the output slots after
+  //    those of chunks 0..q-1 (a block-wide scan over the chunk counts)
+  int carry = 0;
+  for (int q0 = 0; q0 < nq; q0 += THREADS) {
+    const int q = q0 + tid;
+    const unsigned km = (q < nq) ? hmask[q] : 0u;
+    int total;
+    const int ex = block_exclusive_scan<THREADS>(__popc(km), wsum, total);
+    unsigned rem = km;
+    int o = carry + ex;
+    while (rem) {
+      const int b = __ffs(rem) - 1;
+      rem &= rem - 1;
+      if (o < w) so.emit(o, q * 32 + b);
+      ++o;
     }
-    base += __popc(bm);
+    carry += total;
   }
 }
 
@@ -351,10 +328,14 @@ cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* 
                           int32_t* mcount, int32_t* slots, cudaStream_t s) {
   dim3 grid(k, BH);
   const int staged = n <= MAX_STAGED_BINS ? 1 : 0;
-  const size_t smem = staged ? ((size_t)n * sizeof(uint16_t) + 15) / 16 * 16 : 0;
+  // staged bins (u16, padded to 16 bytes) + two chunk masks per 32 positions
+  auto stage_bytes = [](int nn) {
+    return (size_t)((nn + 7) & ~7) * sizeof(uint16_t) + 2 * (size_t)((nn + 31) / 32) * 4;
+  };
+  const size_t smem = staged ? stage_bytes(n) : 0;
   cudaError_t e = cudaFuncSetAttribute(select_topw_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       MAX_STAGED_BINS * (int)sizeof(uint16_t));
+                                       (int)stage_bytes(MAX_STAGED_BINS));
   if (e != cudaSuccess) return e;
   launch_begin(K_SELECT, s);
   select_topw_kernel<<<grid, THREADS, smem, s>>>(S, n, k, w, idx, mcount, slots, staged);

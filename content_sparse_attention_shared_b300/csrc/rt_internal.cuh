@@ -66,6 +66,33 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Exclusive prefix sum over the NT threads of a block (one int each) and the
+// block total.  wsum: NT/32 ints of shared memory.  Contains two barriers, so
+// every thread of the block must call it.
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan(int v, int* wsum, int& total) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  total = 0;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    const int x = wsum[i];
+    before += (i < warp) ? x : 0;
+    total += x;
+  }
+  __syncthreads();  // wsum may be reused at once
+  return before + incl - v;
+}
+
 // Order-preserving map of an fp32 score to an unsigned key (larger score,
 // larger key).  -0 is folded onto +0 so that equal scores give equal keys.
 __device__ __forceinline__ uint32_t score_key(float f) {
@@ -96,7 +123,7 @@ cudaError_t launch_score(const void* qk, rt_dtype dt, int B, int H, int n, int d
 // mcount (atomic integer increments; may be null) and records up to
 // SLOTS_PER_ROW global slot ids (c*w + slot) per position in `slots`
 // [BH, n, SLOTS_PER_ROW] (may be null; entry order is arbitrary).
-constexpr int SLOTS_PER_ROW = 4;
+constexpr int SLOTS_PER_ROW = 8;
 cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* idx,
                           int32_t* mcount, int32_t* slots, cudaStream_t s);
 
