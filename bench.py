@@ -371,46 +371,56 @@ def run_ours(args, wl):
     stream = torch.cuda.current_stream(dev)
 
     def step(qq, vv):
+        # launches go to torch's current stream (the capture stream while a
+        # CUDA graph is being recorded)
         rt.rt_routing_attention(qq, qq, vv, mu, wl.w, causal=True, out=out, idx_out=idx,
-                                assign_out=assign, workspace=ws, stream=stream)
+                                assign_out=assign, workspace=ws)
         if wl.ema:
-            rt.rt_centroid_ema(qq, assign, mu, wl.decay, workspace=ws, stream=stream)
+            rt.rt_centroid_ema(qq, assign, mu, wl.decay, workspace=ws)
 
     for _ in range(max(3, args.warmup)):
         step(q, v)
     torch.cuda.synchronize()
     ws.check()
-    launches_per_step = None
 
-    # ---- device-timed region --------------------------------------------
     n_launch_before = rt.rt_launch_count()
     step(q, v)
     torch.cuda.synchronize()
     launches_per_step = rt.rt_launch_count() - n_launch_before
-    prof_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(launches_per_step * args.steps)]
+
+    # ---- the step as one CUDA graph (no host launch cost per kernel) -----
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        step(q, v)  # warm-up on the capture stream
+    cap.synchronize()
+    with torch.cuda.graph(graph, stream=cap):
+        step(q, v)
+    torch.cuda.synchronize()
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- device-timed region: K graph replays, L2 flushed before each ----
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    rt.rt_profile_set(prof_pairs)
-    l0 = rt.rt_launch_count()
     props = torch.cuda.get_device_properties(dev)
     pci = None
     if hasattr(props, "pci_bus_id"):
         pci = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
                                      getattr(props, "pci_device_id", 0))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
     with ClockSampler(local, pci) as clk:
         for i in range(args.steps):
             flush.zero_()
             ev[i][0].record(stream)
-            step(q, v)
+            graph.replay()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
-    gpu_launches = rt.rt_launch_count() - l0
-    prof_names = [rt.rt_profile_kernel_name(i) for i in range(len(prof_pairs))]
-    rt.rt_profile_set([])
+    gpu_launches = launches_per_step * args.steps  # kernels the replays ran
     step_ms = [a.elapsed_time(b) for a, b in ev]
     t_ms = statistics.mean(step_ms)
     if world > 1:
@@ -420,11 +430,24 @@ def run_ours(args, wl):
         dist.barrier()
     ws.check()
 
-    # per-kernel times over the timed region
+    # ---- per-kernel device times: eager steps behind a sleep kernel, so the
+    # host has every launch queued before the GPU reaches it and the launch
+    # hook's events bracket device time only -------------------------------
+    prof_steps = min(args.steps, 50)
+    prof_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(launches_per_step * prof_steps)]
+    torch.cuda.synchronize()
+    rt.rt_profile_set(prof_pairs)
+    for i in range(prof_steps):
+        flush.zero_()
+        torch.cuda._sleep(400000)  # about 0.2 ms at 2 GHz
+        step(q, v)
+    torch.cuda.synchronize()
+    prof_names = [rt.rt_profile_kernel_name(i) for i in range(len(prof_pairs))]
+    rt.rt_profile_set([])
     per_kind = {}
     for i, (a, b) in enumerate(prof_pairs):
-        name = prof_names[i]
-        per_kind.setdefault(name, []).append(a.elapsed_time(b))
+        per_kind.setdefault(prof_names[i], []).append(a.elapsed_time(b))
     kern = {k2: {"launches": len(v2), "avg_us": 1e3 * statistics.mean(v2),
                  "total_ms": sum(v2)} for k2, v2 in per_kind.items()}
     total_kernel_ms = sum(x["total_ms"] for x in kern.values())
@@ -502,7 +525,8 @@ def run_ours(args, wl):
         "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "n": wl.n, "d": wl.d, "k": wl.k,
                    "w": wl.w, "causal": True, "step": "forward + centroid update" if wl.ema
                    else "forward", "l2": "flushed before every timed step (256 MiB write)",
-                   "graph": False},
+                   "graph": True, "kernel_times": "eager steps behind a sleep kernel, "
+                   "CUDA events around each launch"},
         "tflops": tflops, "tflops_frac_bf16": tflops / peaks["bf16_tflops"],
         "roofline": roof,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,

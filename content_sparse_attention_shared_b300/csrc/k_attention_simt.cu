@@ -148,7 +148,7 @@ cudaError_t launch_t(const void* q, const void* kk, const void* v, int BH, int n
                      void* out, float* yslot, cudaStream_t s) {
   const size_t smem = ((size_t)(QB + KB) * (D + 1) + (size_t)KB * D) * sizeof(float);
   auto kern = attention_simt_kernel<T, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((w + QB - 1) / QB, k, BH);
   launch_begin(K_ATTN_SIMT, s);

@@ -367,10 +367,16 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
     }
   }
 
-  // ---- epilogue: this thread's output row --------------------------------
+  // ---- epilogue ------------------------------------------------------------
+  // Every MMA is complete, so the operand shared memory is free: each thread
+  // stages its normalised O row there as fp32 (16-byte chunks XOR-swizzled by
+  // row, conflict-free), then every warp copies its own 32 rows out with
+  // row-contiguous stores -- bf16 to `out` for a position in exactly one
+  // cluster, fp32 to its slot row in `yslot` otherwise.
   if (!failed) {
-    const int t = my_pos;
-    const bool single = row_valid && my_m == 1;
+    constexpr int CPR = D / 4;        // 16-byte fp32 chunks per row
+    constexpr int RPI = 32 / CPR;     // rows per warp instruction
+    float4* stage = reinterpret_cast<float4*>(sm);
     const float inv_l = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 16) {
@@ -385,23 +391,37 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
 #pragma unroll
         for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(r[j]) * inv_l;
       }
-      if (!row_valid) continue;
-      if (single) {
-        uint4 a, b;
-        a.x = pack_bf16(o[0], o[1]); a.y = pack_bf16(o[2], o[3]);
-        a.z = pack_bf16(o[4], o[5]); a.w = pack_bf16(o[6], o[7]);
-        b.x = pack_bf16(o[8], o[9]); b.y = pack_bf16(o[10], o[11]);
-        b.z = pack_bf16(o[12], o[13]); b.w = pack_bf16(o[14], o[15]);
-        uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)bh * n + t) * D + c0);
-        dst[0] = a;
-        dst[1] = b;
-      } else {
-        float4* dst = reinterpret_cast<float4*>(
-            yslot + (((size_t)bh * k + cluster) * w + slot) * D + c0);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int chunk = c0 / 4 + q4;
+        stage[tid * CPR + (chunk ^ (tid & 7))] =
+            make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
       }
     }
+    __syncwarp();
+    const int single = (row_valid && my_m == 1) ? 1 : 0;
+    const int ch = lane % CPR;
+#pragma unroll 4
+    for (int it = 0; it < 32 / RPI; ++it) {
+      const int rr = it * RPI + lane / CPR;  // row of this warp; its owner is lane rr
+      const int r = warp * 32 + rr;
+      const int t = __shfl_sync(0xffffffffu, my_pos, rr);
+      const int ok = __shfl_sync(0xffffffffu, row_valid ? 1 : 0, rr);
+      const int sg = __shfl_sync(0xffffffffu, single, rr);
+      const int cl = __shfl_sync(0xffffffffu, cluster, rr);
+      const int sl = __shfl_sync(0xffffffffu, slot, rr);
+      const float4 val = stage[r * CPR + (ch ^ (r & 7))];
+      if (!ok) continue;
+      if (sg) {
+        uint2 u;
+        u.x = pack_bf16(val.x, val.y);
+        u.y = pack_bf16(val.z, val.w);
+        *reinterpret_cast<uint2*>(out + ((size_t)bh * n + t) * D + ch * 4) = u;
+      } else {
+        *reinterpret_cast<float4*>(yslot + (((size_t)bh * k + cl) * w + sl) * D + ch * 4) = val;
+      }
+    }
+
   }
 
   tc::tc_fence_before_sync();
@@ -423,7 +443,7 @@ cudaError_t launch_t(const void* q, const void* v, int BH, int n, int k, int w, 
   }
   const size_t smem = 1024 + (size_t)AttnSmem<D, MULTI>::BYTES;
   auto kern = attention_tc_kernel<D, MULTI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   const long long tiles = (long long)BH * tiles_per_bh;
   const float scale_log2 = scale * 1.4426950408889634f;

@@ -137,7 +137,7 @@ __device__ __forceinline__ float group_sum(float v) {
 // 8 normalised features into registers.  Row slots are summed in a fixed
 // order at the end, so the result is deterministic.
 template <typename T, int D>
-__global__ void __launch_bounds__(THREADS2)
+__global__ void __launch_bounds__(THREADS2, 8)
 ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
                   const int32_t* __restrict__ counts, const int32_t* __restrict__ starts,
                   const int32_t* __restrict__ perm, float* __restrict__ mu, float decay) {
@@ -153,6 +153,7 @@ ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
   const int32_t* cnt = counts + ((size_t)h * k + c) * Tn;
   const int32_t* st = starts + ((size_t)h * k + c) * Tn;
   const long long rows_total = (long long)B * n;
+  const float old = (tid < D) ? mu[((size_t)h * k + c) * D + tid] : 0.0f;  // loaded early
 
   // exclusive prefix of the per-tile counts over the tiles
   {
@@ -234,7 +235,6 @@ ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
     float sum = 0.0f;
     for (int r = 0; r < RS; ++r) sum += red[r][tid];
     const float mean_j = sum / (float)N;
-    const float old = mu[((size_t)h * k + c) * D + tid];
     vj = decay * old + (1.0f - decay) * mean_j;
   }
   float sq = warp_sum(vj * vj);
@@ -253,8 +253,7 @@ cudaError_t launch_update(const void* qk, int B, int H, int n, int k, const EmaL
                           float* mu, float decay, cudaStream_t s) {
   const size_t smem = (size_t)(L.T + 1) * sizeof(int32_t);
   auto kern = ema_update_kernel<T, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)(smem < 48 * 1024 ? 48 * 1024 : smem));
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)(smem < 48 * 1024 ? 48 * 1024 : smem));
   if (e != cudaSuccess) return e;
   launch_begin(K_EMA_UPDATE, s);
   kern<<<dim3(k, H), THREADS2, smem, s>>>(static_cast<const T*>(qk), B, H, n, k, L.T, L.counts,
@@ -279,8 +278,7 @@ cudaError_t launch_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                        void* ws, cudaStream_t s) {
   EmaLayout L = ema_layout(ws, B, H, n, k);
   const size_t smem1 = (size_t)(WARPS1 + 2) * k * sizeof(int32_t);
-  cudaError_t e = cudaFuncSetAttribute(ema_bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)(smem1 < 48 * 1024 ? 48 * 1024 : smem1));
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(ema_bucket_kernel), (int)(smem1 < 48 * 1024 ? 48 * 1024 : smem1));
   if (e != cudaSuccess) return e;
   launch_begin(K_EMA_BUCKET, s);
   ema_bucket_kernel<<<dim3(L.T, H), TE, smem1, s>>>(assign, B, H, n, k, L.T, L.counts, L.starts,

@@ -140,7 +140,7 @@ cudaError_t launch_t(const void* qk, int BH, int H, int n, const float* mu, int 
                      int32_t* a, int32_t* mcount, cudaStream_t s) {
   const size_t smem = 2 * (size_t)D * PAD * sizeof(float);
   auto kern = score_simt_kernel<T, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((n + TOK - 1) / TOK, BH);
   launch_begin(K_SCORE_SIMT, s);

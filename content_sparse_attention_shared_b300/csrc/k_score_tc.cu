@@ -76,12 +76,87 @@ __device__ __forceinline__ uint32_t pack2_bf16(bf16 a, bf16 b) {
   return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
 }
 
+// Centroid image of one head, as the score kernel holds it in shared memory:
+// three bf16 planes [kpad x D] (no-swizzle K-major core matrices: chunk
+// (c, jc) at jc*kpad*16 + c*16), then the kpad fp32 row sums.
+__host__ __device__ inline size_t prep_image_bytes(int d, int kpad) {
+  return 3 * (size_t)kpad * d * 2 + (size_t)kpad * 4;
+}
+
+// Split centroid row elements into the three bf16 planes and write one
+// 16-byte chunk (8 features of centroid c) of each plane.
+__device__ __forceinline__ void split_store8(uint8_t* planes, size_t plane_bytes, size_t off,
+                                             const float (&m)[8]) {
+  uint32_t ph[4], pm[4], pl[4];
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    bf16 hi[2], md[2], lo[2];
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+      hi[v] = __float2bfloat16_rn(m[e + v]);
+      const float r1 = m[e + v] - __bfloat162float(hi[v]);
+      md[v] = __float2bfloat16_rn(r1);
+      const float r2 = r1 - __bfloat162float(md[v]);
+      lo[v] = __float2bfloat16_rn(r2);
+    }
+    ph[e / 2] = pack2_bf16(hi[0], hi[1]);
+    pm[e / 2] = pack2_bf16(md[0], md[1]);
+    pl[e / 2] = pack2_bf16(lo[0], lo[1]);
+  }
+  *reinterpret_cast<uint4*>(planes + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+  *reinterpret_cast<uint4*>(planes + plane_bytes + off) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
+  *reinterpret_cast<uint4*>(planes + 2 * plane_bytes + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+}
+
+// Builds every head's centroid image once per call (grid: centroid blocks of
+// 32 x heads), so each score CTA fetches it with bulk copies instead of
+// converting the centroids itself.  Row sums: one warp per centroid row,
+// fixed shuffle order.
 template <int D>
+__global__ void __launch_bounds__(256)
+centroid_prep_kernel(const float* __restrict__ mu, int k, int kpad, uint8_t* __restrict__ image) {
+  const int h = blockIdx.y, c0 = blockIdx.x * 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const size_t plane_bytes = (size_t)kpad * D * 2;
+  uint8_t* img = image + (size_t)h * prep_image_bytes(D, kpad);
+  const float* mu_h = mu + (size_t)h * k * D;
+  for (int it = tid; it < 32 * (D / 8); it += 256) {
+    const int c = c0 + (it & 31), jc = it >> 5;
+    if (c >= kpad) continue;
+    float m[8];
+    if (c < k) {
+      const float4* src = reinterpret_cast<const float4*>(mu_h + (size_t)c * D + jc * 8);
+      const float4 a = __ldg(src), b = __ldg(src + 1);
+      m[0] = a.x; m[1] = a.y; m[2] = a.z; m[3] = a.w;
+      m[4] = b.x; m[5] = b.y; m[6] = b.z; m[7] = b.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m[e] = 0.0f;
+    }
+    split_store8(img, plane_bytes, (size_t)jc * (kpad * 16) + (size_t)c * 16, m);
+  }
+  float* sums = reinterpret_cast<float*>(img + 3 * plane_bytes);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int c = c0 + warp * 4 + u;
+    float v = 0.0f;
+    if (c < k) {
+      const float* r = mu_h + (size_t)c * D + lane * (D / 32);
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) v += __ldg(r + e);
+    }
+    v = warp_sum(v);
+    if (lane == 0 && c < kpad) sums[c] = v;
+  }
+}
+
+template <int D, bool PREP>
 __global__ void __launch_bounds__(THREADS, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
-                const float* __restrict__ mu, int k, int kpad, int acc_cols, int stages,
-                int ctas_per_head, float* __restrict__ S, int32_t* __restrict__ assign,
-                int32_t* __restrict__ mcount, unsigned int* __restrict__ err) {
+                const float* __restrict__ mu, const uint8_t* __restrict__ image, int k, int kpad,
+                int acc_cols, int stages, int ctas_per_head, float* __restrict__ S,
+                int32_t* __restrict__ assign, int32_t* __restrict__ mcount,
+                unsigned int* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -92,7 +167,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
   uint8_t* Bs = As + (size_t)stages * A_BYTES;       // 3 planes x [kpad x D] K-major
   float* sumu = reinterpret_cast<float*>(Bs + 3 * (size_t)plane_bytes);  // [kpad]
 
-  __shared__ uint64_t full_bar[4], empty_bar[4], accf_bar[2], acce_bar[2];
+  __shared__ uint64_t full_bar[4], empty_bar[4], accf_bar[2], acce_bar[2], prep_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int stop_flag;
 
@@ -112,8 +187,19 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
       tc::mbar_init(&accf_bar[i], 1);
       tc::mbar_init(&acce_bar[i], 4);
     }
+    tc::mbar_init(&prep_bar, 1);
     stop_flag = 0;
     tc::fence_mbar_init();
+    if (PREP) {
+      // the head's centroid image, in bulk copies of at most 32 KiB
+      const uint32_t total = (uint32_t)prep_image_bytes(D, kpad);
+      const uint8_t* src = image + (size_t)h * total;
+      tc::mbar_arrive_expect_tx(&prep_bar, total);
+      for (uint32_t off = 0; off < total; off += 32768u) {
+        const uint32_t bytes = min(32768u, total - off);
+        tc::bulk_g2s(Bs + off, src + off, bytes, &prep_bar);
+      }
+    }
     // the first `stages` tiles need no free slot: issue them now
     int i = 0;
     for (int tile = first; tile < ntiles && i < stages; tile += stride, ++i) {
@@ -127,12 +213,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
     }
   }
 
-  // ---- centroid planes for head h (all threads) ---------------------------
-  // item (c, jc): 8 consecutive features of centroid c, split into three bf16
-  // planes and written as one 16-byte chunk per plane at jc*kpad*16 + c*16
-  // (consecutive threads take consecutive c: conflict-free).  Four items per
-  // thread are loaded before any is converted.
-  {
+  if (!PREP) {
+    // ---- centroid planes for head h, built here (all threads) -------------
+    // item (c, jc): 8 consecutive features of centroid c; consecutive threads
+    // take consecutive c (conflict-free 16-byte stores).  Four items per
+    // thread are loaded before any is converted.
     const float* mu_h = mu + (size_t)h * k * D;
     const int items = kpad * (D / 8);
     constexpr int U = 4;
@@ -157,27 +242,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
         const int it = it0 + u * THREADS;
         if (it >= items) break;
         const int c = it % kpad, jc = it / kpad;
-        uint32_t ph[4], pm[4], pl[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          bf16 hi[2], md[2], lo[2];
-#pragma unroll
-          for (int v = 0; v < 2; ++v) {
-            hi[v] = __float2bfloat16_rn(m[u][e + v]);
-            const float r1 = m[u][e + v] - __bfloat162float(hi[v]);
-            md[v] = __float2bfloat16_rn(r1);
-            const float r2 = r1 - __bfloat162float(md[v]);
-            lo[v] = __float2bfloat16_rn(r2);
-          }
-          ph[e / 2] = pack2_bf16(hi[0], hi[1]);
-          pm[e / 2] = pack2_bf16(md[0], md[1]);
-          pl[e / 2] = pack2_bf16(lo[0], lo[1]);
-        }
-        const size_t off = (size_t)jc * (kpad * 16) + (size_t)c * 16;
-        *reinterpret_cast<uint4*>(Bs + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-        *reinterpret_cast<uint4*>(Bs + plane_bytes + off) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
-        *reinterpret_cast<uint4*>(Bs + 2 * (size_t)plane_bytes + off) =
-            make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        split_store8(Bs, (size_t)plane_bytes, (size_t)jc * (kpad * 16) + (size_t)c * 16, m[u]);
       }
     }
     // row sums of the fp32 centroids: one warp per row (fixed shuffle
@@ -191,9 +256,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
         const int c = c0 + u * NW;
         v[u] = 0.0f;
         if (c < k) {
-          const float* row = mu_h + (size_t)c * D + lane * (D / 32);
+          const float* r = mu_h + (size_t)c * D + lane * (D / 32);
 #pragma unroll
-          for (int e = 0; e < D / 32; ++e) v[u] += __ldg(row + e);
+          for (int e = 0; e < D / 32; ++e) v[u] += __ldg(r + e);
         }
       }
 #pragma unroll
@@ -239,6 +304,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
   } else if (warp == 1) {
     // ===================== MMA issuer =======================================
     if (lane == 0) {
+      if (PREP && !tc::mbar_wait_bounded(&prep_bar, 0, WAIT_LIMIT_NS)) {
+        set_timeout(err);
+        stop_flag = 1;
+      }
       const uint32_t idesc = tc::idesc_f16(ROWS, kpad, true, false, false);
       const uint32_t lbo_b = kpad * 16;
       int i = 0;
@@ -278,6 +347,15 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
     const int quad = warp & 3;               // TMEM lane quadrant this warp may read
     const int row = 32 * quad + lane;        // tile row == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+    if (PREP) {
+      // the row sums arrive with the bulk copies
+      bool okp = tc::mbar_wait_bounded(&prep_bar, 0, WAIT_LIMIT_NS);
+      okp = __all_sync(0xffffffffu, okp);
+      if (!okp) {
+        if (lane == 0) set_timeout(err);
+        stop_flag = 1;
+      }
+    }
     int i = grp;
     for (int tile = first + grp * stride; tile < ntiles; tile += 2 * stride, i += 2) {
       const int s = i % stages;
@@ -435,6 +513,47 @@ EncodeTiledFn encode_fn() {
 // swizzle atoms), the three centroid planes, the centroid row sums; as many
 // A stages (up to 4) as fit beside the planes.  Static shared memory (the
 // barriers) takes well under 256 bytes.
+// Tensor map of Q viewed as [rows, D] bf16 with 64-element x 128-row boxes,
+// 128-byte swizzle.  Encoding is host work; the last few maps are kept
+// (keyed by base pointer and shape) so repeated calls on the same tensors
+// skip it.
+bool q_tensor_map(const void* qk, unsigned long long rows, int D, CUtensorMap* out) {
+  struct Entry {
+    const void* ptr;
+    unsigned long long rows;
+    int D;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry cache[8];
+  static int used = 0, next = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].ptr == qk && cache[i].rows == rows && cache[i].D == D) {
+        *out = cache[i].map;
+        return true;
+      }
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BOX_K, (cuuint32_t)ROWS};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qk), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  cache[next] = Entry{qk, rows, D, map};
+  next = (next + 1) % 8;
+  if (used < 8) ++used;
+  *out = map;
+  return true;
+}
+
 bool plan(int d, int k, ScoreCfg& c) {
   c.D = d;
   c.kpad = (k + 15) / 16 * 16;
@@ -454,29 +573,30 @@ bool plan(int d, int k, ScoreCfg& c) {
 
 template <int D>
 cudaError_t launch_t(const ScoreCfg& c, const void* qk, int B, int H, int n, const float* mu,
-                     int k, float* S, int32_t* a, int32_t* mcount, unsigned int* err,
-                     cudaStream_t s) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
+                     int k, float* S, int32_t* a, int32_t* mcount, void* prep,
+                     unsigned int* err, cudaStream_t s) {
   CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)B * H * n};
-  const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)BOX_K, (cuuint32_t)ROWS};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qk), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  auto kern = score_tc_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
+  if (!q_tensor_map(qk, (unsigned long long)B * H * n, D, &map)) return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (prep != nullptr) {
+    launch_begin(K_CENTROID_PREP, s);
+    centroid_prep_kernel<D><<<dim3((c.kpad + 31) / 32, H), 256, 0, s>>>(
+        mu, k, c.kpad, static_cast<uint8_t*>(prep));
+    e = cudaGetLastError();
+    launch_end(K_CENTROID_PREP, s);
+    if (e != cudaSuccess) return e;
+  }
+  auto kern = prep != nullptr ? score_tc_kernel<D, true> : score_tc_kernel<D, false>;
+  e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)c.smem);
   if (e != cudaSuccess) return e;
   const int tiles_per_head = B * ((n + ROWS - 1) / ROWS);
   int cph = 148 / H;
   if (cph < 1) cph = 1;
   if (cph > tiles_per_head) cph = tiles_per_head;
   launch_begin(K_SCORE_TC, s);
-  kern<<<dim3(cph, H), THREADS, c.smem, s>>>(map, B, H, n, mu, k, c.kpad, c.acc_cols, c.stages,
-                                             cph, S, a, mcount, err);
+  kern<<<dim3(cph, H), THREADS, c.smem, s>>>(map, B, H, n, mu,
+                                             static_cast<const uint8_t*>(prep), k, c.kpad,
+                                             c.acc_cols, c.stages, cph, S, a, mcount, err);
   e = cudaGetLastError();
   launch_end(K_SCORE_TC, s);
   return e;
@@ -489,14 +609,20 @@ bool score_tc_supported(rt_dtype dt, int d, int k) {
   return dt == RT_BF16 && (d == 64 || d == 128) && plan(d, k, c) && encode_fn() != nullptr;
 }
 
+size_t score_prep_bytes(int H, int d, int k) {
+  ScoreCfg c;
+  if (!plan(d, k, c)) return 0;
+  return (size_t)H * prep_image_bytes(d, c.kpad);
+}
+
 cudaError_t launch_score(const void* qk, rt_dtype dt, int B, int H, int n, int d, const float* mu,
-                         int k, float* S, int32_t* a, int32_t* mcount, unsigned int* err,
-                         cudaStream_t s) {
+                         int k, float* S, int32_t* a, int32_t* mcount, void* prep,
+                         unsigned int* err, cudaStream_t s) {
   ScoreCfg c;
   if (dt == RT_BF16 && (d == 64 || d == 128) && plan(d, k, c) && encode_fn() != nullptr &&
       (reinterpret_cast<uintptr_t>(qk) & 15u) == 0) {
-    return d == 64 ? launch_t<64>(c, qk, B, H, n, mu, k, S, a, mcount, err, s)
-                   : launch_t<128>(c, qk, B, H, n, mu, k, S, a, mcount, err, s);
+    return d == 64 ? launch_t<64>(c, qk, B, H, n, mu, k, S, a, mcount, prep, err, s)
+                   : launch_t<128>(c, qk, B, H, n, mu, k, S, a, mcount, prep, err, s);
   }
   return launch_score_simt(qk, dt, B * H, H, n, d, mu, k, S, a, mcount, s);
 }

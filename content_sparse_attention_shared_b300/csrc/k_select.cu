@@ -58,7 +58,7 @@ struct SelectOut {
     out[o] = t;
     if (mcount != nullptr) {
       const int prev = atomicAdd(&mcount[(size_t)bh * n + t], 1);
-      if (slots != nullptr && prev < SLOTS_PER_ROW)
+      if (slots != nullptr && (unsigned)prev < (unsigned)SLOTS_PER_ROW)
         slots[((size_t)bh * n + t) * SLOTS_PER_ROW + prev] = c * w + o;
     }
   }
@@ -322,6 +322,163 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
   }
 }
 
+// ---------------------------------------------------------------------------
+// Rows of n <= THREADS * 32 scores, n a multiple of 4.  Warp j owns the
+// contiguous segment [j*seg, (j+1)*seg) (seg a multiple of 128), in chunks of
+// 128 positions; lane l owns positions 4l..4l+3 of every chunk, so every load
+// is a coalesced float4 (512 bytes per warp), four in flight per thread.
+// The w-th largest of the per-thread maxima is a lower bound on the w-th
+// largest score (the w threads holding the largest maxima own w distinct
+// scores at least that large), so every kept score lies in a bin at or above
+// the bin b_L of that maximum.  Only the scores of bin >= b_L (typically a few
+// more than w) become candidates.  Each candidate's rank by (score desc,
+// position asc) decides whether it is kept; each kept candidate's rank by
+// position among the kept ones is its output slot.  No per-score atomics,
+// no bitmap and no ordered compaction pass.  Rows where the bound leaves more
+// than RCAP candidates (many equal scores), or with fewer than w non-empty
+// threads, use the exact radix select.
+// ---------------------------------------------------------------------------
+constexpr int CHUNKS_MAX = 8;  // 128-position chunks per warp
+constexpr int BOUND_N_MAX = THREADS * 4 * CHUNKS_MAX;
+constexpr int RCAP = 1024;
+
+__global__ void __launch_bounds__(THREADS, 7)
+select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
+                         int32_t* __restrict__ idx, int32_t* __restrict__ mcount,
+                         int32_t* __restrict__ slots) {
+  __shared__ unsigned hist[NBINS];
+  __shared__ int cand_t[RCAP];
+  __shared__ float cand_s[RCAP];
+  __shared__ unsigned char cand_keep[RCAP];
+  __shared__ int wsum[4 * WARPS];
+  __shared__ int s_bl, s_ncand;
+
+  const int c = blockIdx.x;
+  const int bh = blockIdx.y;
+  const float* row = S + ((size_t)bh * k + c) * n;
+  const float4* row4 = reinterpret_cast<const float4*>(row);
+  const SelectOut so{idx + ((size_t)bh * k + c) * w, mcount, slots, bh, c, n, w};
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int seg = ((n + WARPS * 128 - 1) / (WARPS * 128)) * 128;  // <= 128 * CHUNKS_MAX
+  const int w0 = warp * seg + 4 * lane;                           // first position of this thread
+
+  for (int b = tid; b < NBINS; b += THREADS) hist[b] = 0u;
+  if (tid == 0) {
+    s_ncand = 0;
+    s_bl = -1;
+  }
+
+  // 1. per-thread maximum
+  float m = -INFINITY;
+#pragma unroll
+  for (int i0 = 0; i0 < CHUNKS_MAX; i0 += 4) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u;
+      const int p = w0 + 128 * i;
+      v[u] = (128 * i < seg && p < n) ? __ldg(row4 + (p >> 2))
+                                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) m = fmaxf(m, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
+  }
+  __syncthreads();  // hist cleared
+  if (w0 < n) atomicAdd(&hist[score_bin(m)], 1u);
+  __syncthreads();
+
+  // 2. bin of the w-th largest maximum (descending scan over the bins)
+  {
+    const int hi_bin = NBINS - 1 - BINS_PER_THREAD * tid;
+    unsigned hb[BINS_PER_THREAD];
+    int lsum = 0;
+#pragma unroll
+    for (int q = 0; q < BINS_PER_THREAD; ++q) {
+      hb[q] = hist[hi_bin - q];
+      lsum += (int)hb[q];
+    }
+    int total;
+    const int excl = block_exclusive_scan<THREADS>(lsum, wsum, total);
+    if (excl < w && w <= excl + lsum) {
+      int cum = excl;
+#pragma unroll
+      for (int q = 0; q < BINS_PER_THREAD; ++q) {
+        if (cum < w && cum + (int)hb[q] >= w) s_bl = hi_bin - q;
+        cum += (int)hb[q];
+      }
+    }
+  }
+  __syncthreads();
+  const int bl = s_bl;  // -1: fewer than w threads hold scores
+
+  // 3. candidates: scores of bin >= b_L.  A float compare against a value a
+  //    little below the bin's lower edge filters first; the bin itself is
+  //    only computed for the few scores that pass.
+  if (bl >= 0) {
+    const float pre = bl > 0 ? (float)bl * (1.0f / 1024.0f) - 1.0f - 1.0e-5f : -INFINITY;
+    uint32_t cmask = 0u;
+#pragma unroll
+    for (int i0 = 0; i0 < CHUNKS_MAX; i0 += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u;
+        const int p = w0 + 128 * i;
+        v[u] = (128 * i < seg && p < n) ? __ldg(row4 + (p >> 2))
+                                        : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (e4[e] >= pre && score_bin(e4[e]) >= bl) cmask |= 1u << (4 * (i0 + u) + e);
+      }
+    }
+    if (cmask != 0u) {
+      int slot = atomicAdd(&s_ncand, __popc(cmask));
+      while (cmask) {
+        const int bit = __ffs(cmask) - 1;
+        cmask &= cmask - 1;
+        const int p = w0 + 128 * (bit >> 2) + (bit & 3);
+        if (slot < RCAP) {
+          cand_t[slot] = p;
+          cand_s[slot] = __ldg(row + p);
+        }
+        ++slot;
+      }
+    }
+  }
+  __syncthreads();
+  const int nc = s_ncand;
+  if (bl < 0 || nc > RCAP) {
+    radix_select_row(row, n, w, so, hist, wsum);  // uniform branch
+    return;
+  }
+
+  // 4. kept: rank by (score desc, position asc) below w
+  for (int i = tid; i < nc; i += THREADS) {
+    const float si = cand_s[i];
+    const int ti = cand_t[i];
+    int rank = 0;
+    for (int j = 0; j < nc; ++j) {
+      const float sj = cand_s[j];
+      rank += (sj > si) | ((sj == si) & (cand_t[j] < ti));
+    }
+    cand_keep[i] = rank < w ? 1 : 0;
+  }
+  __syncthreads();
+
+  // 5. a kept candidate's output slot is its rank by position among the kept
+  for (int i = tid; i < nc; i += THREADS) {
+    if (!cand_keep[i]) continue;
+    const int ti = cand_t[i];
+    int o = 0;
+    for (int j = 0; j < nc; ++j) o += cand_keep[j] & (cand_t[j] < ti);
+    if (o < w) so.emit(o, ti);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* idx,
@@ -333,10 +490,15 @@ cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* 
     return (size_t)((nn + 7) & ~7) * sizeof(uint16_t) + 2 * (size_t)((nn + 31) / 32) * 4;
   };
   const size_t smem = staged ? stage_bytes(n) : 0;
-  cudaError_t e = cudaFuncSetAttribute(select_topw_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)stage_bytes(MAX_STAGED_BINS));
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(select_topw_kernel), (int)stage_bytes(MAX_STAGED_BINS));
   if (e != cudaSuccess) return e;
+  if (n <= BOUND_N_MAX && (n & 3) == 0 && w <= THREADS) {
+    launch_begin(K_SELECT, s);
+    select_topw_bound_kernel<<<grid, THREADS, 0, s>>>(S, n, k, w, idx, mcount, slots);
+    e = cudaGetLastError();
+    launch_end(K_SELECT, s);
+    return e;
+  }
   launch_begin(K_SELECT, s);
   select_topw_kernel<<<grid, THREADS, smem, s>>>(S, n, k, w, idx, mcount, slots, staged);
   e = cudaGetLastError();

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -49,12 +50,31 @@ void launch_end(int kind, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------
+// dynamic shared-memory limits, set once per (kernel, device)
+// ---------------------------------------------------------------------------
+static std::mutex g_attr_mu;
+static std::map<std::pair<const void*, int>, int> g_attr_set;
+
+cudaError_t set_smem_limit(const void* func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  auto key = std::make_pair(func, dev);
+  auto it = g_attr_set.find(key);
+  if (it != g_attr_set.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) g_attr_set[key] = bytes;
+  return e;
+}
+
+// ---------------------------------------------------------------------------
 // workspace layout
 // ---------------------------------------------------------------------------
 static inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct FwdLayout {
-  size_t err, S, mcount, slots, idx, assign, yslot, total;
+  size_t err, S, mcount, slots, idx, assign, yslot, prep, total;
 };
 
 static FwdLayout fwd_layout(int B, int H, int n, int d, int k, int w) {
@@ -68,6 +88,7 @@ static FwdLayout fwd_layout(int B, int H, int n, int d, int k, int w) {
   L.idx = off; off += align256(BH * k * w * sizeof(int32_t));
   L.assign = off; off += align256(BH * n * sizeof(int32_t));
   L.yslot = off; off += align256(BH * k * w * d * sizeof(float));
+  L.prep = off; off += align256(score_prep_bytes(H, d, k));
   L.total = off;
   return L;
 }
@@ -187,7 +208,8 @@ rt_status rt_route_assign(const void* qk, rt_dtype dt, int B, int H, int n, int 
   const int BH = B * H;
   float* S = scores ? scores : reinterpret_cast<float*>(ws + L.S);
   unsigned int* err = reinterpret_cast<unsigned int*>(ws + L.err);
-  st = from_cuda(launch_score(qk, dt, B, H, n, d, centroids, k, S, assign, nullptr, err, s),
+  void* prep = score_prep_bytes(H, d, k) ? static_cast<void*>(ws + L.prep) : nullptr;
+  st = from_cuda(launch_score(qk, dt, B, H, n, d, centroids, k, S, assign, nullptr, prep, err, s),
                  "score kernel");
   if (st != RT_OK) return st;
   st = from_cuda(launch_select(S, BH, n, k, w, idx, nullptr, nullptr, s), "select kernel");
@@ -225,7 +247,8 @@ rt_status rt_routing_attention(const void* q, const void* kp, const void* v, rt_
   float* yslot = reinterpret_cast<float*>(ws + L.yslot);
 
   unsigned int* err = reinterpret_cast<unsigned int*>(ws + L.err);
-  st = from_cuda(launch_score(q, dt, B, H, n, d, centroids, kc, S, assign_out, mcount, err, s),
+  void* prep = score_prep_bytes(H, d, kc) ? static_cast<void*>(ws + L.prep) : nullptr;
+  st = from_cuda(launch_score(q, dt, B, H, n, d, centroids, kc, S, assign_out, mcount, prep, err, s),
                  "score kernel");
   if (st != RT_OK) return st;
   int32_t* slots = reinterpret_cast<int32_t*>(ws + L.slots);

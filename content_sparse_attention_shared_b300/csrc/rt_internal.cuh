@@ -31,6 +31,12 @@ enum KernelId {
 rt_status record_error(rt_status s, const char* msg);
 rt_status validate_shape(rt_dtype dt, int B, int H, int n, int d, int k, int w);
 
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device.  The attribute call is made only the first time a kernel
+// needs more than it was given before on that device, so launches pay a map
+// lookup instead of a driver call.
+cudaError_t set_smem_limit(const void* func, int bytes);
+
 // Called by every launcher around its launch.
 void launch_begin(int kind, cudaStream_t s);
 void launch_end(int kind, cudaStream_t s);
@@ -112,12 +118,15 @@ cudaError_t launch_score_simt(const void* qk, rt_dtype dt, int BH, int H, int n,
                               int32_t* mcount, cudaStream_t s);
 
 // dispatcher: tcgen05 scoring for bf16 with k <= 256 (fp32-accurate via a
-// three-plane split of the centroids), the SIMT kernel otherwise.  err: device
-// error word (may be null).
+// three-plane split of the centroids), the SIMT kernel otherwise.  prep: device
+// scratch of score_prep_bytes(H, d, k) bytes for the per-head centroid image
+// (null: every score CTA builds the image itself).  err: device error word
+// (may be null).
 bool score_tc_supported(rt_dtype dt, int d, int k);
+size_t score_prep_bytes(int H, int d, int k);
 cudaError_t launch_score(const void* qk, rt_dtype dt, int B, int H, int n, int d, const float* mu,
-                         int k, float* S, int32_t* a, int32_t* mcount, unsigned int* err,
-                         cudaStream_t s);
+                         int k, float* S, int32_t* a, int32_t* mcount, void* prep,
+                         unsigned int* err, cudaStream_t s);
 
 // top-w per centroid in ascending position order; counts memberships into
 // mcount (atomic integer increments; may be null) and records up to
