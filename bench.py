@@ -74,6 +74,9 @@ def kernel_work(name, wl):
         return dict(bytes=BH * n * 4 * 2, flops=0.0)
     if name == "ema_update":
         return dict(bytes=BH * n * d * s + wl.H * k * d * 8, flops=3.0 * BH * n * d)
+    if name == "centroid_prep":
+        kpad = (k + 15) // 16 * 16
+        return dict(bytes=wl.H * k * d * 4 + wl.H * (3 * kpad * d * 2 + kpad * 4), flops=0.0)
     return dict(bytes=0, flops=0.0)
 
 
@@ -85,12 +88,14 @@ def alu_peak_tflops(sm_mhz):
 KERNEL_BOUND = {
     "score_simt": "alu", "attention_simt": "alu", "score_tc": "hbm", "attention_tc": "hbm",
     "select_topw": "hbm", "scatter_average": "hbm", "ema_bucket": "hbm", "ema_update": "hbm",
+    "centroid_prep": "hbm",
 }
 
 KERNEL_SOURCES = {
     "score_simt": "k_score_simt.cu", "score_tc": "k_score_tc.cu", "select_topw": "k_select.cu",
     "attention_simt": "k_attention_simt.cu", "attention_tc": "k_attention_tc.cu",
     "scatter_average": "k_scatter.cu", "ema_bucket": "k_ema.cu", "ema_update": "k_ema.cu",
+    "centroid_prep": "k_score_tc.cu",
 }
 
 
