@@ -1,0 +1,402 @@
+// In-cluster causal softmax attention, persistent and pipelined, for clusters
+// of w <= 128 members (the packed case: floor(128 / w) clusters per 128-row
+// tile), bf16 inputs, fp32 accumulation on tcgen05 tensor cores.
+//
+// "Efficient Content-Based Sparse Attention with Routing Transformers":
+// §3 (softmax attention, autoregressive masking) restricted by §4 to the
+// query/key pairs of one cluster.  Members of a cluster are listed in
+// ascending position order, so the causal mask on original positions is the
+// lower triangle in slot order (diagonal included).  Queries double as keys
+// (shared QK), so the keys of a tile are its own rows: one S = Q Q^T MMA
+// covers every cluster of the tile, masked block-diagonally.
+//
+// One CTA per SM walks the tiles first, first + grid, ...  Warp roles:
+//   warps 0-3   producers: read the tile's member positions and membership
+//               counts, gather the Q and V rows with 16-byte cp.async into a
+//               ring of NS stages (no-swizzle core-matrix layouts), and mark a
+//               stage full once their copies have landed;
+//   warp 12     issues the MMAs: S = Q Q^T into the TMEM accumulator of the
+//               tile's group, then O = P V into the same columns;
+//   warps 4-7,  two softmax/epilogue groups taking alternate tiles: softmax of
+//   warps 8-11  their rows from TMEM (only the 16-column chunks holding a valid
+//               key of some row of the warp), P (bf16) into the stage's Q
+//               space, then the O rows, staged in the stage's shared memory and
+//               written row-contiguously: bf16 to `out` for a position in one
+//               cluster, fp32 to its slot row in `yslot` otherwise.
+// So the gathers of the next tiles overlap the softmax, MMAs and stores of
+// the current ones, and every SM stays busy until the last tile.  Every
+// mbarrier wait is bounded; a wait that runs out sets the device error word
+// and the CTA winds down.
+#include "attn_common.cuh"
+
+namespace rt {
+namespace {
+
+using namespace attn;
+constexpr int PTHREADS = 416;  // 13 warps
+constexpr int MMA_WARP = 12;
+constexpr uint64_t WAIT_LIMIT_NS = 200ull * 1000 * 1000;  // 0.2 s
+
+template <int D>
+struct PipeSmem {
+  static constexpr int QB = ROWS * D * 2;     // Q tile (bf16)
+  static constexpr int PB = ROWS * ROWS * 2;  // P tile (bf16), written over Q
+  static constexpr int XB = QB > PB ? QB : PB;
+  static constexpr int STAGE = XB + QB;       // + V tile; also holds the fp32 O rows
+  static constexpr int NS = D == 128 ? 3 : 4;
+  static constexpr int BYTES = NS * STAGE;
+  static_assert(STAGE >= ROWS * D * 4, "a stage must hold the fp32 output rows");
+};
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void producer_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");  // warps 0-3 only
+}
+
+template <int D>
+__global__ void __launch_bounds__(PTHREADS, 1)
+attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int n, int k, int w,
+                      int g, int tiles_per_bh, int ntiles, int causal, float scale_log2,
+                      const int32_t* __restrict__ idx, const int32_t* __restrict__ mcount,
+                      bf16* __restrict__ out, float* __restrict__ yslot,
+                      unsigned int* __restrict__ err) {
+  using L = PipeSmem<D>;
+  constexpr int NS = L::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t full_bar[NS], empty_bar[NS];
+  __shared__ uint64_t sfull_bar[2], pfull_bar[2], ofull_bar[2], tfree_bar[2];
+  __shared__ int pos_s[NS][ROWS];    // member position per tile row (-1: padding)
+  __shared__ int m_s[NS][ROWS];      // its membership count
+  __shared__ int cl_s[NS][ROWS];     // its cluster
+  __shared__ int bh_s[NS];           // the tile's batch*head
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int stop_flag, prod_abort;
+
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int first = blockIdx.x, stride = gridDim.x;
+  const int T = (ntiles > first) ? (ntiles - first + stride - 1) / stride : 0;  // my tiles
+
+  if (warp == MMA_WARP) {
+    tc::tmem_alloc(&tmem_base_sh, 256);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      tc::mbar_init(&full_bar[i], 128);  // every producer thread, once its copies landed
+      tc::mbar_init(&empty_bar[i], 4);   // the four warps of the consuming group
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sfull_bar[i], 1);
+      tc::mbar_init(&pfull_bar[i], 4);
+      tc::mbar_init(&ofull_bar[i], 1);
+      tc::mbar_init(&tfree_bar[i], 4);
+    }
+    stop_flag = 0;
+    prod_abort = 0;
+    tc::fence_mbar_init();
+  }
+  tc::tc_fence_before_sync();
+  __syncthreads();
+  tc::tc_fence_after_sync();
+  const uint32_t tmem = tmem_base_sh;
+  pdl_wait();  // the set-up above overlapped the previous kernel's tail
+
+  auto fail = [&](bool leader) {
+    if (leader) atomicExch(err, (unsigned)DEV_TIMEOUT);
+    stop_flag = 1;
+  };
+
+  if (warp < 4) {
+    // ======================= producers (128 threads) =======================
+    const int r = tid;  // tile row
+    // the row's position and membership count for tile `tile`
+    auto load_meta = [&](int tile, int& p, int& m, int& cluster) {
+      const int bh = tile / tiles_per_bh, lt = tile - bh * tiles_per_bh;
+      const int ci = r / w;
+      cluster = lt * g + ci;
+      p = -1;
+      m = 0;
+      if (ci < g && cluster < k) {
+        p = __ldcg(idx + ((size_t)bh * k + cluster) * w + (r - ci * w));
+        if ((unsigned)p >= (unsigned)n) p = -1;  // defensive
+        else m = __ldcg(mcount + (size_t)bh * n + p);
+      }
+    };
+    int np = -1, nm = 0, ncl = 0;
+    if (T > 0) load_meta(first, np, nm, ncl);
+    for (int i = 0; i < T; ++i) {
+      const int tile = first + i * stride;
+      const int s = i % NS;
+      const uint32_t use = (uint32_t)(i / NS);
+      // the four producer warps agree on giving up (prod_abort has no other
+      // writer), so the named barriers below are always reached by all
+      if (!tc::mbar_wait_bounded(&empty_bar[s], (use & 1u) ^ 1u, WAIT_LIMIT_NS) ||
+          *(volatile int*)&stop_flag)
+        prod_abort = 1;
+      producer_sync();
+      if (*(volatile int*)&prod_abort) { fail(r == 0); break; }
+      const int bh = tile / tiles_per_bh;
+      pos_s[s][r] = np;
+      m_s[s][r] = nm;
+      cl_s[s][r] = ncl;
+      if (r == 0) bh_s[s] = bh;
+      producer_sync();  // the stage's positions are visible to the four warps
+      const bf16* q_bh = q + (size_t)bh * n * D;
+      const bf16* v_bh = v + (size_t)bh * n * D;
+      uint8_t* st = sm + (size_t)s * L::STAGE;
+      gather_kmajor<D>(st, q_bh, pos_s[s], warp, 4);
+      gather_mnmajor<D>(st + L::XB, v_bh, pos_s[s], warp, 4);
+      cp_async_commit();
+      if (i + 1 < T) load_meta(tile + stride, np, nm, ncl);  // next tile, while copies fly
+      cp_async_wait_all();           // this thread's copies have landed
+      tc::fence_proxy_async_smem();  // ... and are visible to the MMA
+      mbar_arrive(&full_bar[s]);     // the stage is full once all 128 arrived
+    }
+  } else if (warp == MMA_WARP) {
+    // ======================= MMA issuer (one thread) =======================
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = tc::idesc_f16(ROWS, ROWS, true, false, false);
+      constexpr uint32_t IDESC_O = tc::idesc_f16(ROWS, D, true, false, true);
+      constexpr uint32_t SBO_QK = (D / 8) * 128;
+      // S(j) needs tile j's rows and a free accumulator; O(j) needs P(j).
+      // Whichever is ready is issued, so O(j) never waits behind the data
+      // of tile j + 1.
+      auto ready_s = [&](int j) {
+        const int s = j % NS, a = j & 1;
+        const uint32_t use_s = (uint32_t)(j / NS), use_a = (uint32_t)(j >> 1);
+        return tc::mbar_test_wait(&full_bar[s], use_s & 1u) &&
+               tc::mbar_test_wait(&tfree_bar[a], (use_a & 1u) ^ 1u);
+      };
+      auto issue_s = [&](int j) {
+        const int s = j % NS, a = j & 1;
+        tc::tc_fence_after_sync();
+        const uint32_t qa = tc::smem_u32(sm + (size_t)s * L::STAGE);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = tc::smem_desc_noswizzle(qa + kk * 256, 128, SBO_QK);
+          tc::mma_f16_ss(tmem + a * 128, ad, ad, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&sfull_bar[a]);
+      };
+      auto ready_o = [&](int j) {
+        return tc::mbar_test_wait(&pfull_bar[j & 1], (uint32_t)(j >> 1) & 1u);
+      };
+      auto issue_o = [&](int j) {
+        const int s = j % NS, a = j & 1;
+        tc::tc_fence_after_sync();
+        const uint32_t pa = tc::smem_u32(sm + (size_t)s * L::STAGE);
+        const uint32_t va = pa + L::XB;
+#pragma unroll
+        for (int kk = 0; kk < ROWS / 16; ++kk) {
+          const uint64_t ad = tc::smem_desc_noswizzle(pa + kk * 256, 128, 2048);
+          const uint64_t bd = tc::smem_desc_noswizzle(va + kk * 256, 128, 2048);
+          tc::mma_f16_ss(tmem + a * 128, ad, bd, IDESC_O, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&ofull_bar[a]);
+      };
+      bool ok = true;
+      int js = 0, jo = 0;
+      uint64_t t_last = tc::globaltimer_ns();
+      while (jo < T) {
+        bool progress = false;
+        if (js < T && ready_s(js)) {
+          issue_s(js++);
+          progress = true;
+        }
+        if (jo < js && ready_o(jo)) {
+          issue_o(jo++);
+          progress = true;
+        }
+        if (progress) {
+          t_last = tc::globaltimer_ns();
+        } else if (*(volatile int*)&stop_flag || tc::globaltimer_ns() - t_last > WAIT_LIMIT_NS) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) fail(true);
+    }
+  } else {
+    // =============== softmax / epilogue groups (warps 4-7, 8-11) ============
+    const int grp = (warp - 4) >> 2;
+    const int quad = warp & 3;
+    const int r = 32 * quad + lane;  // tile row == TMEM lane
+    const uint32_t t_row = tmem + grp * 128 + ((uint32_t)(32 * quad) << 16);
+    const int ci = r / w;
+    const int row_lo = ci * w, row_hi = row_lo + w;
+    constexpr int CPR = D / 4;     // 16-byte fp32 chunks per output row
+    constexpr int RPI = 32 / CPR;  // rows per warp instruction in the copy-out
+    for (int j = grp; j < T; j += 2) {
+      const int s = j % NS;
+      const uint32_t use_s = (uint32_t)(j / NS), use_a = (uint32_t)(j >> 1);
+      // S is ready; the stage's row data is then complete as well (the MMA
+      // waited for it) and cannot change before this group releases it.
+      bool ok = tc::mbar_wait_bounded(&sfull_bar[grp], use_a & 1u, WAIT_LIMIT_NS) &&
+                tc::mbar_wait_bounded(&full_bar[s], use_s & 1u, WAIT_LIMIT_NS) &&
+                !*(volatile int*)&stop_flag;
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) { fail(lane == 0); break; }
+      tc::tc_fence_after_sync();
+      const int my_pos = pos_s[s][r];
+      const bool row_valid = my_pos >= 0;
+      uint8_t* st = sm + (size_t)s * L::STAGE;
+
+      // ---- softmax of this row over its cluster's keys ---------------------
+      int jmin = row_lo, jmax = causal ? r + 1 : row_hi;
+      if (!row_valid || jmax <= jmin) { jmin = ROWS; jmax = 0; }
+      const int wlo = __reduce_min_sync(0xffffffffu, jmin);
+      const int whi = __reduce_max_sync(0xffffffffu, jmax);
+      const int ch_lo = (whi > wlo) ? (wlo >> 4) : 0;
+      const int ch_hi = (whi > wlo) ? ((whi + 15) >> 4) : 0;
+      float mrow = -INFINITY;
+      for (int ch = ch_lo; ch < ch_hi; ++ch) {
+        uint32_t rr[16];
+        tc::tmem_ld16(t_row + ch * 16, rr);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int col = ch * 16 + jj;
+          if (col >= jmin && col < jmax) mrow = fmaxf(mrow, __uint_as_float(rr[jj]));
+        }
+      }
+      const float mscaled = (mrow == -INFINITY) ? 0.0f : mrow * scale_log2;
+      float lsum = 0.0f;
+      const uint32_t prow = tc::smem_u32(st) + (r >> 3) * 2048 + (r & 7) * 16;
+#pragma unroll 1
+      for (int ch = 0; ch < ROWS / 16; ++ch) {
+        uint32_t pk[8];
+        if (ch >= ch_lo && ch < ch_hi) {
+          uint32_t rr[16];
+          tc::tmem_ld16(t_row + ch * 16, rr);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 16; jj += 2) {
+            const int col = ch * 16 + jj;
+            const bool ok0 = col >= jmin && col < jmax;
+            const bool ok1 = col + 1 >= jmin && col + 1 < jmax;
+            const float e0 = ok0 ? exp2f(__uint_as_float(rr[jj]) * scale_log2 - mscaled) : 0.0f;
+            const float e1 = ok1 ? exp2f(__uint_as_float(rr[jj + 1]) * scale_log2 - mscaled) : 0.0f;
+            const uint32_t pp = pack_bf16(e0, e1);
+            pk[jj >> 1] = pp;
+            lsum += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xffff0000u);
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) pk[jj] = 0u;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t addr = prow + (2 * ch + h) * 128;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * h]),
+                       "r"(pk[4 * h + 1]), "r"(pk[4 * h + 2]), "r"(pk[4 * h + 3])
+                       : "memory");
+        }
+      }
+      tc::fence_proxy_async_smem();  // P (generic writes) before the MMA reads it
+      tc::tc_fence_before_sync();    // S reads done before O overwrites the columns
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pfull_bar[grp]);
+
+      // ---- O rows: TMEM -> fp32 staging (the stage's shared memory) ---------
+      ok = tc::mbar_wait_bounded(&ofull_bar[grp], use_a & 1u, WAIT_LIMIT_NS) &&
+           !*(volatile int*)&stop_flag;
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) { fail(lane == 0); break; }
+      tc::tc_fence_after_sync();
+      float4* stage = reinterpret_cast<float4*>(st);
+      const float inv_l = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        uint32_t rr[16];
+        tc::tmem_ld16(t_row + c0, rr);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chunk = c0 / 4 + q4;
+          stage[r * CPR + (chunk ^ (r & 7))] =
+              make_float4(__uint_as_float(rr[4 * q4]) * inv_l, __uint_as_float(rr[4 * q4 + 1]) * inv_l,
+                          __uint_as_float(rr[4 * q4 + 2]) * inv_l,
+                          __uint_as_float(rr[4 * q4 + 3]) * inv_l);
+        }
+      }
+      tc::tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tfree_bar[grp]);  // the accumulator may be reused
+
+      // ---- copy-out: each warp writes its own 32 rows, row-contiguously -----
+      const int bh = bh_s[s];
+      const int my_m = m_s[s][r];
+      const int my_cl = cl_s[s][r];
+      const int my_slot = r - ci * w;
+      const int single = (row_valid && my_m == 1) ? 1 : 0;
+      const int chn = lane % CPR;
+#pragma unroll 4
+      for (int it = 0; it < 32 / RPI; ++it) {
+        const int rr_ = it * RPI + lane / CPR;  // row of this warp; owner is lane rr_
+        const int row = 32 * quad + rr_;
+        const int t = __shfl_sync(0xffffffffu, my_pos, rr_);
+        const int sg = __shfl_sync(0xffffffffu, single, rr_);
+        const int cl = __shfl_sync(0xffffffffu, my_cl, rr_);
+        const int sl = __shfl_sync(0xffffffffu, my_slot, rr_);
+        const float4 val = stage[row * CPR + (chn ^ (row & 7))];
+        if (t < 0) continue;
+        if (sg) {
+          uint2 u;
+          u.x = pack_bf16(val.x, val.y);
+          u.y = pack_bf16(val.z, val.w);
+          *reinterpret_cast<uint2*>(out + ((size_t)bh * n + t) * D + chn * 4) = u;
+        } else {
+          *reinterpret_cast<float4*>(yslot + (((size_t)bh * k + cl) * w + sl) * D + chn * 4) = val;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);  // the stage may be refilled
+    }
+  }
+
+  tc::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == MMA_WARP) tc::tmem_dealloc(tmem, 256);
+}
+
+template <int D>
+cudaError_t launch_pipe(const void* q, const void* v, int BH, int n, int k, int w, int causal,
+                        float scale, const int32_t* idx, const int32_t* mcount, void* out,
+                        float* yslot, unsigned int* err, cudaStream_t s) {
+  const int g = ROWS / w;
+  const int tiles_per_bh = (k + g - 1) / g;
+  const long long ntiles = (long long)BH * tiles_per_bh;
+  if (ntiles > 0x7fffffff) return cudaErrorInvalidValue;
+  const size_t smem = 1024 + (size_t)PipeSmem<D>::BYTES;
+  auto kern = attention_pipe_kernel<D>;
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = (int)(ntiles < sms ? ntiles : sms);
+  const float scale_log2 = scale * 1.4426950408889634f;
+  launch_begin(K_ATTN_TC, s);
+  e = launch_pdl(kern, dim3(grid), dim3(PTHREADS), smem, s, static_cast<const bf16*>(q),
+                 static_cast<const bf16*>(v), n, k, w, g, tiles_per_bh, (int)ntiles, causal,
+                 scale_log2, idx, mcount, static_cast<bf16*>(out), yslot, err);
+  launch_end(K_ATTN_TC, s);
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_attention_pipe(const void* q, const void* v, int BH, int n, int d, int k,
+                                  int w, int causal, float scale, const int32_t* idx,
+                                  const int32_t* mcount, void* out, float* yslot,
+                                  unsigned int* err, cudaStream_t s) {
+  return d == 64 ? launch_pipe<64>(q, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, err, s)
+                 : launch_pipe<128>(q, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, err, s);
+}
+
+}  // namespace rt

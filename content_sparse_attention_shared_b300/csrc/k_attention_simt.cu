@@ -32,11 +32,11 @@ __device__ __forceinline__ void load_rows(float* dst, int ld, const T* __restric
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int r = warp; r < count; r += THREADS / 32) {
     const int slot = first + r;
-    const int t = (slot < limit) ? pos[slot] : -1;
+    const int t = (slot < limit) ? __ldcg(pos + slot) : -1;
     if ((unsigned)t < (unsigned)n_rows_total) {  // defensive: never read outside the head
       const T* row = src + (size_t)t * D;
 #pragma unroll
-      for (int i = 0; i < D / 32; ++i) dst[r * ld + lane + 32 * i] = to_f32(row[lane + 32 * i]);
+      for (int i = 0; i < D / 32; ++i) dst[r * ld + lane + 32 * i] = to_f32(__ldcg(row + lane + 32 * i));
     } else {
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) dst[r * ld + lane + 32 * i] = 0.0f;
@@ -50,6 +50,8 @@ attention_simt_kernel(const T* __restrict__ q, const T* __restrict__ kk, const T
                       int n, int k, int w, int causal, float scale,
                       const int32_t* __restrict__ idx, const int32_t* __restrict__ mcount,
                       T* __restrict__ out, float* __restrict__ yslot) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float smem[];
   constexpr int LDQ = D + 1;
   float* Qs = smem;              // [QB][D+1]
@@ -130,7 +132,7 @@ attention_simt_kernel(const T* __restrict__ q, const T* __restrict__ kk, const T
     const int t = pos[qi];
     if ((unsigned)t >= (unsigned)n) continue;
     const float inv_l = 1.0f / l[r];
-    if (mcount[(size_t)bh * n + t] == 1) {
+    if (__ldcg(mcount + (size_t)bh * n + t) == 1) {
       T* orow = out + head_off + (size_t)t * D;
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) orow[lane + 32 * i] = from_f32<T>(acc[r][i] * inv_l);
@@ -152,10 +154,9 @@ cudaError_t launch_t(const void* q, const void* kk, const void* v, int BH, int n
   if (e != cudaSuccess) return e;
   dim3 grid((w + QB - 1) / QB, k, BH);
   launch_begin(K_ATTN_SIMT, s);
-  kern<<<grid, THREADS, smem, s>>>(static_cast<const T*>(q), static_cast<const T*>(kk),
-                                   static_cast<const T*>(v), n, k, w, causal, scale, idx, mcount,
-                                   static_cast<T*>(out), yslot);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, grid, dim3(THREADS), smem, s, static_cast<const T*>(q),
+                 static_cast<const T*>(kk), static_cast<const T*>(v), n, k, w, causal, scale, idx,
+                 mcount, static_cast<T*>(out), yslot);
   launch_end(K_ATTN_SIMT, s);
   return e;
 }

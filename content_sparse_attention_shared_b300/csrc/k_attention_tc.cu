@@ -30,74 +30,26 @@
 // the no-swizzle core-matrix layouts (Q/K: K-major; V: MN-major).  The MMA
 // completions are waited on with a bounded mbarrier wait; a wait that runs
 // out sets the device error word and the CTA gives up its tile.
-#include "rt_internal.cuh"
-#include "tc_ptx.cuh"
+#include "attn_common.cuh"
 
 namespace rt {
 namespace {
 
 using bf16 = __nv_bfloat16;
-constexpr int ROWS = 128;
+using attn::ROWS;
+using attn::cp_async_commit;
+using attn::cp_async_wait_all;
+using attn::pack_bf16;
 constexpr int THREADS = 128;
 constexpr uint64_t WAIT_LIMIT_NS = 200ull * 1000 * 1000;  // 0.2 s
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;  // 0 source bytes: zero fill, nothing read
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-
-// Gather 128 rows (positions pos[r], -1 = zero row) of D bf16 into the K-major
-// no-swizzle layout: chunk (r, kc) at (r/8)*(D/8)*128 + kc*128 + (r%8)*16.
-// A warp covers 8 rows x 4 chunks per instruction (512 contiguous bytes).
 template <int D>
-__device__ __forceinline__ void gather_kmajor(uint8_t* dst, const bf16* __restrict__ src,
-                                              const int* pos) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int KC = D / 8;                // chunks per row
-  constexpr int ITEMS = (ROWS / 8) * (KC / 4);
-  const uint32_t base = tc::smem_u32(dst);
-  for (int it = warp; it < ITEMS; it += THREADS / 32) {
-    const int rg = it / (KC / 4);
-    const int kc = (it % (KC / 4)) * 4 + (lane >> 3);
-    const int r = rg * 8 + (lane & 7);
-    const int p = pos[r];
-    const uint32_t off = rg * (KC * 128) + kc * 128 + (lane & 7) * 16;
-    const bf16* g = src + (size_t)(p < 0 ? 0 : p) * D + kc * 8;
-    cp_async16(base + off, g, p >= 0);
-  }
+__device__ __forceinline__ void gather_kmajor(uint8_t* dst, const bf16* src, const int* pos) {
+  attn::gather_kmajor<D>(dst, src, pos, threadIdx.x >> 5, THREADS / 32);
 }
-
-// Gather 128 key rows of V (D features) into the MN-major no-swizzle layout
-// used as the B operand of O = P V (N = features, K = keys): chunk
-// (j, ec) at ec*2048 + (j/8)*128 + (j%8)*16.
 template <int D>
-__device__ __forceinline__ void gather_mnmajor(uint8_t* dst, const bf16* __restrict__ src,
-                                               const int* pos) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int EC = D / 8;
-  constexpr int ITEMS = (ROWS / 8) * (EC / 4);
-  const uint32_t base = tc::smem_u32(dst);
-  for (int it = warp; it < ITEMS; it += THREADS / 32) {
-    const int jg = it / (EC / 4);
-    const int ec = (it % (EC / 4)) * 4 + (lane >> 3);
-    const int j = jg * 8 + (lane & 7);
-    const int p = pos[j];
-    const uint32_t off = ec * 2048 + jg * 128 + (lane & 7) * 16;
-    const bf16* g = src + (size_t)(p < 0 ? 0 : p) * D + ec * 8;
-    cp_async16(base + off, g, p >= 0);
-  }
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
+__device__ __forceinline__ void gather_mnmajor(uint8_t* dst, const bf16* src, const int* pos) {
+  attn::gather_mnmajor<D>(dst, src, pos, threadIdx.x >> 5, THREADS / 32);
 }
 
 // Shared-memory plan (bytes, after 1 KiB alignment slack).
@@ -122,6 +74,8 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
                     bf16* __restrict__ out, float* __restrict__ yslot,
                     unsigned int* __restrict__ err) {
   using L = AttnSmem<D, MULTI>;
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -164,11 +118,11 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
   }
   int my_pos = -1;
   if (row_valid) {
-    my_pos = __ldg(idx_bh + (size_t)cluster * w + slot);
+    my_pos = __ldcg(idx_bh + (size_t)cluster * w + slot);
     if ((unsigned)my_pos >= (unsigned)n) { my_pos = -1; row_valid = false; }  // defensive
   }
   // membership count of this row's position, loaded now, used by the epilogue
-  const int my_m = row_valid ? __ldg(mcount + (size_t)bh * n + my_pos) : 0;
+  const int my_m = row_valid ? __ldcg(mcount + (size_t)bh * n + my_pos) : 0;
   qpos[tid] = my_pos;
   __syncthreads();
 
@@ -212,7 +166,7 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
       const int ks = kb * ROWS + tid;
       int p = -1;
       if (ks < w) {
-        p = __ldg(idx_bh + (size_t)cluster * w + ks);
+        p = __ldcg(idx_bh + (size_t)cluster * w + ks);
         if ((unsigned)p >= (unsigned)n) p = -1;
       }
       __syncthreads();  // previous block's buffers are free (all reads done)
@@ -448,10 +402,9 @@ cudaError_t launch_t(const void* q, const void* v, int BH, int n, int k, int w, 
   const long long tiles = (long long)BH * tiles_per_bh;
   const float scale_log2 = scale * 1.4426950408889634f;
   launch_begin(K_ATTN_TC, s);
-  kern<<<(unsigned)tiles, THREADS, smem, s>>>(
-      static_cast<const bf16*>(q), static_cast<const bf16*>(v), n, k, w, g, tiles_per_bh, R,
-      causal, scale_log2, idx, mcount, static_cast<bf16*>(out), yslot, err);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3((unsigned)tiles), dim3(THREADS), smem, s, static_cast<const bf16*>(q),
+                 static_cast<const bf16*>(v), n, k, w, g, tiles_per_bh, R, causal, scale_log2, idx,
+                 mcount, static_cast<bf16*>(out), yslot, err);
   launch_end(K_ATTN_TC, s);
   return e;
 }
@@ -467,6 +420,8 @@ cudaError_t launch_attention_tc(const void* q, const void* v, int BH, int n, int
                                 const int32_t* mcount, void* out, float* yslot,
                                 unsigned int* err, cudaStream_t s) {
   const bool multi = w > ROWS;
+  if (!multi)
+    return launch_attention_pipe(q, v, BH, n, d, k, w, causal, scale, idx, mcount, out, yslot, err, s);
   if (d == 64) {
     return multi ? launch_t<64, true>(q, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, err, s)
                  : launch_t<64, false>(q, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, err, s);

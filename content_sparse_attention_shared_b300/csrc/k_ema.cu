@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(TE)
 ema_bucket_kernel(const int32_t* __restrict__ assign, int B, int H, int n, int k, int T,
                   int32_t* __restrict__ counts, int32_t* __restrict__ starts,
                   int32_t* __restrict__ perm) {
+  pdl_trigger();
   extern __shared__ int32_t sm[];
   int32_t* warp_cnt = sm;                 // [WARPS1][k]
   int32_t* tot = sm + WARPS1 * k;         // [k]
@@ -56,6 +57,7 @@ ema_bucket_kernel(const int32_t* __restrict__ assign, int B, int H, int n, int k
   const int tile = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < (WARPS1 + 2) * k; i += TE) sm[i] = 0;
+  pdl_wait();
   __syncthreads();
 
   const long long g = (long long)tile * TE + tid;
@@ -63,7 +65,7 @@ ema_bucket_kernel(const int32_t* __restrict__ assign, int B, int H, int n, int k
   int a = -1;
   if (g < rows) {
     const int b = (int)(g / n), t = (int)(g % n);
-    a = assign[((size_t)b * H + h) * n + t];
+    a = __ldcg(assign + ((size_t)b * H + h) * n + t);
     if (a < 0 || a >= k) a = -1;  // out-of-range assignment: ignored
   }
   const unsigned peers = __match_any_sync(0xffffffffu, a);
@@ -106,13 +108,13 @@ ema_bucket_kernel(const int32_t* __restrict__ assign, int B, int H, int n, int k
 
 // 8 consecutive features of a row as fp32
 __device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  const float4 a = __ldcg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
   x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
   x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[8]) {
-  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint4 u = __ldcg(reinterpret_cast<const uint4*>(p));
   const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -141,6 +143,8 @@ __global__ void __launch_bounds__(THREADS2, 8)
 ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
                   const int32_t* __restrict__ counts, const int32_t* __restrict__ starts,
                   const int32_t* __restrict__ perm, float* __restrict__ mu, float decay) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int CH = D / 8;          // threads per row
   constexpr int RS = THREADS2 / CH;  // rows in flight per pass over the list
   constexpr int LIST = 1024;         // rows listed per round
@@ -153,7 +157,7 @@ ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
   const int32_t* cnt = counts + ((size_t)h * k + c) * Tn;
   const int32_t* st = starts + ((size_t)h * k + c) * Tn;
   const long long rows_total = (long long)B * n;
-  const float old = (tid < D) ? mu[((size_t)h * k + c) * D + tid] : 0.0f;  // loaded early
+  const float old = (tid < D) ? __ldcg(mu + ((size_t)h * k + c) * D + tid) : 0.0f;  // early
 
   // exclusive prefix of the per-tile counts over the tiles
   {
@@ -162,7 +166,7 @@ ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
     for (int i0 = 0; i0 < Tn; i0 += THREADS2) {
       const int i = i0 + tid;
       int total;
-      const int ex = block_exclusive_scan<THREADS2>(i < Tn ? __ldg(cnt + i) : 0, wsum, total);
+      const int ex = block_exclusive_scan<THREADS2>(i < Tn ? __ldcg(cnt + i) : 0, wsum, total);
       if (i < Tn) offs[i] = carry + ex;
       carry += total;
     }
@@ -188,9 +192,9 @@ ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
         const int mid = (a0 + a1 + 1) >> 1;
         if (offs[mid] <= f) a0 = mid; else a1 = mid - 1;
       }
-      const int p = __ldg(st + a0) + (f - offs[a0]);
+      const int p = __ldcg(st + a0) + (f - offs[a0]);
       int g = -1;
-      if (p >= 0 && p < TE) g = __ldg(perm + (size_t)h * Tn * TE + (size_t)a0 * TE + p);
+      if (p >= 0 && p < TE) g = __ldcg(perm + (size_t)h * Tn * TE + (size_t)a0 * TE + p);
       if (g < 0 || (long long)g >= rows_total) g = -1;  // defensive
       rowlist[i] = g;
     }
@@ -256,9 +260,9 @@ cudaError_t launch_update(const void* qk, int B, int H, int n, int k, const EmaL
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)(smem < 48 * 1024 ? 48 * 1024 : smem));
   if (e != cudaSuccess) return e;
   launch_begin(K_EMA_UPDATE, s);
-  kern<<<dim3(k, H), THREADS2, smem, s>>>(static_cast<const T*>(qk), B, H, n, k, L.T, L.counts,
-                                           L.starts, L.perm, mu, decay);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3(k, H), dim3(THREADS2), smem, s, static_cast<const T*>(qk), B, H, n, k,
+                 L.T, (const int32_t*)L.counts, (const int32_t*)L.starts, (const int32_t*)L.perm,
+                 mu, decay);
   launch_end(K_EMA_UPDATE, s);
   return e;
 }
@@ -281,9 +285,8 @@ cudaError_t launch_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(ema_bucket_kernel), (int)(smem1 < 48 * 1024 ? 48 * 1024 : smem1));
   if (e != cudaSuccess) return e;
   launch_begin(K_EMA_BUCKET, s);
-  ema_bucket_kernel<<<dim3(L.T, H), TE, smem1, s>>>(assign, B, H, n, k, L.T, L.counts, L.starts,
-                                                     L.perm);
-  e = cudaGetLastError();
+  e = launch_pdl(ema_bucket_kernel, dim3(L.T, H), dim3(TE), smem1, s, assign, B, H, n, k, L.T,
+                 L.counts, L.starts, L.perm);
   launch_end(K_EMA_BUCKET, s);
   if (e != cudaSuccess) return e;
   if (dt == RT_F32) {

@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(THREADS)
 scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ idx,
                const int32_t* __restrict__ mcount, const int32_t* __restrict__ slots,
                const float* __restrict__ yslot, T* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int CH = D / 8;    // 8-feature chunks per row
   constexpr int PER = D / 32;  // contiguous features per lane on the warp-wide path
   const long long g = (long long)blockIdx.x * THREADS + threadIdx.x;
@@ -102,7 +104,7 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
   const int ch = (int)(g - r * CH);
   const int lane = threadIdx.x & 31;
   const bool active = r < BHn;
-  const int m = active ? __ldg(mcount + r) : 1;
+  const int m = active ? __ldcg(mcount + r) : 1;
 
   // rare: positions in more than SLOTS_PER_ROW clusters, one warp pass each
   unsigned slow = __ballot_sync(0xffffffffu, active && ch == 0 && m > SLOTS_PER_ROW);
@@ -126,7 +128,7 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
         int lo = 0, hi = w - 1;
         while (lo <= hi) {
           const int mid = (lo + hi) >> 1;
-          const int v = __ldg(list + mid);
+          const int v = __ldcg(list + mid);
           if (v == t) { slot = mid; break; }
           if (v < t) lo = mid + 1; else hi = mid - 1;
         }
@@ -158,7 +160,7 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
   int ids[8];
   {
     const int4* sp = reinterpret_cast<const int4*>(slots + r * SLOTS_PER_ROW);
-    const int4 a = __ldg(sp), b = __ldg(sp + 1);
+    const int4 a = __ldcg(sp), b = __ldcg(sp + 1);
     ids[0] = a.x; ids[1] = a.y; ids[2] = a.z; ids[3] = a.w;
     ids[4] = b.x; ids[5] = b.y; ids[6] = b.z; ids[7] = b.w;
   }
@@ -173,8 +175,8 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
   for (int i = 0; i < 8; ++i) {
     if (i < m) {
       const float4* p = reinterpret_cast<const float4*>(ybase + (size_t)ids[i] * D);
-      y[i][0] = __ldg(p);
-      y[i][1] = __ldg(p + 1);
+      y[i][0] = __ldcg(p);
+      y[i][1] = __ldcg(p + 1);
     }
   }
 #pragma unroll
@@ -197,9 +199,8 @@ cudaError_t launch_t(int BH, int n, int k, int w, const int32_t* idx, const int3
   const long long threads = rows * (D / 8);
   const long long blocks = (threads + THREADS - 1) / THREADS;
   launch_begin(K_SCATTER, s);
-  scatter_kernel<T, D><<<(unsigned)blocks, THREADS, 0, s>>>(rows, n, k, w, idx, mcount, slots,
-                                                            yslot, static_cast<T*>(out));
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(scatter_kernel<T, D>, dim3((unsigned)blocks), dim3(THREADS), 0, s,
+                             rows, n, k, w, idx, mcount, slots, yslot, static_cast<T*>(out));
   launch_end(K_SCATTER, s);
   return e;
 }

@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(THREADS)
 score_simt_kernel(const T* __restrict__ qk, int H, int n, const float* __restrict__ mu,
                   int k, float* __restrict__ S, int32_t* __restrict__ assign,
                   int32_t* __restrict__ mcount) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float smem[];
   float* rT = smem;             // [D][PAD]
   float* muT = smem + D * PAD;  // [D][PAD]
@@ -46,7 +48,7 @@ score_simt_kernel(const T* __restrict__ qk, int H, int n, const float* __restric
     if (t < n) {
       const T* row = qk + ((size_t)bh * n + t) * D;
 #pragma unroll
-      for (int i = 0; i < D / 32; ++i) x[i] = to_f32(row[lane + 32 * i]);
+      for (int i = 0; i < D / 32; ++i) x[i] = to_f32(__ldcg(row + lane + 32 * i));
     } else {
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) x[i] = 0.0f;
@@ -79,7 +81,7 @@ score_simt_kernel(const T* __restrict__ qk, int H, int n, const float* __restric
     for (int e = tid; e < CCH * D; e += THREADS) {
       const int cl = e / D, j = e % D;
       const int c = c0 + cl;
-      muT[j * PAD + cl] = (c < k) ? mu[((size_t)h * k + c) * D + j] : 0.0f;
+      muT[j * PAD + cl] = (c < k) ? __ldcg(mu + ((size_t)h * k + c) * D + j) : 0.0f;
     }
     __syncthreads();
     float acc[4][4];
@@ -144,8 +146,8 @@ cudaError_t launch_t(const void* qk, int BH, int H, int n, const float* mu, int 
   if (e != cudaSuccess) return e;
   dim3 grid((n + TOK - 1) / TOK, BH);
   launch_begin(K_SCORE_SIMT, s);
-  kern<<<grid, THREADS, smem, s>>>(static_cast<const T*>(qk), H, n, mu, k, S, a, mcount);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, grid, dim3(THREADS), smem, s, static_cast<const T*>(qk), H, n, mu, k, S, a,
+                 mcount);
   launch_end(K_SCORE_SIMT, s);
   return e;
 }

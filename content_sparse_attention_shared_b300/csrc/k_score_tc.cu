@@ -27,10 +27,6 @@
 // from TMEM, writes them centroid-major [BH,k,n] with coalesced stores and
 // takes the argmax.  Every mbarrier wait is bounded; a wait that runs out
 // sets the device error word and the CTA stops.
-#include <cuda.h>
-
-#include <mutex>
-
 #include "rt_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -115,6 +111,8 @@ __device__ __forceinline__ void split_store8(uint8_t* planes, size_t plane_bytes
 template <int D>
 __global__ void __launch_bounds__(256)
 centroid_prep_kernel(const float* __restrict__ mu, int k, int kpad, uint8_t* __restrict__ image) {
+  pdl_trigger();
+  pdl_wait();
   const int h = blockIdx.y, c0 = blockIdx.x * 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const size_t plane_bytes = (size_t)kpad * D * 2;
@@ -126,7 +124,7 @@ centroid_prep_kernel(const float* __restrict__ mu, int k, int kpad, uint8_t* __r
     float m[8];
     if (c < k) {
       const float4* src = reinterpret_cast<const float4*>(mu_h + (size_t)c * D + jc * 8);
-      const float4 a = __ldg(src), b = __ldg(src + 1);
+      const float4 a = __ldcg(src), b = __ldcg(src + 1);
       m[0] = a.x; m[1] = a.y; m[2] = a.z; m[3] = a.w;
       m[4] = b.x; m[5] = b.y; m[6] = b.z; m[7] = b.w;
     } else {
@@ -143,7 +141,7 @@ centroid_prep_kernel(const float* __restrict__ mu, int k, int kpad, uint8_t* __r
     if (c < k) {
       const float* r = mu_h + (size_t)c * D + lane * (D / 32);
 #pragma unroll
-      for (int e = 0; e < D / 32; ++e) v += __ldg(r + e);
+      for (int e = 0; e < D / 32; ++e) v += __ldcg(r + e);
     }
     v = warp_sum(v);
     if (lane == 0 && c < kpad) sums[c] = v;
@@ -171,6 +169,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
   __shared__ uint32_t tmem_base_sh;
   __shared__ int stop_flag;
 
+  pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y;
   const int tiles_per_bh = (n + ROWS - 1) / ROWS;
@@ -190,6 +189,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
     tc::mbar_init(&prep_bar, 1);
     stop_flag = 0;
     tc::fence_mbar_init();
+  }
+  pdl_wait();  // every global access below comes after the previous kernel
+  if (tid == 0) {
     if (PREP) {
       // the head's centroid image, in bulk copies of at most 32 KiB
       const uint32_t total = (uint32_t)prep_image_bytes(D, kpad);
@@ -229,7 +231,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
         const int c = it % kpad, jc = it / kpad;
         if (it < items && c < k) {
           const float4* src = reinterpret_cast<const float4*>(mu_h + (size_t)c * D + jc * 8);
-          const float4 a = __ldg(src), b = __ldg(src + 1);
+          const float4 a = __ldcg(src), b = __ldcg(src + 1);
           m[u][0] = a.x; m[u][1] = a.y; m[u][2] = a.z; m[u][3] = a.w;
           m[u][4] = b.x; m[u][5] = b.y; m[u][6] = b.z; m[u][7] = b.w;
         } else {
@@ -258,7 +260,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
         if (c < k) {
           const float* r = mu_h + (size_t)c * D + lane * (D / 32);
 #pragma unroll
-          for (int e = 0; e < D / 32; ++e) v[u] += __ldg(r + e);
+          for (int e = 0; e < D / 32; ++e) v[u] += __ldcg(r + e);
         }
       }
 #pragma unroll
@@ -490,70 +492,16 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
+// Tensor map of Q viewed as [rows, D] bf16 with 64-element x 128-row boxes,
+// 128-byte swizzle.
+bool q_tensor_map(const void* qk, unsigned long long rows, int D, CUtensorMap* out) {
+  return bf16_tensor_map_2d(qk, rows, (unsigned)D, BOX_K, ROWS, out);
 }
 
 // Shared-memory plan: 1 KiB alignment slack, A stages (1024-byte aligned
 // swizzle atoms), the three centroid planes, the centroid row sums; as many
 // A stages (up to 4) as fit beside the planes.  Static shared memory (the
 // barriers) takes well under 256 bytes.
-// Tensor map of Q viewed as [rows, D] bf16 with 64-element x 128-row boxes,
-// 128-byte swizzle.  Encoding is host work; the last few maps are kept
-// (keyed by base pointer and shape) so repeated calls on the same tensors
-// skip it.
-bool q_tensor_map(const void* qk, unsigned long long rows, int D, CUtensorMap* out) {
-  struct Entry {
-    const void* ptr;
-    unsigned long long rows;
-    int D;
-    CUtensorMap map;
-  };
-  static std::mutex mu;
-  static Entry cache[8];
-  static int used = 0, next = 0;
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    for (int i = 0; i < used; ++i)
-      if (cache[i].ptr == qk && cache[i].rows == rows && cache[i].D == D) {
-        *out = cache[i].map;
-        return true;
-      }
-  }
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)BOX_K, (cuuint32_t)ROWS};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qk), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return false;
-  std::lock_guard<std::mutex> lk(mu);
-  cache[next] = Entry{qk, rows, D, map};
-  next = (next + 1) % 8;
-  if (used < 8) ++used;
-  *out = map;
-  return true;
-}
-
 bool plan(int d, int k, ScoreCfg& c) {
   c.D = d;
   c.kpad = (k + 15) / 16 * 16;
@@ -580,9 +528,8 @@ cudaError_t launch_t(const ScoreCfg& c, const void* qk, int B, int H, int n, con
   cudaError_t e;
   if (prep != nullptr) {
     launch_begin(K_CENTROID_PREP, s);
-    centroid_prep_kernel<D><<<dim3((c.kpad + 31) / 32, H), 256, 0, s>>>(
-        mu, k, c.kpad, static_cast<uint8_t*>(prep));
-    e = cudaGetLastError();
+    e = launch_pdl(centroid_prep_kernel<D>, dim3((c.kpad + 31) / 32, H), dim3(256), 0, s, mu, k,
+                   c.kpad, static_cast<uint8_t*>(prep));
     launch_end(K_CENTROID_PREP, s);
     if (e != cudaSuccess) return e;
   }
@@ -594,10 +541,9 @@ cudaError_t launch_t(const ScoreCfg& c, const void* qk, int B, int H, int n, con
   if (cph < 1) cph = 1;
   if (cph > tiles_per_head) cph = tiles_per_head;
   launch_begin(K_SCORE_TC, s);
-  kern<<<dim3(cph, H), THREADS, c.smem, s>>>(map, B, H, n, mu,
-                                             static_cast<const uint8_t*>(prep), k, c.kpad,
-                                             c.acc_cols, c.stages, cph, S, a, mcount, err);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3(cph, H), dim3(THREADS), c.smem, s, map, B, H, n, mu,
+                 static_cast<const uint8_t*>(prep), k, c.kpad, c.acc_cols, c.stages, cph, S, a,
+                 mcount, err);
   launch_end(K_SCORE_TC, s);
   return e;
 }
@@ -606,7 +552,7 @@ cudaError_t launch_t(const ScoreCfg& c, const void* qk, int B, int H, int n, con
 
 bool score_tc_supported(rt_dtype dt, int d, int k) {
   ScoreCfg c;
-  return dt == RT_BF16 && (d == 64 || d == 128) && plan(d, k, c) && encode_fn() != nullptr;
+  return dt == RT_BF16 && (d == 64 || d == 128) && plan(d, k, c) && tensor_maps_available();
 }
 
 size_t score_prep_bytes(int H, int d, int k) {
@@ -619,7 +565,7 @@ cudaError_t launch_score(const void* qk, rt_dtype dt, int B, int H, int n, int d
                          int k, float* S, int32_t* a, int32_t* mcount, void* prep,
                          unsigned int* err, cudaStream_t s) {
   ScoreCfg c;
-  if (dt == RT_BF16 && (d == 64 || d == 128) && plan(d, k, c) && encode_fn() != nullptr &&
+  if (dt == RT_BF16 && (d == 64 || d == 128) && plan(d, k, c) && tensor_maps_available() &&
       (reinterpret_cast<uintptr_t>(qk) & 15u) == 0) {
     return d == 64 ? launch_t<64>(c, qk, B, H, n, mu, k, S, a, mcount, prep, err, s)
                    : launch_t<128>(c, qk, B, H, n, mu, k, S, a, mcount, prep, err, s);

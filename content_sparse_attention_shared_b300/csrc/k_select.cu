@@ -77,7 +77,7 @@ __device__ void radix_select_row(const float* __restrict__ row, int n, int w, co
     for (int b = tid; b < 256; b += THREADS) hist[b] = 0u;
     __syncthreads();
     for (int t = tid; t < n; t += THREADS) {
-      const uint32_t key = score_key(__ldg(row + t));
+      const uint32_t key = score_key(__ldcg(row + t));
       if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
     }
     __syncthreads();
@@ -120,7 +120,7 @@ __device__ void radix_select_row(const float* __restrict__ row, int n, int w, co
   int out_base = 0, eq_base = 0, buf = 0;
   for (int t0 = 0; t0 < n && out_base < w; t0 += THREADS, buf ^= 1) {
     const int t = t0 + tid;
-    const uint32_t key = (t < n) ? score_key(__ldg(row + t)) : 0u;
+    const uint32_t key = (t < n) ? score_key(__ldcg(row + t)) : 0u;
     const bool gt = (t < n) && key > kstar;
     const bool eq = (t < n) && key == kstar;
     const unsigned be = __ballot_sync(0xffffffffu, eq);
@@ -155,6 +155,7 @@ __device__ void radix_select_row(const float* __restrict__ row, int n, int w, co
 __global__ void __launch_bounds__(THREADS)
 select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __restrict__ idx,
                    int32_t* __restrict__ mcount, int32_t* __restrict__ slots, int staged) {
+  pdl_trigger();
   extern __shared__ __align__(16) uint16_t sbin[];  // [n] when staged
   __shared__ unsigned hist[NBINS];
   __shared__ int cand_t[CAND_CAP];
@@ -169,12 +170,14 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   if (!staged) {
+    pdl_wait();
     radix_select_row(row, n, w, so, hist, wsum);
     return;
   }
 
   for (int b = tid; b < NBINS; b += THREADS) hist[b] = 0u;
   if (tid == 0) s_ncand = 0;
+  pdl_wait();
   __syncthreads();
 
   // 1. bins + histogram: one vectorised read of the row
@@ -186,7 +189,7 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
     for (; i + 3 * THREADS < n4; i += 4 * THREADS) {
       float4 v[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __ldg(row4 + i + u * THREADS);
+      for (int u = 0; u < 4; ++u) v[u] = __ldcg(row4 + i + u * THREADS);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int b0 = score_bin(v[u].x), b1 = score_bin(v[u].y);
@@ -202,7 +205,7 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
       }
     }
     for (; i < n4; i += THREADS) {
-      const float4 v = __ldg(row4 + i);
+      const float4 v = __ldcg(row4 + i);
       const int b0 = score_bin(v.x), b1 = score_bin(v.y);
       const int b2 = score_bin(v.z), b3 = score_bin(v.w);
       uint2 packed;
@@ -215,7 +218,7 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
       atomicAdd(&hist[b3], 1u);
     }
     for (int t = 4 * n4 + tid; t < n; t += THREADS) {
-      const int b = score_bin(__ldg(row + t));
+      const int b = score_bin(__ldcg(row + t));
       sbin[t] = (uint16_t)b;
       atomicAdd(&hist[b], 1u);
     }
@@ -284,7 +287,7 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
         const int slot = atomicAdd(&s_ncand, 1);
         const int t = q * 32 + b;
         cand_t[slot] = t;
-        cand_s[slot] = __ldg(row + t);
+        cand_s[slot] = __ldcg(row + t);
       }
     }
     __syncthreads();
@@ -346,6 +349,7 @@ __global__ void __launch_bounds__(THREADS, 7)
 select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
                          int32_t* __restrict__ idx, int32_t* __restrict__ mcount,
                          int32_t* __restrict__ slots) {
+  pdl_trigger();
   __shared__ unsigned hist[NBINS];
   __shared__ int cand_t[RCAP];
   __shared__ float cand_s[RCAP];
@@ -367,6 +371,7 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
     s_ncand = 0;
     s_bl = -1;
   }
+  pdl_wait();
 
   // 1. per-thread maximum
   float m = -INFINITY;
@@ -377,7 +382,7 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u;
       const int p = w0 + 128 * i;
-      v[u] = (128 * i < seg && p < n) ? __ldg(row4 + (p >> 2))
+      v[u] = (128 * i < seg && p < n) ? __ldcg(row4 + (p >> 2))
                                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
 #pragma unroll
@@ -424,7 +429,7 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
       for (int u = 0; u < 4; ++u) {
         const int i = i0 + u;
         const int p = w0 + 128 * i;
-        v[u] = (128 * i < seg && p < n) ? __ldg(row4 + (p >> 2))
+        v[u] = (128 * i < seg && p < n) ? __ldcg(row4 + (p >> 2))
                                         : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       }
 #pragma unroll
@@ -443,7 +448,7 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
         const int p = w0 + 128 * (bit >> 2) + (bit & 3);
         if (slot < RCAP) {
           cand_t[slot] = p;
-          cand_s[slot] = __ldg(row + p);
+          cand_s[slot] = __ldcg(row + p);
         }
         ++slot;
       }
@@ -494,14 +499,14 @@ cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* 
   if (e != cudaSuccess) return e;
   if (n <= BOUND_N_MAX && (n & 3) == 0 && w <= THREADS) {
     launch_begin(K_SELECT, s);
-    select_topw_bound_kernel<<<grid, THREADS, 0, s>>>(S, n, k, w, idx, mcount, slots);
-    e = cudaGetLastError();
+    e = launch_pdl(select_topw_bound_kernel, grid, dim3(THREADS), 0, s, S, n, k, w, idx, mcount,
+                   slots);
     launch_end(K_SELECT, s);
     return e;
   }
   launch_begin(K_SELECT, s);
-  select_topw_kernel<<<grid, THREADS, smem, s>>>(S, n, k, w, idx, mcount, slots, staged);
-  e = cudaGetLastError();
+  e = launch_pdl(select_topw_kernel, grid, dim3(THREADS), smem, s, S, n, k, w, idx, mcount, slots,
+                 staged);
   launch_end(K_SELECT, s);
   return e;
 }

@@ -69,6 +69,71 @@ cudaError_t set_smem_limit(const void* func, int bytes) {
 }
 
 // ---------------------------------------------------------------------------
+// tensor maps (cuTensorMapEncodeTiled through the runtime's driver entry
+// point), with a small cache
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool tensor_maps_available() { return encode_fn() != nullptr; }
+
+bool bf16_tensor_map_2d(const void* base, unsigned long long rows, unsigned cols,
+                        unsigned box_cols, unsigned box_rows, CUtensorMap* out) {
+  struct Entry {
+    const void* ptr;
+    unsigned long long rows;
+    unsigned cols, box_cols, box_rows;
+    CUtensorMap map;
+  };
+  constexpr int N = 16;
+  static std::mutex mu;
+  static Entry cache[N];
+  static int used = 0, next = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].ptr == base && cache[i].rows == rows && cache[i].cols == cols &&
+          cache[i].box_cols == box_cols && cache[i].box_rows == box_rows) {
+        *out = cache[i].map;
+        return true;
+      }
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || box_cols * 2 != 128) return false;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  cache[next] = Entry{base, rows, cols, box_cols, box_rows, map};
+  next = (next + 1) % N;
+  if (used < N) ++used;
+  *out = map;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
 // workspace layout
 // ---------------------------------------------------------------------------
 static inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }

@@ -1,10 +1,13 @@
 // Internal declarations shared by the kernels and the C-ABI layer.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
 #include <stddef.h>
+
+#include <utility>
 
 #include "../../include/routing_attention.h"
 
@@ -36,6 +39,42 @@ rt_status validate_shape(rt_dtype dt, int B, int H, int n, int d, int k, int w);
 // needs more than it was given before on that device, so launches pay a map
 // lookup instead of a driver call.
 cudaError_t set_smem_limit(const void* func, int bytes);
+
+// 2-D tensor map of a row-major bf16 matrix [rows, cols] (cols contiguous)
+// with boxes of box_cols x box_rows elements and 128-byte swizzle (box_cols *
+// 2 must be 128).  Encoding is host work; recent maps are cached (keyed by
+// base pointer, shape and box) so repeated calls on the same tensors skip it.
+bool tensor_maps_available();
+bool bf16_tensor_map_2d(const void* base, unsigned long long rows, unsigned cols,
+                        unsigned box_cols, unsigned box_rows, CUtensorMap* out);
+
+// Programmatic dependent launch: every kernel of the library is launched with
+// programmatic stream serialization allowed, tells the runtime at its start
+// that its dependents may be scheduled (pdl_trigger), and waits for its
+// predecessor grid to complete, with its memory visible (pdl_wait), before it
+// reads or writes any global memory.  Only shared-memory / TMEM set-up comes
+// before pdl_wait, so the set-up overlaps the predecessor's tail.  Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Called by every launcher around its launch.
 void launch_begin(int kind, cudaStream_t s);
@@ -149,6 +188,12 @@ cudaError_t launch_attention_tc(const void* q, const void* v, int BH, int n, int
                                 int causal, float scale, const int32_t* idx,
                                 const int32_t* mcount, void* out, float* yslot,
                                 unsigned int* err, cudaStream_t s);
+
+// the same, persistent and pipelined, for w <= 128 (bf16 only).
+cudaError_t launch_attention_pipe(const void* q, const void* v, int BH, int n, int d, int k,
+                                  int w, int causal, float scale, const int32_t* idx,
+                                  const int32_t* mcount, void* out, float* yslot,
+                                  unsigned int* err, cudaStream_t s);
 
 // zero rows (mcount == 0) and the mean over clusters (mcount >= 2).
 cudaError_t launch_scatter(rt_dtype dt, int BH, int n, int d, int k, int w,
