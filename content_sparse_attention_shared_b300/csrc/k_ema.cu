@@ -106,22 +106,33 @@ ema_bucket_kernel(const int32_t* __restrict__ assign, int B, int H, int n, int k
   }
 }
 
-// 8 consecutive features of a row as fp32
-__device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
-  const float4 a = __ldcg(reinterpret_cast<const float4*>(p));
-  const float4 b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[8]) {
-  const uint4 u = __ldcg(reinterpret_cast<const uint4*>(p));
-  const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    x[2 * e] = __uint_as_float(w4[e] << 16);
-    x[2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+// 8 consecutive features of a row, kept in their storage format and read as
+// fp32 on use.
+template <typename T> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+  uint4 u;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) {
+    u = __ldcg(reinterpret_cast<const uint4*>(p));
   }
-}
+  __device__ __forceinline__ void zero() { u = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ float at(int j) const {
+    const uint32_t w = j < 2 ? u.x : j < 4 ? u.y : j < 6 ? u.z : u.w;
+    return (j & 1) ? __uint_as_float(w & 0xffff0000u) : __uint_as_float(w << 16);
+  }
+};
+template <> struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = __ldcg(reinterpret_cast<const float4*>(p));
+    b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+  }
+  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ float at(int j) const {
+    const float4& q = j < 4 ? a : b;
+    const int e = j & 3;
+    return e == 0 ? q.x : e == 1 ? q.y : e == 2 ? q.z : q.w;
+  }
+};
 
 // Sum over the CH consecutive lanes that hold one row (CH a power of two).
 template <int CH>
@@ -148,7 +159,8 @@ ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
   constexpr int CH = D / 8;          // threads per row
   constexpr int RS = THREADS2 / CH;  // rows in flight per pass over the list
   constexpr int LIST = 1024;         // rows listed per round
-  extern __shared__ int32_t offs[];  // [Tn + 1]
+  extern __shared__ int32_t offs[];  // [Tn + 1] offsets, then [Tn] bucket starts
+  int32_t* sts = offs + Tn + 1;
   __shared__ int rowlist[LIST];
   __shared__ float red[RS][D];
   __shared__ float nrm_part[WARPS2];
@@ -167,7 +179,10 @@ ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
       const int i = i0 + tid;
       int total;
       const int ex = block_exclusive_scan<THREADS2>(i < Tn ? __ldcg(cnt + i) : 0, wsum, total);
-      if (i < Tn) offs[i] = carry + ex;
+      if (i < Tn) {
+        offs[i] = carry + ex;
+        sts[i] = __ldcg(st + i);
+      }
       carry += total;
     }
     if (tid == 0) offs[Tn] = carry;
@@ -192,42 +207,47 @@ ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
         const int mid = (a0 + a1 + 1) >> 1;
         if (offs[mid] <= f) a0 = mid; else a1 = mid - 1;
       }
-      const int p = __ldcg(st + a0) + (f - offs[a0]);
+      const int p = sts[a0] + (f - offs[a0]);
       int g = -1;
       if (p >= 0 && p < TE) g = __ldcg(perm + (size_t)h * Tn * TE + (size_t)a0 * TE + p);
       if (g < 0 || (long long)g >= rows_total) g = -1;  // defensive
       rowlist[i] = g;
     }
     __syncthreads();
-    // uniform trip count: the shuffles below involve every lane of the warp
+    // uniform trip count: the shuffles below involve every lane of the warp.
+    // Two rows in flight per thread, each kept as its raw 16 bytes (8 bf16 or
+    // 4 fp32 -- for fp32 rows the thread's 8 features are two 16-byte halves)
+    // and converted when used, which keeps the register count low.
     for (int base = 0; base < nl; base += 2 * RS) {
-      float x[2][8];
+      Raw8<T> x[2];
       int gg[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int i = base + rs + u * RS;
         gg[u] = (i < nl) ? rowlist[i] : -1;
         if (gg[u] >= 0) {
-          const int b = gg[u] / n, t = gg[u] - (gg[u] / n) * n;
-          load8(qk + (((size_t)b * H + h) * n + t) * D + ch * 8, x[u]);
+          const int b = gg[u] / n, t = gg[u] - b * n;
+          x[u].load(qk + (((size_t)b * H + h) * n + t) * D + ch * 8);
         } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) x[u][j] = 0.0f;
+          x[u].zero();
         }
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         float sx = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sx += x[u][j];
+        for (int j = 0; j < 8; ++j) sx += x[u].at(j);
         const float mean = group_sum<CH>(sx) / (float)D;
         float ss = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) { x[u][j] -= mean; ss = fmaf(x[u][j], x[u][j], ss); }
+        for (int j = 0; j < 8; ++j) {
+          const float a = x[u].at(j) - mean;
+          ss = fmaf(a, a, ss);
+        }
         ss = group_sum<CH>(ss);
         const float inv = (gg[u] >= 0 && ss > 0.0f) ? 1.0f / sqrtf(ss) : 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = fmaf(x[u][j], inv, acc[j]);
+        for (int j = 0; j < 8; ++j) acc[j] = fmaf(x[u].at(j) - mean, inv, acc[j]);
       }
     }
   }
@@ -255,7 +275,7 @@ ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
 template <typename T, int D>
 cudaError_t launch_update(const void* qk, int B, int H, int n, int k, const EmaLayout& L,
                           float* mu, float decay, cudaStream_t s) {
-  const size_t smem = (size_t)(L.T + 1) * sizeof(int32_t);
+  const size_t smem = (size_t)(2 * L.T + 1) * sizeof(int32_t);
   auto kern = ema_update_kernel<T, D>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)(smem < 48 * 1024 ? 48 * 1024 : smem));
   if (e != cudaSuccess) return e;

@@ -91,7 +91,7 @@ __device__ __forceinline__ void store8(T* dst, const float (&v)[8]) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, 6)
 scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ idx,
                const int32_t* __restrict__ mcount, const int32_t* __restrict__ slots,
                const float* __restrict__ yslot, T* __restrict__ out) {
@@ -105,6 +105,14 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
   const int lane = threadIdx.x & 31;
   const bool active = r < BHn;
   const int m = active ? __ldcg(mcount + r) : 1;
+  // the recorded slot ids are loaded together with the count (one round trip
+  // instead of two); only rows with 2 <= m <= SLOTS_PER_ROW use them
+  int4 sa = make_int4(0, 0, 0, 0), sb = sa;
+  if (active) {
+    const int4* sp = reinterpret_cast<const int4*>(slots + r * SLOTS_PER_ROW);
+    sa = __ldcg(sp);
+    sb = __ldcg(sp + 1);
+  }
 
   // rare: positions in more than SLOTS_PER_ROW clusters, one warp pass each
   unsigned slow = __ballot_sync(0xffffffffu, active && ch == 0 && m > SLOTS_PER_ROW);
@@ -157,33 +165,32 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
     store8<T>(dst, acc);
     return;
   }
-  int ids[8];
-  {
-    const int4* sp = reinterpret_cast<const int4*>(slots + r * SLOTS_PER_ROW);
-    const int4 a = __ldcg(sp), b = __ldcg(sp + 1);
-    ids[0] = a.x; ids[1] = a.y; ids[2] = a.z; ids[3] = a.w;
-    ids[4] = b.x; ids[5] = b.y; ids[6] = b.z; ids[7] = b.w;
-  }
+  int ids[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
   for (int i = 0; i < 8; ++i)
     if (i >= m) ids[i] = 0x7fffffff;
   sort8(ids);
   const long long bh = r / n;
   const float* ybase = yslot + (size_t)bh * k * w * D + ch * 8;
-  float4 y[8][2];
+  // slot rows summed in ascending cluster order, four loads in flight at a time
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (i < m) {
-      const float4* p = reinterpret_cast<const float4*>(ybase + (size_t)ids[i] * D);
-      y[i][0] = __ldcg(p);
-      y[i][1] = __ldcg(p + 1);
+  for (int i0 = 0; i0 < 8; i0 += 4) {
+    if (i0 >= m) break;
+    float4 y[4][2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (i0 + u < m) {
+        const float4* p = reinterpret_cast<const float4*>(ybase + (size_t)ids[i0 + u] * D);
+        y[u][0] = __ldcg(p);
+        y[u][1] = __ldcg(p + 1);
+      }
     }
-  }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (i < m) {
-      acc[0] += y[i][0].x; acc[1] += y[i][0].y; acc[2] += y[i][0].z; acc[3] += y[i][0].w;
-      acc[4] += y[i][1].x; acc[5] += y[i][1].y; acc[6] += y[i][1].z; acc[7] += y[i][1].w;
+    for (int u = 0; u < 4; ++u) {
+      if (i0 + u < m) {
+        acc[0] += y[u][0].x; acc[1] += y[u][0].y; acc[2] += y[u][0].z; acc[3] += y[u][0].w;
+        acc[4] += y[u][1].x; acc[5] += y[u][1].y; acc[6] += y[u][1].z; acc[7] += y[u][1].w;
+      }
     }
   }
   const float fm = (float)m;

@@ -329,7 +329,9 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
 // Rows of n <= THREADS * 32 scores, n a multiple of 4.  Warp j owns the
 // contiguous segment [j*seg, (j+1)*seg) (seg a multiple of 128), in chunks of
 // 128 positions; lane l owns positions 4l..4l+3 of every chunk, so every load
-// is a coalesced float4 (512 bytes per warp), four in flight per thread.
+// is a coalesced float4 (512 bytes per warp), four in flight per thread.  Each
+// thread keeps its two largest scores; the row is read a second time only by
+// a thread whose second largest score is itself a candidate.
 // The w-th largest of the per-thread maxima is a lower bound on the w-th
 // largest score (the w threads holding the largest maxima own w distinct
 // scores at least that large), so every kept score lies in a bin at or above
@@ -373,8 +375,10 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
   }
   pdl_wait();
 
-  // 1. per-thread maximum
-  float m = -INFINITY;
+  // 1. per-thread maximum, and the two largest scores with their slots
+  //    (bit 4*i+e: chunk i, element e)
+  float m1 = -INFINITY, m2 = -INFINITY;
+  int b1 = -1, b2 = -1;
 #pragma unroll
   for (int i0 = 0; i0 < CHUNKS_MAX; i0 += 4) {
     float4 v[4];
@@ -386,8 +390,22 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
                                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) m = fmaxf(m, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
+    for (int u = 0; u < 4; ++u) {
+      const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = e4[e];
+        const int b = 4 * (i0 + u) + e;
+        if (x > m1) {
+          m2 = m1; b2 = b1;
+          m1 = x; b1 = b;
+        } else if (x > m2) {
+          m2 = x; b2 = b;
+        }
+      }
+    }
   }
+  const float m = m1;
   __syncthreads();  // hist cleared
   if (w0 < n) atomicAdd(&hist[score_bin(m)], 1u);
   __syncthreads();
@@ -421,24 +439,33 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
   //    only computed for the few scores that pass.
   if (bl >= 0) {
     const float pre = bl > 0 ? (float)bl * (1.0f / 1024.0f) - 1.0f - 1.0e-5f : -INFINITY;
+    auto is_cand = [&](float x) { return x >= pre && score_bin(x) >= bl; };
     uint32_t cmask = 0u;
+    bool fast = false;
+    if (b2 >= 0 && is_cand(m2)) {
+      // a third score of this thread may qualify too: read the segment again
 #pragma unroll
-    for (int i0 = 0; i0 < CHUNKS_MAX; i0 += 4) {
-      float4 v[4];
+      for (int i0 = 0; i0 < CHUNKS_MAX; i0 += 4) {
+        float4 v[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u;
-        const int p = w0 + 128 * i;
-        v[u] = (128 * i < seg && p < n) ? __ldcg(row4 + (p >> 2))
-                                        : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u;
+          const int p = w0 + 128 * i;
+          v[u] = (128 * i < seg && p < n) ? __ldcg(row4 + (p >> 2))
+                                          : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (is_cand(e4[e])) cmask |= 1u << (4 * (i0 + u) + e);
+        }
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (e4[e] >= pre && score_bin(e4[e]) >= bl) cmask |= 1u << (4 * (i0 + u) + e);
-      }
+    } else if (b1 >= 0 && is_cand(m1)) {
+      // every other score of the thread is <= m2, which does not qualify
+      cmask = 1u << b1;
+      fast = true;
     }
     if (cmask != 0u) {
       int slot = atomicAdd(&s_ncand, __popc(cmask));
@@ -448,7 +475,7 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
         const int p = w0 + 128 * (bit >> 2) + (bit & 3);
         if (slot < RCAP) {
           cand_t[slot] = p;
-          cand_s[slot] = __ldcg(row + p);
+          cand_s[slot] = fast ? m1 : __ldcg(row + p);
         }
         ++slot;
       }
