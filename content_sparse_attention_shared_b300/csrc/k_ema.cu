@@ -11,10 +11,9 @@
 //
 // No floating-point atomics: kernel 1 counting-sorts the rows of every tile
 // of 256 rows by centroid (a stable, position-ordered bucket per centroid),
-// kernel 2 gives each (head, centroid) one CTA that walks its buckets tile by
-// tile, re-normalises each row on the fly, sums in a fixed order (warp
-// round-robin, then warps in order), blends and renormalises.  The result is
-// deterministic.
+// kernel 2 gives each (centroid, head) one CTA that lists its rows from the
+// buckets, re-normalises each row on the fly, sums them in a fixed order,
+// blends and renormalises.  The result is deterministic.
 #include "rt_internal.cuh"
 
 namespace rt {
@@ -142,6 +141,83 @@ __device__ __forceinline__ float group_sum(float v) {
   return v;
 }
 
+// Adds the normalised rows rowlist[0 .. nl) of head h into acc (this
+// thread's 8 features; CH threads share a row, RS rows in flight).  The trip
+// count is uniform: the shuffles involve every lane of the warp.  Two rows in
+// flight per thread, each kept as its raw 16 bytes (8 bf16 or 2 x 4 fp32) and
+// converted when used, which keeps the register count low.
+template <typename T, int D>
+__device__ __forceinline__ void add_rows(const T* __restrict__ qk, int H, int n, int h,
+                                         const int* rowlist, int nl, float (&acc)[8]) {
+  constexpr int CH = D / 8;
+  constexpr int RS = THREADS2 / CH;
+  const int ch = threadIdx.x % CH, rs = threadIdx.x / CH;
+  for (int base = 0; base < nl; base += 2 * RS) {
+    Raw8<T> x[2];
+    int gg[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = base + rs + u * RS;
+      gg[u] = (i < nl) ? rowlist[i] : -1;
+      if (gg[u] >= 0) {
+        const int b = gg[u] / n, t = gg[u] - b * n;
+        x[u].load(qk + (((size_t)b * H + h) * n + t) * D + ch * 8);
+      } else {
+        x[u].zero();
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float sx = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sx += x[u].at(j);
+      const float mean = group_sum<CH>(sx) / (float)D;
+      float ss = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float a = x[u].at(j) - mean;
+        ss = fmaf(a, a, ss);
+      }
+      ss = group_sum<CH>(ss);
+      const float inv = (gg[u] >= 0 && ss > 0.0f) ? 1.0f / sqrtf(ss) : 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(x[u].at(j) - mean, inv, acc[j]);
+    }
+  }
+}
+
+// Sums the row slots' partial sums in a fixed order, blends the mean into
+// the centroid (`old` = its previous value, loaded by threads < D) and
+// renormalises it.  Every thread of the block calls it.
+template <int D>
+__device__ __forceinline__ void finish_centroid(const float (&acc)[8], int N, float old,
+                                                float decay, float* __restrict__ mu_c) {
+  constexpr int CH = D / 8;
+  constexpr int RS = THREADS2 / CH;
+  __shared__ float red[RS][D];
+  __shared__ float nrm_part[WARPS2];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ch = tid % CH, rs = tid / CH;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) red[rs][ch * 8 + j] = acc[j];
+  __syncthreads();
+  float vj = 0.0f;
+  if (tid < D) {
+    float sum = 0.0f;
+    for (int r = 0; r < RS; ++r) sum += red[r][tid];
+    const float mean_j = sum / (float)N;
+    vj = decay * old + (1.0f - decay) * mean_j;
+  }
+  float sq = warp_sum(vj * vj);
+  if (lane == 0) nrm_part[warp] = sq;
+  __syncthreads();
+  if (tid < D) {
+    float tot = 0.0f;
+    for (int wv = 0; wv < WARPS2; ++wv) tot += nrm_part[wv];
+    mu_c[tid] = tot > 0.0f ? vj / sqrtf(tot) : vj;
+  }
+}
+
 // One CTA per (centroid, head).  The centroid's rows (bucket entries of every
 // tile, in tile order, so in position order) are first listed in shared
 // memory, one lookup per row by one thread; then CH threads share each row,
@@ -156,16 +232,12 @@ ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
                   const int32_t* __restrict__ perm, float* __restrict__ mu, float decay) {
   pdl_trigger();
   pdl_wait();
-  constexpr int CH = D / 8;          // threads per row
-  constexpr int RS = THREADS2 / CH;  // rows in flight per pass over the list
   constexpr int LIST = 1024;         // rows listed per round
   extern __shared__ int32_t offs[];  // [Tn + 1] offsets, then [Tn] bucket starts
   int32_t* sts = offs + Tn + 1;
   __shared__ int rowlist[LIST];
-  __shared__ float red[RS][D];
-  __shared__ float nrm_part[WARPS2];
   const int c = blockIdx.x, h = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int32_t* cnt = counts + ((size_t)h * k + c) * Tn;
   const int32_t* st = starts + ((size_t)h * k + c) * Tn;
   const long long rows_total = (long long)B * n;
@@ -191,7 +263,6 @@ ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
   const int N = offs[Tn];
   if (N == 0) return;  // no assigned row: centroid unchanged
 
-  const int ch = tid % CH, rs = tid / CH;
   float acc[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
@@ -214,62 +285,9 @@ ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
       rowlist[i] = g;
     }
     __syncthreads();
-    // uniform trip count: the shuffles below involve every lane of the warp.
-    // Two rows in flight per thread, each kept as its raw 16 bytes (8 bf16 or
-    // 4 fp32 -- for fp32 rows the thread's 8 features are two 16-byte halves)
-    // and converted when used, which keeps the register count low.
-    for (int base = 0; base < nl; base += 2 * RS) {
-      Raw8<T> x[2];
-      int gg[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int i = base + rs + u * RS;
-        gg[u] = (i < nl) ? rowlist[i] : -1;
-        if (gg[u] >= 0) {
-          const int b = gg[u] / n, t = gg[u] - b * n;
-          x[u].load(qk + (((size_t)b * H + h) * n + t) * D + ch * 8);
-        } else {
-          x[u].zero();
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        float sx = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) sx += x[u].at(j);
-        const float mean = group_sum<CH>(sx) / (float)D;
-        float ss = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float a = x[u].at(j) - mean;
-          ss = fmaf(a, a, ss);
-        }
-        ss = group_sum<CH>(ss);
-        const float inv = (gg[u] >= 0 && ss > 0.0f) ? 1.0f / sqrtf(ss) : 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = fmaf(x[u].at(j) - mean, inv, acc[j]);
-      }
-    }
+    add_rows<T, D>(qk, H, n, h, rowlist, nl, acc);
   }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) red[rs][ch * 8 + j] = acc[j];
-  __syncthreads();
-  float vj = 0.0f;
-  if (tid < D) {
-    float sum = 0.0f;
-    for (int r = 0; r < RS; ++r) sum += red[r][tid];
-    const float mean_j = sum / (float)N;
-    vj = decay * old + (1.0f - decay) * mean_j;
-  }
-  float sq = warp_sum(vj * vj);
-  if (lane == 0) nrm_part[warp] = sq;
-  __syncthreads();
-  if (tid < D) {
-    float tot = 0.0f;
-    for (int wv = 0; wv < WARPS2; ++wv) tot += nrm_part[wv];
-    const float out = tot > 0.0f ? vj / sqrtf(tot) : vj;
-    mu[((size_t)h * k + c) * D + tid] = out;
-  }
+  finish_centroid<D>(acc, N, old, decay, mu + ((size_t)h * k + c) * D);
 }
 
 template <typename T, int D>
