@@ -73,6 +73,7 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
   __shared__ int m_s[NS][ROWS];      // its membership count
   __shared__ int cl_s[NS][ROWS];     // its cluster
   __shared__ int bh_s[NS];           // the tile's batch*head
+  __shared__ unsigned long long dst_s[2][ROWS];  // per group: output row address | kind
   __shared__ uint32_t tmem_base_sh;
   __shared__ int stop_flag, prod_abort;
 
@@ -253,48 +254,63 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
       const int whi = __reduce_max_sync(0xffffffffu, jmax);
       const int ch_lo = (whi > wlo) ? (wlo >> 4) : 0;
       const int ch_hi = (whi > wlo) ? ((whi + 15) >> 4) : 0;
+      // TMEM is read two 16-column chunks per wait
       float mrow = -INFINITY;
-      for (int ch = ch_lo; ch < ch_hi; ++ch) {
-        uint32_t rr[16];
-        tc::tmem_ld16(t_row + ch * 16, rr);
+      for (int ch = ch_lo; ch < ch_hi; ch += 2) {
+        uint32_t rr[2][16];
+        tc::tmem_ld16(t_row + ch * 16, rr[0]);
+        if (ch + 1 < ch_hi) tc::tmem_ld16(t_row + (ch + 1) * 16, rr[1]);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const int col = ch * 16 + jj;
-          if (col >= jmin && col < jmax) mrow = fmaxf(mrow, __uint_as_float(rr[jj]));
+        for (int hh = 0; hh < 2; ++hh) {
+          if (ch + hh >= ch_hi) break;
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int col = (ch + hh) * 16 + jj;
+            if (col >= jmin && col < jmax) mrow = fmaxf(mrow, __uint_as_float(rr[hh][jj]));
+          }
         }
       }
       const float mscaled = (mrow == -INFINITY) ? 0.0f : mrow * scale_log2;
       float lsum = 0.0f;
       const uint32_t prow = tc::smem_u32(st) + (r >> 3) * 2048 + (r & 7) * 16;
-#pragma unroll 1
-      for (int ch = 0; ch < ROWS / 16; ++ch) {
-        uint32_t pk[8];
-        if (ch >= ch_lo && ch < ch_hi) {
-          uint32_t rr[16];
-          tc::tmem_ld16(t_row + ch * 16, rr);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int jj = 0; jj < 16; jj += 2) {
-            const int col = ch * 16 + jj;
-            const bool ok0 = col >= jmin && col < jmax;
-            const bool ok1 = col + 1 >= jmin && col + 1 < jmax;
-            const float e0 = ok0 ? exp2f(__uint_as_float(rr[jj]) * scale_log2 - mscaled) : 0.0f;
-            const float e1 = ok1 ? exp2f(__uint_as_float(rr[jj + 1]) * scale_log2 - mscaled) : 0.0f;
-            const uint32_t pp = pack_bf16(e0, e1);
-            pk[jj >> 1] = pp;
-            lsum += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xffff0000u);
-          }
-        } else {
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) pk[jj] = 0u;
-        }
+      auto store_chunk = [&](int ch, const uint32_t (&pk)[8]) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const uint32_t addr = prow + (2 * ch + h) * 128;
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * h]),
                        "r"(pk[4 * h + 1]), "r"(pk[4 * h + 2]), "r"(pk[4 * h + 3])
                        : "memory");
+        }
+      };
+      {
+        const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll 1
+        for (int ch = 0; ch < ROWS / 16; ++ch)
+          if (ch < ch_lo || ch >= ch_hi) store_chunk(ch, zero);
+      }
+#pragma unroll 1
+      for (int ch = ch_lo; ch < ch_hi; ch += 2) {
+        uint32_t rr[2][16];
+        tc::tmem_ld16(t_row + ch * 16, rr[0]);
+        if (ch + 1 < ch_hi) tc::tmem_ld16(t_row + (ch + 1) * 16, rr[1]);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          if (ch + hh >= ch_hi) break;
+          uint32_t pk[8];
+#pragma unroll
+          for (int jj = 0; jj < 16; jj += 2) {
+            const int col = (ch + hh) * 16 + jj;
+            const bool ok0 = col >= jmin && col < jmax;
+            const bool ok1 = col + 1 >= jmin && col + 1 < jmax;
+            const float e0 = ok0 ? exp2f(__uint_as_float(rr[hh][jj]) * scale_log2 - mscaled) : 0.0f;
+            const float e1 = ok1 ? exp2f(__uint_as_float(rr[hh][jj + 1]) * scale_log2 - mscaled) : 0.0f;
+            const uint32_t pp = pack_bf16(e0, e1);
+            pk[jj >> 1] = pp;
+            lsum += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xffff0000u);
+          }
+          store_chunk(ch + hh, pk);
         }
       }
       tc::fence_proxy_async_smem();  // P (generic writes) before the MMA reads it
@@ -329,29 +345,41 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
       if (lane == 0) mbar_arrive(&tfree_bar[grp]);  // the accumulator may be reused
 
       // ---- copy-out: each warp writes its own 32 rows, row-contiguously -----
-      const int bh = bh_s[s];
-      const int my_m = m_s[s][r];
-      const int my_cl = cl_s[s][r];
-      const int my_slot = r - ci * w;
-      const int single = (row_valid && my_m == 1) ? 1 : 0;
+      // The owner of a row publishes where the row goes (bf16 into `out`,
+      // fp32 into its slot row of `yslot`, or nowhere for padding); then the
+      // warp copies row after row, every lane moving 16 bytes of it.
+      {
+        const int bh = bh_s[s];
+        const int my_m = m_s[s][r];
+        const int my_cl = cl_s[s][r];
+        void* dst = nullptr;
+        int kind = 0;  // 0 none, 1 bf16 out, 2 fp32 slot row
+        if (row_valid) {
+          if (my_m == 1) {
+            dst = out + ((size_t)bh * n + my_pos) * D;
+            kind = 1;
+          } else {
+            dst = yslot + (((size_t)bh * k + my_cl) * w + (r - ci * w)) * D;
+            kind = 2;
+          }
+        }
+        dst_s[grp][r] = reinterpret_cast<unsigned long long>(dst) | (unsigned long long)kind;
+      }
+      __syncwarp();
       const int chn = lane % CPR;
 #pragma unroll 4
       for (int it = 0; it < 32 / RPI; ++it) {
-        const int rr_ = it * RPI + lane / CPR;  // row of this warp; owner is lane rr_
-        const int row = 32 * quad + rr_;
-        const int t = __shfl_sync(0xffffffffu, my_pos, rr_);
-        const int sg = __shfl_sync(0xffffffffu, single, rr_);
-        const int cl = __shfl_sync(0xffffffffu, my_cl, rr_);
-        const int sl = __shfl_sync(0xffffffffu, my_slot, rr_);
+        const int row = 32 * quad + it * RPI + lane / CPR;
+        const unsigned long long dk = dst_s[grp][row];
         const float4 val = stage[row * CPR + (chn ^ (row & 7))];
-        if (t < 0) continue;
-        if (sg) {
+        const int kind = (int)(dk & 3u);
+        if (kind == 1) {
           uint2 u;
           u.x = pack_bf16(val.x, val.y);
           u.y = pack_bf16(val.z, val.w);
-          *reinterpret_cast<uint2*>(out + ((size_t)bh * n + t) * D + chn * 4) = u;
-        } else {
-          *reinterpret_cast<float4*>(yslot + (((size_t)bh * k + cl) * w + sl) * D + chn * 4) = val;
+          reinterpret_cast<uint2*>(dk & ~3ull)[chn] = u;
+        } else if (kind == 2) {
+          reinterpret_cast<float4*>(dk & ~3ull)[chn] = val;
         }
       }
       __syncwarp();
