@@ -336,6 +336,27 @@ def run_reference(args, wl):
 
 
 # ---------------------------------------------------------------------------
+# multi-rank bookkeeping (one process per GPU; no data-path collective)
+# ---------------------------------------------------------------------------
+
+def slowest_rank_ms(t_ms, device=None):
+    """The step time of the slowest rank (all-reduce MAX); t_ms itself when
+    running alone."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(t_ms)
+    tt = torch.tensor([float(t_ms)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, t_ms):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world / (t_ms * 1e-3)
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 
@@ -427,11 +448,8 @@ def run_ours(args, wl):
         torch.cuda.synchronize()
     gpu_launches = launches_per_step * args.steps  # kernels the replays ran
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    t_ms = statistics.mean(step_ms)
+    t_ms = slowest_rank_ms(statistics.mean(step_ms), dev)
     if world > 1:
-        tt = torch.tensor([t_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms = float(tt.item())
         dist.barrier()
     ws.check()
 
@@ -475,11 +493,7 @@ def run_ours(args, wl):
         out_h.copy_(out, non_blocking=True)
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = slowest_rank_ms(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev), dev)
 
     if rank != 0:
         if world > 1:
@@ -489,7 +503,7 @@ def run_ours(args, wl):
     peaks = _peaks()
     clocks = clk.summary()
     tokens = wl.tokens * world
-    value = tokens / (t_ms * 1e-3)
+    value = job_tokens_per_s(wl.tokens, world, t_ms)
     tflops = wl.nominal_flops() * world / (t_ms * 1e-3) / 1e12
 
     # dominant kernel roofline
@@ -534,7 +548,8 @@ def run_ours(args, wl):
                    "CUDA events around each launch"},
         "tflops": tflops, "tflops_frac_bf16": tflops / peaks["bf16_tflops"],
         "roofline": roof,
-        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_tokens_per_s(wl.tokens, world, e2e_ms), "unit": UNIT,
+                "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": gpu_launches, "launches_per_step": launches_per_step,
         "clocks": clocks, "kernels": kern,
