@@ -92,18 +92,27 @@ KERNEL_BOUND = {
 }
 
 KERNEL_SOURCES = {
-    "score_simt": "k_score_simt.cu", "score_tc": "k_score_tc.cu", "select_topw": "k_select.cu",
-    "attention_simt": "k_attention_simt.cu", "attention_tc": "k_attention_tc.cu",
-    "scatter_average": "k_scatter.cu", "ema_bucket": "k_ema.cu", "ema_update": "k_ema.cu",
-    "centroid_prep": "k_score_tc.cu",
+    "score_simt": ["k_score_simt.cu"], "score_tc": ["k_score_tc.cu", "tc_ptx.cuh"],
+    "centroid_prep": ["k_score_tc.cu"], "select_topw": ["k_select.cu"],
+    "attention_simt": ["k_attention_simt.cu"],
+    "attention_tc": ["k_attention_tc.cu", "k_attention_pipe.cu", "attn_common.cuh", "tc_ptx.cuh"],
+    "scatter_average": ["k_scatter.cu"], "ema_bucket": ["k_ema.cu"], "ema_update": ["k_ema.cu"],
 }
 
 
 def kernel_source_hash(name):
-    p = os.path.join(ROOT, "content_sparse_attention_shared_b300", "csrc", KERNEL_SOURCES.get(name, ""))
-    if not os.path.isfile(p):
+    """Hash of the source files a kernel kind is built from (so a stored ncu
+    traffic figure is only used while those sources are unchanged)."""
+    files = KERNEL_SOURCES.get(name)
+    if not files:
         return None
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for f in files:
+        p = os.path.join(ROOT, "content_sparse_attention_shared_b300", "csrc", f)
+        if not os.path.isfile(p):
+            return None
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def traffic_for(name, wl_name):
