@@ -70,6 +70,30 @@ __device__ __forceinline__ void gather_mnmajor(uint8_t* dst, const bf16* __restr
   }
 }
 
+// Gather 128 rows (positions pos[r], -1 = zero row) of D bf16 into the
+// 128-byte-swizzled row layout: D/64 blocks of [128 rows x 128 bytes], row r
+// of block kb at kb*16384 + r*128, its 16-byte chunk j XOR-permuted to
+// (j ^ (r % 8)).  Read as the K-major operand of S = Q K^T and as the MN-major
+// operand of O = P V.  A warp instruction moves four whole 128-byte row pieces
+// (eight lanes per row: full-line global reads, conflict-free shared writes).
+template <int D>
+__device__ __forceinline__ void gather_sw128(uint8_t* dst, const bf16* __restrict__ src,
+                                             const int* pos, int warp, int nwarps) {
+  const int lane = threadIdx.x & 31;
+  constexpr int KB = D / 64;
+  constexpr int ITEMS = (ROWS / 4) * KB;
+  const uint32_t base = tc::smem_u32(dst);
+  const int jj = lane & 7;
+  for (int it = warp; it < ITEMS; it += nwarps) {
+    const int kb = it % KB;
+    const int r = (it / KB) * 4 + (lane >> 3);
+    const int p = pos[r];
+    const uint32_t off = kb * (ROWS * 128) + r * 128 + ((jj ^ (r & 7)) << 4);
+    const bf16* g = src + (size_t)(p < 0 ? 0 : p) * D + kb * 64 + jj * 8;
+    cp_async16(base + off, g, p >= 0);
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);

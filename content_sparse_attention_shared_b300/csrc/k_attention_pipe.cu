@@ -13,8 +13,9 @@
 // One CTA per SM walks the tiles first, first + grid, ...  Warp roles:
 //   warps 0-3   producers: read the tile's member positions and membership
 //               counts, gather the Q and V rows with 16-byte cp.async into a
-//               ring of NS stages (no-swizzle core-matrix layouts), and mark a
-//               stage full once their copies have landed;
+//               ring of NS stages (128-byte-swizzled rows, read as the K-major
+//               operand of S and the MN-major operand of O), and mark a stage
+//               full once their copies have landed;
 //   warp 12     issues the MMAs: S = Q Q^T into the TMEM accumulator of the
 //               tile's group, then O = P V into the same columns;
 //   warps 4-7,  two softmax/epilogue groups taking alternate tiles: softmax of
@@ -150,8 +151,8 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
       const bf16* q_bh = q + (size_t)bh * n * D;
       const bf16* v_bh = v + (size_t)bh * n * D;
       uint8_t* st = sm + (size_t)s * L::STAGE;
-      gather_kmajor<D>(st, q_bh, pos_s[s], warp, 4);
-      gather_mnmajor<D>(st + L::XB, v_bh, pos_s[s], warp, 4);
+      gather_sw128<D>(st, q_bh, pos_s[s], warp, 4);
+      gather_sw128<D>(st + L::XB, v_bh, pos_s[s], warp, 4);
       cp_async_commit();
       if (i + 1 < T) load_meta(tile + stride, np, nm, ncl);  // next tile, while copies fly
       cp_async_wait_all();           // this thread's copies have landed
@@ -163,7 +164,6 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
     if (lane == 0) {
       constexpr uint32_t IDESC_S = tc::idesc_f16(ROWS, ROWS, true, false, false);
       constexpr uint32_t IDESC_O = tc::idesc_f16(ROWS, D, true, false, true);
-      constexpr uint32_t SBO_QK = (D / 8) * 128;
       // S(j) needs tile j's rows and a free accumulator; O(j) needs P(j).
       // Whichever is ready is issued, so O(j) never waits behind the data
       // of tile j + 1.
@@ -179,7 +179,7 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
         const uint32_t qa = tc::smem_u32(sm + (size_t)s * L::STAGE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = tc::smem_desc_noswizzle(qa + kk * 256, 128, SBO_QK);
+          const uint64_t ad = tc::smem_desc_sw128(qa + (kk / 4) * (ROWS * 128) + (kk % 4) * 32, 1024);
           tc::mma_f16_ss(tmem + a * 128, ad, ad, IDESC_S, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(&sfull_bar[a]);
@@ -195,7 +195,7 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
 #pragma unroll
         for (int kk = 0; kk < ROWS / 16; ++kk) {
           const uint64_t ad = tc::smem_desc_noswizzle(pa + kk * 256, 128, 2048);
-          const uint64_t bd = tc::smem_desc_noswizzle(va + kk * 256, 128, 2048);
+          const uint64_t bd = tc::smem_desc_sw128_mn(va + kk * 2048, ROWS * 128, 1024);
           tc::mma_f16_ss(tmem + a * 128, ad, bd, IDESC_O, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(&ofull_bar[a]);
