@@ -329,59 +329,56 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
 // Rows of n <= THREADS * 32 scores, n a multiple of 4.  Warp j owns the
 // contiguous segment [j*seg, (j+1)*seg) (seg a multiple of 128), in chunks of
 // 128 positions; lane l owns positions 4l..4l+3 of every chunk, so every load
-// is a coalesced float4 (512 bytes per warp), four in flight per thread.  Each
-// thread keeps its two largest scores; the row is read a second time only by
-// a thread whose second largest score is itself a candidate.
+// is a coalesced float4 (512 bytes per warp), four in flight per thread.
 // The w-th largest of the per-thread maxima is a lower bound on the w-th
 // largest score (the w threads holding the largest maxima own w distinct
 // scores at least that large), so every kept score lies in a bin at or above
-// the bin b_L of that maximum.  Only the scores of bin >= b_L (typically a few
-// more than w) become candidates.  Each candidate's rank by (score desc,
-// position asc) decides whether it is kept; each kept candidate's rank by
-// position among the kept ones is its output slot.  No per-score atomics,
-// no bitmap and no ordered compaction pass.  Rows where the bound leaves more
-// than RCAP candidates (many equal scores), or with fewer than w non-empty
-// threads, use the exact radix select.
+// the bin b_L of that maximum; b_L is found by bisection over the bins with
+// block-wide counts (no histogram).  Only threads whose maximum reaches b_L
+// read their scores again; the scores of bin >= b_L (typically a few more than
+// w) become candidates, appended with one shared-memory atomic per warp and
+// packed as 64-bit keys (score key, complemented position)
+// so that one integer compare orders them by (score desc, position asc).  A
+// candidate is kept when fewer than w keys exceed its own; kept positions are
+// set in a position bitmap, and a block-wide scan over the bitmap words puts
+// them out in ascending order.  Rows where the bound leaves more than RCAP
+// candidates (many equal scores), or with fewer than w non-empty threads, use
+// the exact radix select.
 // ---------------------------------------------------------------------------
 constexpr int CHUNKS_MAX = 8;  // 128-position chunks per warp
 constexpr int BOUND_N_MAX = THREADS * 4 * CHUNKS_MAX;
 constexpr int RCAP = 1024;
+static_assert(BOUND_N_MAX / 32 == THREADS, "one position-bitmap word per thread");
+
+__device__ __forceinline__ unsigned long long cand_key(float x, int p) {
+  return ((unsigned long long)score_key(x) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)p);
+}
 
 __global__ void __launch_bounds__(THREADS, 7)
 select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
                          int32_t* __restrict__ idx, int32_t* __restrict__ mcount,
                          int32_t* __restrict__ slots) {
   pdl_trigger();
-  __shared__ unsigned hist[NBINS];
-  __shared__ int cand_t[RCAP];
-  __shared__ float cand_s[RCAP];
-  __shared__ unsigned char cand_keep[RCAP];
+  __shared__ unsigned hist[256];  // radix fallback
+  __shared__ __align__(16) unsigned long long ckey[RCAP + 1];
+  __shared__ unsigned kept[THREADS];  // position bitmap, 32 positions per word
   __shared__ int wsum[4 * WARPS];
-  __shared__ int s_bl, s_ncand;
+  __shared__ int s_ncand;
 
   const int c = blockIdx.x;
   const int bh = blockIdx.y;
   const float* row = S + ((size_t)bh * k + c) * n;
   const float4* row4 = reinterpret_cast<const float4*>(row);
   const SelectOut so{idx + ((size_t)bh * k + c) * w, mcount, slots, bh, c, n, w};
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int seg = ((n + WARPS * 128 - 1) / (WARPS * 128)) * 128;  // <= 128 * CHUNKS_MAX
-  const int w0 = warp * seg + 4 * lane;                           // first position of this thread
+  const int w0 = warp * seg + 4 * (tid & 31);                     // first position of this thread
 
-  for (int b = tid; b < NBINS; b += THREADS) hist[b] = 0u;
-  if (tid == 0) {
-    s_ncand = 0;
-    s_bl = -1;
-  }
+  kept[tid] = 0u;
+  if (tid == 0) s_ncand = 0;
   pdl_wait();
 
-  // 1. per-thread maximum, and the two largest scores with their slots
-  //    (bit 4*i+e: chunk i, element e)
-  float m1 = -INFINITY, m2 = -INFINITY;
-  int b1 = -1, b2 = -1;
-#pragma unroll
-  for (int i0 = 0; i0 < CHUNKS_MAX; i0 += 4) {
-    float4 v[4];
+  auto load_chunks = [&](int i0, float4 (&v)[4]) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u;
@@ -389,96 +386,84 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
       v[u] = (128 * i < seg && p < n) ? __ldcg(row4 + (p >> 2))
                                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float x = e4[e];
-        const int b = 4 * (i0 + u) + e;
-        if (x > m1) {
-          m2 = m1; b2 = b1;
-          m1 = x; b1 = b;
-        } else if (x > m2) {
-          m2 = x; b2 = b;
-        }
-      }
-    }
-  }
-  const float m = m1;
-  __syncthreads();  // hist cleared
-  if (w0 < n) atomicAdd(&hist[score_bin(m)], 1u);
-  __syncthreads();
+  };
 
-  // 2. bin of the w-th largest maximum (descending scan over the bins)
+  // 1. per-thread maximum
+  float m = -INFINITY;
+#pragma unroll
+  for (int i0 = 0; i0 < CHUNKS_MAX; i0 += 4) {
+    float4 v[4];
+    load_chunks(i0, v);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) m = fmaxf(m, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
+  }
+  const int mbin = w0 < n ? score_bin(m) : -1;
+
+  // 2. b_L = the largest bin b with at least w thread maxima in bins >= b,
+  //    by bisection over the bins with block-wide counts (no histogram, no
+  //    shared-memory atomics); -1 when fewer than w threads hold scores
+  int bl;
   {
-    const int hi_bin = NBINS - 1 - BINS_PER_THREAD * tid;
-    unsigned hb[BINS_PER_THREAD];
-    int lsum = 0;
-#pragma unroll
-    for (int q = 0; q < BINS_PER_THREAD; ++q) {
-      hb[q] = hist[hi_bin - q];
-      lsum += (int)hb[q];
-    }
-    int total;
-    const int excl = block_exclusive_scan<THREADS>(lsum, wsum, total);
-    if (excl < w && w <= excl + lsum) {
-      int cum = excl;
-#pragma unroll
-      for (int q = 0; q < BINS_PER_THREAD; ++q) {
-        if (cum < w && cum + (int)hb[q] >= w) s_bl = hi_bin - q;
-        cum += (int)hb[q];
+    int lo = 0, hi = NBINS - 1;  // invariant: count(>= lo) >= w, count(>= hi + 1) < w
+    if (__syncthreads_count(mbin >= 0) < w) {
+      bl = -1;
+    } else {
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__syncthreads_count(mbin >= mid) >= w) lo = mid;
+        else hi = mid - 1;
       }
+      bl = lo;
     }
   }
-  __syncthreads();
-  const int bl = s_bl;  // -1: fewer than w threads hold scores
 
-  // 3. candidates: scores of bin >= b_L.  A float compare against a value a
-  //    little below the bin's lower edge filters first; the bin itself is
-  //    only computed for the few scores that pass.
-  if (bl >= 0) {
-    const float pre = bl > 0 ? (float)bl * (1.0f / 1024.0f) - 1.0f - 1.0e-5f : -INFINITY;
-    auto is_cand = [&](float x) { return x >= pre && score_bin(x) >= bl; };
+  // 3. candidates: scores of bin >= b_L, read again only by the threads whose
+  //    maximum qualifies.  A float compare against a value a little below the
+  //    bin's lower edge filters first; the bin itself is only computed for
+  //    the few scores that pass.  One shared-memory atomic per warp reserves
+  //    the warp's candidate slots.
+  {
+    const bool mine = bl >= 0 && mbin >= bl;
+    // (finite for bin 0, so that the -inf padding past n never qualifies)
+    const float pre = bl > 0 ? (float)bl * (1.0f / 1024.0f) - 1.0f - 1.0e-5f : -3.0e38f;
     uint32_t cmask = 0u;
-    bool fast = false;
-    if (b2 >= 0 && is_cand(m2)) {
-      // a third score of this thread may qualify too: read the segment again
+    float x0 = 0.0f, x1 = 0.0f;  // the first two candidate scores (usually all of them)
+    if (mine) {
 #pragma unroll
       for (int i0 = 0; i0 < CHUNKS_MAX; i0 += 4) {
         float4 v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = i0 + u;
-          const int p = w0 + 128 * i;
-          v[u] = (128 * i < seg && p < n) ? __ldcg(row4 + (p >> 2))
-                                          : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        }
+        load_chunks(i0, v);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (is_cand(e4[e])) cmask |= 1u << (4 * (i0 + u) + e);
+          for (int e = 0; e < 4; ++e) {
+            if (e4[e] >= pre && score_bin(e4[e]) >= bl) {
+              if (cmask == 0u) x0 = e4[e];
+              else if ((cmask & (cmask - 1u)) == 0u) x1 = e4[e];
+              cmask |= 1u << (4 * (i0 + u) + e);
+            }
+          }
         }
       }
-    } else if (b1 >= 0 && is_cand(m1)) {
-      // every other score of the thread is <= m2, which does not qualify
-      cmask = 1u << b1;
-      fast = true;
     }
-    if (cmask != 0u) {
-      int slot = atomicAdd(&s_ncand, __popc(cmask));
-      while (cmask) {
-        const int bit = __ffs(cmask) - 1;
-        cmask &= cmask - 1;
-        const int p = w0 + 128 * (bit >> 2) + (bit & 3);
-        if (slot < RCAP) {
-          cand_t[slot] = p;
-          cand_s[slot] = fast ? m1 : __ldcg(row + p);
-        }
-        ++slot;
-      }
+    const int cnt = __popc(cmask);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if ((tid & 31) >= o) incl += y;
+    }
+    const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+    int base = 0;
+    if ((tid & 31) == 31 && wtot > 0) base = atomicAdd(&s_ncand, wtot);
+    base = __shfl_sync(0xffffffffu, base, 31);
+    int slot = base + incl - cnt;
+    for (int j = 0; cmask != 0u; cmask &= cmask - 1u, ++slot, ++j) {
+      const int bit = __ffs(cmask) - 1;
+      const int p = w0 + 128 * (bit >> 2) + (bit & 3);
+      const float x = j == 0 ? x0 : j == 1 ? x1 : __ldcg(row + p);
+      if (slot < RCAP) ckey[slot] = cand_key(x, p);
     }
   }
   __syncthreads();
@@ -487,27 +472,33 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
     radix_select_row(row, n, w, so, hist, wsum);  // uniform branch
     return;
   }
+  if (tid == 0) ckey[nc] = 0ull;  // pad to an even count (0 is below every key)
+  __syncthreads();
 
-  // 4. kept: rank by (score desc, position asc) below w
+  // 4. kept: fewer than w candidate keys above its own
+  const int nc2 = (nc + 1) & ~1;
   for (int i = tid; i < nc; i += THREADS) {
-    const float si = cand_s[i];
-    const int ti = cand_t[i];
+    const unsigned long long ki = ckey[i];
     int rank = 0;
-    for (int j = 0; j < nc; ++j) {
-      const float sj = cand_s[j];
-      rank += (sj > si) | ((sj == si) & (cand_t[j] < ti));
+    for (int j = 0; j < nc2; j += 2) {
+      const ulonglong2 kj = *reinterpret_cast<const ulonglong2*>(&ckey[j]);
+      rank += (kj.x > ki) + (kj.y > ki);
     }
-    cand_keep[i] = rank < w ? 1 : 0;
+    if (rank < w) {
+      const int p = (int)(0xFFFFFFFFu - (uint32_t)ki);
+      atomicOr(&kept[p >> 5], 1u << (p & 31));
+    }
   }
   __syncthreads();
 
-  // 5. a kept candidate's output slot is its rank by position among the kept
-  for (int i = tid; i < nc; i += THREADS) {
-    if (!cand_keep[i]) continue;
-    const int ti = cand_t[i];
-    int o = 0;
-    for (int j = 0; j < nc; ++j) o += cand_keep[j] & (cand_t[j] < ti);
-    if (o < w) so.emit(o, ti);
+  // 5. ordered emission: word q's kept positions go to the output slots after
+  //    those of words 0..q-1
+  {
+    const unsigned km = kept[tid];
+    int total;
+    int o = block_exclusive_scan<THREADS>(__popc(km), wsum, total);
+    for (unsigned rem = km; rem != 0u; rem &= rem - 1u, ++o)
+      if (o < w) so.emit(o, tid * 32 + __ffs(rem) - 1);
   }
 }
 
