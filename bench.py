@@ -70,10 +70,9 @@ def kernel_work(name, wl):
         return dict(bytes=byts, flops=4.0 * BH * k * w * w * d)
     if name == "scatter_average":
         return dict(bytes=BH * n * 4 + BH * n * d * s, flops=0.0)
-    if name == "ema_bucket":
-        return dict(bytes=BH * n * 4 * 2, flops=0.0)
     if name == "ema_update":
-        return dict(bytes=BH * n * d * s + wl.H * k * d * 8, flops=3.0 * BH * n * d)
+        # rows, assignments, centroids read and written
+        return dict(bytes=BH * n * d * s + BH * n * 4 + wl.H * k * d * 8, flops=3.0 * BH * n * d)
     if name == "centroid_prep":
         kpad = (k + 15) // 16 * 16
         return dict(bytes=wl.H * k * d * 4 + wl.H * (3 * kpad * d * 2 + kpad * 4), flops=0.0)
@@ -87,7 +86,7 @@ def alu_peak_tflops(sm_mhz):
 
 KERNEL_BOUND = {
     "score_simt": "alu", "attention_simt": "alu", "score_tc": "hbm", "attention_tc": "hbm",
-    "select_topw": "hbm", "scatter_average": "hbm", "ema_bucket": "hbm", "ema_update": "hbm",
+    "select_topw": "hbm", "scatter_average": "hbm", "ema_update": "hbm",
     "centroid_prep": "hbm",
 }
 
@@ -96,7 +95,7 @@ KERNEL_SOURCES = {
     "centroid_prep": ["k_score_tc.cu"], "select_topw": ["k_select.cu"],
     "attention_simt": ["k_attention_simt.cu"],
     "attention_tc": ["k_attention_tc.cu", "k_attention_pipe.cu", "attn_common.cuh", "tc_ptx.cuh"],
-    "scatter_average": ["k_scatter.cu"], "ema_bucket": ["k_ema.cu"], "ema_update": ["k_ema.cu"],
+    "scatter_average": ["k_scatter.cu"], "ema_update": ["k_ema.cu"],
 }
 
 

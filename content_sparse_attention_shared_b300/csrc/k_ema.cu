@@ -9,101 +9,21 @@
 //     mu_c <- normalise(decay * mu_c + (1 - decay) * mean of the assigned r_t),
 // and leaves a centroid without rows untouched.
 //
-// No floating-point atomics: kernel 1 counting-sorts the rows of every tile
-// of 256 rows by centroid (a stable, position-ordered bucket per centroid),
-// kernel 2 gives each (centroid, head) one CTA that lists its rows from the
-// buckets, re-normalises each row on the fly, sums them in a fixed order,
-// blends and renormalises.  The result is deterministic.
+// No floating-point atomics and one kernel: each (centroid, head) CTA scans
+// the head's assignments itself (coalesced 16-byte loads, 8192 rows per pass),
+// lists its rows in a fixed order with one block-wide scan, re-normalises
+// each row on the fly, sums them in that order, blends and renormalises.  The
+// result is deterministic.
 #include "rt_internal.cuh"
 
 namespace rt {
 namespace {
 
-constexpr int TE = 256;  // rows per tile = threads of kernel 1
-constexpr int WARPS1 = TE / 32;
 constexpr int THREADS2 = 256;
 constexpr int WARPS2 = THREADS2 / 32;
-
-struct EmaLayout {
-  int T;  // tiles per head
-  int32_t* counts;  // [H][k][T]
-  int32_t* starts;  // [H][k][T]
-  int32_t* perm;    // [H][T*TE]
-};
-
-EmaLayout ema_layout(void* ws, int B, int H, int n, int k) {
-  EmaLayout L;
-  const long long rows = (long long)B * n;
-  L.T = (int)((rows + TE - 1) / TE);
-  char* p = static_cast<char*>(ws);
-  L.counts = reinterpret_cast<int32_t*>(p);
-  p += ((size_t)H * k * L.T * 4 + 255) / 256 * 256;
-  L.starts = reinterpret_cast<int32_t*>(p);
-  p += ((size_t)H * k * L.T * 4 + 255) / 256 * 256;
-  L.perm = reinterpret_cast<int32_t*>(p);
-  return L;
-}
-
-__global__ void __launch_bounds__(TE)
-ema_bucket_kernel(const int32_t* __restrict__ assign, int B, int H, int n, int k, int T,
-                  int32_t* __restrict__ counts, int32_t* __restrict__ starts,
-                  int32_t* __restrict__ perm) {
-  pdl_trigger();
-  extern __shared__ int32_t sm[];
-  int32_t* warp_cnt = sm;                 // [WARPS1][k]
-  int32_t* tot = sm + WARPS1 * k;         // [k]
-  int32_t* start = tot + k;               // [k]
-  const int tile = blockIdx.x, h = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < (WARPS1 + 2) * k; i += TE) sm[i] = 0;
-  pdl_wait();
-  __syncthreads();
-
-  const long long g = (long long)tile * TE + tid;
-  const long long rows = (long long)B * n;
-  int a = -1;
-  if (g < rows) {
-    const int b = (int)(g / n), t = (int)(g % n);
-    a = __ldcg(assign + ((size_t)b * H + h) * n + t);
-    if (a < 0 || a >= k) a = -1;  // out-of-range assignment: ignored
-  }
-  const unsigned peers = __match_any_sync(0xffffffffu, a);
-  const int rank = __popc(peers & ((1u << lane) - 1u));
-  if (a >= 0 && rank == 0) warp_cnt[warp * k + a] = __popc(peers);
-  __syncthreads();
-  // per centroid: exclusive prefix over warps (in place) and the tile total
-  for (int c = tid; c < k; c += TE) {
-    int run = 0;
-    for (int wv = 0; wv < WARPS1; ++wv) {
-      const int x = warp_cnt[wv * k + c];
-      warp_cnt[wv * k + c] = run;
-      run += x;
-    }
-    tot[c] = run;
-  }
-  __syncthreads();
-  {
-    // exclusive prefix of the tile totals over centroids (bucket starts)
-    __shared__ int wsum[WARPS1];
-    int carry = 0;
-    for (int c0 = 0; c0 < k; c0 += TE) {
-      const int c = c0 + tid;
-      int total;
-      const int ex = block_exclusive_scan<TE>(c < k ? tot[c] : 0, wsum, total);
-      if (c < k) start[c] = carry + ex;
-      carry += total;
-    }
-  }
-  __syncthreads();
-  for (int c = tid; c < k; c += TE) {
-    counts[((size_t)h * k + c) * T + tile] = tot[c];
-    starts[((size_t)h * k + c) * T + tile] = start[c];
-  }
-  if (a >= 0) {
-    const int p = start[a] + warp_cnt[warp * k + a] + rank;
-    perm[(size_t)h * T * TE + (size_t)tile * TE + p] = (int32_t)g;
-  }
-}
+constexpr int SCAN_PER_THREAD = 32;                    // assignments per thread per pass
+constexpr int SCAN_ROWS = THREADS2 * SCAN_PER_THREAD;  // rows per pass
+constexpr int LIST = 2048;                             // rows listed per summation round
 
 // 8 consecutive features of a row, kept in their storage format and read as
 // fp32 on use.
@@ -152,11 +72,12 @@ __device__ __forceinline__ void add_rows(const T* __restrict__ qk, int H, int n,
   constexpr int CH = D / 8;
   constexpr int RS = THREADS2 / CH;
   const int ch = threadIdx.x % CH, rs = threadIdx.x / CH;
-  for (int base = 0; base < nl; base += 2 * RS) {
-    Raw8<T> x[2];
-    int gg[2];
+  constexpr int RIF = 2;
+  for (int base = 0; base < nl; base += RIF * RS) {
+    Raw8<T> x[RIF];
+    int gg[RIF];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < RIF; ++u) {
       const int i = base + rs + u * RS;
       gg[u] = (i < nl) ? rowlist[i] : -1;
       if (gg[u] >= 0) {
@@ -167,7 +88,7 @@ __device__ __forceinline__ void add_rows(const T* __restrict__ qk, int H, int n,
       }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < RIF; ++u) {
       float sx = 0.0f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) sx += x[u].at(j);
@@ -218,121 +139,97 @@ __device__ __forceinline__ void finish_centroid(const float (&acc)[8], int N, fl
   }
 }
 
-// One CTA per (centroid, head).  The centroid's rows (bucket entries of every
-// tile, in tile order, so in position order) are first listed in shared
-// memory, one lookup per row by one thread; then CH threads share each row,
-// every thread reading one 16-byte chunk of 8 features: the row's mean and
-// centred norm come from shuffles inside the group and the thread adds its
-// 8 normalised features into registers.  Row slots are summed in a fixed
+// One CTA per (centroid, head).  Pass by pass over each sequence's n
+// positions, thread i examines positions base + 1024 j + 4 i + e (j < 8,
+// e < 4; one coalesced 16-byte load per j), keeps a 32-bit mask of the rows assigned to this
+// centroid, and a block-wide exclusive scan of the mask counts places them in
+// a shared list in (thread, j, e) order.  Then CH threads share each listed
+// row, every thread reading one 16-byte chunk of 8 features: the row's mean
+// and centred norm come from shuffles inside the group and the thread adds
+// its 8 normalised features into registers.  Row slots are summed in a fixed
 // order at the end, so the result is deterministic.
 template <typename T, int D>
 __global__ void __launch_bounds__(THREADS2, 8)
-ema_update_kernel(const T* __restrict__ qk, int B, int H, int n, int k, int Tn,
-                  const int32_t* __restrict__ counts, const int32_t* __restrict__ starts,
-                  const int32_t* __restrict__ perm, float* __restrict__ mu, float decay) {
+ema_update_kernel(const T* __restrict__ qk, const int32_t* __restrict__ assign, int B, int H,
+                  int n, int k, float* __restrict__ mu, float decay) {
   pdl_trigger();
-  pdl_wait();
-  constexpr int LIST = 1024;         // rows listed per round
-  extern __shared__ int32_t offs[];  // [Tn + 1] offsets, then [Tn] bucket starts
-  int32_t* sts = offs + Tn + 1;
   __shared__ int rowlist[LIST];
+  __shared__ int wsum[WARPS2];
   const int c = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x;
-  const int32_t* cnt = counts + ((size_t)h * k + c) * Tn;
-  const int32_t* st = starts + ((size_t)h * k + c) * Tn;
-  const long long rows_total = (long long)B * n;
-  const float old = (tid < D) ? __ldcg(mu + ((size_t)h * k + c) * D + tid) : 0.0f;  // early
-
-  // exclusive prefix of the per-tile counts over the tiles
-  {
-    __shared__ int wsum[WARPS2];
-    int carry = 0;
-    for (int i0 = 0; i0 < Tn; i0 += THREADS2) {
-      const int i = i0 + tid;
-      int total;
-      const int ex = block_exclusive_scan<THREADS2>(i < Tn ? __ldcg(cnt + i) : 0, wsum, total);
-      if (i < Tn) {
-        offs[i] = carry + ex;
-        sts[i] = __ldcg(st + i);
-      }
-      carry += total;
-    }
-    if (tid == 0) offs[Tn] = carry;
-  }
-  __syncthreads();
-  const int N = offs[Tn];
-  if (N == 0) return;  // no assigned row: centroid unchanged
+  const bool vec = (n & 3) == 0 && (reinterpret_cast<uintptr_t>(assign) & 15u) == 0;
+  pdl_wait();
+  const float old = (tid < D) ? __ldcg(mu + ((size_t)h * k + c) * D + tid) : 0.0f;
 
   float acc[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-
-  for (int f0 = 0; f0 < N; f0 += LIST) {
-    const int nl = min(LIST, N - f0);
-    __syncthreads();  // the previous round's list is consumed
-    for (int i = tid; i < nl; i += THREADS2) {
-      const int f = f0 + i;
-      // tile holding flattened entry f: last tl with offs[tl] <= f
-      int a0 = 0, a1 = Tn - 1;
-      while (a0 < a1) {
-        const int mid = (a0 + a1 + 1) >> 1;
-        if (offs[mid] <= f) a0 = mid; else a1 = mid - 1;
+  int N = 0;
+  for (int b = 0; b < B; ++b) {
+    const int32_t* arow = assign + ((size_t)b * H + h) * n;
+    for (int t0 = 0; t0 < n; t0 += SCAN_ROWS) {
+      // this thread's rows of the pass: bit 4 j + e <-> position t0 + 1024 j + 4 tid + e
+      uint32_t mask = 0u;
+#pragma unroll 4
+      for (int j = 0; j < SCAN_PER_THREAD / 4; ++j) {
+        const int t = t0 + j * (4 * THREADS2) + 4 * tid;
+        if (vec && t + 3 < n) {
+          const int4 a4 = __ldcg(reinterpret_cast<const int4*>(arow + t));
+          mask |= (uint32_t)(a4.x == c) << (4 * j + 0);
+          mask |= (uint32_t)(a4.y == c) << (4 * j + 1);
+          mask |= (uint32_t)(a4.z == c) << (4 * j + 2);
+          mask |= (uint32_t)(a4.w == c) << (4 * j + 3);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (t + e < n) mask |= (uint32_t)(__ldcg(arow + t + e) == c) << (4 * j + e);
+        }
       }
-      const int p = sts[a0] + (f - offs[a0]);
-      int g = -1;
-      if (p >= 0 && p < TE) g = __ldcg(perm + (size_t)h * Tn * TE + (size_t)a0 * TE + p);
-      if (g < 0 || (long long)g >= rows_total) g = -1;  // defensive
-      rowlist[i] = g;
+      int total;
+      const int ex = block_exclusive_scan<THREADS2>(__popc(mask), wsum, total);
+      // (out-of-range assignments never equal c, so they are never listed)
+      for (int sub = 0; sub < total; sub += LIST) {
+        int r = ex;
+        for (uint32_t mm = mask; mm != 0u; mm &= mm - 1u, ++r) {
+          const int bit = __ffs(mm) - 1;
+          if (r >= sub && r < sub + LIST)
+            rowlist[r - sub] = b * n + t0 + (bit >> 2) * (4 * THREADS2) + 4 * tid + (bit & 3);
+        }
+        __syncthreads();
+        add_rows<T, D>(qk, H, n, h, rowlist, min(LIST, total - sub), acc);
+        __syncthreads();  // the list may be rewritten
+      }
+      N += total;
     }
-    __syncthreads();
-    add_rows<T, D>(qk, H, n, h, rowlist, nl, acc);
   }
+  if (N == 0) return;  // no assigned row: centroid unchanged (uniform)
   finish_centroid<D>(acc, N, old, decay, mu + ((size_t)h * k + c) * D);
 }
 
 template <typename T, int D>
-cudaError_t launch_update(const void* qk, int B, int H, int n, int k, const EmaLayout& L,
+cudaError_t launch_update(const void* qk, const int32_t* assign, int B, int H, int n, int k,
                           float* mu, float decay, cudaStream_t s) {
-  const size_t smem = (size_t)(2 * L.T + 1) * sizeof(int32_t);
   auto kern = ema_update_kernel<T, D>;
-  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)(smem < 48 * 1024 ? 48 * 1024 : smem));
-  if (e != cudaSuccess) return e;
   launch_begin(K_EMA_UPDATE, s);
-  e = launch_pdl(kern, dim3(k, H), dim3(THREADS2), smem, s, static_cast<const T*>(qk), B, H, n, k,
-                 L.T, (const int32_t*)L.counts, (const int32_t*)L.starts, (const int32_t*)L.perm,
-                 mu, decay);
+  cudaError_t e = launch_pdl(kern, dim3(k, H), dim3(THREADS2), 0, s, static_cast<const T*>(qk),
+                             assign, B, H, n, k, mu, decay);
   launch_end(K_EMA_UPDATE, s);
   return e;
 }
 
 }  // namespace
 
-size_t ema_workspace_bytes(int B, int H, int n, int k) {
-  const long long rows = (long long)B * n;
-  const long long T = (rows + TE - 1) / TE;
-  size_t a = ((size_t)H * k * T * 4 + 255) / 256 * 256;
-  size_t p = ((size_t)H * T * TE * 4 + 255) / 256 * 256;
-  return 2 * a + p;
-}
+size_t ema_workspace_bytes(int, int, int, int) { return 0; }
 
 cudaError_t launch_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                        const int32_t* assign, float* mu, int k, float decay,
-                       void* ws, cudaStream_t s) {
-  EmaLayout L = ema_layout(ws, B, H, n, k);
-  const size_t smem1 = (size_t)(WARPS1 + 2) * k * sizeof(int32_t);
-  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(ema_bucket_kernel), (int)(smem1 < 48 * 1024 ? 48 * 1024 : smem1));
-  if (e != cudaSuccess) return e;
-  launch_begin(K_EMA_BUCKET, s);
-  e = launch_pdl(ema_bucket_kernel, dim3(L.T, H), dim3(TE), smem1, s, assign, B, H, n, k, L.T,
-                 L.counts, L.starts, L.perm);
-  launch_end(K_EMA_BUCKET, s);
-  if (e != cudaSuccess) return e;
+                       void* /*ws*/, cudaStream_t s) {
   if (dt == RT_F32) {
-    return d == 64 ? launch_update<float, 64>(qk, B, H, n, k, L, mu, decay, s)
-                   : launch_update<float, 128>(qk, B, H, n, k, L, mu, decay, s);
+    return d == 64 ? launch_update<float, 64>(qk, assign, B, H, n, k, mu, decay, s)
+                   : launch_update<float, 128>(qk, assign, B, H, n, k, mu, decay, s);
   }
-  return d == 64 ? launch_update<__nv_bfloat16, 64>(qk, B, H, n, k, L, mu, decay, s)
-                 : launch_update<__nv_bfloat16, 128>(qk, B, H, n, k, L, mu, decay, s);
+  return d == 64 ? launch_update<__nv_bfloat16, 64>(qk, assign, B, H, n, k, mu, decay, s)
+                 : launch_update<__nv_bfloat16, 128>(qk, assign, B, H, n, k, mu, decay, s);
 }
 
 }  // namespace rt
