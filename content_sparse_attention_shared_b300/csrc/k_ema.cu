@@ -23,7 +23,8 @@ constexpr int THREADS2 = 256;
 constexpr int WARPS2 = THREADS2 / 32;
 constexpr int SCAN_PER_THREAD = 32;                    // assignments per thread per pass
 constexpr int SCAN_ROWS = THREADS2 * SCAN_PER_THREAD;  // rows per pass
-constexpr int LIST = 2048;                             // rows listed per summation round
+constexpr int LIST = 1024;                             // rows listed per summation round
+constexpr int STAGE_BYTES = 24 * 1024;                 // rows staged in shared memory per round
 
 // 8 consecutive features of a row, kept in their storage format and read as
 // fp32 on use.
@@ -32,6 +33,9 @@ template <> struct Raw8<__nv_bfloat16> {
   uint4 u;
   __device__ __forceinline__ void load(const __nv_bfloat16* p) {
     u = __ldcg(reinterpret_cast<const uint4*>(p));
+  }
+  __device__ __forceinline__ void load_shared(const uint8_t* p) {
+    u = *reinterpret_cast<const uint4*>(p);
   }
   __device__ __forceinline__ void zero() { u = make_uint4(0u, 0u, 0u, 0u); }
   __device__ __forceinline__ float at(int j) const {
@@ -44,6 +48,10 @@ template <> struct Raw8<float> {
   __device__ __forceinline__ void load(const float* p) {
     a = __ldcg(reinterpret_cast<const float4*>(p));
     b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+  }
+  __device__ __forceinline__ void load_shared(const uint8_t* p) {
+    a = *reinterpret_cast<const float4*>(p);
+    b = *reinterpret_cast<const float4*>(p + 16);
   }
   __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
   __device__ __forceinline__ float at(int j) const {
@@ -61,49 +69,64 @@ __device__ __forceinline__ float group_sum(float v) {
   return v;
 }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   (unsigned)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+
 // Adds the normalised rows rowlist[0 .. nl) of head h into acc (this
-// thread's 8 features; CH threads share a row, RS rows in flight).  The trip
-// count is uniform: the shuffles involve every lane of the warp.  Two rows in
-// flight per thread, each kept as its raw 16 bytes (8 bf16 or 2 x 4 fp32) and
-// converted when used, which keeps the register count low.
+// thread's 8 features).  Round by round, the rows are first copied into the
+// shared stage with 16-byte cp.async copies (every row of the round in flight
+// at once), then CH threads share each staged row: its mean and centred norm
+// come from shuffles inside the group, and the thread adds its 8 normalised
+// features into registers.  The trip counts are uniform: the shuffles involve
+// every lane of the warp.  Ends with a block barrier (the stage is free).
 template <typename T, int D>
 __device__ __forceinline__ void add_rows(const T* __restrict__ qk, int H, int n, int h,
-                                         const int* rowlist, int nl, float (&acc)[8]) {
+                                         const int* rowlist, int nl, float (&acc)[8],
+                                         uint8_t* stage) {
   constexpr int CH = D / 8;
   constexpr int RS = THREADS2 / CH;
-  const int ch = threadIdx.x % CH, rs = threadIdx.x / CH;
-  constexpr int RIF = 2;
-  for (int base = 0; base < nl; base += RIF * RS) {
-    Raw8<T> x[RIF];
-    int gg[RIF];
-#pragma unroll
-    for (int u = 0; u < RIF; ++u) {
-      const int i = base + rs + u * RS;
-      gg[u] = (i < nl) ? rowlist[i] : -1;
-      if (gg[u] >= 0) {
-        const int b = gg[u] / n, t = gg[u] - b * n;
-        x[u].load(qk + (((size_t)b * H + h) * n + t) * D + ch * 8);
-      } else {
-        x[u].zero();
-      }
+  constexpr int RB = D * (int)sizeof(T);  // bytes per row
+  constexpr int CPR = RB / 16;            // 16-byte chunks per row
+  constexpr int SR = STAGE_BYTES / RB;    // rows per round
+  const int tid = threadIdx.x;
+  const int ch = tid % CH, rs = tid / CH;
+  for (int r0 = 0; r0 < nl; r0 += SR) {
+    const int nr = min(SR, nl - r0);
+    for (int i = tid; i < nr * CPR; i += THREADS2) {
+      const int r = i / CPR, cc = i - r * CPR;
+      const int g = rowlist[r0 + r];
+      const int b = g / n, t = g - b * n;
+      cp_async16(stage + r * RB + cc * 16,
+                 reinterpret_cast<const uint8_t*>(qk + (((size_t)b * H + h) * n + t) * D) +
+                     cc * 16);
     }
-#pragma unroll
-    for (int u = 0; u < RIF; ++u) {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    for (int base = 0; base < nr; base += RS) {
+      const int i = base + rs;
+      Raw8<T> x;
+      if (i < nr) x.load_shared(stage + i * RB + ch * 8 * (int)sizeof(T));
+      else x.zero();
       float sx = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) sx += x[u].at(j);
+      for (int j = 0; j < 8; ++j) sx += x.at(j);
       const float mean = group_sum<CH>(sx) / (float)D;
       float ss = 0.0f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float a = x[u].at(j) - mean;
+        const float a = x.at(j) - mean;
         ss = fmaf(a, a, ss);
       }
       ss = group_sum<CH>(ss);
-      const float inv = (gg[u] >= 0 && ss > 0.0f) ? 1.0f / sqrtf(ss) : 0.0f;
+      const float inv = (i < nr && ss > 0.0f) ? 1.0f / sqrtf(ss) : 0.0f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = fmaf(x[u].at(j) - mean, inv, acc[j]);
+      for (int j = 0; j < 8; ++j) acc[j] = fmaf(x.at(j) - mean, inv, acc[j]);
     }
+    __syncthreads();  // the stage may be refilled
   }
 }
 
@@ -112,10 +135,10 @@ __device__ __forceinline__ void add_rows(const T* __restrict__ qk, int H, int n,
 // renormalises it.  Every thread of the block calls it.
 template <int D>
 __device__ __forceinline__ void finish_centroid(const float (&acc)[8], int N, float old,
-                                                float decay, float* __restrict__ mu_c) {
+                                                float decay, float* __restrict__ mu_c,
+                                                float (*red)[D] /* [RS][D], shared */) {
   constexpr int CH = D / 8;
   constexpr int RS = THREADS2 / CH;
-  __shared__ float red[RS][D];
   __shared__ float nrm_part[WARPS2];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ch = tid % CH, rs = tid / CH;
@@ -141,20 +164,21 @@ __device__ __forceinline__ void finish_centroid(const float (&acc)[8], int N, fl
 
 // One CTA per (centroid, head).  Pass by pass over each sequence's n
 // positions, thread i examines positions base + 1024 j + 4 i + e (j < 8,
-// e < 4; one coalesced 16-byte load per j), keeps a 32-bit mask of the rows assigned to this
-// centroid, and a block-wide exclusive scan of the mask counts places them in
-// a shared list in (thread, j, e) order.  Then CH threads share each listed
-// row, every thread reading one 16-byte chunk of 8 features: the row's mean
-// and centred norm come from shuffles inside the group and the thread adds
-// its 8 normalised features into registers.  Row slots are summed in a fixed
-// order at the end, so the result is deterministic.
+// e < 4; one coalesced 16-byte load per j), keeps a 32-bit mask of the rows
+// assigned to this centroid, and a block-wide exclusive scan of the mask
+// counts places them in a shared list in (thread, j, e) order.  The listed
+// rows are then staged in shared memory and summed (add_rows); the row slots'
+// partial sums are combined in a fixed order at the end, so the result is
+// deterministic.
 template <typename T, int D>
-__global__ void __launch_bounds__(THREADS2, 8)
+__global__ void __launch_bounds__(THREADS2, 7)
 ema_update_kernel(const T* __restrict__ qk, const int32_t* __restrict__ assign, int B, int H,
                   int n, int k, float* __restrict__ mu, float decay) {
   pdl_trigger();
   __shared__ int rowlist[LIST];
   __shared__ int wsum[WARPS2];
+  __shared__ __align__(16) uint8_t stage[STAGE_BYTES];  // staged rows, then the partial sums
+  static_assert(STAGE_BYTES >= THREADS2 / (D / 8) * D * 4, "the stage holds the partial sums");
   const int c = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x;
   const bool vec = (n & 3) == 0 && (reinterpret_cast<uintptr_t>(assign) & 15u) == 0;
@@ -196,14 +220,14 @@ ema_update_kernel(const T* __restrict__ qk, const int32_t* __restrict__ assign, 
             rowlist[r - sub] = b * n + t0 + (bit >> 2) * (4 * THREADS2) + 4 * tid + (bit & 3);
         }
         __syncthreads();
-        add_rows<T, D>(qk, H, n, h, rowlist, min(LIST, total - sub), acc);
-        __syncthreads();  // the list may be rewritten
+        add_rows<T, D>(qk, H, n, h, rowlist, min(LIST, total - sub), acc, stage);
       }
       N += total;
     }
   }
   if (N == 0) return;  // no assigned row: centroid unchanged (uniform)
-  finish_centroid<D>(acc, N, old, decay, mu + ((size_t)h * k + c) * D);
+  finish_centroid<D>(acc, N, old, decay, mu + ((size_t)h * k + c) * D,
+                     reinterpret_cast<float (*)[D]>(stage));
 }
 
 template <typename T, int D>
