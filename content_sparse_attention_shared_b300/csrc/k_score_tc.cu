@@ -118,19 +118,38 @@ centroid_prep_kernel(const float* __restrict__ mu, int k, int kpad, uint8_t* __r
   const size_t plane_bytes = (size_t)kpad * D * 2;
   uint8_t* img = image + (size_t)h * prep_image_bytes(D, kpad);
   const float* mu_h = mu + (size_t)h * k * D;
-  for (int it = tid; it < 32 * (D / 8); it += 256) {
+  // every global load first (one round trip), then the conversion: item u of
+  // this thread is 8 features (chunk warp + 8u) of centroid c0 + lane; the row
+  // sums read D/32 consecutive features per lane of rows c0 + 4 warp + u
+  constexpr int ITEMS = 32 * (D / 8) / 256;
+  float4 ld[ITEMS][2];
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) {
+    const int it = tid + 256 * u;
     const int c = c0 + (it & 31), jc = it >> 5;
-    if (c >= kpad) continue;
-    float m[8];
     if (c < k) {
       const float4* src = reinterpret_cast<const float4*>(mu_h + (size_t)c * D + jc * 8);
-      const float4 a = __ldcg(src), b = __ldcg(src + 1);
-      m[0] = a.x; m[1] = a.y; m[2] = a.z; m[3] = a.w;
-      m[4] = b.x; m[5] = b.y; m[6] = b.z; m[7] = b.w;
+      ld[u][0] = __ldcg(src);
+      ld[u][1] = __ldcg(src + 1);
     } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) m[e] = 0.0f;
+      ld[u][0] = ld[u][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
+  }
+  float rv[4][D / 32];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int c = c0 + warp * 4 + u;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e)
+      rv[u][e] = c < k ? __ldcg(mu_h + (size_t)c * D + lane * (D / 32) + e) : 0.0f;
+  }
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) {
+    const int it = tid + 256 * u;
+    const int c = c0 + (it & 31), jc = it >> 5;
+    if (c >= kpad) continue;
+    const float m[8] = {ld[u][0].x, ld[u][0].y, ld[u][0].z, ld[u][0].w,
+                        ld[u][1].x, ld[u][1].y, ld[u][1].z, ld[u][1].w};
     split_store8(img, plane_bytes, (size_t)jc * (kpad * 16) + (size_t)c * 16, m);
   }
   float* sums = reinterpret_cast<float*>(img + 3 * plane_bytes);
@@ -138,11 +157,8 @@ centroid_prep_kernel(const float* __restrict__ mu, int k, int kpad, uint8_t* __r
   for (int u = 0; u < 4; ++u) {
     const int c = c0 + warp * 4 + u;
     float v = 0.0f;
-    if (c < k) {
-      const float* r = mu_h + (size_t)c * D + lane * (D / 32);
 #pragma unroll
-      for (int e = 0; e < D / 32; ++e) v += __ldcg(r + e);
-    }
+    for (int e = 0; e < D / 32; ++e) v += rv[u][e];
     v = warp_sum(v);
     if (lane == 0 && c < kpad) sums[c] = v;
   }
