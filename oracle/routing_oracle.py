@@ -22,6 +22,8 @@ Steps (per batch b and head h, with Q shared as K):
   a6 scatter     O[t] = mean of t's per-cluster outputs; 0 if t is in no cluster
   a7 update      mu_c <- normalise(decay * mu_c + (1 - decay) * mean of the r_t
                  with a_t = c, over every sequence of the batch); unchanged if none
+  a7' variant    the same step with the tokens of c's own top-w lists in place of
+                 the argmax assignment (centroid_ema_topw)
 
 Parity status: every function below is pinned by tests in
 ``tests/test_oracle_pins.py`` (closed forms, invariants, brute force, library
@@ -43,6 +45,7 @@ __all__ = [
     "routing_attention_head",
     "routing_attention",
     "centroid_ema",
+    "centroid_ema_topw",
 ]
 
 
@@ -234,6 +237,41 @@ def centroid_ema(qk: np.ndarray, assign: np.ndarray, mu: np.ndarray, decay: floa
             if cnt == 0:
                 continue
             mean = rh[sel].sum(axis=0) / cnt
+            blended = decay * mu[h, c] + (1.0 - decay) * mean
+            nrm = np.sqrt((blended * blended).sum())
+            out[h, c] = blended / nrm if nrm > 0 else blended
+    return out
+
+
+def centroid_ema_topw(qk: np.ndarray, idx: np.ndarray, mu: np.ndarray, decay: float) -> np.ndarray:
+    """a7 variant: the centroid step driven by the top-w membership.
+
+    qk [B, H, n, d] (raw rows; normalised as in a1), idx [B, H, k, w] (each
+    centroid's kept positions, as a3/a4 produce them; entries outside [0, n)
+    are ignored), mu [H, k, d].  Returns the updated centroids (float64).
+
+    Source: §4 "Routing attention with clustering" (balanced clusters through
+    a top-k assignment; centroids shared across sequences and learned online),
+    §2 (mini-batch spherical k-means).  Reading: the pages do not say which
+    membership moves a centroid; centroid_ema takes the argmax assignment,
+    this variant takes the tokens each centroid selected itself.  Centroid c of
+    head h moves toward the mean of the normalised rows listed in idx[b, h, c]
+    for every sequence b (a token listed by several centroids counts for each
+    of them), blended with weight (1 - decay) and put back on the unit sphere;
+    with no valid entry it is left exactly as it was.
+    """
+    qk = np.asarray(qk, dtype=np.float64)
+    B, H, n, d = qk.shape
+    idx = np.asarray(idx)
+    mu = np.asarray(mu, dtype=np.float64)
+    out = mu.copy()
+    r = normalise_rows(qk)
+    for h in range(H):
+        for c in range(mu.shape[1]):
+            rows = [r[b, h, t] for b in range(B) for t in idx[b, h, c] if 0 <= t < n]
+            if not rows:
+                continue
+            mean = np.sum(rows, axis=0) / len(rows)
             blended = decay * mu[h, c] + (1.0 - decay) * mean
             nrm = np.sqrt((blended * blended).sum())
             out[h, c] = blended / nrm if nrm > 0 else blended

@@ -230,11 +230,55 @@ def check_ema_special_cases():
     np.testing.assert_allclose(np.linalg.norm(out[:2], axis=1), 1.0, atol=1e-12)
 
 
+def check_ema_topw_special_cases():
+    rng = np.random.default_rng(21)
+    d, kc = 8, 3
+    e = _zero_mean_orthonormal(d, 3, rng)
+    mu = np.stack([e[0], e[1], e[2]])
+    ang = 0.4
+    t_plus = math.cos(ang) * e[0] + math.sin(ang) * e[1]
+    t_minus = math.cos(ang) * e[0] - math.sin(ang) * e[1]
+    x = np.zeros((2, 1, 3, d))
+    x[0, 0, 0] = 3 + 2 * t_plus
+    x[1, 0, 0] = -1 + 5 * t_minus
+    x[0, 0, 1] = 2 * e[1]
+    x[1, 0, 1] = 4 * e[1]
+    x[0, 0, 2] = 7 * t_plus
+    x[1, 0, 2] = 0.5 * t_minus
+    # lists equal to the argmax partition (-1: no entry): the argmax step's
+    # closed forms hold -- mean of the +-ang rotations is e0, an empty list
+    # leaves its centroid bit-exact
+    idx = np.array([[[[0, 2], [1, -1], [-1, -1]]], [[[0, 2], [1, -1], [-1, -1]]]])
+    out0 = orc.centroid_ema_topw(x, idx, mu[None], 0.0)[0]
+    np.testing.assert_allclose(out0[0], e[0], atol=1e-12)
+    np.testing.assert_allclose(out0[1], e[1], atol=1e-12)
+    assert np.array_equal(out0[2], mu[2])
+    np.testing.assert_allclose(orc.centroid_ema_topw(x, idx, mu[None], 1.0)[0], mu, atol=1e-15)
+    # a token listed by two centroids counts for both: centroid 2 lists tokens
+    # 0 and 1 of sequence 0 -> normalise(t_plus + e1) at decay 0
+    idx2 = idx.copy()
+    idx2[0, 0, 2] = [0, 1]
+    got = orc.centroid_ema_topw(x, idx2, mu[None], 0.0)[0]
+    want = (t_plus + e[1]) / np.linalg.norm(t_plus + e[1])
+    np.testing.assert_allclose(got[2], want, atol=1e-12)
+    np.testing.assert_allclose(got[0], e[0], atol=1e-12)
+    # the argmax step and this one agree when every centroid's list is exactly
+    # its argmax class (random rows, w tokens per centroid and sequence)
+    B, n, w = 2, 12, 4
+    xr = rng.standard_normal((B, 1, n, d))
+    a = np.stack([rng.permutation(np.repeat(np.arange(kc), w)) for _ in range(B)])[:, None]
+    lists = np.stack([[np.sort(np.nonzero(a[b, 0] == c)[0]) for c in range(kc)]
+                      for b in range(B)])[:, None]
+    mur = rng.standard_normal((1, kc, d))
+    np.testing.assert_allclose(orc.centroid_ema_topw(xr, lists, mur, 0.3),
+                               orc.centroid_ema(xr, a, mur, 0.3), atol=1e-12)
+
+
 ALL_CHECKS = [
     check_normalise_closed_form, check_scores_cosine, check_assign_ties,
     check_top_w_exhaustive, check_top_w_invariants, check_full_attention_k1,
     check_k_copies_average, check_rows_sum_to_one, check_v_ones_and_coverage,
-    check_w1_and_first_slot, check_ema_special_cases,
+    check_w1_and_first_slot, check_ema_special_cases, check_ema_topw_special_cases,
 ]
 
 
@@ -326,6 +370,12 @@ def _mut_scores_transposed(r, mu):
 
 _ORIG_ATT = orc.cluster_attention
 _ORIG_EMA = orc.centroid_ema
+_ORIG_EMA_TOPW = orc.centroid_ema_topw
+
+
+def _mut_ema_topw_first_sequence(qk, idx, mu, decay):
+    qk = np.asarray(qk)
+    return _ORIG_EMA_TOPW(qk[:1], np.asarray(idx)[:1], mu, decay)
 
 MUTANTS = [
     ("normalise_rows", _mut_no_centering),
@@ -336,6 +386,7 @@ MUTANTS = [
     ("centroid_ema", _mut_ema_swapped),
     ("kmeans_assign", _mut_argmax_last),
     ("centroid_scores", _mut_scores_transposed),
+    ("centroid_ema_topw", _mut_ema_topw_first_sequence),
 ]
 
 
