@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     Workspace,
     load_library,
     rt_centroid_ema,
+    rt_centroid_ema_topw,
     rt_launch_count,
     rt_profile_kernel_name,
     rt_profile_set,

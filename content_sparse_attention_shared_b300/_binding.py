@@ -30,6 +30,8 @@ SIGNATURES = {
                                       _vp]),
     "rt_centroid_ema": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_int,
                                  _c_float, _vp, _c_size, _vp]),
+    "rt_centroid_ema_topw": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp,
+                                      _c_int, _c_float, _vp, _c_size, _vp]),
     "rt_route_assign_noalloc": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int,
                                          _c_int, _vp, _vp, _vp]),
     "rt_workspace_init": (_c_int, [_vp, _c_size, _vp]),
@@ -187,6 +189,19 @@ def rt_centroid_ema(qk: torch.Tensor, assign: torch.Tensor, centroids: torch.Ten
     ws = _ws(workspace, B, H, n, d, k, 1, qk.dtype, qk.device)
     _check(load_library().rt_centroid_ema(
         _ptr(qk), _dtype_code(qk), B, H, n, d, _ptr(assign), _ptr(centroids), k, float(decay),
+        ws.ptr, ws.nbytes, _stream(stream)))
+    return centroids
+
+
+def rt_centroid_ema_topw(qk: torch.Tensor, idx: torch.Tensor, centroids: torch.Tensor,
+                         decay: float, workspace: Optional[Workspace] = None,
+                         stream=None) -> torch.Tensor:
+    """The centroid step driven by the top-w lists idx [B,H,k,w] (in place)."""
+    B, H, n, d = qk.shape
+    k, w = centroids.shape[1], idx.shape[-1]
+    ws = _ws(workspace, B, H, n, d, k, 1, qk.dtype, qk.device)
+    _check(load_library().rt_centroid_ema_topw(
+        _ptr(qk), _dtype_code(qk), B, H, n, d, _ptr(idx), w, _ptr(centroids), k, float(decay),
         ws.ptr, ws.nbytes, _stream(stream)))
     return centroids
 

@@ -230,6 +230,66 @@ ema_update_kernel(const T* __restrict__ qk, const int32_t* __restrict__ assign, 
                      reinterpret_cast<float (*)[D]>(stage));
 }
 
+// The variant driven by the top-w membership.  One CTA per (centroid, head)
+// lists the positions of its own lists idx[b, h, c, :] for every sequence b
+// (four consecutive entries per thread, one block scan keeps the list order,
+// entries outside [0, n) are skipped), then stages and sums the rows exactly
+// as above and blends with N = the number of listed rows.
+template <typename T, int D>
+__global__ void __launch_bounds__(THREADS2, 7)
+ema_topw_kernel(const T* __restrict__ qk, const int32_t* __restrict__ idx, int B, int H, int n,
+                int k, int w, float* __restrict__ mu, float decay) {
+  pdl_trigger();
+  __shared__ int rowlist[LIST];
+  __shared__ int wsum[WARPS2];
+  __shared__ __align__(16) uint8_t stage[STAGE_BYTES];  // staged rows, then the partial sums
+  static_assert(LIST == 4 * THREADS2, "four list entries per thread");
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int tid = threadIdx.x;
+  pdl_wait();
+  const float old = (tid < D) ? __ldcg(mu + ((size_t)h * k + c) * D + tid) : 0.0f;
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  int N = 0;
+  for (int b = 0; b < B; ++b) {
+    const int32_t* list = idx + (((size_t)b * H + h) * k + c) * w;
+    for (int i0 = 0; i0 < w; i0 += LIST) {
+      const int here = min(LIST, w - i0);
+      int ent[4];
+      uint32_t vm = 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 4 * tid + e;
+        ent[e] = i < here ? __ldcg(list + i0 + i) : -1;
+        vm |= (ent[e] >= 0 && ent[e] < n ? 1u : 0u) << e;
+      }
+      int total;
+      int o = block_exclusive_scan<THREADS2>(__popc(vm), wsum, total);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if ((vm >> e) & 1u) rowlist[o++] = b * n + ent[e];
+      __syncthreads();
+      add_rows<T, D>(qk, H, n, h, rowlist, total, acc, stage);
+      N += total;
+    }
+  }
+  if (N == 0) return;  // no valid entry: centroid unchanged (uniform)
+  finish_centroid<D>(acc, N, old, decay, mu + ((size_t)h * k + c) * D,
+                     reinterpret_cast<float (*)[D]>(stage));
+}
+
+template <typename T, int D>
+cudaError_t launch_topw(const void* qk, const int32_t* idx, int B, int H, int n, int k, int w,
+                        float* mu, float decay, cudaStream_t s) {
+  auto kern = ema_topw_kernel<T, D>;
+  launch_begin(K_EMA_TOPW, s);
+  cudaError_t e = launch_pdl(kern, dim3(k, H), dim3(THREADS2), 0, s, static_cast<const T*>(qk),
+                             idx, B, H, n, k, w, mu, decay);
+  launch_end(K_EMA_TOPW, s);
+  return e;
+}
+
 template <typename T, int D>
 cudaError_t launch_update(const void* qk, const int32_t* assign, int B, int H, int n, int k,
                           float* mu, float decay, cudaStream_t s) {
@@ -254,6 +314,17 @@ cudaError_t launch_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
   }
   return d == 64 ? launch_update<__nv_bfloat16, 64>(qk, assign, B, H, n, k, mu, decay, s)
                  : launch_update<__nv_bfloat16, 128>(qk, assign, B, H, n, k, mu, decay, s);
+}
+
+cudaError_t launch_ema_topw(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                            const int32_t* idx, int w, float* mu, int k, float decay,
+                            cudaStream_t s) {
+  if (dt == RT_F32) {
+    return d == 64 ? launch_topw<float, 64>(qk, idx, B, H, n, k, w, mu, decay, s)
+                   : launch_topw<float, 128>(qk, idx, B, H, n, k, w, mu, decay, s);
+  }
+  return d == 64 ? launch_topw<__nv_bfloat16, 64>(qk, idx, B, H, n, k, w, mu, decay, s)
+                 : launch_topw<__nv_bfloat16, 128>(qk, idx, B, H, n, k, w, mu, decay, s);
 }
 
 }  // namespace rt

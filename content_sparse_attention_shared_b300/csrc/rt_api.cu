@@ -242,7 +242,7 @@ int rt_profile_kernel_id(int i) {
 const char* rt_kernel_name(int id) {
   static const char* names[K_NUM_KINDS] = {
       "score_simt", "score_tc", "select_topw", "attention_simt", "attention_tc",
-      "scatter_average", "ema_bucket", "ema_update", "centroid_prep"};
+      "scatter_average", "ema_topw", "ema_update", "centroid_prep"};
   if (id < 0 || id >= K_NUM_KINDS) return "unknown";
   return names[id];
 }
@@ -354,6 +354,28 @@ rt_status rt_centroid_ema(const void* qk, rt_dtype dt, int B, int H, int n, int 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = from_cuda(launch_ema(qk, dt, B, H, n, d, assign, centroids, k, decay, ws + 256, s),
                  "centroid update kernels");
+  if (st != RT_OK) return st;
+  return ok();
+}
+
+rt_status rt_centroid_ema_topw(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                               const int32_t* idx, int w, float* centroids, int k, float decay,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  rt_status st = check_shape(dt, B, H, n, d, k, w);
+  if (st != RT_OK) return st;
+  if (!qk || !idx || !centroids) return fail(RT_ERR_INVALID_ARG, "null qk/idx/centroids");
+  if (!(decay >= 0.0f && decay <= 1.0f)) return fail(RT_ERR_INVALID_ARG, "decay must be in [0, 1]");
+  if (!aligned16(qk) || !aligned16(idx) || !aligned16(centroids))
+    return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (k > 4096) return fail(RT_ERR_UNSUPPORTED, "k above 4096 for the centroid update");
+  const size_t need = ema_total(B, H, n, k);
+  if (!workspace || workspace_bytes < need)
+    return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  st = from_cuda(launch_ema_topw(qk, dt, B, H, n, d, idx, w, centroids, k, decay,
+                                 static_cast<cudaStream_t>(stream)),
+                 "top-w centroid update kernel");
   if (st != RT_OK) return st;
   return ok();
 }

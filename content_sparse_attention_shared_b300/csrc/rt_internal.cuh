@@ -23,7 +23,7 @@ enum KernelId {
   K_ATTN_SIMT = 3,
   K_ATTN_TC = 4,
   K_SCATTER = 5,
-  K_EMA_BUCKET = 6,
+  K_EMA_TOPW = 6,
   K_EMA_UPDATE = 7,
   K_CENTROID_PREP = 8,
   K_NUM_KINDS = 9
@@ -206,5 +206,10 @@ size_t ema_workspace_bytes(int B, int H, int n, int k);
 cudaError_t launch_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                        const int32_t* assign, float* mu, int k, float decay,
                        void* ws, cudaStream_t s);
+// the centroid step driven by the top-w lists idx [B,H,k,w] instead of an
+// assignment (entries outside [0, n) are skipped)
+cudaError_t launch_ema_topw(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                            const int32_t* idx, int w, float* mu, int k, float decay,
+                            cudaStream_t s);
 
 }  // namespace rt

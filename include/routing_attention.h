@@ -117,11 +117,39 @@ rt_status rt_routing_attention(const void* q, const void* k, const void* v, rt_d
  *   assign    [B,H,n]    int32 in [0, k)
  *   centroids [H,k,d]    fp32, updated in place
  *   decay     in [0, 1]
- * The reduction is a counting sort by centroid followed by a segmented sum in
- * a fixed order: results are deterministic. */
+ * Each centroid's rows are listed in a fixed order and summed in that order,
+ * with no floating-point atomics: results are deterministic.  Needs a
+ * workspace of at least rt_workspace_bytes(B, H, n, d, k, 1, dt) bytes (only
+ * its device status word is used). */
 rt_status rt_centroid_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                           const int32_t* assign, float* centroids, int k, float decay,
                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* The same step driven by the top-w membership instead of the argmax
+ * assignment: centroid c of head h moves toward the normalised rows its own
+ * lists chose.  The pages do not say which membership moves a centroid
+ * (§4 "Routing attention with clustering": balanced clusters through a top-k
+ * assignment, centroids learned online; §2: mini-batch spherical k-means);
+ * rt_centroid_ema takes the argmax, this call the alternative.  For every
+ * head h and centroid c:
+ *   L = the entries t of idx[b,h,c,0..w) over every sequence b with 0 <= t < n
+ *       (a position listed by several centroids counts for each of them);
+ *   N = |L|;  if N > 0:
+ *   mu_c <- normalise(decay * mu_c + (1 - decay) * (1/N) * sum_{t in L} r_t)
+ * otherwise mu_c is left bit-exact.
+ *   qk        [B,H,n,d]  dtype dt
+ *   idx       [B,H,k,w]  int32, ascending per list (as rt_route_assign and
+ *                        rt_routing_attention return it); other entries are
+ *                        skipped
+ *   centroids [H,k,d]    fp32, updated in place
+ *   decay     in [0, 1]
+ * Deterministic (rows summed in list order, no floating-point atomics).
+ * Errors: RT_ERR_INVALID_ARG for null or misaligned pointers or decay out of
+ * range, RT_ERR_UNSUPPORTED for d not in {64, 128} or k > 4096,
+ * RT_ERR_WORKSPACE for a missing or short workspace (as rt_centroid_ema). */
+rt_status rt_centroid_ema_topw(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                               const int32_t* idx, int w, float* centroids, int k, float decay,
+                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* Clears the device status word at the start of a new workspace (an async
  * memset of its first 256 bytes on `stream`).  Call once after allocating a

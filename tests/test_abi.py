@@ -100,6 +100,19 @@ def test_ema_validation(lib):
     assert r == bnd.RT_ERR_WORKSPACE
 
 
+def test_ema_topw_validation(lib):
+    def call(qk=FAKE, d=64, n=64, idx=FAKE, w=4, k=4, decay=0.5, wsb=1 << 30):
+        return lib.rt_centroid_ema_topw(qk, 1, 1, 1, n, d, idx, w, FAKE, k, ctypes.c_float(decay),
+                                        FAKE, wsb, None)
+    assert call(decay=1.5) == bnd.RT_ERR_INVALID_ARG
+    assert call(idx=None) == bnd.RT_ERR_INVALID_ARG
+    assert call(idx=FAKE + 4) == bnd.RT_ERR_INVALID_ARG   # misaligned
+    assert call(d=96) == bnd.RT_ERR_UNSUPPORTED
+    assert call(w=65) == bnd.RT_ERR_INVALID_ARG           # w > n
+    assert call(wsb=8) == bnd.RT_ERR_WORKSPACE
+    assert lib.rt_last_error_detail() != b""
+
+
 def test_route_validation(lib):
     r = lib.rt_route_assign(FAKE, 1, 1, 1, 64, 64, FAKE, 4, 16, None, None, None, FAKE, 1 << 30,
                             None)

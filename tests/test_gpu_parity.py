@@ -87,6 +87,18 @@ def check_ema(wl, res, decay):
             assert np.array_equal(got[h, c], wl.centroids[h, c].astype(np.float64))
 
 
+def check_ema_topw(wl, res, decay):
+    """The top-w centroid step on the GPU's own index lists vs the oracle."""
+    mu_gpu = res["mu"].clone()
+    idx_t = torch.from_numpy(res["idx"]).cuda()
+    rt.rt_centroid_ema_topw(res["q"], idx_t, mu_gpu, decay, workspace=res["ws"])
+    torch.cuda.synchronize()
+    want = orc.centroid_ema_topw(wl.q_f32().astype(np.float64), res["idx"], wl.centroids, decay)
+    got = mu_gpu.cpu().numpy().astype(np.float64)
+    err = np.max(np.abs(got - want))
+    assert err <= ph.TOL_EMA, f"top-w centroid update error {err:.3g}"
+
+
 # ---------------------------------------------------------------------------
 # the five measured configurations, full size
 # ---------------------------------------------------------------------------
@@ -234,3 +246,38 @@ def test_bad_arguments_raise_on_gpu():
     mu = torch.zeros((1, 4, 64), device="cuda")
     with pytest.raises(rt.RoutingAttentionError):
         rt.rt_routing_attention(q, k2, q, mu, 16)
+
+
+# ---------------------------------------------------------------------------
+# the centroid step driven by the top-w lists
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", [
+    (1, 8, 8192, 128, 128, 64, "bf16"),   # the measured workload's shape
+    (2, 2, 640, 64, 10, 64, "f32"),        # several sequences, fp32 rows
+    (3, 1, 777, 128, 24, 129, "bf16"),     # odd n and w
+], ids=lambda c: "b{}h{}n{}d{}k{}w{}{}".format(*c))
+def test_topw_centroid_update(case):
+    B, H, n, d, k, w, dt = case
+    wl = make_random(B, H, n, d, k, w, dtype=dt, seed=n + 7 * k + w, centroid_init="tokens")
+    res = run_gpu(wl)
+    check_ema_topw(wl, res, 0.999)
+    check_ema_topw(wl, res, 0.0)
+
+
+def test_topw_centroid_update_skips_invalid_entries():
+    # lists padded with -1 and n: those entries are skipped; a list with no
+    # valid entry leaves its centroid bit-exact
+    B, H, n, d, k, w = 1, 1, 64, 64, 3, 8
+    wl = make_random(B, H, n, d, k, w, dtype="bf16", seed=11, centroid_init="tokens")
+    q, v, mu = ph.to_device(wl)
+    idx = np.full((B, H, k, w), -1, dtype=np.int32)
+    idx[0, 0, 0, :4] = [1, 5, 9, 30]
+    idx[0, 0, 1, :] = [2, 3, 4, 5, 6, 7, n, n + 5]
+    mu_gpu = mu.clone()
+    rt.rt_centroid_ema_topw(q, torch.from_numpy(idx).cuda(), mu_gpu, 0.0)
+    torch.cuda.synchronize()
+    want = orc.centroid_ema_topw(wl.q_f32().astype(np.float64), idx, wl.centroids, 0.0)
+    got = mu_gpu.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(got - want)) <= ph.TOL_EMA
+    assert np.array_equal(got[0, 2], wl.centroids[0, 2].astype(np.float64))
