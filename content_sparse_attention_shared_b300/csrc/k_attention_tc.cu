@@ -8,24 +8,18 @@
 // lower triangle in slot order (diagonal included).  Queries double as keys
 // (shared QK).
 //
-// Work unit: a tile of 128 query rows (TMEM lanes).
-//   * w <= 128 ("packed"): g = floor(128 / w) whole clusters share a tile.
-//     With shared QK the keys of the tile are its own rows, so one
-//     S = Q Q^T (128 x 128) MMA covers every cluster of the tile and the mask
-//     is block-diagonal (same cluster) and causal inside each block.  Padding
-//     rows are zero-filled and masked.
-//   * w > 128 ("multi"): a cluster spans ceil(w/128) row tiles; each row tile
-//     walks its key blocks of 128 (causal: up to its own) with an online
-//     softmax, the partial P V of each block read back from TMEM and
-//     accumulated in registers.
-// Each of the 128 threads owns one row: it reads its S row from TMEM,
-// applies the mask and the softmax in registers, writes its P row (bf16) to
-// shared memory in the MMA operand layout, and after O = P V reads its O row
-// back.  Only the 16-column chunks that hold a valid key for some row of the
-// warp are read and exponentiated; the other chunks of P are written as
-// zeros.  P reuses the shared memory of the key operand once S = Q K^T is
-// done, and O reuses S's TMEM columns, so a packed CTA needs 64 KiB of shared
-// memory and 128 TMEM columns (three CTAs per SM at d = 128, four at d = 64).
+// This kernel serves clusters wider than one 128-row tile (w > 128; narrower
+// clusters go to the pipelined kernel in k_attention_pipe.cu).  Work unit: a
+// row tile of 128 consecutive slots of one cluster (TMEM lanes); it walks the
+// cluster's key blocks of 128 (causal: up to its own block) with an online
+// softmax, the partial P V of each block read back from TMEM and accumulated
+// in registers.  Each of the 128 threads owns one row: it reads its S row
+// from TMEM, applies the mask and the softmax in registers, writes its P row
+// (bf16) to shared memory in the MMA operand layout, and after O = P V reads
+// its O row back.  Only the 16-column chunks that hold a valid key for some
+// row of the warp are read and exponentiated; the other chunks of P are
+// written as zeros.  P reuses the shared memory of the key block once
+// S = Q K^T is done, and O reuses S's TMEM columns (128 columns per CTA).
 // Rows are gathered from HBM by position with 16-byte cp.async straight into
 // the no-swizzle core-matrix layouts (Q/K: K-major; V: MN-major).  The MMA
 // completions are waited on with a bounded mbarrier wait; a wait that runs
@@ -52,35 +46,34 @@ __device__ __forceinline__ void gather_mnmajor(uint8_t* dst, const bf16* src, co
   attn::gather_mnmajor<D>(dst, src, pos, threadIdx.x >> 5, THREADS / 32);
 }
 
-// Shared-memory plan (bytes, after 1 KiB alignment slack).
-//   packed: [Q then P: max(Q, P)] [V]
-//   multi:  [Q] [K then P: max(K, P)] [V]
-template <int D, bool MULTI>
+// Shared-memory plan (bytes, after 1 KiB alignment slack):
+//   [Q] [K then P: max(K, P)] [V]
+template <int D>
 struct AttnSmem {
   static constexpr int QB = ROWS * D * 2;
   static constexpr int PB = ROWS * ROWS * 2;
   static constexpr int XB = QB > PB ? QB : PB;
   static constexpr int Q_OFF = 0;
-  static constexpr int KP_OFF = MULTI ? QB : 0;      // K (multi) / P region
-  static constexpr int V_OFF = MULTI ? QB + XB : XB;
+  static constexpr int KP_OFF = QB;  // K block, then P
+  static constexpr int V_OFF = QB + XB;
   static constexpr int BYTES = V_OFF + QB;
 };
 
-template <int D, bool MULTI>
-__global__ void __launch_bounds__(THREADS, MULTI ? 2 : 3)
+template <int D>
+__global__ void __launch_bounds__(THREADS, 2)
 attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int n, int k, int w,
-                    int g, int tiles_per_bh, int R, int causal, float scale_log2,
+                    int tiles_per_bh, int R, int causal, float scale_log2,
                     const int32_t* __restrict__ idx, const int32_t* __restrict__ mcount,
                     bf16* __restrict__ out, float* __restrict__ yslot,
                     unsigned int* __restrict__ err) {
-  using L = AttnSmem<D, MULTI>;
+  using L = AttnSmem<D>;
   pdl_trigger();
   pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   uint8_t* Qs = sm + L::Q_OFF;   // K-major [128 x D]
-  uint8_t* KPs = sm + L::KP_OFF; // K-major keys (multi) / P [128 x 128 keys]
+  uint8_t* KPs = sm + L::KP_OFF; // K-major keys, then P [128 x 128 keys]
   uint8_t* Vs = sm + L::V_OFF;   // MN-major [128 keys x D]
 
   __shared__ uint64_t bar_s, bar_o;
@@ -96,26 +89,12 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
   const bf16* q_bh = q + (size_t)bh * n * D;
   const bf16* v_bh = v + (size_t)bh * n * D;
 
-  // ---- row mapping (thread tid owns tile row tid) ------------------------
-  int cluster, slot, row_lo, row_hi;  // row_lo/hi: key columns of this row's cluster
-  bool row_valid;
-  int nkb = 1, rt = 0;
-  if (!MULTI) {
-    const int ci = tid / w;
-    cluster = lt * g + ci;
-    slot = tid - ci * w;
-    row_valid = (ci < g) && (cluster < k);
-    row_lo = ci * w;
-    row_hi = row_lo + w;
-  } else {
-    cluster = lt / R;
-    rt = lt % R;
-    slot = rt * ROWS + tid;
-    row_valid = slot < w;
-    nkb = causal ? rt + 1 : R;
-    row_lo = 0;
-    row_hi = w;
-  }
+  // ---- row mapping (thread tid owns tile row tid: slot rt*128 + tid) ------
+  const int cluster = lt / R;
+  const int rt = lt % R;
+  const int slot = rt * ROWS + tid;
+  bool row_valid = slot < w;
+  const int nkb = causal ? rt + 1 : R;
   int my_pos = -1;
   if (row_valid) {
     my_pos = __ldcg(idx_bh + (size_t)cluster * w + slot);
@@ -128,10 +107,6 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
 
   gather_kmajor<D>(Qs, q_bh, qpos);
   cp_async_commit();
-  if (!MULTI) {
-    gather_mnmajor<D>(Vs, v_bh, qpos);
-    cp_async_commit();
-  }
 
   if (warp == 0) {
     tc::tmem_alloc(&tmem_base_sh, 128);
@@ -153,16 +128,17 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
   constexpr uint32_t SBO_QK = (D / 8) * 128;  // 8-row group stride, K-major [rows x D]
 
   float m_run = -INFINITY, l_run = 0.0f;
-  float o_acc[MULTI ? D : 1];
+  float o_acc[D];
 #pragma unroll
-  for (int i = 0; i < (MULTI ? D : 1); ++i) o_acc[i] = 0.0f;
+  for (int i = 0; i < D; ++i) o_acc[i] = 0.0f;
   uint32_t phase = 0;
   bool failed = false;
 
   for (int kb = 0; kb < nkb && !failed; ++kb) {
+    // key / value rows of key block kb (the diagonal block's keys are the
+    // tile's own rows: Q serves as K there)
     const uint8_t* Kop = Qs;
-    if (MULTI) {
-      // key / value rows of key block kb
+    {
       const int ks = kb * ROWS + tid;
       int p = -1;
       if (ks < w) {
@@ -179,8 +155,6 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
       gather_mnmajor<D>(Vs, v_bh, kpos);
       cp_async_commit();
       cp_async_wait_all();
-    } else {
-      asm volatile("cp.async.wait_group 1;" ::: "memory");  // Q landed; V may be in flight
     }
     tc::fence_proxy_async_smem();
     tc::tc_fence_before_sync();
@@ -208,18 +182,12 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
     tc::tc_fence_after_sync();
 
     // ---- softmax on this thread's row -----------------------------------
-    // valid key columns [jmin, jmax): inside the row's cluster block
-    // (packed), key slot < w, and causal: key slot <= own slot.
-    int jmin, jmax;
-    if (!MULTI) {
-      jmin = row_lo;
-      jmax = causal ? tid + 1 : row_hi;
-    } else {
-      const int kslot0 = kb * ROWS;
-      jmin = 0;
-      jmax = min(ROWS, w - kslot0);
-      if (causal) jmax = min(jmax, slot - kslot0 + 1);
-    }
+    // valid key columns [jmin, jmax): key slot < w, and causal: key slot <=
+    // own slot
+    const int kslot0 = kb * ROWS;
+    int jmin = 0;
+    int jmax = min(ROWS, w - kslot0);
+    if (causal) jmax = min(jmax, slot - kslot0 + 1);
     if (!row_valid || jmax <= jmin) { jmin = ROWS; jmax = 0; }
     // chunks of 16 columns that hold a valid column for some row of the warp
     const int wlo = __reduce_min_sync(0xffffffffu, jmin);
@@ -242,8 +210,8 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
     const float m_new = fmaxf(m_run, mrow);
     const float mscaled = (m_new == -INFINITY) ? 0.0f : m_new * scale_log2;
     float lsum = 0.0f;
-    // P overwrites the key operand (packed: Q; multi: the K block or, on the
-    // diagonal block, the otherwise unused K buffer): S = Q K^T is complete.
+    // P overwrites the key block (on the diagonal block, the otherwise unused
+    // K buffer): S = Q K^T is complete.
     uint8_t* Ps = KPs;
     const uint32_t prow = tc::smem_u32(Ps) + (tid >> 3) * 2048 + (tid & 7) * 16;
 #pragma unroll 1
@@ -281,7 +249,6 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
     l_run = l_run * alpha + lsum;
     m_run = m_new;
 
-    if (!MULTI) cp_async_wait_all();  // V landed
     tc::fence_proxy_async_smem();
     tc::tc_fence_before_sync();
     __syncthreads();
@@ -308,17 +275,15 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
     tc::tc_fence_after_sync();
     phase ^= 1u;
 
-    if (MULTI) {
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        uint32_t r[16];
-        tc::tmem_ld16(t_row + c0, r);
-        tc::tmem_ld_wait();
+    for (int c0 = 0; c0 < D; c0 += 16) {
+      uint32_t r[16];
+      tc::tmem_ld16(t_row + c0, r);
+      tc::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) o_acc[c0 + j] = o_acc[c0 + j] * alpha + __uint_as_float(r[j]);
-      }
-      tc::tc_fence_before_sync();  // O read before the next block's S overwrites it
+      for (int j = 0; j < 16; ++j) o_acc[c0 + j] = o_acc[c0 + j] * alpha + __uint_as_float(r[j]);
     }
+    tc::tc_fence_before_sync();  // O read before the next block's S overwrites it
   }
 
   // ---- epilogue ------------------------------------------------------------
@@ -335,16 +300,8 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 16) {
       float o[16];
-      if (MULTI) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) o[j] = o_acc[c0 + j] * inv_l;
-      } else {
-        uint32_t r[16];
-        tc::tmem_ld16(t_row + c0, r);  // warp-collective: every thread loads
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(r[j]) * inv_l;
-      }
+      for (int j = 0; j < 16; ++j) o[j] = o_acc[c0 + j] * inv_l;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         const int chunk = c0 / 4 + q4;
@@ -383,27 +340,21 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
   if (warp == 0) tc::tmem_dealloc(tmem, 128);
 }
 
-template <int D, bool MULTI>
+template <int D>
 cudaError_t launch_t(const void* q, const void* v, int BH, int n, int k, int w, int causal,
                      float scale, const int32_t* idx, const int32_t* mcount, void* out,
                      float* yslot, unsigned int* err, cudaStream_t s) {
-  int g = 1, R = 1, tiles_per_bh;
-  if (!MULTI) {
-    g = ROWS / w;
-    tiles_per_bh = (k + g - 1) / g;
-  } else {
-    R = (w + ROWS - 1) / ROWS;
-    tiles_per_bh = k * R;
-  }
-  const size_t smem = 1024 + (size_t)AttnSmem<D, MULTI>::BYTES;
-  auto kern = attention_tc_kernel<D, MULTI>;
+  const int R = (w + ROWS - 1) / ROWS;  // row tiles (and key blocks) per cluster
+  const int tiles_per_bh = k * R;
+  const size_t smem = 1024 + (size_t)AttnSmem<D>::BYTES;
+  auto kern = attention_tc_kernel<D>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   const long long tiles = (long long)BH * tiles_per_bh;
   const float scale_log2 = scale * 1.4426950408889634f;
   launch_begin(K_ATTN_TC, s);
   e = launch_pdl(kern, dim3((unsigned)tiles), dim3(THREADS), smem, s, static_cast<const bf16*>(q),
-                 static_cast<const bf16*>(v), n, k, w, g, tiles_per_bh, R, causal, scale_log2, idx,
+                 static_cast<const bf16*>(v), n, k, w, tiles_per_bh, R, causal, scale_log2, idx,
                  mcount, static_cast<bf16*>(out), yslot, err);
   launch_end(K_ATTN_TC, s);
   return e;
@@ -419,15 +370,10 @@ cudaError_t launch_attention_tc(const void* q, const void* v, int BH, int n, int
                                 int causal, float scale, const int32_t* idx,
                                 const int32_t* mcount, void* out, float* yslot,
                                 unsigned int* err, cudaStream_t s) {
-  const bool multi = w > ROWS;
-  if (!multi)
+  if (w <= ROWS)
     return launch_attention_pipe(q, v, BH, n, d, k, w, causal, scale, idx, mcount, out, yslot, err, s);
-  if (d == 64) {
-    return multi ? launch_t<64, true>(q, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, err, s)
-                 : launch_t<64, false>(q, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, err, s);
-  }
-  return multi ? launch_t<128, true>(q, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, err, s)
-               : launch_t<128, false>(q, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, err, s);
+  return d == 64 ? launch_t<64>(q, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, err, s)
+                 : launch_t<128>(q, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, err, s);
 }
 
 }  // namespace rt
