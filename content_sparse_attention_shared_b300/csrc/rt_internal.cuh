@@ -182,7 +182,8 @@ cudaError_t launch_attention_simt(const void* q, const void* kk, const void* v, 
                                   float scale, const int32_t* idx, const int32_t* mcount,
                                   void* out, float* yslot, cudaStream_t s);
 
-// the same on tcgen05 tensor cores (bf16 only); err: device error word.
+// the same on tcgen05 tensor cores (bf16 only): the pipelined kernel below
+// for w <= 128, the key-block kernel above that; err: device error word.
 bool attention_tc_supported(rt_dtype dt, int d, int w);
 cudaError_t launch_attention_tc(const void* q, const void* v, int BH, int n, int d, int k, int w,
                                 int causal, float scale, const int32_t* idx,
@@ -200,8 +201,9 @@ cudaError_t launch_scatter(rt_dtype dt, int BH, int n, int d, int k, int w,
                            const int32_t* idx, const int32_t* mcount, const int32_t* slots,
                            const float* yslot, void* out, cudaStream_t s);
 
-// centroid update: bucket the rows by centroid per tile, then a segmented
-// sum per (head, centroid) and the blend/renormalise.
+// centroid update: one CTA per (head, centroid) lists its rows, sums them
+// normalised in a fixed order, blends and renormalises (no workspace needed
+// beyond the status word: ema_workspace_bytes returns 0).
 size_t ema_workspace_bytes(int B, int H, int n, int k);
 cudaError_t launch_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                        const int32_t* assign, float* mu, int k, float decay,
