@@ -24,6 +24,8 @@ Steps (per batch b and head h, with Q shared as K):
                  with a_t = c, over every sequence of the batch); unchanged if none
   a7' variant    the same step with the tokens of c's own top-w lists in place of
                  the argmax assignment (centroid_ema_topw)
+  local          the companion layer: causal attention of every position over the
+                 `window` positions ending at it (local_attention)
 
 Parity status: every function below is pinned by tests in
 ``tests/test_oracle_pins.py`` (closed forms, invariants, brute force, library
@@ -46,6 +48,7 @@ __all__ = [
     "routing_attention",
     "centroid_ema",
     "centroid_ema_topw",
+    "local_attention",
 ]
 
 
@@ -276,3 +279,28 @@ def centroid_ema_topw(qk: np.ndarray, idx: np.ndarray, mu: np.ndarray, decay: fl
             nrm = np.sqrt((blended * blended).sum())
             out[h, c] = blended / nrm if nrm > 0 else blended
     return out
+
+
+def local_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int,
+                    scale: float) -> np.ndarray:
+    """Local (sliding-window) causal attention of one (batch, head).
+
+    q, k, v: [n, d].  Position t attends to the positions
+    max(0, t - window + 1) .. t (itself included); returns O [n, d].
+
+    Source: §3 (causal and local attention choose each query's key set from
+    positions alone; softmax rows, autoregressive masking), §6 "Local vs
+    Global" (local attention with windows of 512 and 1024 positions, combined
+    with routing layers).  Readings: the window counts the position itself
+    (window 1 returns V); the raw rows with the given scale, as in a5.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n = q.shape[0]
+    t = np.arange(n)
+    logits = scale * (q @ k.T)
+    visible = (t[None, :] <= t[:, None]) & (t[None, :] > t[:, None] - window)
+    logits = np.where(visible, logits, -np.inf)
+    e = np.exp(logits - logits.max(axis=1, keepdims=True))
+    return (e / e.sum(axis=1, keepdims=True)) @ v

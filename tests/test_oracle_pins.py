@@ -274,11 +274,44 @@ def check_ema_topw_special_cases():
                                orc.centroid_ema(xr, a, mur, 0.3), atol=1e-12)
 
 
+def check_local_attention():
+    rng = np.random.default_rng(22)
+    n, d = 37, 8
+    q = rng.standard_normal((n, d))
+    v = rng.standard_normal((n, d))
+    scale = 1.0 / math.sqrt(d)
+    # a window covering the sequence is full causal attention
+    np.testing.assert_allclose(orc.local_attention(q, q, v, n, scale),
+                               _sdpa(q, q, v, True, scale), atol=1e-12)
+    np.testing.assert_allclose(orc.local_attention(q, q, v, 10 * n, scale),
+                               _sdpa(q, q, v, True, scale), atol=1e-12)
+    # window 1: every position sees itself only
+    np.testing.assert_allclose(orc.local_attention(q, q, v, 1, scale), v, atol=1e-15)
+    # row t is the last row of causal attention over the window's positions
+    # (the pinned cluster step on a cluster of consecutive positions)
+    for W in (2, 5, 16):
+        got = orc.local_attention(q, q, v, W, scale)
+        for t in (0, 1, W - 1, W, n - 1):
+            members = np.arange(max(0, t - W + 1), t + 1)
+            want = orc.cluster_attention(q, q, v, members, True, scale)[-1]
+            np.testing.assert_allclose(got[t], want, atol=1e-12)
+    # and SDPA with the band as an explicit mask
+    import torch
+    W = 6
+    tt = torch.arange(n)
+    band = (tt[None, :] <= tt[:, None]) & (tt[None, :] > tt[:, None] - W)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None], torch.from_numpy(q)[None], torch.from_numpy(v)[None],
+        attn_mask=band[None], scale=scale)[0].numpy()
+    np.testing.assert_allclose(orc.local_attention(q, q, v, W, scale), ref, atol=1e-12)
+
+
 ALL_CHECKS = [
     check_normalise_closed_form, check_scores_cosine, check_assign_ties,
     check_top_w_exhaustive, check_top_w_invariants, check_full_attention_k1,
     check_k_copies_average, check_rows_sum_to_one, check_v_ones_and_coverage,
     check_w1_and_first_slot, check_ema_special_cases, check_ema_topw_special_cases,
+    check_local_attention,
 ]
 
 
@@ -371,6 +404,11 @@ def _mut_scores_transposed(r, mu):
 _ORIG_ATT = orc.cluster_attention
 _ORIG_EMA = orc.centroid_ema
 _ORIG_EMA_TOPW = orc.centroid_ema_topw
+_ORIG_LOCAL = orc.local_attention
+
+
+def _mut_local_window_off_by_one(q, k, v, window, scale):
+    return _ORIG_LOCAL(q, k, v, window + 1, scale)
 
 
 def _mut_ema_topw_first_sequence(qk, idx, mu, decay):
@@ -387,6 +425,7 @@ MUTANTS = [
     ("kmeans_assign", _mut_argmax_last),
     ("centroid_scores", _mut_scores_transposed),
     ("centroid_ema_topw", _mut_ema_topw_first_sequence),
+    ("local_attention", _mut_local_window_off_by_one),
 ]
 
 
