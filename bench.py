@@ -79,6 +79,43 @@ def kernel_work(name, wl):
     return dict(bytes=0, flops=0.0)
 
 
+LOCAL_WINDOW = 512  # the pages' local-attention window (§6 "Local vs Global")
+
+
+def local_attention_timing(wl, q, v, flush, stream, steps):
+    """Device time of the companion layer, rt_local_attention (shared QK,
+    causal window of LOCAL_WINDOW positions), on the workload's own rows: CUDA
+    events around each call on the launching stream, L2 flushed before each."""
+    import torch
+    import content_sparse_attention_shared_b300 as rt
+
+    if wl.dtype != "bf16" or wl.d not in (64, 128):
+        return None
+    W = min(LOCAL_WINDOW, wl.n)
+    out = torch.empty_like(v)
+    ws = rt.Workspace(256, q.device)
+    for _ in range(3):
+        rt.rt_local_attention(q, q, v, W, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    reps = max(10, min(steps, 50))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for i in range(reps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        rt.rt_local_attention(q, q, v, W, out=out, workspace=ws)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ws.check()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    n = wl.n
+    keys = W * (W + 1) // 2 + (n - W) * W  # sum over positions of min(t + 1, W)
+    flops = 4.0 * wl.d * keys * wl.B * wl.H
+    return {"window": W, "ms": ms, "tokens_per_s": wl.tokens / (ms * 1e-3),
+            "tflops": flops / (ms * 1e-3) / 1e12,
+            "timing": "CUDA events around each call, L2 flushed before each (256 MiB write)"}
+
+
 def alu_peak_tflops(sm_mhz):
     # fp32 FMA: 148 SMs x 128 lanes x 2 flop per cycle
     return 148 * 128 * 2 * sm_mhz * 1e6 / 1e12
@@ -503,6 +540,9 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     e2e_ms = slowest_rank_ms(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev), dev)
 
+    # ---- the companion layer on the same rows, for comparison -------------
+    local = local_attention_timing(wl, q, v, flush, stream, args.steps)
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -561,6 +601,7 @@ def run_ours(args, wl):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": gpu_launches, "launches_per_step": launches_per_step,
         "clocks": clocks, "kernels": kern,
+        "local_attention": local,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, wl)

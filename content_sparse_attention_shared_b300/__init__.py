@@ -12,6 +12,7 @@ from ._binding import (  # noqa: F401
     rt_centroid_ema,
     rt_centroid_ema_topw,
     rt_launch_count,
+    rt_local_attention,
     rt_profile_kernel_name,
     rt_profile_set,
     rt_route_assign,

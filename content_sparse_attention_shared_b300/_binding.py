@@ -32,6 +32,8 @@ SIGNATURES = {
                                  _c_float, _vp, _c_size, _vp]),
     "rt_centroid_ema_topw": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp,
                                       _c_int, _c_float, _vp, _c_size, _vp]),
+    "rt_local_attention": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                    _c_float, _vp, _vp, _c_size, _vp]),
     "rt_route_assign_noalloc": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int,
                                          _c_int, _vp, _vp, _vp]),
     "rt_workspace_init": (_c_int, [_vp, _c_size, _vp]),
@@ -204,6 +206,20 @@ def rt_centroid_ema_topw(qk: torch.Tensor, idx: torch.Tensor, centroids: torch.T
         _ptr(qk), _dtype_code(qk), B, H, n, d, _ptr(idx), w, _ptr(centroids), k, float(decay),
         ws.ptr, ws.nbytes, _stream(stream)))
     return centroids
+
+
+def rt_local_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int,
+                       scale: float = 0.0, out: Optional[torch.Tensor] = None,
+                       workspace: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """Local causal attention over the `window` positions ending at each one."""
+    B, H, n, d = q.shape
+    if out is None:
+        out = torch.empty_like(v)
+    ws = workspace if workspace is not None else Workspace(256, q.device)
+    _check(load_library().rt_local_attention(
+        _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, H, n, d, int(window), float(scale),
+        _ptr(out), ws.ptr, ws.nbytes, _stream(stream)))
+    return out
 
 
 def rt_launch_count() -> int:

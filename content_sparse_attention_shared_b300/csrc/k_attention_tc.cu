@@ -59,7 +59,13 @@ struct AttnSmem {
   static constexpr int BYTES = V_OFF + QB;
 };
 
-template <int D>
+// LOCAL = false: clusters wider than one tile (positions from idx, w > 128).
+// LOCAL = true:  local attention -- tile lt holds positions lt*128 .. +127,
+//                w is the window (a row sees the w positions ending at its
+//                own), and its key blocks are the 128-position blocks from the
+//                one holding lt*128 - w + 1 up to lt; idx, mcount and yslot
+//                are not used and every row goes to `out`.
+template <int D, bool LOCAL>
 __global__ void __launch_bounds__(THREADS, 2)
 attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int n, int k, int w,
                     int tiles_per_bh, int R, int causal, float scale_log2,
@@ -89,19 +95,31 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
   const bf16* q_bh = q + (size_t)bh * n * D;
   const bf16* v_bh = v + (size_t)bh * n * D;
 
-  // ---- row mapping (thread tid owns tile row tid: slot rt*128 + tid) ------
-  const int cluster = lt / R;
-  const int rt = lt % R;
-  const int slot = rt * ROWS + tid;
-  bool row_valid = slot < w;
-  const int nkb = causal ? rt + 1 : R;
+  // ---- row mapping (thread tid owns tile row tid) ----------------------------
+  // clusters: slot rt*128 + tid of cluster lt / R; local: position lt*128 + tid
+  int cluster = 0, rt, slot = 0, nkb, kb0 = 0;
+  bool row_valid;
   int my_pos = -1;
-  if (row_valid) {
-    my_pos = __ldcg(idx_bh + (size_t)cluster * w + slot);
-    if ((unsigned)my_pos >= (unsigned)n) { my_pos = -1; row_valid = false; }  // defensive
+  if (LOCAL) {
+    rt = lt;
+    row_valid = lt * ROWS + tid < n;
+    if (row_valid) my_pos = lt * ROWS + tid;
+    const int first = lt * ROWS - w + 1;  // first position any row of the tile sees
+    kb0 = first > 0 ? first / ROWS : 0;
+    nkb = lt - kb0 + 1;
+  } else {
+    cluster = lt / R;
+    rt = lt % R;
+    slot = rt * ROWS + tid;
+    row_valid = slot < w;
+    nkb = causal ? rt + 1 : R;
+    if (row_valid) {
+      my_pos = __ldcg(idx_bh + (size_t)cluster * w + slot);
+      if ((unsigned)my_pos >= (unsigned)n) { my_pos = -1; row_valid = false; }  // defensive
+    }
   }
   // membership count of this row's position, loaded now, used by the epilogue
-  const int my_m = row_valid ? __ldcg(mcount + (size_t)bh * n + my_pos) : 0;
+  const int my_m = (!LOCAL && row_valid) ? __ldcg(mcount + (size_t)bh * n + my_pos) : 1;
   qpos[tid] = my_pos;
   __syncthreads();
 
@@ -135,20 +153,23 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
   bool failed = false;
 
   for (int kb = 0; kb < nkb && !failed; ++kb) {
-    // key / value rows of key block kb (the diagonal block's keys are the
+    // key / value rows of key block kbi (the diagonal block's keys are the
     // tile's own rows: Q serves as K there)
+    const int kbi = kb0 + kb;
     const uint8_t* Kop = Qs;
     {
-      const int ks = kb * ROWS + tid;
+      const int ks = kbi * ROWS + tid;
       int p = -1;
-      if (ks < w) {
+      if (LOCAL) {
+        if (ks < n) p = ks;
+      } else if (ks < w) {
         p = __ldcg(idx_bh + (size_t)cluster * w + ks);
         if ((unsigned)p >= (unsigned)n) p = -1;
       }
       __syncthreads();  // previous block's buffers are free (all reads done)
       kpos[tid] = p;
       __syncthreads();
-      if (kb != rt) {
+      if (kbi != rt) {
         gather_kmajor<D>(KPs, q_bh, kpos);
         Kop = KPs;
       }
@@ -182,12 +203,18 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
     tc::tc_fence_after_sync();
 
     // ---- softmax on this thread's row -----------------------------------
-    // valid key columns [jmin, jmax): key slot < w, and causal: key slot <=
-    // own slot
-    const int kslot0 = kb * ROWS;
-    int jmin = 0;
-    int jmax = min(ROWS, w - kslot0);
-    if (causal) jmax = min(jmax, slot - kslot0 + 1);
+    // valid key columns [jmin, jmax).  Clusters: key slot < w, and causal:
+    // key slot <= own slot.  Local: key position in [pos - w + 1, pos], < n.
+    int jmin = 0, jmax;
+    if (LOCAL) {
+      const int pk0 = kbi * ROWS;
+      jmin = max(0, my_pos - w + 1 - pk0);
+      jmax = min(min(ROWS, my_pos - pk0 + 1), n - pk0);
+    } else {
+      const int kslot0 = kbi * ROWS;
+      jmax = min(ROWS, w - kslot0);
+      if (causal) jmax = min(jmax, slot - kslot0 + 1);
+    }
     if (!row_valid || jmax <= jmin) { jmin = ROWS; jmax = 0; }
     // chunks of 16 columns that hold a valid column for some row of the warp
     const int wlo = __reduce_min_sync(0xffffffffu, jmin);
@@ -310,7 +337,7 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
       }
     }
     __syncwarp();
-    const int single = (row_valid && my_m == 1) ? 1 : 0;
+    const int single = (row_valid && (LOCAL || my_m == 1)) ? 1 : 0;
     const int ch = lane % CPR;
 #pragma unroll 4
     for (int it = 0; it < 32 / RPI; ++it) {
@@ -347,7 +374,7 @@ cudaError_t launch_t(const void* q, const void* v, int BH, int n, int k, int w, 
   const int R = (w + ROWS - 1) / ROWS;  // row tiles (and key blocks) per cluster
   const int tiles_per_bh = k * R;
   const size_t smem = 1024 + (size_t)AttnSmem<D>::BYTES;
-  auto kern = attention_tc_kernel<D>;
+  auto kern = attention_tc_kernel<D, false>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   const long long tiles = (long long)BH * tiles_per_bh;
@@ -360,7 +387,32 @@ cudaError_t launch_t(const void* q, const void* v, int BH, int n, int k, int w, 
   return e;
 }
 
+template <int D>
+cudaError_t launch_local_t(const void* q, const void* v, int BH, int n, int window, float scale,
+                           void* out, unsigned int* err, cudaStream_t s) {
+  const int tiles_per_bh = (n + ROWS - 1) / ROWS;
+  const size_t smem = 1024 + (size_t)AttnSmem<D>::BYTES;
+  auto kern = attention_tc_kernel<D, true>;
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
+  if (e != cudaSuccess) return e;
+  const long long tiles = (long long)BH * tiles_per_bh;
+  const float scale_log2 = scale * 1.4426950408889634f;
+  launch_begin(K_LOCAL_ATTN, s);
+  e = launch_pdl(kern, dim3((unsigned)tiles), dim3(THREADS), smem, s, static_cast<const bf16*>(q),
+                 static_cast<const bf16*>(v), n, 0, window, tiles_per_bh, 1, 1, scale_log2,
+                 static_cast<const int32_t*>(nullptr), static_cast<const int32_t*>(nullptr),
+                 static_cast<bf16*>(out), static_cast<float*>(nullptr), err);
+  launch_end(K_LOCAL_ATTN, s);
+  return e;
+}
+
 }  // namespace
+
+cudaError_t launch_local_attention(const void* q, const void* v, int BH, int n, int d, int window,
+                                   float scale, void* out, unsigned int* err, cudaStream_t s) {
+  return d == 64 ? launch_local_t<64>(q, v, BH, n, window, scale, out, err, s)
+                 : launch_local_t<128>(q, v, BH, n, window, scale, out, err, s);
+}
 
 bool attention_tc_supported(rt_dtype dt, int d, int w) {
   return dt == RT_BF16 && (d == 64 || d == 128) && w >= 1;

@@ -242,7 +242,7 @@ int rt_profile_kernel_id(int i) {
 const char* rt_kernel_name(int id) {
   static const char* names[K_NUM_KINDS] = {
       "score_simt", "score_tc", "select_topw", "attention_simt", "attention_tc",
-      "scatter_average", "ema_topw", "ema_update", "centroid_prep"};
+      "scatter_average", "ema_topw", "ema_update", "centroid_prep", "local_attention"};
   if (id < 0 || id >= K_NUM_KINDS) return "unknown";
   return names[id];
 }
@@ -376,6 +376,33 @@ rt_status rt_centroid_ema_topw(const void* qk, rt_dtype dt, int B, int H, int n,
   st = from_cuda(launch_ema_topw(qk, dt, B, H, n, d, idx, w, centroids, k, decay,
                                  static_cast<cudaStream_t>(stream)),
                  "top-w centroid update kernel");
+  if (st != RT_OK) return st;
+  return ok();
+}
+
+rt_status rt_local_attention(const void* q, const void* kp, const void* v, rt_dtype dt, int B,
+                             int H, int n, int d, int window, float scale, void* out,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 1 || H < 1 || n < 1) return fail(RT_ERR_INVALID_ARG, "B, H and n must be positive");
+  if (window < 1) return fail(RT_ERR_INVALID_ARG, "window must be at least 1");
+  if (dt != RT_BF16 && dt != RT_F32) return fail(RT_ERR_INVALID_ARG, "unknown dtype");
+  if (dt != RT_BF16) return fail(RT_ERR_UNSUPPORTED, "local attention takes bf16 rows");
+  if (d != 64 && d != 128) return fail(RT_ERR_UNSUPPORTED, "d must be 64 or 128");
+  if ((long long)B * H * n > 0x7fffffffLL) return fail(RT_ERR_UNSUPPORTED, "B*H*n too large");
+  if (!q || !kp || !v || !out) return fail(RT_ERR_INVALID_ARG, "null tensor pointer");
+  if (kp != q) return fail(RT_ERR_UNSUPPORTED, "separate keys: only shared QK (k == q)");
+  if (!std::isfinite(scale)) return fail(RT_ERR_INVALID_ARG, "scale is not finite");
+  if (!aligned16(q) || !aligned16(v) || !aligned16(out))
+    return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (!workspace || workspace_bytes < 256)
+    return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need 256", workspace_bytes);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (scale <= 0.0f) scale = 1.0f / sqrtf((float)d);
+  unsigned int* err = static_cast<unsigned int*>(workspace);
+  rt_status st = from_cuda(launch_local_attention(q, v, B * H, n, d, window, scale, out, err,
+                                                  static_cast<cudaStream_t>(stream)),
+                           "local attention kernel");
   if (st != RT_OK) return st;
   return ok();
 }

@@ -26,7 +26,8 @@ enum KernelId {
   K_EMA_TOPW = 6,
   K_EMA_UPDATE = 7,
   K_CENTROID_PREP = 8,
-  K_NUM_KINDS = 9
+  K_LOCAL_ATTN = 9,
+  K_NUM_KINDS = 10
 };
 
 // Error detail for the calling host thread (rt_last_error_detail) and the
@@ -189,6 +190,11 @@ cudaError_t launch_attention_tc(const void* q, const void* v, int BH, int n, int
                                 int causal, float scale, const int32_t* idx,
                                 const int32_t* mcount, void* out, float* yslot,
                                 unsigned int* err, cudaStream_t s);
+
+// local (sliding-window) causal attention, shared QK, bf16: every position
+// attends to the `window` positions ending at it; out [BH, n, d].
+cudaError_t launch_local_attention(const void* q, const void* v, int BH, int n, int d, int window,
+                                   float scale, void* out, unsigned int* err, cudaStream_t s);
 
 // the same, persistent and pipelined, for w <= 128 (bf16 only).
 cudaError_t launch_attention_pipe(const void* q, const void* v, int BH, int n, int d, int k,

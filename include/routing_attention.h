@@ -151,6 +151,25 @@ rt_status rt_centroid_ema_topw(const void* qk, rt_dtype dt, int B, int H, int n,
                                const int32_t* idx, int w, float* centroids, int k, float decay,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* Local (sliding-window) causal attention, the layer the pages pair with
+ * routing attention (§3: causal and local attention choose each query's keys
+ * from positions alone; §6 "Local vs Global": local attention with windows of
+ * 512 and 1024 positions, combined with routing layers):
+ *   out[b,h,t] = sum_{s = max(0, t-window+1)}^{t} softmax_s(scale <q_t, k_s>) v_s
+ * (the window counts the position itself: window 1 returns V).
+ *   q, k, v  [B,H,n,d] bf16 (dt must be RT_BF16; RT_F32 -> RT_ERR_UNSUPPORTED);
+ *            shared QK only: k must be the same pointer as q
+ *   window   >= 1 (a window >= n is full causal attention)
+ *   scale    <= 0 selects 1/sqrt(d)
+ *   out      [B,H,n,d] bf16 (fp32 accumulation, one rounding)
+ *   workspace at least 256 bytes, 256-byte aligned (its first word is the
+ *            device status word, as for the other calls)
+ * d in {64, 128}; tcgen05 tensor cores, 128-row query tiles walking their
+ * window's 128-position key blocks with an online softmax. */
+rt_status rt_local_attention(const void* q, const void* k, const void* v, rt_dtype dt,
+                             int B, int H, int n, int d, int window, float scale, void* out,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
 /* Clears the device status word at the start of a new workspace (an async
  * memset of its first 256 bytes on `stream`).  Call once after allocating a
  * workspace; the compute calls only ever set the word. */

@@ -113,6 +113,20 @@ def test_ema_topw_validation(lib):
     assert lib.rt_last_error_detail() != b""
 
 
+def test_local_attention_validation(lib):
+    def call(q=FAKE, k=FAKE, dt=1, n=256, d=64, window=64, ws=FAKE, wsb=1 << 20):
+        return lib.rt_local_attention(q, k, FAKE, dt, 1, 1, n, d, window, ctypes.c_float(0.0),
+                                      FAKE, ws, wsb, None)
+    assert call(dt=0) == bnd.RT_ERR_UNSUPPORTED          # fp32 rows
+    assert call(window=0) == bnd.RT_ERR_INVALID_ARG
+    assert call(k=FAKE + 4096) == bnd.RT_ERR_UNSUPPORTED  # separate keys
+    assert call(d=96) == bnd.RT_ERR_UNSUPPORTED
+    assert call(q=None, k=None) == bnd.RT_ERR_INVALID_ARG
+    assert call(wsb=8) == bnd.RT_ERR_WORKSPACE
+    assert call(ws=FAKE + 16) == bnd.RT_ERR_INVALID_ARG   # workspace not 256-aligned
+    assert lib.rt_last_error_detail() != b""
+
+
 def test_route_validation(lib):
     r = lib.rt_route_assign(FAKE, 1, 1, 1, 64, 64, FAKE, 4, 16, None, None, None, FAKE, 1 << 30,
                             None)

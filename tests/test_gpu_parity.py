@@ -281,3 +281,52 @@ def test_topw_centroid_update_skips_invalid_entries():
     got = mu_gpu.cpu().numpy().astype(np.float64)
     assert np.max(np.abs(got - want)) <= ph.TOL_EMA
     assert np.array_equal(got[0, 2], wl.centroids[0, 2].astype(np.float64))
+
+
+# ---------------------------------------------------------------------------
+# local (sliding-window) causal attention
+# ---------------------------------------------------------------------------
+
+LOCAL_CASES = [
+    # B, H, n, d, window
+    (1, 2, 1000, 128, 256),
+    (2, 1, 777, 64, 100),
+    (1, 1, 300, 128, 1000),   # window >= n: full causal attention
+    (1, 1, 200, 64, 1),       # window 1: every position returns its own V row
+    (1, 1, 513, 128, 129),    # window one past a key block, ragged last tile
+]
+
+
+@pytest.mark.parametrize("case", LOCAL_CASES, ids=lambda c: "b{}h{}n{}d{}win{}".format(*c))
+def test_local_attention(case):
+    B, H, n, d, W = case
+    wl = make_random(B, H, n, d, 1, 1, dtype="bf16", seed=n + W)
+    q, v, _ = ph.to_device(wl)
+    out = rt.rt_local_attention(q, q, v, W)
+    torch.cuda.synchronize()
+    q64, v64 = wl.q_f32().astype(np.float64), wl.v_f32().astype(np.float64)
+    got = ph.out_to_f64(out)
+    for b in range(B):
+        for h in range(H):
+            want = orc.local_attention(q64[b, h], q64[b, h], v64[b, h], W, 1 / math.sqrt(d))
+            assert np.max(np.abs(got[b, h] - want)) <= ph.TOL_OUT["bf16"]
+    if W == 1:
+        assert torch.equal(out, v)
+
+
+def test_local_attention_full_size_sampled():
+    # the measured shape with the pages' window of 512, checked on blocks of
+    # rows: rows t0..t0+63 need only positions t0-511 .. t0+63
+    B, H, n, d, W = 1, 8, 8192, 128, 512
+    wl = make_random(B, H, n, d, 1, 1, dtype="bf16", seed=5)
+    q, v, _ = ph.to_device(wl)
+    out = rt.rt_local_attention(q, q, v, W)
+    torch.cuda.synchronize()
+    q64, v64 = wl.q_f32().astype(np.float64), wl.v_f32().astype(np.float64)
+    got = ph.out_to_f64(out)
+    for h in range(H):
+        for t0 in (0, 448, 4000, n - 64):
+            lo = max(0, t0 - W + 1)
+            want = orc.local_attention(q64[0, h, lo:t0 + 64], q64[0, h, lo:t0 + 64],
+                                       v64[0, h, lo:t0 + 64], W, 1 / math.sqrt(d))[t0 - lo:]
+            assert np.max(np.abs(got[0, h, t0:t0 + 64] - want)) <= ph.TOL_OUT["bf16"]
