@@ -21,7 +21,10 @@
  *   - the centroid update blends the mean of the normalised rows assigned to
  *     each centroid (argmax assignment, over the whole batch) into the
  *     centroid with weight (1 - decay), then renormalises; a centroid with no
- *     assigned row is left unchanged.
+ *     assigned row is left unchanged (rt_centroid_ema_topw takes each
+ *     centroid's own top-w lists instead of the argmax);
+ *   - rt_local_attention is the sliding-window causal layer the pages pair
+ *     with routing attention (a position sees the window ending at itself).
  *
  * Conventions for every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous,
