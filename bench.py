@@ -82,6 +82,14 @@ def kernel_work(name, wl):
 LOCAL_WINDOW = 512  # the pages' local-attention window (§6 "Local vs Global")
 
 
+def local_attention_flops(BH, n, d, window):
+    """Useful flops of causal local attention: QK^T and PV over the
+    min(t + 1, window) keys of every position t (2 d each, twice)."""
+    W = min(window, n)
+    keys = W * (W + 1) // 2 + (n - W) * W  # sum over t of min(t + 1, W)
+    return 4.0 * d * keys * BH
+
+
 def local_attention_timing(wl, q, v, flush, stream, steps):
     """Device time of the companion layer, rt_local_attention (shared QK,
     causal window of LOCAL_WINDOW positions), on the workload's own rows: CUDA
@@ -108,9 +116,7 @@ def local_attention_timing(wl, q, v, flush, stream, steps):
     torch.cuda.synchronize()
     ws.check()
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    n = wl.n
-    keys = W * (W + 1) // 2 + (n - W) * W  # sum over positions of min(t + 1, W)
-    flops = 4.0 * wl.d * keys * wl.B * wl.H
+    flops = local_attention_flops(wl.B * wl.H, wl.n, wl.d, W)
     return {"window": W, "ms": ms, "tokens_per_s": wl.tokens / (ms * 1e-3),
             "tflops": flops / (ms * 1e-3) / 1e12,
             "timing": "CUDA events around each call, L2 flushed before each (256 MiB write)"}

@@ -56,3 +56,11 @@ def test_single_process_needs_no_group():
     import bench
     assert bench.slowest_rank_ms(3.25) == 3.25
     assert bench.job_tokens_per_s(8192, 1, 0.1) == pytest.approx(8192 / 1e-4)
+
+
+def test_local_attention_flop_count():
+    # closed form vs a direct sum over positions (window below, at and above n)
+    import bench
+    for n, d, W in ((10, 4, 3), (37, 8, 37), (5, 2, 9), (8192, 128, 512)):
+        keys = sum(min(t + 1, W) for t in range(n))
+        assert bench.local_attention_flops(2, n, d, W) == 4.0 * d * keys * 2
