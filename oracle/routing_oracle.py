@@ -26,6 +26,10 @@ Steps (per batch b and head h, with Q shared as K):
                  the argmax assignment (centroid_ema_topw)
   local          the companion layer: causal attention of every position over the
                  `window` positions ending at it (local_attention)
+  backward       gradients of a5..a6 with respect to the shared Q/K rows and V,
+                 routing held fixed (routing_attention_head_backward)
+  separate QK    queries and keys routed separately by the same centroids
+                 (routing_attention_head_separate)
 
 Parity status: every function below is pinned by tests in
 ``tests/test_oracle_pins.py`` (closed forms, invariants, brute force, library
@@ -49,6 +53,8 @@ __all__ = [
     "centroid_ema",
     "centroid_ema_topw",
     "local_attention",
+    "routing_attention_head_backward",
+    "routing_attention_head_separate",
 ]
 
 
@@ -304,3 +310,82 @@ def local_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int,
     logits = np.where(visible, logits, -np.inf)
     e = np.exp(logits - logits.max(axis=1, keepdims=True))
     return (e / e.sum(axis=1, keepdims=True)) @ v
+
+
+def routing_attention_head_backward(q, v, idx, dO, causal: bool = True, scale=None):
+    """Gradients of a5..a6 (shared Q/K) for one (batch, head).
+
+    q, v [n, d]; idx [k, w] the clusters' ascending member lists (routing, a1..a4,
+    is held fixed: it is piecewise constant in q, and the centroids learn by the
+    k-means step a7, not by gradients -- §2, §4); dO [n, d] the gradient of the
+    loss with respect to O.  Returns (dq, dv), each [n, d]; dq collects both the
+    query and the key role of every shared row.
+
+    Per cluster, with P = softmax(scale Q_c Q_c^T + causal mask), Y_c = P V_c and
+    O = the mean of a position's Y rows (a6): dY_c[i] = dO[p_i] / m_{p_i};
+    dV_c = P^T dY_c; dP = dY_c V_c^T; dS = P * (dP - rowsum(dP * P));
+    dq[p_i] += scale (dS Q_c)_i (query role) + scale (dS^T Q_c)_i (key role).
+    Source: §3 (softmax attention rows), §4 (only same-cluster pairs).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    dO = np.asarray(dO, dtype=np.float64)
+    n, d = q.shape
+    if scale is None or scale <= 0:
+        scale = 1.0 / np.sqrt(d)
+    idx = np.asarray(idx)
+    m = membership_counts(idx, n)
+    dq = np.zeros_like(q)
+    dv = np.zeros_like(v)
+    for members in idx:
+        qc, vc = q[members], v[members]
+        _, P = cluster_attention(q, q, v, members, causal, scale, return_probs=True)
+        dY = dO[members] / m[members][:, None]
+        dVc = P.T @ dY
+        dP = dY @ vc.T
+        dS = P * (dP - (dP * P).sum(axis=1, keepdims=True))
+        np.add.at(dq, members, scale * (dS @ qc) + scale * (dS.T @ qc))
+        np.add.at(dv, members, dVc)
+    return dq, dv
+
+
+def routing_attention_head_separate(q, k, v, mu, w: int, causal: bool = True, scale=None):
+    """Routing with separate queries and keys, for one (batch, head).
+
+    Queries and keys are each normalised (a1), scored against the same
+    centroids (a2) and each centroid keeps its w best queries and, separately,
+    its w best keys (a3, a4).  Inside cluster c every listed query attends to
+    the listed keys at positions not after its own (causal) with softmax
+    (a5); a position's output is the mean over the clusters that listed it as
+    a query and gave it at least one visible key, zero if none (a6).
+    Returns dict(O, idx_q, idx_k).
+
+    Source: §4 "Routing attention with clustering" (queries and keys routed to
+    the same clusters; only same-cluster query/key pairs attend), §3.
+    Reading: a (query, cluster) pair with no visible key carries no output and
+    is left out of that position's mean.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n, d = q.shape
+    if scale is None or scale <= 0:
+        scale = 1.0 / np.sqrt(d)
+    idx_q = top_w_per_centroid(centroid_scores(normalise_rows(q), mu), w)
+    idx_k = top_w_per_centroid(centroid_scores(normalise_rows(k), mu), w)
+    acc = np.zeros((n, d))
+    cnt = np.zeros(n, dtype=np.int64)
+    for c in range(idx_q.shape[0]):
+        pq, pk = idx_q[c], idx_k[c]
+        logits = scale * (q[pq] @ k[pk].T)
+        visible = (pk[None, :] <= pq[:, None]) if causal else np.ones((len(pq), len(pk)), bool)
+        logits = np.where(visible, logits, -np.inf)
+        has = visible.any(axis=1)
+        e = np.exp(logits[has] - logits[has].max(axis=1, keepdims=True))
+        Y = (e / e.sum(axis=1, keepdims=True)) @ v[pk]
+        np.add.at(acc, pq[has], Y)
+        np.add.at(cnt, pq[has], 1)
+    O = np.zeros((n, d))
+    hit = cnt > 0
+    O[hit] = acc[hit] / cnt[hit, None]
+    return {"O": O, "idx_q": idx_q, "idx_k": idx_k}

@@ -306,12 +306,110 @@ def check_local_attention():
     np.testing.assert_allclose(orc.local_attention(q, q, v, W, scale), ref, atol=1e-12)
 
 
+def _torch_forward_shared(q, v, idx, causal, scale):
+    """a5..a6 written with torch ops (autograd builds the backward)."""
+    import torch
+    n, d = q.shape
+    out = torch.zeros((n, d), dtype=torch.float64)
+    counts = torch.zeros(n, dtype=torch.float64)
+    for members in idx:
+        p = torch.as_tensor(np.asarray(members), dtype=torch.long)
+        qc = q[p]
+        S = scale * (qc @ qc.T)
+        if causal:
+            keep = torch.tril(torch.ones_like(S, dtype=torch.bool))
+            S = S.masked_fill(~keep, float("-inf"))
+        Y = torch.softmax(S, dim=1) @ v[p]
+        out = out.index_add(0, p, Y)
+        counts = counts.index_add(0, p, torch.ones(len(p), dtype=torch.float64))
+    return out / counts.clamp(min=1.0)[:, None]
+
+
+def check_backward_autograd():
+    import torch
+    rng = np.random.default_rng(23)
+    n, d, kc, w = 24, 6, 3, 10   # k*w > n: some positions sit in several clusters
+    for causal in (True, False):
+        q = rng.standard_normal((n, d))
+        v = rng.standard_normal((n, d))
+        mu = orc.normalise_rows(rng.standard_normal((kc, d)))
+        dO = rng.standard_normal((n, d))
+        scale = 1.0 / math.sqrt(d)
+        res = orc.routing_attention_head(q, q, v, mu, w, causal=causal, scale=scale)
+        assert orc.membership_counts(res["idx"], n).max() >= 2
+        dq, dv = orc.routing_attention_head_backward(q, v, res["idx"], dO, causal, scale)
+        qt = torch.tensor(q, requires_grad=True)
+        vt = torch.tensor(v, requires_grad=True)
+        out = _torch_forward_shared(qt, vt, res["idx"], causal, scale)
+        np.testing.assert_allclose(out.detach().numpy(), res["O"], atol=1e-12)
+        (out * torch.from_numpy(dO)).sum().backward()
+        np.testing.assert_allclose(dq, qt.grad.numpy(), atol=1e-10)
+        np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-10)
+
+
+def check_backward_finite_difference():
+    rng = np.random.default_rng(24)
+    n, d, kc, w = 8, 3, 2, 5
+    q = rng.standard_normal((n, d))
+    v = rng.standard_normal((n, d))
+    mu = orc.normalise_rows(rng.standard_normal((kc, d)))
+    dO = rng.standard_normal((n, d))
+    idx = orc.routing_attention_head(q, q, v, mu, w)["idx"]
+    dq, dv = orc.routing_attention_head_backward(q, v, idx, dO)
+
+    def loss(qq, vv):
+        return float((orc.routing_attention_head(qq, qq, vv, mu, w, idx=idx)["O"] * dO).sum())
+
+    eps = 1e-6
+    for (i, j) in ((0, 0), (3, 1), (n - 1, d - 1)):
+        e = np.zeros((n, d))
+        e[i, j] = eps
+        np.testing.assert_allclose((loss(q + e, v) - loss(q - e, v)) / (2 * eps), dq[i, j],
+                                   atol=1e-6)
+        np.testing.assert_allclose((loss(q, v + e) - loss(q, v - e)) / (2 * eps), dv[i, j],
+                                   atol=1e-6)
+
+
+def check_separate_routing():
+    rng = np.random.default_rng(25)
+    n, d, kc, w = 30, 8, 4, 9
+    q = rng.standard_normal((n, d))
+    kk = rng.standard_normal((n, d))
+    v = rng.standard_normal((n, d))
+    mu = orc.normalise_rows(rng.standard_normal((kc, d)))
+    scale = 1.0 / math.sqrt(d)
+    # keys equal to the queries: the shared-QK step
+    shared = orc.routing_attention_head(q, q, v, mu, w, causal=True, scale=scale)
+    sep = orc.routing_attention_head_separate(q, q, v, mu, w, causal=True, scale=scale)
+    np.testing.assert_allclose(sep["O"], shared["O"], atol=1e-12)
+    assert np.array_equal(sep["idx_q"], shared["idx"]) and np.array_equal(sep["idx_k"], shared["idx"])
+    # one centroid taking every position: full attention with separate keys
+    mu1 = orc.normalise_rows(rng.standard_normal((1, d)))
+    for causal in (True, False):
+        got = orc.routing_attention_head_separate(q, kk, v, mu1, n, causal=causal, scale=scale)["O"]
+        np.testing.assert_allclose(got, _sdpa(q, kk, v, causal, scale), atol=1e-12)
+    # a query whose cluster's only key comes later sees nothing (causal): zero
+    # row; without the mask it returns that key's value row exactly
+    e = _zero_mean_orthonormal(d, 2, rng)
+    qq = np.stack([e[0], -e[0], e[1], -e[1]])
+    kq = np.stack([-e[0], e[1], -e[1], e[0]])
+    vv = rng.standard_normal((4, d))
+    m1 = e[0][None]
+    got = orc.routing_attention_head_separate(qq, kq, vv, m1, 1, causal=True, scale=scale)
+    assert got["idx_q"].tolist() == [[0]] and got["idx_k"].tolist() == [[3]]
+    assert np.all(got["O"] == 0.0)
+    got = orc.routing_attention_head_separate(qq, kq, vv, m1, 1, causal=False, scale=scale)
+    np.testing.assert_allclose(got["O"][0], vv[3], atol=1e-15)
+    assert np.all(got["O"][1:] == 0.0)
+
+
 ALL_CHECKS = [
     check_normalise_closed_form, check_scores_cosine, check_assign_ties,
     check_top_w_exhaustive, check_top_w_invariants, check_full_attention_k1,
     check_k_copies_average, check_rows_sum_to_one, check_v_ones_and_coverage,
     check_w1_and_first_slot, check_ema_special_cases, check_ema_topw_special_cases,
-    check_local_attention,
+    check_local_attention, check_backward_autograd, check_backward_finite_difference,
+    check_separate_routing,
 ]
 
 
@@ -405,15 +503,47 @@ _ORIG_ATT = orc.cluster_attention
 _ORIG_EMA = orc.centroid_ema
 _ORIG_EMA_TOPW = orc.centroid_ema_topw
 _ORIG_LOCAL = orc.local_attention
+_ORIG_BWD = orc.routing_attention_head_backward
+_ORIG_SEP = orc.routing_attention_head_separate
 
 
-def _mut_local_window_off_by_one(q, k, v, window, scale):
-    return _ORIG_LOCAL(q, k, v, window + 1, scale)
+def _mut_backward_no_key_role(q, v, idx, dO, causal=True, scale=None):
+    # drops the key-role term of dq: recomputed as the query role alone
+    q = np.asarray(q, dtype=np.float64)
+    n, d = q.shape
+    sc = scale if scale and scale > 0 else 1.0 / np.sqrt(d)
+    dq, dv = _ORIG_BWD(q, v, idx, dO, causal, scale)
+    m = orc.membership_counts(idx, n)
+    dq2 = np.zeros_like(q)
+    for members in np.asarray(idx):
+        qc, vc = q[members], np.asarray(v, dtype=np.float64)[members]
+        _, P = orc.cluster_attention(q, q, v, members, causal, sc, return_probs=True)
+        dY = np.asarray(dO, dtype=np.float64)[members] / m[members][:, None]
+        dP = dY @ vc.T
+        dS = P * (dP - (dP * P).sum(axis=1, keepdims=True))
+        np.add.at(dq2, members, sc * (dS @ qc))
+    return dq2, dv
 
 
-def _mut_ema_topw_first_sequence(qk, idx, mu, decay):
-    qk = np.asarray(qk)
-    return _ORIG_EMA_TOPW(qk[:1], np.asarray(idx)[:1], mu, decay)
+def _mut_separate_keys_follow_queries(q, k, v, mu, w, causal=True, scale=None):
+    # the keys take the queries' member lists instead of their own
+    res = _ORIG_SEP(q, k, v, mu, w, causal, scale)
+    q64, k64, v64 = (np.asarray(a, dtype=np.float64) for a in (q, k, v))
+    n, d = q64.shape
+    sc = scale if scale and scale > 0 else 1.0 / np.sqrt(d)
+    acc = np.zeros((n, d))
+    cnt = np.zeros(n, dtype=np.int64)
+    for pq in res["idx_q"]:
+        logits = sc * (q64[pq] @ k64[pq].T)
+        vis = (pq[None, :] <= pq[:, None]) if causal else np.ones((len(pq), len(pq)), bool)
+        logits = np.where(vis, logits, -np.inf)
+        ex = np.exp(logits - logits.max(axis=1, keepdims=True))
+        np.add.at(acc, pq, (ex / ex.sum(axis=1, keepdims=True)) @ v64[pq])
+        np.add.at(cnt, pq, 1)
+    O = np.zeros((n, d))
+    O[cnt > 0] = acc[cnt > 0] / cnt[cnt > 0, None]
+    return {"O": O, "idx_q": res["idx_q"], "idx_k": res["idx_q"]}
+
 
 MUTANTS = [
     ("normalise_rows", _mut_no_centering),
@@ -426,6 +556,8 @@ MUTANTS = [
     ("centroid_scores", _mut_scores_transposed),
     ("centroid_ema_topw", _mut_ema_topw_first_sequence),
     ("local_attention", _mut_local_window_off_by_one),
+    ("routing_attention_head_backward", _mut_backward_no_key_role),
+    ("routing_attention_head_separate", _mut_separate_keys_follow_queries),
 ]
 
 
