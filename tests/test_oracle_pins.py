@@ -545,6 +545,15 @@ def _mut_separate_keys_follow_queries(q, k, v, mu, w, causal=True, scale=None):
     return {"O": O, "idx_q": res["idx_q"], "idx_k": res["idx_q"]}
 
 
+def _mut_ema_topw_first_sequence(qk, idx, mu, decay):
+    qk = np.asarray(qk)
+    return _ORIG_EMA_TOPW(qk[:1], np.asarray(idx)[:1], mu, decay)
+
+
+def _mut_local_window_off_by_one(q, k, v, window, scale):
+    return _ORIG_LOCAL(q, k, v, window + 1, scale)
+
+
 MUTANTS = [
     ("normalise_rows", _mut_no_centering),
     ("cluster_attention", _mut_mask_flipped),
