@@ -1,20 +1,26 @@
 """Routing-attention benchmark (one JSON line on stdout, rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload c3] [--no-graph]
+                    [--workload c3] [--no-configs] [--no-cpu-baseline]
 
 A step is one pass of the whole hot path over one batch of synthetic input:
 routing (normalise, score, argmax, top-w per centroid, position sort),
-in-cluster causal attention, the averaging scatter and the centroid update.
-The default workload is the n=8192, H=8, d=128 configuration
-(mix128_bf16_b1h8_n8192_d128_k128_w64).
+in-cluster causal attention, the averaging scatter and, where the workload
+has one, the centroid update.  The headline workload is the n=8192, H=8,
+d=128 configuration (mix128_bf16_b1h8_n8192_d128_k128_w64).
 
-ours:       CUDA library; device time with CUDA events per step, L2 flushed
-            (256 MiB write) before every timed step; e2e = the same step with
-            pinned-host inputs copied in and the output copied out inside the
-            timed region; per-kernel times from the library's launch hook.
-reference:  the fp64 CPU oracle on the host cores, each step a bounded sample
-            (one head of the batch) scaled to the same tokens/s metric.
+ours:       CUDA library; device time with CUDA events per step (K replays of
+            the step captured as one CUDA graph), L2 flushed (256 MiB write)
+            before every timed step; e2e = the same step through the public
+            API with pinned-host inputs copied in and the output copied out
+            inside the timed region; per-kernel times from the library's launch
+            hook.  At one GPU the line also carries `configs`: the same
+            measurements (fewer steps) on every one of the five workloads, each
+            with the oracle timed on one core and on all host cores.
+reference:  the fp64 CPU oracle on the host cores: every step runs all heads
+            of the workload, one head per worker process (spawned, one BLAS
+            thread each, as many workers as heads or cores), and is timed as
+            a whole.
 """
 
 from __future__ import annotations
@@ -23,7 +29,9 @@ import argparse
 import hashlib
 import json
 import math
+import multiprocessing as mp
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -53,7 +61,8 @@ def _peaks():
 
 # ---------------------------------------------------------------------------
 # algorithmic work per launch, by kernel kind (bytes moved that the method
-# must move, or flops it must do); see the design doc for the derivations.
+# must move, or flops it must do): rows read and written once, scores written
+# and read once, index lists, per-slot output rows.
 # ---------------------------------------------------------------------------
 
 def kernel_work(name, wl):
@@ -70,9 +79,12 @@ def kernel_work(name, wl):
         return dict(bytes=byts, flops=4.0 * BH * k * w * w * d)
     if name == "scatter_average":
         return dict(bytes=BH * n * 4 + BH * n * d * s, flops=0.0)
+    if name == "ema_bucket":
+        # the assignments, read once (the row ids it writes are scratch)
+        return dict(bytes=BH * n * 4, flops=0.0)
     if name == "ema_update":
-        # rows, assignments, centroids read and written
-        return dict(bytes=BH * n * d * s + BH * n * 4 + wl.H * k * d * 8, flops=3.0 * BH * n * d)
+        # rows read once, centroids read and written
+        return dict(bytes=BH * n * d * s + wl.H * k * d * 8, flops=3.0 * BH * n * d)
     if name == "centroid_prep":
         kpad = (k + 15) // 16 * 16
         return dict(bytes=wl.H * k * d * 4 + wl.H * (3 * kpad * d * 2 + kpad * 4), flops=0.0)
@@ -130,7 +142,7 @@ def alu_peak_tflops(sm_mhz):
 KERNEL_BOUND = {
     "score_simt": "alu", "attention_simt": "alu", "score_tc": "hbm", "attention_tc": "hbm",
     "select_topw": "hbm", "scatter_average": "hbm", "ema_update": "hbm",
-    "centroid_prep": "hbm",
+    "ema_bucket": "hbm", "centroid_prep": "hbm",
 }
 
 KERNEL_SOURCES = {
@@ -138,7 +150,7 @@ KERNEL_SOURCES = {
     "centroid_prep": ["k_score_tc.cu"], "select_topw": ["k_select.cu"],
     "attention_simt": ["k_attention_simt.cu"],
     "attention_tc": ["k_attention_tc.cu", "k_attention_pipe.cu", "attn_common.cuh", "tc_ptx.cuh"],
-    "scatter_average": ["k_scatter.cu"], "ema_update": ["k_ema.cu"],
+    "scatter_average": ["k_scatter.cu"], "ema_update": ["k_ema.cu"], "ema_bucket": ["k_ema.cu"],
 }
 
 
@@ -319,70 +331,131 @@ class ClockSampler:
 # CPU oracle timing (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
 
-def oracle_head_seconds(wl, head, reps=1):
-    """Time the oracle's full step (a1..a7) on one head of the batch."""
+ONE_THREAD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+_WORKER = {}
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or "unknown"
+
+
+def _oracle_worker_init(wl_id):
+    """Spawned worker: one BLAS thread, its own copy of the workload (drawn
+    from the same seed, so nothing large crosses the process boundary)."""
+    os.environ.update(ONE_THREAD_ENV)
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    from workloads import make_workload
+    _WORKER["wl"] = make_workload(wl_id)
+
+
+def _oracle_head(h):
+    """The oracle's step on head h: a1..a6 on every sequence of the head, then
+    a7 on the head's centroids (when the workload has it).  Returns the
+    seconds spent in the oracle (input decoding excluded)."""
     import numpy as np
 
     import oracle.routing_oracle as orc
 
-    q64 = wl.q_f32().astype(np.float64)[:, head:head + 1]
-    v64 = wl.v_f32().astype(np.float64)[:, head:head + 1]
-    mu = wl.centroids[head:head + 1]
-    best = float("inf")
-    for _ in range(reps):
+    wl = _WORKER["wl"]
+    q64 = wl.q_f32()[:, h:h + 1].astype(np.float64)
+    v64 = wl.v_f32()[:, h:h + 1].astype(np.float64)
+    mu = wl.centroids[h:h + 1]
+    t0 = time.perf_counter()
+    _, _, a = orc.routing_attention(q64, q64, v64, mu, wl.w, causal=True)
+    if wl.ema:
+        orc.centroid_ema(q64, a, mu, wl.decay)
+    return time.perf_counter() - t0
+
+
+class OraclePool:
+    """Spawned worker processes running the oracle head by head.  Spawned, not
+    forked: the parent may hold a CUDA context."""
+
+    def __init__(self, wl_id, workers):
+        self.workers = workers
+        self.pool = mp.get_context("spawn").Pool(workers, initializer=_oracle_worker_init,
+                                                 initargs=(wl_id,))
+
+    def one_head(self, h=0):
+        return self.pool.apply(_oracle_head, (h,))
+
+    def step(self, H):
+        """Wall time of one whole step: every head, one per worker at a time."""
         t0 = time.perf_counter()
-        _, _, a = orc.routing_attention(q64, q64, v64, mu, wl.w, causal=True)
-        if wl.ema:
-            orc.centroid_ema(q64, a, mu, wl.decay)
-        best = min(best, time.perf_counter() - t0)
-    return best
+        self.pool.map(_oracle_head, range(H), chunksize=1)
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
 
 
-ONE_THREAD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+def oracle_baseline(wl_id, wl):
+    """The oracle as it stands on this host: one head on one core (scaled to
+    the step by the head count), and one whole step with the heads spread over
+    min(H, cores) worker processes."""
+    nproc = os.cpu_count() or 1
+    workers = max(1, min(wl.H, nproc))
+    pool = OraclePool(wl_id, workers)
+    try:
+        one = pool.one_head(0)
+        allc = pool.step(wl.H)
+    finally:
+        pool.close()
+    one_step = one * wl.H
+    return {
+        "value": wl.tokens / allc, "unit": UNIT, "cores": workers, "kind": "oracle",
+        "sample": f"one whole step of {wl.name} (every head; forward"
+                  f"{' + centroid update' if wl.ema else ''}), fp64 numpy oracle, heads spread "
+                  f"over {workers} spawned worker processes with one BLAS thread each; "
+                  f"{allc:.2f} s for the step",
+        "single_core": {"value": wl.tokens / one_step, "unit": UNIT, "cores": 1,
+                        "sample": f"head 0 alone on one thread ({one:.2f} s) x {wl.H} heads"},
+        "nproc": nproc, "cpu_model": cpu_model(),
+    }
 
 
-def cpu_baseline(wl_id, wl):
-    """The oracle as it stands, timed in a child process pinned to one BLAS
-    thread: every head of one step once (the reference arm, H steps)."""
-    env = dict(os.environ, **ONE_THREAD_ENV)
-    env.pop("RANK", None), env.pop("WORLD_SIZE", None), env.pop("LOCAL_RANK", None)
-    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", wl_id,
-           "--steps", str(wl.H), "--warmup", "0"]
-    res = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
-    line = None
-    for ln in res.stdout.splitlines():
-        if ln.startswith("{"):
-            line = json.loads(ln)
-    if res.returncode != 0 or line is None:
-        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
-                "sample": "oracle run failed: " + res.stderr.strip()[-200:]}
-    return {"value": line["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"one step of {wl.name} (forward + centroid update), each of the "
-                      f"{wl.H} heads once, fp64 numpy oracle on 1 thread; mean head time "
-                      f"x {wl.H} heads = {line['ms_per_step'] / 1e3:.2f} s per step"}
+def base_config(wl):
+    """The `config` object both arms print (same keys)."""
+    return {"workload": wl.name, "B": wl.B, "H": wl.H, "n": wl.n, "d": wl.d, "k": wl.k,
+            "w": wl.w, "causal": True,
+            "step": "forward + centroid update" if wl.ema else "forward"}
 
 
-def run_reference(args, wl):
+def run_reference(args, wl_id, wl):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    for i in range(args.warmup):
-        oracle_head_seconds(wl, i % wl.H)
-    times = []
-    for i in range(args.steps):
-        times.append(oracle_head_seconds(wl, i % wl.H) * wl.H)
+    nproc = os.cpu_count() or 1
+    workers = max(1, min(wl.H, nproc))
+    pool = OraclePool(wl_id, workers)
+    t_start = time.perf_counter()
+    try:
+        for _ in range(args.warmup):
+            pool.step(wl.H)
+        times = [pool.step(wl.H) for _ in range(args.steps)]
+    finally:
+        pool.close()
     step_s = statistics.mean(times)
     value = wl.tokens / step_s
+    sample = (f"each step: every head of {wl.name} through the fp64 oracle, heads spread over "
+              f"{workers} spawned worker processes (one BLAS thread each)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "n": wl.n, "d": wl.d, "k": wl.k,
-                       "w": wl.w, "step": "forward + centroid update"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"each step: one head of {wl.name} through the fp64 "
-                                       f"oracle on 1 thread, x {wl.H} heads"},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "data": "synthetic", "config": base_config(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": workers, "kind": "oracle",
+                             "sample": sample, "nproc": nproc, "cpu_model": cpu_model()},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": time.perf_counter() - t_start}
     print(json.dumps(line), flush=True)
 
 
@@ -411,13 +484,226 @@ def job_tokens_per_s(tokens_per_rank, world, t_ms):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args, wl):
-    import numpy as np
+def step_bytes(wl):
+    """Algorithmic bytes of one whole step (sum over the kernels' rows)."""
+    names = ["score_tc", "select_topw", "attention_tc", "scatter_average"]
+    if wl.ema:
+        names += ["ema_bucket", "ema_update"]
+    return sum(kernel_work(nm, wl)["bytes"] for nm in names)
+
+
+def causal_flops(wl):
+    """Flops of the causal products inside the clusters: row i of a cluster
+    meets i + 1 keys, for QK^T and PV (2 d flops each)."""
+    return 4.0 * wl.d * (wl.w * (wl.w + 1) / 2) * wl.k * wl.B * wl.H
+
+
+class Measured:
+    """Device measurements of one workload (the library's tensors stay on the
+    GPU until close())."""
+
+    def __init__(self, wl, dev):
+        import numpy as np
+        import torch
+
+        import content_sparse_attention_shared_b300 as rt
+
+        self.wl, self.dev = wl, dev
+        if wl.dtype == "f32":
+            q_h, v_h = torch.from_numpy(wl.q), torch.from_numpy(wl.v)
+        else:
+            q_h = torch.from_numpy(wl.q.view(np.int16)).view(torch.bfloat16)
+            v_h = torch.from_numpy(wl.v.view(np.int16)).view(torch.bfloat16)
+        self.q_h, self.v_h = q_h.pin_memory(), v_h.pin_memory()
+        self.q, self.v = self.q_h.to(dev), self.v_h.to(dev)
+        self.mu = torch.from_numpy(wl.centroids).to(dev)
+        self.out = torch.empty_like(self.v)
+        self.idx = torch.empty((wl.B, wl.H, wl.k, wl.w), dtype=torch.int32, device=dev)
+        self.assign = torch.empty((wl.B, wl.H, wl.n), dtype=torch.int32, device=dev)
+        self.ws = rt.Workspace.for_shape(wl.B, wl.H, wl.n, wl.d, wl.k, wl.w, self.q.dtype, dev)
+        self.rt = rt
+
+    def step(self, qq=None, vv=None):
+        # launches go to torch's current stream (the capture stream while a
+        # CUDA graph is being recorded)
+        rt, wl = self.rt, self.wl
+        qq = self.q if qq is None else qq
+        vv = self.v if vv is None else vv
+        rt.rt_routing_attention(qq, qq, vv, self.mu, wl.w, causal=True, out=self.out,
+                                idx_out=self.idx, assign_out=self.assign, workspace=self.ws)
+        if wl.ema:
+            rt.rt_centroid_ema(qq, self.assign, self.mu, wl.decay, workspace=self.ws)
+
+    def capture(self, warmup):
+        import torch
+        for _ in range(max(3, warmup)):
+            self.step()
+        torch.cuda.synchronize()
+        self.ws.check()
+        n0 = self.rt.rt_launch_count()
+        self.step()
+        torch.cuda.synchronize()
+        self.launches_per_step = self.rt.rt_launch_count() - n0
+        self.graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(self.dev)
+        cap.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(cap):
+            self.step()  # warm-up on the capture stream
+        cap.synchronize()
+        with torch.cuda.graph(self.graph, stream=cap):
+            self.step()
+        torch.cuda.synchronize()
+        for _ in range(max(3, warmup)):
+            self.graph.replay()
+        torch.cuda.synchronize()
+
+    def timed(self, steps, flush, stream, world, clocks=None, soak_ms=0.0):
+        """K graph replays, L2 flushed (outside the events) before each.
+        With `clocks` (a ClockSampler), the sampler runs over `soak_ms` of
+        untimed replays immediately before the timed region and over the
+        region itself."""
+        import torch
+        import torch.distributed as dist
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+        def region():
+            if soak_ms > 0:
+                t_end = time.perf_counter() + soak_ms * 1e-3
+                while time.perf_counter() < t_end:
+                    for _ in range(20):
+                        flush.zero_()
+                        self.graph.replay()
+                    torch.cuda.synchronize()
+            for i in range(steps):
+                flush.zero_()
+                ev[i][0].record(stream)
+                self.graph.replay()
+                ev[i][1].record(stream)
+            torch.cuda.synchronize()
+
+        if clocks is not None:
+            with clocks:
+                region()
+        else:
+            region()
+        t_ms = slowest_rank_ms(statistics.mean(a.elapsed_time(b) for a, b in ev), self.dev)
+        if world > 1:
+            dist.barrier()
+        self.ws.check()
+        return t_ms
+
+    def kernel_times(self, steps, flush):
+        """Per-kernel device times: eager steps behind a sleep kernel, so the
+        host has every launch queued before the GPU reaches it and the launch
+        hook's events bracket device time only."""
+        import torch
+        rt = self.rt
+        prof_steps = min(steps, 50)
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(self.launches_per_step * prof_steps)]
+        torch.cuda.synchronize()
+        rt.rt_profile_set(pairs)
+        for _ in range(prof_steps):
+            flush.zero_()
+            torch.cuda._sleep(400000)  # about 0.2 ms at 2 GHz
+            self.step()
+        torch.cuda.synchronize()
+        names = [rt.rt_profile_kernel_name(i) for i in range(len(pairs))]
+        rt.rt_profile_set([])
+        per_kind = {}
+        for i, (a, b) in enumerate(pairs):
+            per_kind.setdefault(names[i], []).append(a.elapsed_time(b))
+        kern = {k2: {"launches": len(v2), "avg_us": 1e3 * statistics.mean(v2),
+                     "total_ms": sum(v2)} for k2, v2 in per_kind.items()}
+        total = sum(x["total_ms"] for x in kern.values())
+        peaks = _peaks()
+        for name, x in kern.items():
+            x["share"] = x["total_ms"] / total if total else None
+            wk = kernel_work(name, self.wl)
+            x["hbm_gbs"] = wk["bytes"] / (x["avg_us"] * 1e-6) / 1e9 if x["avg_us"] else None
+            x["hbm_frac"] = x["hbm_gbs"] / peaks["hbm_gbs"] if x["hbm_gbs"] else None
+        return kern
+
+    def e2e(self, steps, flush, stream, world):
+        """The same step through the public API from pinned host buffers: Q and
+        V copied in and the output copied out inside the timed region."""
+        import torch
+        import torch.distributed as dist
+        out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            self.q.copy_(self.q_h, non_blocking=True)
+            self.v.copy_(self.v_h, non_blocking=True)
+            self.step()
+            out_h.copy_(self.out, non_blocking=True)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = slowest_rank_ms(statistics.mean(a.elapsed_time(b) for a, b in ev), self.dev)
+        h2d = (self.q_h.numel() * self.q_h.element_size() + self.v_h.numel() * self.v_h.element_size())
+        d2h = out_h.numel() * out_h.element_size()
+        return e2e_ms, h2d, d2h
+
+    def close(self):
+        import torch
+        for name in ("graph", "q", "v", "mu", "out", "idx", "assign", "ws", "q_h", "v_h"):
+            if hasattr(self, name):
+                delattr(self, name)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
+def roofline_for(kern, wl, peaks):
+    dname, dstat = max(kern.items(), key=lambda kv: kv[1]["total_ms"])
+    work = kernel_work(dname, wl)
+    bound = KERNEL_BOUND.get(dname, "hbm")
+    avg_s = dstat["avg_us"] * 1e-6
+    if bound == "hbm":
+        achieved, peak, unit = work["bytes"] / avg_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    elif bound == "tensor":
+        achieved, peak, unit = work["flops"] / avg_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = (work["flops"] / avg_s / 1e12, alu_peak_tflops(peaks["sm_max_mhz"]),
+                                "TFLOP/s")
+    return {"kernel": dname, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic_for(dname, wl.name),
+            "peak_source": (peaks["source"] if bound != "alu"
+                            else "derived: 148 SMs x 128 fp32 lanes x 2 flop x max SM clock"),
+            "algorithmic_per_launch": work["bytes"] if bound == "hbm" else work["flops"]}
+
+
+def config_entry(wl, t_ms, kern, peaks, cpu):
+    """The per-workload record of the `configs` map."""
+    s = t_ms * 1e-3
+    entry = {"workload": wl.name, "ms_per_step": t_ms, "tokens_per_s": wl.tokens / s,
+             "tflops_nominal": wl.nominal_flops() / s / 1e12,
+             "tflops_causal": causal_flops(wl) / s / 1e12,
+             "tflops_frac_bf16": wl.nominal_flops() / s / 1e12 / peaks["bf16_tflops"],
+             "step_hbm_frac": step_bytes(wl) / s / 1e9 / peaks["hbm_gbs"],
+             "step": "forward + centroid update" if wl.ema else "forward",
+             "kernels": {k2: {"avg_us": v2["avg_us"], "share": v2["share"],
+                              "hbm_frac": v2["hbm_frac"]} for k2, v2 in kern.items()}}
+    if cpu is not None:
+        entry["cpu_oracle"] = cpu
+    return entry
+
+
+def run_ours(args, wl_id, wl):
     import torch
     import torch.distributed as dist
 
     import content_sparse_attention_shared_b300 as rt
     from content_sparse_attention_shared_b300 import build as rt_build
+    from workloads import CONFIG_ORDER, make_workload
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -428,189 +714,80 @@ def run_ours(args, wl):
     dev = torch.device("cuda", local)
     rt_build.build()
     rt.load_library()
-
-    if wl.dtype == "f32":
-        q_h = torch.from_numpy(wl.q)
-        v_h = torch.from_numpy(wl.v)
-    else:
-        q_h = torch.from_numpy(wl.q.view(np.int16)).view(torch.bfloat16)
-        v_h = torch.from_numpy(wl.v.view(np.int16)).view(torch.bfloat16)
-    q_h, v_h = q_h.pin_memory(), v_h.pin_memory()
-    mu0 = torch.from_numpy(wl.centroids).to(dev)
-    q = q_h.to(dev)
-    v = v_h.to(dev)
-    mu = mu0.clone()
-    out = torch.empty_like(v)
-    idx = torch.empty((wl.B, wl.H, wl.k, wl.w), dtype=torch.int32, device=dev)
-    assign = torch.empty((wl.B, wl.H, wl.n), dtype=torch.int32, device=dev)
-    ws = rt.Workspace.for_shape(wl.B, wl.H, wl.n, wl.d, wl.k, wl.w, q.dtype, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    peaks = _peaks()
 
-    def step(qq, vv):
-        # launches go to torch's current stream (the capture stream while a
-        # CUDA graph is being recorded)
-        rt.rt_routing_attention(qq, qq, vv, mu, wl.w, causal=True, out=out, idx_out=idx,
-                                assign_out=assign, workspace=ws)
-        if wl.ema:
-            rt.rt_centroid_ema(qq, assign, mu, wl.decay, workspace=ws)
-
-    for _ in range(max(3, args.warmup)):
-        step(q, v)
-    torch.cuda.synchronize()
-    ws.check()
-
-    n_launch_before = rt.rt_launch_count()
-    step(q, v)
-    torch.cuda.synchronize()
-    launches_per_step = rt.rt_launch_count() - n_launch_before
-
-    # ---- the step as one CUDA graph (no host launch cost per kernel) -----
-    graph = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    with torch.cuda.stream(cap):
-        step(q, v)  # warm-up on the capture stream
-    cap.synchronize()
-    with torch.cuda.graph(graph, stream=cap):
-        step(q, v)
-    torch.cuda.synchronize()
-    for _ in range(max(3, args.warmup)):
-        graph.replay()
-    torch.cuda.synchronize()
-
-    # ---- device-timed region: K graph replays, L2 flushed before each ----
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     props = torch.cuda.get_device_properties(dev)
     pci = None
     if hasattr(props, "pci_bus_id"):
         pci = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
                                      getattr(props, "pci_device_id", 0))
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local, pci) as clk:
-        for i in range(args.steps):
-            flush.zero_()
-            ev[i][0].record(stream)
-            graph.replay()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-    gpu_launches = launches_per_step * args.steps  # kernels the replays ran
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    t_ms = slowest_rank_ms(statistics.mean(step_ms), dev)
-    if world > 1:
-        dist.barrier()
-    ws.check()
 
-    # ---- per-kernel device times: eager steps behind a sleep kernel, so the
-    # host has every launch queued before the GPU reaches it and the launch
-    # hook's events bracket device time only -------------------------------
-    prof_steps = min(args.steps, 50)
-    prof_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(launches_per_step * prof_steps)]
-    torch.cuda.synchronize()
-    rt.rt_profile_set(prof_pairs)
-    for i in range(prof_steps):
-        flush.zero_()
-        torch.cuda._sleep(400000)  # about 0.2 ms at 2 GHz
-        step(q, v)
-    torch.cuda.synchronize()
-    prof_names = [rt.rt_profile_kernel_name(i) for i in range(len(prof_pairs))]
-    rt.rt_profile_set([])
-    per_kind = {}
-    for i, (a, b) in enumerate(prof_pairs):
-        per_kind.setdefault(prof_names[i], []).append(a.elapsed_time(b))
-    kern = {k2: {"launches": len(v2), "avg_us": 1e3 * statistics.mean(v2),
-                 "total_ms": sum(v2)} for k2, v2 in per_kind.items()}
-    total_kernel_ms = sum(x["total_ms"] for x in kern.values())
-    for x in kern.values():
-        x["share"] = x["total_ms"] / total_kernel_ms if total_kernel_ms else None
+    # ---- the headline workload ------------------------------------------
+    m = Measured(wl, dev)
+    m.capture(args.warmup)
+    clk = ClockSampler(local, pci)
+    t_ms = m.timed(args.steps, flush, stream, world, clocks=clk, soak_ms=args.soak_ms)
+    gpu_launches = m.launches_per_step * args.steps  # kernels the timed replays ran
+    kern = m.kernel_times(args.steps, flush)
+    e2e_ms, h2d, d2h = m.e2e(args.steps, flush, stream, world)
+    local_attn = local_attention_timing(wl, m.q, m.v, flush, stream, args.steps)
+    launches_per_step = m.launches_per_step
+    m.close()
 
-    # ---- end-to-end through the public API with host buffers -------------
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()
-        e2e_ev[i][0].record(stream)
-        q.copy_(q_h, non_blocking=True)
-        v.copy_(v_h, non_blocking=True)
-        step(q, v)
-        out_h.copy_(out, non_blocking=True)
-        e2e_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = slowest_rank_ms(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev), dev)
-
-    # ---- the companion layer on the same rows, for comparison -------------
-    local = local_attention_timing(wl, q, v, flush, stream, args.steps)
+    # ---- every workload, at one GPU --------------------------------------
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = {}
+        csteps = max(10, min(args.steps, 50))
+        for cid in CONFIG_ORDER:
+            cw = wl if cid == wl_id else make_workload(cid)
+            if cid == wl_id:
+                ct, ck = t_ms, kern
+            else:
+                cm = Measured(cw, dev)
+                cm.capture(args.warmup)
+                ct = cm.timed(csteps, flush, stream, world)
+                ck = cm.kernel_times(csteps, flush)
+                cm.close()
+            cpu = None if args.no_cpu_baseline else oracle_baseline(cid, cw)
+            configs[cid] = config_entry(cw, ct, ck, peaks, cpu)
+            configs[cid]["steps"] = args.steps if cid == wl_id else csteps
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    peaks = _peaks()
-    clocks = clk.summary()
-    tokens = wl.tokens * world
     value = job_tokens_per_s(wl.tokens, world, t_ms)
     tflops = wl.nominal_flops() * world / (t_ms * 1e-3) / 1e12
-
-    # dominant kernel roofline
-    dom = max(kern.items(), key=lambda kv: kv[1]["total_ms"])
-    dname, dstat = dom
-    work = kernel_work(dname, wl)
-    bound = KERNEL_BOUND.get(dname, "hbm")
-    avg_s = dstat["avg_us"] * 1e-6
-    if bound == "hbm":
-        achieved = work["bytes"] / avg_s / 1e9
-        peak = peaks["hbm_gbs"]
-        unit = "GB/s"
-    elif bound == "tensor":
-        achieved = work["flops"] / avg_s / 1e12
-        peak = peaks["bf16_tflops"]
-        unit = "TFLOP/s"
-    else:
-        achieved = work["flops"] / avg_s / 1e12
-        peak = alu_peak_tflops(peaks["sm_max_mhz"])
-        unit = "TFLOP/s"
-    traffic = traffic_for(dname, wl.name)
-    roof = {"kernel": dname, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": traffic,
-            "peak_source": (peaks["source"] if bound != "alu"
-                            else "derived: 148 SMs x 128 fp32 lanes x 2 flop x max SM clock"),
-            "algorithmic_per_launch": work["bytes"] if bound == "hbm" else work["flops"]}
-    for name, x in kern.items():
-        wk = kernel_work(name, wl)
-        x["hbm_gbs"] = wk["bytes"] / (x["avg_us"] * 1e-6) / 1e9 if x["avg_us"] else None
-        x["hbm_frac"] = x["hbm_gbs"] / peaks["hbm_gbs"] if x["hbm_gbs"] else None
-
-    h2d = (q_h.numel() * q_h.element_size() + v_h.numel() * v_h.element_size())
-    d2h = out_h.numel() * out_h.element_size()
+    clocks = clk.summary()
+    clocks["window"] = (f"{args.soak_ms:.0f} ms of untimed replays immediately before the timed "
+                        f"region, then the timed region")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "n": wl.n, "d": wl.d, "k": wl.k,
-                   "w": wl.w, "causal": True, "step": "forward + centroid update" if wl.ema
-                   else "forward", "l2": "flushed before every timed step (256 MiB write)",
-                   "graph": True, "kernel_times": "eager steps behind a sleep kernel, "
-                   "CUDA events around each launch"},
-        "tflops": tflops, "tflops_frac_bf16": tflops / peaks["bf16_tflops"],
-        "roofline": roof,
+        "config": base_config(wl),
+        "timing": {"l2": "flushed before every timed step (256 MiB write)",
+                   "graph": "the step captured once as a CUDA graph, replayed per step",
+                   "kernel_times": "eager steps behind a sleep kernel, CUDA events around each "
+                                   "launch (includes a few us of launch gap per kernel)"},
+        "tflops": tflops, "tflops_causal": causal_flops(wl) * world / (t_ms * 1e-3) / 1e12,
+        "tflops_frac_bf16": tflops / peaks["bf16_tflops"],
+        "roofline": roofline_for(kern, wl, peaks),
         "e2e": {"value": job_tokens_per_s(wl.tokens, world, e2e_ms), "unit": UNIT,
-                "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": gpu_launches, "launches_per_step": launches_per_step,
         "clocks": clocks, "kernels": kern,
-        "local_attention": local,
+        "local_attention": local_attn,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, wl)
+        line["cpu_baseline"] = (configs[wl_id]["cpu_oracle"] if configs
+                                else oracle_baseline(wl_id, wl))
+    if configs is not None:
+        line["configs"] = configs
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -624,15 +801,19 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c3", help="c1..c5 (default: the n=8192 configuration)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="measure the headline workload only (no `configs` map)")
+    ap.add_argument("--soak-ms", type=float, default=300.0,
+                    help="untimed replays right before the timed region, for the clock record")
     args = ap.parse_args()
     if args.impl == "reference":
         os.environ.update(ONE_THREAD_ENV)  # before numpy is imported
     from workloads import make_workload
     wl = make_workload(args.workload)
     if args.impl == "reference":
-        run_reference(args, wl)
+        run_reference(args, args.workload, wl)
     else:
-        run_ours(args, wl)
+        run_ours(args, args.workload, wl)
 
 
 if __name__ == "__main__":

@@ -10,6 +10,8 @@ from ._binding import (  # noqa: F401
     Workspace,
     load_library,
     rt_centroid_ema,
+    rt_centroid_ema_apply,
+    rt_centroid_ema_sums,
     rt_centroid_ema_topw,
     rt_launch_count,
     rt_local_attention,
@@ -18,5 +20,6 @@ from ._binding import (  # noqa: F401
     rt_route_assign,
     rt_route_assign_noalloc,
     rt_routing_attention,
+    rt_routing_attention_separate,
     rt_workspace_bytes,
 )

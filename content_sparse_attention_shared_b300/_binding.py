@@ -28,16 +28,23 @@ SIGNATURES = {
     "rt_routing_attention": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                       _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp, _c_size,
                                       _vp]),
+    "rt_routing_attention_separate": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                               _vp, _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp,
+                                               _vp, _vp, _c_size, _vp]),
     "rt_centroid_ema": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_int,
                                  _c_float, _vp, _c_size, _vp]),
     "rt_centroid_ema_topw": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp,
                                       _c_int, _c_float, _vp, _c_size, _vp]),
+    "rt_centroid_ema_sums": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp,
+                                      _vp, _c_size, _vp]),
+    "rt_centroid_ema_apply": (_c_int, [_vp, _c_int, _c_int, _vp, _c_int, _c_float, _vp]),
     "rt_local_attention": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                     _c_float, _vp, _vp, _c_size, _vp]),
     "rt_route_assign_noalloc": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int,
                                          _c_int, _vp, _vp, _vp]),
     "rt_workspace_init": (_c_int, [_vp, _c_size, _vp]),
     "rt_check_device_status": (_c_int, [_vp, _c_size, _vp]),
+    "rt_debug_inject_wait_timeout": (_c_int, [ctypes.c_uint, ctypes.c_ulonglong]),
     "rt_status_string": (ctypes.c_char_p, [_c_int]),
     "rt_last_error_detail": (ctypes.c_char_p, []),
     "rt_launch_count": (ctypes.c_int64, []),
@@ -184,6 +191,26 @@ def rt_routing_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     return out
 
 
+def rt_routing_attention_separate(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                                  centroids: torch.Tensor, w: int, causal: bool = True,
+                                  scale: float = 0.0, out: Optional[torch.Tensor] = None,
+                                  idx_q_out: Optional[torch.Tensor] = None,
+                                  idx_k_out: Optional[torch.Tensor] = None,
+                                  assign_out: Optional[torch.Tensor] = None,
+                                  workspace: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """Routing attention with queries and keys routed separately."""
+    B, H, n, d = q.shape
+    kc = centroids.shape[1]
+    if out is None:
+        out = torch.empty_like(v)
+    ws = _ws(workspace, B, H, n, d, kc, w, q.dtype, q.device)
+    _check(load_library().rt_routing_attention_separate(
+        _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, H, n, d, _ptr(centroids), kc, w,
+        1 if causal else 0, float(scale), _ptr(out), _ptr(idx_q_out), _ptr(idx_k_out),
+        _ptr(assign_out), ws.ptr, ws.nbytes, _stream(stream)))
+    return out
+
+
 def rt_centroid_ema(qk: torch.Tensor, assign: torch.Tensor, centroids: torch.Tensor, decay: float,
                     workspace: Optional[Workspace] = None, stream=None) -> torch.Tensor:
     B, H, n, d = qk.shape
@@ -208,6 +235,29 @@ def rt_centroid_ema_topw(qk: torch.Tensor, idx: torch.Tensor, centroids: torch.T
     return centroids
 
 
+def rt_centroid_ema_sums(qk: torch.Tensor, assign: torch.Tensor, k: int,
+                         sums: Optional[torch.Tensor] = None,
+                         workspace: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """This shard's per-centroid sums of normalised rows and counts, [H,k,d+1]."""
+    B, H, n, d = qk.shape
+    if sums is None:
+        sums = torch.empty((H, k, d + 1), dtype=torch.float32, device=qk.device)
+    ws = _ws(workspace, B, H, n, d, k, 1, qk.dtype, qk.device)
+    _check(load_library().rt_centroid_ema_sums(
+        _ptr(qk), _dtype_code(qk), B, H, n, d, _ptr(assign), k, _ptr(sums), ws.ptr, ws.nbytes,
+        _stream(stream)))
+    return sums
+
+
+def rt_centroid_ema_apply(sums: torch.Tensor, centroids: torch.Tensor, decay: float,
+                          stream=None) -> torch.Tensor:
+    """The centroid step from (all-reduced) sums [H,k,d+1], in place."""
+    H, k, d = centroids.shape
+    _check(load_library().rt_centroid_ema_apply(
+        _ptr(sums), H, d, _ptr(centroids), k, float(decay), _stream(stream)))
+    return centroids
+
+
 def rt_local_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int,
                        scale: float = 0.0, out: Optional[torch.Tensor] = None,
                        workspace: Optional[Workspace] = None, stream=None) -> torch.Tensor:
@@ -220,6 +270,15 @@ def rt_local_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window
         _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, H, n, d, int(window), float(scale),
         _ptr(out), ws.ptr, ws.nbytes, _stream(stream)))
     return out
+
+
+RT_DEBUG_SCORE, RT_DEBUG_ATTENTION, RT_DEBUG_LOCAL_ATTENTION = 1, 2, 4
+
+
+def rt_debug_inject_wait_timeout(kernels: int, limit_ns: int) -> None:
+    """Test aid: the selected kernels start with a bounded wait that runs out
+    (0, 0 turns it off)."""
+    _check(load_library().rt_debug_inject_wait_timeout(int(kernels), int(limit_ns)))
 
 
 def rt_launch_count() -> int:

@@ -62,7 +62,7 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
                       int g, int tiles_per_bh, int ntiles, int causal, float scale_log2,
                       const int32_t* __restrict__ idx, const int32_t* __restrict__ mcount,
                       bf16* __restrict__ out, float* __restrict__ yslot,
-                      unsigned int* __restrict__ err) {
+                      unsigned int* __restrict__ err, uint64_t fault_ns) {
   using L = PipeSmem<D>;
   constexpr int NS = L::NS;
   extern __shared__ uint8_t smem_raw[];
@@ -107,13 +107,18 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
   tc::tc_fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
   pdl_wait();  // the set-up above overlapped the previous kernel's tail
+  // a failed pass or the injected test timeout: no copy or MMA has been
+  // issued, so the CTA goes straight to the teardown (TMEM is given back)
+  const bool skip = pass_failed(err) || injected_wait_timeout(fault_ns, err);
 
   auto fail = [&](bool leader) {
     if (leader) atomicExch(err, (unsigned)DEV_TIMEOUT);
     stop_flag = 1;
   };
 
-  if (warp < 4) {
+  if (skip) {
+    // nothing to do
+  } else if (warp < 4) {
     // ======================= producers (128 threads) =======================
     const int r = tid;  // tile row
     // the row's position and membership count for tile `tile`
@@ -412,7 +417,8 @@ cudaError_t launch_pipe(const void* q, const void* v, int BH, int n, int k, int 
   launch_begin(K_ATTN_TC, s);
   e = launch_pdl(kern, dim3(grid), dim3(PTHREADS), smem, s, static_cast<const bf16*>(q),
                  static_cast<const bf16*>(v), n, k, w, g, tiles_per_bh, (int)ntiles, causal,
-                 scale_log2, idx, mcount, static_cast<bf16*>(out), yslot, err);
+                 scale_log2, idx, mcount, static_cast<bf16*>(out), yslot, err,
+                 injected_limit_ns(K_ATTN_TC));
   launch_end(K_ATTN_TC, s);
   return e;
 }

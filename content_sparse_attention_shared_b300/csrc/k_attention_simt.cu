@@ -11,6 +11,9 @@
 //
 // One CTA takes 64 query slots of one cluster and walks the cluster's key
 // slots in blocks of 64 with an online (running max / running sum) softmax.
+// With SEP (separate queries and keys) the key and value rows come from the
+// keys' own lists (idx_k) and the causal mask compares original positions; a
+// query with no visible key gets a zero row and is not counted in mvis.
 // Gathered K and V rows are staged in shared memory as fp32; each warp owns 8
 // query rows.  The epilogue writes a row straight to the output when the
 // position belongs to exactly one cluster, else to the per-slot buffer that
@@ -44,14 +47,17 @@ __device__ __forceinline__ void load_rows(float* dst, int ld, const T* __restric
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool SEP>
 __global__ void __launch_bounds__(THREADS)
 attention_simt_kernel(const T* __restrict__ q, const T* __restrict__ kk, const T* __restrict__ v,
                       int n, int k, int w, int causal, float scale,
-                      const int32_t* __restrict__ idx, const int32_t* __restrict__ mcount,
-                      T* __restrict__ out, float* __restrict__ yslot) {
+                      const int32_t* __restrict__ idx, const int32_t* __restrict__ idx_k,
+                      const int32_t* __restrict__ mcount, int32_t* __restrict__ mvis,
+                      T* __restrict__ out, float* __restrict__ yslot,
+                      const unsigned int* __restrict__ err) {
   pdl_trigger();
   pdl_wait();
+  if (status_set(err)) return;  // uniform: only earlier kernels set the word
   extern __shared__ float smem[];
   constexpr int LDQ = D + 1;
   float* Qs = smem;              // [QB][D+1]
@@ -63,9 +69,13 @@ attention_simt_kernel(const T* __restrict__ q, const T* __restrict__ kk, const T
   const int bh = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t* pos = idx + ((size_t)bh * k + c) * w;
+  const int32_t* kpos = SEP ? idx_k + ((size_t)bh * k + c) * w : pos;
   const size_t head_off = (size_t)bh * n * D;
+  __shared__ int qp_s[QB], kp_s[KB];  // positions (SEP's causal mask)
 
   load_rows<T, D>(Qs, LDQ, q + head_off, pos, q0, QB, w, n);
+  if (SEP)
+    for (int i = threadIdx.x; i < QB; i += THREADS) qp_s[i] = q0 + i < w ? __ldcg(pos + q0 + i) : -1;
 
   float m[ROWS_PER_WARP], l[ROWS_PER_WARP], acc[ROWS_PER_WARP][D / 32];
 #pragma unroll
@@ -76,11 +86,13 @@ attention_simt_kernel(const T* __restrict__ q, const T* __restrict__ kk, const T
     for (int i = 0; i < D / 32; ++i) acc[r][i] = 0.0f;
   }
 
-  const int kend = causal ? min(w, q0 + QB) : w;
+  const int kend = (causal && !SEP) ? min(w, q0 + QB) : w;
   for (int kb0 = 0; kb0 < kend; kb0 += KB) {
     __syncthreads();
-    load_rows<T, D>(Ks, LDQ, kk + head_off, pos, kb0, KB, w, n);
-    load_rows<T, D>(Vs, D, v + head_off, pos, kb0, KB, w, n);
+    load_rows<T, D>(Ks, LDQ, kk + head_off, kpos, kb0, KB, w, n);
+    load_rows<T, D>(Vs, D, v + head_off, kpos, kb0, KB, w, n);
+    if (SEP)
+      for (int i = threadIdx.x; i < KB; i += THREADS) kp_s[i] = kb0 + i < w ? __ldcg(kpos + kb0 + i) : -1;
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < ROWS_PER_WARP; ++r) {
@@ -98,8 +110,15 @@ attention_simt_kernel(const T* __restrict__ q, const T* __restrict__ kk, const T
         d1 = fmaf(qv, k1[j], d1);
       }
       const int j0 = kb0 + lane, j1 = kb0 + lane + 32;
-      const bool v0 = j0 < w && (!causal || j0 <= qi);
-      const bool v1 = j1 < w && (!causal || j1 <= qi);
+      bool v0, v1;
+      if (SEP) {
+        const int qp = qp_s[rl];
+        v0 = j0 < w && (!causal || kp_s[lane] <= qp);
+        v1 = j1 < w && (!causal || kp_s[lane + 32] <= qp);
+      } else {
+        v0 = j0 < w && (!causal || j0 <= qi);
+        v1 = j1 < w && (!causal || j1 <= qi);
+      }
       const float s0 = v0 ? d0 * scale : -INFINITY;
       const float s1 = v1 ? d1 * scale : -INFINITY;
       const float mb = warp_max(fmaxf(s0, s1));
@@ -131,8 +150,10 @@ attention_simt_kernel(const T* __restrict__ q, const T* __restrict__ kk, const T
     if (qi >= w) continue;
     const int t = pos[qi];
     if ((unsigned)t >= (unsigned)n) continue;
-    const float inv_l = 1.0f / l[r];
-    if (__ldcg(mcount + (size_t)bh * n + t) == 1) {
+    const float inv_l = l[r] > 0.0f ? 1.0f / l[r] : 0.0f;  // no visible key: zero row
+    const int m_all = __ldcg(mcount + (size_t)bh * n + t);
+    if (SEP && m_all != 1 && l[r] > 0.0f && lane == 0) atomicAdd(mvis + (size_t)bh * n + t, 1);
+    if (m_all == 1) {
       T* orow = out + head_off + (size_t)t * D;
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) orow[lane + 32 * i] = from_f32<T>(acc[r][i] * inv_l);
@@ -146,17 +167,19 @@ attention_simt_kernel(const T* __restrict__ q, const T* __restrict__ kk, const T
 
 template <typename T, int D>
 cudaError_t launch_t(const void* q, const void* kk, const void* v, int BH, int n, int k, int w,
-                     int causal, float scale, const int32_t* idx, const int32_t* mcount,
-                     void* out, float* yslot, cudaStream_t s) {
+                     int causal, float scale, const int32_t* idx, const int32_t* idx_k,
+                     const int32_t* mcount, int32_t* mvis, void* out, float* yslot,
+                     unsigned int* err, cudaStream_t s) {
   const size_t smem = ((size_t)(QB + KB) * (D + 1) + (size_t)KB * D) * sizeof(float);
-  auto kern = attention_simt_kernel<T, D>;
+  auto kern = idx_k != nullptr ? attention_simt_kernel<T, D, true> : attention_simt_kernel<T, D, false>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((w + QB - 1) / QB, k, BH);
   launch_begin(K_ATTN_SIMT, s);
   e = launch_pdl(kern, grid, dim3(THREADS), smem, s, static_cast<const T*>(q),
                  static_cast<const T*>(kk), static_cast<const T*>(v), n, k, w, causal, scale, idx,
-                 mcount, static_cast<T*>(out), yslot);
+                 idx_k, mcount, mvis, static_cast<T*>(out), yslot,
+                 static_cast<const unsigned int*>(err));
   launch_end(K_ATTN_SIMT, s);
   return e;
 }
@@ -165,15 +188,16 @@ cudaError_t launch_t(const void* q, const void* kk, const void* v, int BH, int n
 
 cudaError_t launch_attention_simt(const void* q, const void* kk, const void* v, rt_dtype dt,
                                   int BH, int n, int d, int k, int w, int causal,
-                                  float scale, const int32_t* idx, const int32_t* mcount,
-                                  void* out, float* yslot, cudaStream_t s) {
+                                  float scale, const int32_t* idx, const int32_t* idx_k,
+                                  const int32_t* mcount, int32_t* mvis, void* out, float* yslot,
+                                  unsigned int* err, cudaStream_t s) {
   if (dt == RT_F32) {
-    return d == 64 ? launch_t<float, 64>(q, kk, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, s)
-                   : launch_t<float, 128>(q, kk, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, s);
+    return d == 64 ? launch_t<float, 64>(q, kk, v, BH, n, k, w, causal, scale, idx, idx_k, mcount, mvis, out, yslot, err, s)
+                   : launch_t<float, 128>(q, kk, v, BH, n, k, w, causal, scale, idx, idx_k, mcount, mvis, out, yslot, err, s);
   }
   return d == 64
-             ? launch_t<__nv_bfloat16, 64>(q, kk, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, s)
-             : launch_t<__nv_bfloat16, 128>(q, kk, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, s);
+             ? launch_t<__nv_bfloat16, 64>(q, kk, v, BH, n, k, w, causal, scale, idx, idx_k, mcount, mvis, out, yslot, err, s)
+             : launch_t<__nv_bfloat16, 128>(q, kk, v, BH, n, k, w, causal, scale, idx, idx_k, mcount, mvis, out, yslot, err, s);
 }
 
 }  // namespace rt

@@ -9,7 +9,10 @@
 // (shared QK).
 //
 // This kernel serves clusters wider than one 128-row tile (w > 128; narrower
-// clusters go to the pipelined kernel in k_attention_pipe.cu).  Work unit: a
+// clusters go to the pipelined kernel in k_attention_pipe.cu), routing with
+// separate queries and keys (any w; queries and keys of a cluster come from
+// their own lists, the mask compares original positions), and local
+// attention.  Work unit: a
 // row tile of 128 consecutive slots of one cluster (TMEM lanes); it walks the
 // cluster's key blocks of 128 (causal: up to its own block) with an online
 // softmax, the partial P V of each block read back from TMEM and accumulated
@@ -59,22 +62,40 @@ struct AttnSmem {
   static constexpr int BYTES = V_OFF + QB;
 };
 
-// LOCAL = false: clusters wider than one tile (positions from idx, w > 128).
-// LOCAL = true:  local attention -- tile lt holds positions lt*128 .. +127,
+// MODE_CLUSTER:  shared QK, clusters wider than one tile (positions from
+//                idx, w > 128).
+// MODE_LOCAL:    local attention -- tile lt holds positions lt*128 .. +127,
 //                w is the window (a row sees the w positions ending at its
 //                own), and its key blocks are the 128-position blocks from the
 //                one holding lt*128 - w + 1 up to lt; idx, mcount and yslot
 //                are not used and every row goes to `out`.
-template <int D, bool LOCAL>
+// MODE_SEPARATE: separate queries and keys.  Query rows come from idx (the
+//                queries' lists), key and value rows from idx_k (the keys'
+//                lists), keys from `kk`; every key block of the cluster is
+//                visited, and with causal=1 a key is visible to a query when
+//                its position is not after the query's.  A query row with no
+//                visible key is written as zeros and is not counted in
+//                mvis[position] (the number of visible memberships the
+//                scatter divides by).
+constexpr int MODE_CLUSTER = 0, MODE_LOCAL = 1, MODE_SEPARATE = 2;
+
+template <int D, int MODE>
 __global__ void __launch_bounds__(THREADS, 2)
-attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int n, int k, int w,
+attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ kk,
+                    const bf16* __restrict__ v, int n, int k, int w,
                     int tiles_per_bh, int R, int causal, float scale_log2,
-                    const int32_t* __restrict__ idx, const int32_t* __restrict__ mcount,
+                    const int32_t* __restrict__ idx, const int32_t* __restrict__ idx_k,
+                    const int32_t* __restrict__ mcount, int32_t* __restrict__ mvis,
                     bf16* __restrict__ out, float* __restrict__ yslot,
-                    unsigned int* __restrict__ err) {
+                    unsigned int* __restrict__ err, uint64_t fault_ns) {
+  constexpr bool LOCAL = MODE == MODE_LOCAL;
+  constexpr bool SEP = MODE == MODE_SEPARATE;
   using L = AttnSmem<D>;
   pdl_trigger();
   pdl_wait();
+  // nothing is in flight and no TMEM is held yet: a failed pass or the
+  // injected test timeout returns here
+  if (pass_failed(err) || injected_wait_timeout(fault_ns, err)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -91,8 +112,10 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
   const int tile = blockIdx.x;
   const int bh = tile / tiles_per_bh;
   const int lt = tile % tiles_per_bh;
-  const int32_t* idx_bh = idx + (size_t)bh * k * w;
+  const int32_t* idx_bh = LOCAL ? nullptr : idx + (size_t)bh * k * w;
+  const int32_t* kidx_bh = SEP ? idx_k + (size_t)bh * k * w : idx_bh;
   const bf16* q_bh = q + (size_t)bh * n * D;
+  const bf16* k_bh = (SEP ? kk : q) + (size_t)bh * n * D;
   const bf16* v_bh = v + (size_t)bh * n * D;
 
   // ---- row mapping (thread tid owns tile row tid) ----------------------------
@@ -112,7 +135,7 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
     rt = lt % R;
     slot = rt * ROWS + tid;
     row_valid = slot < w;
-    nkb = causal ? rt + 1 : R;
+    nkb = (causal && !SEP) ? rt + 1 : R;
     if (row_valid) {
       my_pos = __ldcg(idx_bh + (size_t)cluster * w + slot);
       if ((unsigned)my_pos >= (unsigned)n) { my_pos = -1; row_valid = false; }  // defensive
@@ -163,14 +186,14 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
       if (LOCAL) {
         if (ks < n) p = ks;
       } else if (ks < w) {
-        p = __ldcg(idx_bh + (size_t)cluster * w + ks);
+        p = __ldcg(kidx_bh + (size_t)cluster * w + ks);
         if ((unsigned)p >= (unsigned)n) p = -1;
       }
       __syncthreads();  // previous block's buffers are free (all reads done)
       kpos[tid] = p;
       __syncthreads();
-      if (kbi != rt) {
-        gather_kmajor<D>(KPs, q_bh, kpos);
+      if (SEP || kbi != rt) {
+        gather_kmajor<D>(KPs, k_bh, kpos);
         Kop = KPs;
       }
       gather_mnmajor<D>(Vs, v_bh, kpos);
@@ -210,6 +233,19 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
       const int pk0 = kbi * ROWS;
       jmin = max(0, my_pos - w + 1 - pk0);
       jmax = min(min(ROWS, my_pos - pk0 + 1), n - pk0);
+    } else if (SEP) {
+      // keys of the block in ascending position order: the visible ones are
+      // the first `jmax`, those at positions <= this row's
+      const int nvalid = min(ROWS, w - kbi * ROWS);
+      jmax = nvalid;
+      if (causal) {
+        int lo = 0, hi = nvalid;  // first key position above my_pos
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (kpos[mid] <= my_pos) lo = mid + 1; else hi = mid;
+        }
+        jmax = lo;
+      }
     } else {
       const int kslot0 = kbi * ROWS;
       jmax = min(ROWS, w - kslot0);
@@ -337,6 +373,7 @@ attention_tc_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int 
       }
     }
     __syncwarp();
+    if (SEP && row_valid && my_m != 1 && l_run > 0.0f) atomicAdd(mvis + (size_t)bh * n + my_pos, 1);
     const int single = (row_valid && (LOCAL || my_m == 1)) ? 1 : 0;
     const int ch = lane % CPR;
 #pragma unroll 4
@@ -374,15 +411,39 @@ cudaError_t launch_t(const void* q, const void* v, int BH, int n, int k, int w, 
   const int R = (w + ROWS - 1) / ROWS;  // row tiles (and key blocks) per cluster
   const int tiles_per_bh = k * R;
   const size_t smem = 1024 + (size_t)AttnSmem<D>::BYTES;
-  auto kern = attention_tc_kernel<D, false>;
+  auto kern = attention_tc_kernel<D, MODE_CLUSTER>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   const long long tiles = (long long)BH * tiles_per_bh;
   const float scale_log2 = scale * 1.4426950408889634f;
   launch_begin(K_ATTN_TC, s);
   e = launch_pdl(kern, dim3((unsigned)tiles), dim3(THREADS), smem, s, static_cast<const bf16*>(q),
-                 static_cast<const bf16*>(v), n, k, w, tiles_per_bh, R, causal, scale_log2, idx,
-                 mcount, static_cast<bf16*>(out), yslot, err);
+                 static_cast<const bf16*>(q), static_cast<const bf16*>(v), n, k, w, tiles_per_bh,
+                 R, causal, scale_log2, idx, static_cast<const int32_t*>(nullptr), mcount,
+                 static_cast<int32_t*>(nullptr), static_cast<bf16*>(out), yslot, err,
+                 injected_limit_ns(K_ATTN_TC));
+  launch_end(K_ATTN_TC, s);
+  return e;
+}
+
+template <int D>
+cudaError_t launch_sep_t(const void* q, const void* kk, const void* v, int BH, int n, int k,
+                         int w, int causal, float scale, const int32_t* idx_q,
+                         const int32_t* idx_k, const int32_t* mcount, int32_t* mvis, void* out,
+                         float* yslot, unsigned int* err, cudaStream_t s) {
+  const int R = (w + ROWS - 1) / ROWS;
+  const int tiles_per_bh = k * R;
+  const size_t smem = 1024 + (size_t)AttnSmem<D>::BYTES;
+  auto kern = attention_tc_kernel<D, MODE_SEPARATE>;
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
+  if (e != cudaSuccess) return e;
+  const long long tiles = (long long)BH * tiles_per_bh;
+  const float scale_log2 = scale * 1.4426950408889634f;
+  launch_begin(K_ATTN_TC, s);
+  e = launch_pdl(kern, dim3((unsigned)tiles), dim3(THREADS), smem, s, static_cast<const bf16*>(q),
+                 static_cast<const bf16*>(kk), static_cast<const bf16*>(v), n, k, w, tiles_per_bh,
+                 R, causal, scale_log2, idx_q, idx_k, mcount, mvis, static_cast<bf16*>(out),
+                 yslot, err, injected_limit_ns(K_ATTN_TC));
   launch_end(K_ATTN_TC, s);
   return e;
 }
@@ -392,16 +453,18 @@ cudaError_t launch_local_t(const void* q, const void* v, int BH, int n, int wind
                            void* out, unsigned int* err, cudaStream_t s) {
   const int tiles_per_bh = (n + ROWS - 1) / ROWS;
   const size_t smem = 1024 + (size_t)AttnSmem<D>::BYTES;
-  auto kern = attention_tc_kernel<D, true>;
+  auto kern = attention_tc_kernel<D, MODE_LOCAL>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   const long long tiles = (long long)BH * tiles_per_bh;
   const float scale_log2 = scale * 1.4426950408889634f;
   launch_begin(K_LOCAL_ATTN, s);
   e = launch_pdl(kern, dim3((unsigned)tiles), dim3(THREADS), smem, s, static_cast<const bf16*>(q),
-                 static_cast<const bf16*>(v), n, 0, window, tiles_per_bh, 1, 1, scale_log2,
+                 static_cast<const bf16*>(q), static_cast<const bf16*>(v), n, 0, window,
+                 tiles_per_bh, 1, 1, scale_log2, static_cast<const int32_t*>(nullptr),
                  static_cast<const int32_t*>(nullptr), static_cast<const int32_t*>(nullptr),
-                 static_cast<bf16*>(out), static_cast<float*>(nullptr), err);
+                 static_cast<int32_t*>(nullptr), static_cast<bf16*>(out),
+                 static_cast<float*>(nullptr), err, injected_limit_ns(K_LOCAL_ATTN));
   launch_end(K_LOCAL_ATTN, s);
   return e;
 }
@@ -412,6 +475,17 @@ cudaError_t launch_local_attention(const void* q, const void* v, int BH, int n, 
                                    float scale, void* out, unsigned int* err, cudaStream_t s) {
   return d == 64 ? launch_local_t<64>(q, v, BH, n, window, scale, out, err, s)
                  : launch_local_t<128>(q, v, BH, n, window, scale, out, err, s);
+}
+
+cudaError_t launch_attention_separate_tc(const void* q, const void* kk, const void* v, int BH,
+                                         int n, int d, int k, int w, int causal, float scale,
+                                         const int32_t* idx_q, const int32_t* idx_k,
+                                         const int32_t* mcount, int32_t* mvis, void* out,
+                                         float* yslot, unsigned int* err, cudaStream_t s) {
+  return d == 64 ? launch_sep_t<64>(q, kk, v, BH, n, k, w, causal, scale, idx_q, idx_k, mcount,
+                                    mvis, out, yslot, err, s)
+                 : launch_sep_t<128>(q, kk, v, BH, n, k, w, causal, scale, idx_q, idx_k, mcount,
+                                     mvis, out, yslot, err, s);
 }
 
 bool attention_tc_supported(rt_dtype dt, int d, int w) {

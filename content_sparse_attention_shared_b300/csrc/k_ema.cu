@@ -9,11 +9,14 @@
 //     mu_c <- normalise(decay * mu_c + (1 - decay) * mean of the assigned r_t),
 // and leaves a centroid without rows untouched.
 //
-// No floating-point atomics and one kernel: each (centroid, head) CTA scans
-// the head's assignments itself (coalesced 16-byte loads, 8192 rows per pass),
-// lists its rows in a fixed order with one block-wide scan, re-normalises
-// each row on the fly, sums them in that order, blends and renormalises.  The
-// result is deterministic.
+// A segmented reduction with no floating-point atomics that reads every
+// assignment and every row once: a bucketing kernel sorts every chunk's rows
+// by centroid with integer counts, then one CTA per (centroid, head)
+// concatenates its own rows chunk by chunk and sums them, normalised, in that
+// order -- an order fixed by the assignments alone, so the result is
+// deterministic.  The second kernel can stop before the blend and write each
+// centroid's raw sum and count instead, so that shards of a batch can be
+// combined with one all-reduce.
 #include "rt_internal.cuh"
 
 namespace rt {
@@ -21,8 +24,6 @@ namespace {
 
 constexpr int THREADS2 = 256;
 constexpr int WARPS2 = THREADS2 / 32;
-constexpr int SCAN_PER_THREAD = 32;                    // assignments per thread per pass
-constexpr int SCAN_ROWS = THREADS2 * SCAN_PER_THREAD;  // rows per pass
 constexpr int LIST = 1024;                             // rows listed per summation round
 constexpr int STAGE_BYTES = 24 * 1024;                 // rows staged in shared memory per round
 
@@ -130,29 +131,17 @@ __device__ __forceinline__ void add_rows(const T* __restrict__ qk, int H, int n,
   }
 }
 
-// Sums the row slots' partial sums in a fixed order, blends the mean into
-// the centroid (`old` = its previous value, loaded by threads < D) and
-// renormalises it.  Every thread of the block calls it.
+// Blends the mean sum/N into the centroid (`old` = its previous value) and
+// renormalises it; threads tid < D hold feature tid.  Every thread of the
+// block calls it (it contains a barrier); N > 0.
 template <int D>
-__device__ __forceinline__ void finish_centroid(const float (&acc)[8], int N, float old,
-                                                float decay, float* __restrict__ mu_c,
-                                                float (*red)[D] /* [RS][D], shared */) {
-  constexpr int CH = D / 8;
-  constexpr int RS = THREADS2 / CH;
+__device__ __forceinline__ void blend_store(float sum, int N, float old, float decay,
+                                            float* __restrict__ mu_c) {
   __shared__ float nrm_part[WARPS2];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ch = tid % CH, rs = tid / CH;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) red[rs][ch * 8 + j] = acc[j];
-  __syncthreads();
   float vj = 0.0f;
-  if (tid < D) {
-    float sum = 0.0f;
-    for (int r = 0; r < RS; ++r) sum += red[r][tid];
-    const float mean_j = sum / (float)N;
-    vj = decay * old + (1.0f - decay) * mean_j;
-  }
-  float sq = warp_sum(vj * vj);
+  if (tid < D) vj = decay * old + (1.0f - decay) * (sum / (float)N);
+  const float sq = warp_sum(vj * vj);
   if (lane == 0) nrm_part[warp] = sq;
   __syncthreads();
   if (tid < D) {
@@ -162,18 +151,143 @@ __device__ __forceinline__ void finish_centroid(const float (&acc)[8], int N, fl
   }
 }
 
-// One CTA per (centroid, head).  Pass by pass over each sequence's n
-// positions, thread i examines positions base + 1024 j + 4 i + e (j < 8,
-// e < 4; one coalesced 16-byte load per j), keeps a 32-bit mask of the rows
-// assigned to this centroid, and a block-wide exclusive scan of the mask
-// counts places them in a shared list in (thread, j, e) order.  The listed
-// rows are then staged in shared memory and summed (add_rows); the row slots'
-// partial sums are combined in a fixed order at the end, so the result is
-// deterministic.
-template <typename T, int D>
+// Sums the row slots' partial sums in a fixed order.  FINAL: blends the mean
+// into the centroid (`old` = its previous value, loaded by threads < D; a
+// centroid with N = 0 is left untouched).  Otherwise writes the raw sum and
+// the count N (as a float) to part_c[0 .. D].  Every thread of the block calls
+// it.
+template <int D, bool FINAL>
+__device__ __forceinline__ void finish_centroid(const float (&acc)[8], int N, float old,
+                                                float decay, float* __restrict__ mu_c,
+                                                float* __restrict__ part_c,
+                                                float (*red)[D] /* [RS][D], shared */) {
+  constexpr int CH = D / 8;
+  constexpr int RS = THREADS2 / CH;
+  const int tid = threadIdx.x;
+  const int ch = tid % CH, rs = tid / CH;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) red[rs][ch * 8 + j] = acc[j];
+  __syncthreads();
+  float sum = 0.0f;
+  if (tid < D)
+    for (int r = 0; r < RS; ++r) sum += red[r][tid];
+  if (!FINAL) {
+    if (tid < D) part_c[tid] = sum;
+    if (tid == 0) part_c[D] = (float)N;
+    return;
+  }
+  if (N == 0) return;  // uniform
+  blend_store<D>(sum, N, old, decay, mu_c);
+}
+
+// ---------------------------------------------------------------------------
+// Argmax-driven step as a segmented reduction in two kernels, with no
+// floating-point atomics and no per-centroid re-scan of the assignments:
+//
+// ema_bucket_kernel: one CTA per (chunk of R = 1024*M consecutive positions of
+//   one sequence, head).  It reads the chunk's assignments once and sorts the
+//   chunk's rows by centroid, stably, with integer counts only: warp w owns a
+//   stripe of 128*M consecutive positions, handled 32 at a time in position
+//   order; __match_any_sync gives each row its rank among the earlier rows of
+//   the stripe with the same centroid (per-warp counters in shared memory),
+//   and one block-wide exclusive scan over the (centroid, warp) counts turns
+//   ranks into places.  Writes, per chunk and centroid, (first place, count)
+//   and, per place, the row id b*n + t (`perm`, the chunk's own range of the
+//   head's B*n entries).  Rows with an assignment outside [0, k) are skipped.
+// ema_segment_kernel: one CTA per (centroid, head) concatenates its rows
+//   chunk by chunk in chunk order (a block scan over the chunks' counts), so
+//   it reads B*n/R pairs and its own rows only; the rows are then staged,
+//   normalised and summed in that fixed order (add_rows), the mean blended
+//   into the centroid and renormalised (finish_centroid).
+// The order of every sum is a function of the assignments alone, so the
+// result is deterministic.
+// ---------------------------------------------------------------------------
+constexpr int BUCKET_THREADS = 256;
+constexpr int BUCKET_WARPS = BUCKET_THREADS / 32;
+constexpr int BUCKET_ROWS = 1024;  // positions per chunk for M = 1
+
+template <int M>
+__global__ void __launch_bounds__(BUCKET_THREADS)
+ema_bucket_kernel(const int32_t* __restrict__ assign, int H, int n, int k, int cps,
+                  int nchunks, int2* __restrict__ offcnt, int32_t* __restrict__ perm, int Bn,
+                  const unsigned int* __restrict__ err) {
+  pdl_trigger();
+  constexpr int G = 4 * M;  // groups of 32 positions per warp stripe
+  constexpr int R = BUCKET_ROWS * M;
+  extern __shared__ int whist[];  // [BUCKET_WARPS][k]: counts, then places
+  __shared__ int wsum[BUCKET_WARPS];
+  const int j = blockIdx.x, h = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = j / cps;
+  const int t0 = (j - b * cps) * R;
+  for (int i = tid; i < BUCKET_WARPS * k; i += BUCKET_THREADS) whist[i] = 0;
+  pdl_wait();
+  const bool failed = status_set(err);
+  const int32_t* arow = assign + ((size_t)b * H + h) * n;
+  int a[G];
+#pragma unroll
+  for (int e = 0; e < G; ++e) {
+    const int t = t0 + warp * (32 * G) + 32 * e + lane;
+    int c = t < n ? __ldcg(arow + t) : -1;
+    a[e] = (c >= 0 && c < k) ? c : -1;
+  }
+  if (failed) return;  // uniform: only earlier kernels set the word
+  __syncthreads();  // counters cleared
+  // rank of each row among the earlier rows of this warp's stripe with the
+  // same centroid (groups in position order, lanes in position order)
+  int rank[G];
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int e = 0; e < G; ++e) {
+    const int c = a[e];
+    const unsigned peers = __match_any_sync(0xffffffffu, c);
+    rank[e] = c >= 0 ? whist[warp * k + c] + __popc(peers & lt) : 0;
+    __syncwarp();
+    if (c >= 0 && lane == __ffs(peers) - 1) whist[warp * k + c] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // exclusive scan of the counts in (centroid, warp) order: thread tid takes
+  // the consecutive items [tid*P, tid*P + P) of item c*BUCKET_WARPS + w
+  const int items = BUCKET_WARPS * k;
+  const int P = (items + BUCKET_THREADS - 1) / BUCKET_THREADS;
+  const int i0 = tid * P;
+  int local = 0;
+  for (int i = i0; i < i0 + P && i < items; ++i)
+    local += whist[(i % BUCKET_WARPS) * k + i / BUCKET_WARPS];
+  int total;
+  int run = block_exclusive_scan<BUCKET_THREADS>(local, wsum, total);
+  for (int i = i0; i < i0 + P && i < items; ++i) {
+    int& x = whist[(i % BUCKET_WARPS) * k + i / BUCKET_WARPS];
+    const int cnt = x;
+    x = run;
+    run += cnt;
+  }
+  __syncthreads();
+  // (first place, count) of every centroid in this chunk
+  int2* oc = offcnt + ((size_t)h * nchunks + j) * k;
+  for (int c = tid; c < k; c += BUCKET_THREADS) {
+    const int first = whist[c];
+    const int next = c + 1 < k ? whist[c + 1] : total;
+    oc[c] = make_int2(first, next - first);
+  }
+  int32_t* pp = perm + (size_t)h * Bn + (size_t)b * n + t0;
+#pragma unroll
+  for (int e = 0; e < G; ++e) {
+    const int c = a[e];
+    if (c >= 0) {
+      const int t = t0 + warp * (32 * G) + 32 * e + lane;
+      pp[whist[warp * k + c] + rank[e]] = b * n + t;
+    }
+  }
+}
+
+template <typename T, int D, bool FINAL>
 __global__ void __launch_bounds__(THREADS2, 7)
-ema_update_kernel(const T* __restrict__ qk, const int32_t* __restrict__ assign, int B, int H,
-                  int n, int k, float* __restrict__ mu, float decay) {
+ema_segment_kernel(const T* __restrict__ qk, const int2* __restrict__ offcnt,
+                   const int32_t* __restrict__ perm, int H, int n, int k, int cps, int R,
+                   int nchunks, int Bn, float* __restrict__ mu, float decay,
+                   float* __restrict__ out, const unsigned int* __restrict__ err) {
   pdl_trigger();
   __shared__ int rowlist[LIST];
   __shared__ int wsum[WARPS2];
@@ -181,53 +295,56 @@ ema_update_kernel(const T* __restrict__ qk, const int32_t* __restrict__ assign, 
   static_assert(STAGE_BYTES >= THREADS2 / (D / 8) * D * 4, "the stage holds the partial sums");
   const int c = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x;
-  const bool vec = (n & 3) == 0 && (reinterpret_cast<uintptr_t>(assign) & 15u) == 0;
   pdl_wait();
-  const float old = (tid < D) ? __ldcg(mu + ((size_t)h * k + c) * D + tid) : 0.0f;
+  const bool failed = status_set(err);
+  const float old = (FINAL && tid < D) ? __ldcg(mu + ((size_t)h * k + c) * D + tid) : 0.0f;
 
   float acc[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
   int N = 0;
-  for (int b = 0; b < B; ++b) {
-    const int32_t* arow = assign + ((size_t)b * H + h) * n;
-    for (int t0 = 0; t0 < n; t0 += SCAN_ROWS) {
-      // this thread's rows of the pass: bit 4 j + e <-> position t0 + 1024 j + 4 tid + e
-      uint32_t mask = 0u;
-#pragma unroll 4
-      for (int j = 0; j < SCAN_PER_THREAD / 4; ++j) {
-        const int t = t0 + j * (4 * THREADS2) + 4 * tid;
-        if (vec && t + 3 < n) {
-          const int4 a4 = __ldcg(reinterpret_cast<const int4*>(arow + t));
-          mask |= (uint32_t)(a4.x == c) << (4 * j + 0);
-          mask |= (uint32_t)(a4.y == c) << (4 * j + 1);
-          mask |= (uint32_t)(a4.z == c) << (4 * j + 2);
-          mask |= (uint32_t)(a4.w == c) << (4 * j + 3);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (t + e < n) mask |= (uint32_t)(__ldcg(arow + t + e) == c) << (4 * j + e);
-        }
-      }
-      int total;
-      const int ex = block_exclusive_scan<THREADS2>(__popc(mask), wsum, total);
-      // (out-of-range assignments never equal c, so they are never listed)
-      for (int sub = 0; sub < total; sub += LIST) {
-        int r = ex;
-        for (uint32_t mm = mask; mm != 0u; mm &= mm - 1u, ++r) {
-          const int bit = __ffs(mm) - 1;
-          if (r >= sub && r < sub + LIST)
-            rowlist[r - sub] = b * n + t0 + (bit >> 2) * (4 * THREADS2) + 4 * tid + (bit & 3);
-        }
-        __syncthreads();
-        add_rows<T, D>(qk, H, n, h, rowlist, min(LIST, total - sub), acc, stage);
-      }
-      N += total;
+  const int32_t* perm_h = perm + (size_t)h * Bn;
+  __shared__ int ex_s[THREADS2];        // first list place of each chunk of the block
+  __shared__ long long base_s[THREADS2];  // perm index of its first entry
+  for (int j0 = 0; j0 < nchunks; j0 += THREADS2) {
+    // chunk j0 + tid: its rows of centroid c, perm_h[base + first .. + cnt)
+    const int j = j0 + tid;
+    const int nthis = min(THREADS2, nchunks - j0);
+    int2 fc = make_int2(0, 0);
+    long long base = 0;
+    if (j < nchunks) {
+      fc = __ldcg(offcnt + ((size_t)h * nchunks + j) * k + c);
+      const int b = j / cps;
+      base = (long long)b * n + (long long)(j - b * cps) * R + fc.x;
     }
+    if (failed) return;  // uniform: only earlier kernels set the word
+    int total;
+    const int ex = block_exclusive_scan<THREADS2>(fc.y, wsum, total);
+    ex_s[tid] = ex;
+    base_s[tid] = base;
+    __syncthreads();
+    for (int sub = 0; sub < total; sub += LIST) {
+      // one entry per thread: the chunk holding list place p is the last one
+      // whose first place is <= p (ex_s is non-decreasing)
+      const int nl = min(LIST, total - sub);
+      for (int i = tid; i < nl; i += THREADS2) {
+        const int p = sub + i;
+        int lo = 0, hi = nthis - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (ex_s[mid] <= p) lo = mid; else hi = mid - 1;
+        }
+        rowlist[i] = __ldcg(perm_h + base_s[lo] + (p - ex_s[lo]));
+      }
+      __syncthreads();
+      add_rows<T, D>(qk, H, n, h, rowlist, nl, acc, stage);
+    }
+    N += total;
+    __syncthreads();  // ex_s / base_s may be rewritten
   }
-  if (N == 0) return;  // no assigned row: centroid unchanged (uniform)
-  finish_centroid<D>(acc, N, old, decay, mu + ((size_t)h * k + c) * D,
-                     reinterpret_cast<float (*)[D]>(stage));
+  finish_centroid<D, FINAL>(acc, N, old, decay, mu + ((size_t)h * k + c) * D,
+                            out + ((size_t)h * k + c) * (D + 1),
+                            reinterpret_cast<float (*)[D]>(stage));
 }
 
 // The variant driven by the top-w membership.  One CTA per (centroid, head)
@@ -238,7 +355,8 @@ ema_update_kernel(const T* __restrict__ qk, const int32_t* __restrict__ assign, 
 template <typename T, int D>
 __global__ void __launch_bounds__(THREADS2, 7)
 ema_topw_kernel(const T* __restrict__ qk, const int32_t* __restrict__ idx, int B, int H, int n,
-                int k, int w, float* __restrict__ mu, float decay) {
+                int k, int w, float* __restrict__ mu, float decay,
+                const unsigned int* __restrict__ err) {
   pdl_trigger();
   __shared__ int rowlist[LIST];
   __shared__ int wsum[WARPS2];
@@ -247,6 +365,7 @@ ema_topw_kernel(const T* __restrict__ qk, const int32_t* __restrict__ idx, int B
   const int c = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x;
   pdl_wait();
+  if (status_set(err)) return;  // uniform: only earlier kernels set the word
   const float old = (tid < D) ? __ldcg(mu + ((size_t)h * k + c) * D + tid) : 0.0f;
   float acc[8];
 #pragma unroll
@@ -274,57 +393,142 @@ ema_topw_kernel(const T* __restrict__ qk, const int32_t* __restrict__ idx, int B
       N += total;
     }
   }
-  if (N == 0) return;  // no valid entry: centroid unchanged (uniform)
-  finish_centroid<D>(acc, N, old, decay, mu + ((size_t)h * k + c) * D,
-                     reinterpret_cast<float (*)[D]>(stage));
+  finish_centroid<D, true>(acc, N, old, decay, mu + ((size_t)h * k + c) * D, nullptr,
+                           reinterpret_cast<float (*)[D]>(stage));
+}
+
+// The step from combined sums: red [H][k][D+1] holds every centroid's sum of
+// normalised rows and its count (as produced above, summed over shards).
+template <int D>
+__global__ void __launch_bounds__(THREADS2)
+ema_apply_kernel(const float* __restrict__ red, int k, float* __restrict__ mu, float decay) {
+  pdl_trigger();
+  pdl_wait();
+  const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const float* r = red + ((size_t)h * k + c) * (D + 1);
+  const float Nf = __ldcg(r + D);
+  const float sum = tid < D ? __ldcg(r + tid) : 0.0f;
+  const float old = tid < D ? __ldcg(mu + ((size_t)h * k + c) * D + tid) : 0.0f;
+  const int N = (int)Nf;
+  if (N <= 0) return;  // uniform
+  blend_store<D>(sum, N, old, decay, mu + ((size_t)h * k + c) * D);
 }
 
 template <typename T, int D>
 cudaError_t launch_topw(const void* qk, const int32_t* idx, int B, int H, int n, int k, int w,
-                        float* mu, float decay, cudaStream_t s) {
+                        float* mu, float decay, unsigned int* err, cudaStream_t s) {
   auto kern = ema_topw_kernel<T, D>;
   launch_begin(K_EMA_TOPW, s);
   cudaError_t e = launch_pdl(kern, dim3(k, H), dim3(THREADS2), 0, s, static_cast<const T*>(qk),
-                             idx, B, H, n, k, w, mu, decay);
+                             idx, B, H, n, k, w, mu, decay, static_cast<const unsigned int*>(err));
   launch_end(K_EMA_TOPW, s);
   return e;
 }
 
-template <typename T, int D>
+inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// ---- plan of the bucket-and-segment path ----------------------------------
+// rows per bucketing chunk: 1024 * M, with M the smallest of 1, 2, 4 whose
+// chunk covers at least k positions (so the per-chunk counts never outgrow the
+// row list)
+inline int bucket_m(int k) { return k <= 1024 ? 1 : k <= 2048 ? 2 : 4; }
+
+struct BucketPlan {
+  int M, R, cps, nchunks;
+  size_t perm_bytes, offcnt_bytes;
+};
+
+inline BucketPlan bucket_plan(int B, int H, int n, int k) {
+  BucketPlan p;
+  p.M = bucket_m(k);
+  p.R = BUCKET_ROWS * p.M;
+  p.cps = (n + p.R - 1) / p.R;
+  p.nchunks = B * p.cps;
+  p.perm_bytes = align256((size_t)H * B * n * sizeof(int32_t));
+  p.offcnt_bytes = align256((size_t)H * p.nchunks * k * sizeof(int2));
+  return p;
+}
+
+// FINAL: update mu in place.  Otherwise write every centroid's raw sum and
+// count to out [H][k][D+1] and leave mu alone.
+template <typename T, int D, bool FINAL>
 cudaError_t launch_update(const void* qk, const int32_t* assign, int B, int H, int n, int k,
-                          float* mu, float decay, cudaStream_t s) {
-  auto kern = ema_update_kernel<T, D>;
+                          float* mu, float decay, float* out, void* ws, unsigned int* err,
+                          cudaStream_t s) {
+  const unsigned int* cerr = err;
+  cudaError_t e;
+  const BucketPlan p = bucket_plan(B, H, n, k);
+  int32_t* perm = static_cast<int32_t*>(ws);
+  int2* offcnt = reinterpret_cast<int2*>(static_cast<uint8_t*>(ws) + p.perm_bytes);
+  const int Bn = B * n;
+  const size_t smem = (size_t)BUCKET_WARPS * k * sizeof(int);
+  auto bucket = p.M == 1 ? ema_bucket_kernel<1> : p.M == 2 ? ema_bucket_kernel<2> : ema_bucket_kernel<4>;
+  e = set_smem_limit(reinterpret_cast<const void*>(bucket), (int)smem);
+  if (e != cudaSuccess) return e;
+  launch_begin(K_EMA_BUCKET, s);
+  e = launch_pdl(bucket, dim3(p.nchunks, H), dim3(BUCKET_THREADS), smem, s, assign, H, n, k,
+                 p.cps, p.nchunks, offcnt, perm, Bn, cerr);
+  launch_end(K_EMA_BUCKET, s);
+  if (e != cudaSuccess) return e;
+  auto kern = ema_segment_kernel<T, D, FINAL>;
   launch_begin(K_EMA_UPDATE, s);
-  cudaError_t e = launch_pdl(kern, dim3(k, H), dim3(THREADS2), 0, s, static_cast<const T*>(qk),
-                             assign, B, H, n, k, mu, decay);
+  e = launch_pdl(kern, dim3(k, H), dim3(THREADS2), 0, s, static_cast<const T*>(qk),
+                 static_cast<const int2*>(offcnt), static_cast<const int32_t*>(perm), H, n, k,
+                 p.cps, p.R, p.nchunks, Bn, mu, decay, out, cerr);
   launch_end(K_EMA_UPDATE, s);
   return e;
 }
 
+template <bool FINAL>
+cudaError_t launch_update_any(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                              const int32_t* assign, float* mu, int k, float decay, float* out,
+                              void* ws, unsigned int* err, cudaStream_t s) {
+  if (dt == RT_F32) {
+    return d == 64 ? launch_update<float, 64, FINAL>(qk, assign, B, H, n, k, mu, decay, out, ws, err, s)
+                   : launch_update<float, 128, FINAL>(qk, assign, B, H, n, k, mu, decay, out, ws, err, s);
+  }
+  return d == 64
+             ? launch_update<__nv_bfloat16, 64, FINAL>(qk, assign, B, H, n, k, mu, decay, out, ws, err, s)
+             : launch_update<__nv_bfloat16, 128, FINAL>(qk, assign, B, H, n, k, mu, decay, out, ws, err, s);
+}
+
 }  // namespace
 
-size_t ema_workspace_bytes(int, int, int, int) { return 0; }
+size_t ema_workspace_bytes(int B, int H, int n, int /*d*/, int k, rt_dtype /*dt*/) {
+  const BucketPlan p = bucket_plan(B, H, n, k);
+  return p.perm_bytes + p.offcnt_bytes;
+}
 
 cudaError_t launch_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
-                       const int32_t* assign, float* mu, int k, float decay,
-                       void* /*ws*/, cudaStream_t s) {
-  if (dt == RT_F32) {
-    return d == 64 ? launch_update<float, 64>(qk, assign, B, H, n, k, mu, decay, s)
-                   : launch_update<float, 128>(qk, assign, B, H, n, k, mu, decay, s);
-  }
-  return d == 64 ? launch_update<__nv_bfloat16, 64>(qk, assign, B, H, n, k, mu, decay, s)
-                 : launch_update<__nv_bfloat16, 128>(qk, assign, B, H, n, k, mu, decay, s);
+                       const int32_t* assign, float* mu, int k, float decay, void* ws,
+                       unsigned int* err, cudaStream_t s) {
+  return launch_update_any<true>(qk, dt, B, H, n, d, assign, mu, k, decay, nullptr, ws, err, s);
+}
+
+cudaError_t launch_ema_sums(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                            const int32_t* assign, int k, float* sums, void* ws,
+                            unsigned int* err, cudaStream_t s) {
+  return launch_update_any<false>(qk, dt, B, H, n, d, assign, nullptr, k, 0.0f, sums, ws, err, s);
+}
+
+cudaError_t launch_ema_apply(const float* sums, int H, int d, float* mu, int k, float decay,
+                             cudaStream_t s) {
+  launch_begin(K_EMA_UPDATE, s);
+  cudaError_t e = d == 64 ? launch_pdl(ema_apply_kernel<64>, dim3(k, H), dim3(THREADS2), 0, s, sums, k, mu, decay)
+                          : launch_pdl(ema_apply_kernel<128>, dim3(k, H), dim3(THREADS2), 0, s, sums, k, mu, decay);
+  launch_end(K_EMA_UPDATE, s);
+  return e;
 }
 
 cudaError_t launch_ema_topw(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                             const int32_t* idx, int w, float* mu, int k, float decay,
-                            cudaStream_t s) {
+                            unsigned int* err, cudaStream_t s) {
   if (dt == RT_F32) {
-    return d == 64 ? launch_topw<float, 64>(qk, idx, B, H, n, k, w, mu, decay, s)
-                   : launch_topw<float, 128>(qk, idx, B, H, n, k, w, mu, decay, s);
+    return d == 64 ? launch_topw<float, 64>(qk, idx, B, H, n, k, w, mu, decay, err, s)
+                   : launch_topw<float, 128>(qk, idx, B, H, n, k, w, mu, decay, err, s);
   }
-  return d == 64 ? launch_topw<__nv_bfloat16, 64>(qk, idx, B, H, n, k, w, mu, decay, s)
-                 : launch_topw<__nv_bfloat16, 128>(qk, idx, B, H, n, k, w, mu, decay, s);
+  return d == 64 ? launch_topw<__nv_bfloat16, 64>(qk, idx, B, H, n, k, w, mu, decay, err, s)
+                 : launch_topw<__nv_bfloat16, 128>(qk, idx, B, H, n, k, w, mu, decay, err, s);
 }
 
 }  // namespace rt

@@ -16,7 +16,9 @@
 // clusters than that (only with many near-identical centroids) is served by
 // the whole warp: every lane binary-searches a different cluster's ascending
 // member list, and the rows found are summed in ascending cluster order.
-// Either way the result is deterministic.
+// Either way the result is deterministic.  With separate queries and keys a
+// position's divisor is its count of visible memberships (`mdiv`; the rows of
+// memberships without a visible key are zero), and 0 gives a zero row.
 #include "rt_internal.cuh"
 
 namespace rt {
@@ -93,10 +95,12 @@ __device__ __forceinline__ void store8(T* dst, const float (&v)[8]) {
 template <typename T, int D>
 __global__ void __launch_bounds__(THREADS, 6)
 scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ idx,
-               const int32_t* __restrict__ mcount, const int32_t* __restrict__ slots,
-               const float* __restrict__ yslot, T* __restrict__ out) {
+               const int32_t* __restrict__ mcount, const int32_t* __restrict__ mdiv,
+               const int32_t* __restrict__ slots, const float* __restrict__ yslot,
+               T* __restrict__ out, const unsigned int* __restrict__ err) {
   pdl_trigger();
   pdl_wait();
+  const bool failed = status_set(err);
   constexpr int CH = D / 8;    // 8-feature chunks per row
   constexpr int PER = D / 32;  // contiguous features per lane on the warp-wide path
   const long long g = (long long)blockIdx.x * THREADS + threadIdx.x;
@@ -105,6 +109,8 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
   const int lane = threadIdx.x & 31;
   const bool active = r < BHn;
   const int m = active ? __ldcg(mcount + r) : 1;
+  // divisor of the mean (m itself unless the visible count is given)
+  const int dv = (active && mdiv != nullptr && m >= 2) ? __ldcg(mdiv + r) : m;
   // the recorded slot ids are loaded together with the count (one round trip
   // instead of two); only rows with 2 <= m <= SLOTS_PER_ROW use them
   int4 sa = make_int4(0, 0, 0, 0), sb = sa;
@@ -114,13 +120,15 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
     sb = __ldcg(sp + 1);
   }
 
+  if (failed) return;  // uniform: only earlier kernels set the word
+
   // rare: positions in more than SLOTS_PER_ROW clusters, one warp pass each
   unsigned slow = __ballot_sync(0xffffffffu, active && ch == 0 && m > SLOTS_PER_ROW);
   while (slow) {
     const int src = __ffs(slow) - 1;
     slow &= slow - 1;
     const long long gt = __shfl_sync(0xffffffffu, r, src);
-    const int mm = __shfl_sync(0xffffffffu, m, src);
+    const int mm = __shfl_sync(0xffffffffu, dv, src);
     const long long bh = gt / n;
     const int t = (int)(gt - bh * n);
     const float* ybase = yslot + (size_t)bh * k * w * D;
@@ -152,7 +160,7 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
     const float fm = (float)mm;
     float o[PER];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) o[i] = acc[i] / fm;
+    for (int i = 0; i < PER; ++i) o[i] = mm > 0 ? acc[i] / fm : 0.0f;
     store_row<T, PER>(out + gt * D + lane * PER, o);
   }
 
@@ -166,9 +174,10 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
     return;
   }
   int ids[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+  const int kw = k * w;
 #pragma unroll
   for (int i = 0; i < 8; ++i)
-    if (i >= m) ids[i] = 0x7fffffff;
+    if (i >= m || (unsigned)ids[i] >= (unsigned)kw) ids[i] = 0x7fffffff;  // (defensive)
   sort8(ids);
   const long long bh = r / n;
   const float* ybase = yslot + (size_t)bh * k * w * D + ch * 8;
@@ -179,7 +188,7 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
     float4 y[4][2];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      if (i0 + u < m) {
+      if (i0 + u < m && ids[i0 + u] != 0x7fffffff) {
         const float4* p = reinterpret_cast<const float4*>(ybase + (size_t)ids[i0 + u] * D);
         y[u][0] = __ldcg(p);
         y[u][1] = __ldcg(p + 1);
@@ -187,27 +196,29 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      if (i0 + u < m) {
+      if (i0 + u < m && ids[i0 + u] != 0x7fffffff) {
         acc[0] += y[u][0].x; acc[1] += y[u][0].y; acc[2] += y[u][0].z; acc[3] += y[u][0].w;
         acc[4] += y[u][1].x; acc[5] += y[u][1].y; acc[6] += y[u][1].z; acc[7] += y[u][1].w;
       }
     }
   }
-  const float fm = (float)m;
+  const float fm = (float)dv;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = acc[i] / fm;
+  for (int i = 0; i < 8; ++i) acc[i] = dv > 0 ? acc[i] / fm : 0.0f;
   store8<T>(dst, acc);
 }
 
 template <typename T, int D>
 cudaError_t launch_t(int BH, int n, int k, int w, const int32_t* idx, const int32_t* mcount,
-                     const int32_t* slots, const float* yslot, void* out, cudaStream_t s) {
+                     const int32_t* mdiv, const int32_t* slots, const float* yslot, void* out,
+                     unsigned int* err, cudaStream_t s) {
   const long long rows = (long long)BH * n;
   const long long threads = rows * (D / 8);
   const long long blocks = (threads + THREADS - 1) / THREADS;
   launch_begin(K_SCATTER, s);
   cudaError_t e = launch_pdl(scatter_kernel<T, D>, dim3((unsigned)blocks), dim3(THREADS), 0, s,
-                             rows, n, k, w, idx, mcount, slots, yslot, static_cast<T*>(out));
+                             rows, n, k, w, idx, mcount, mdiv, slots, yslot, static_cast<T*>(out),
+                             static_cast<const unsigned int*>(err));
   launch_end(K_SCATTER, s);
   return e;
 }
@@ -215,14 +226,15 @@ cudaError_t launch_t(int BH, int n, int k, int w, const int32_t* idx, const int3
 }  // namespace
 
 cudaError_t launch_scatter(rt_dtype dt, int BH, int n, int d, int k, int w,
-                           const int32_t* idx, const int32_t* mcount, const int32_t* slots,
-                           const float* yslot, void* out, cudaStream_t s) {
+                           const int32_t* idx, const int32_t* mcount, const int32_t* mdiv,
+                           const int32_t* slots, const float* yslot, void* out,
+                           unsigned int* err, cudaStream_t s) {
   if (dt == RT_F32) {
-    return d == 64 ? launch_t<float, 64>(BH, n, k, w, idx, mcount, slots, yslot, out, s)
-                   : launch_t<float, 128>(BH, n, k, w, idx, mcount, slots, yslot, out, s);
+    return d == 64 ? launch_t<float, 64>(BH, n, k, w, idx, mcount, mdiv, slots, yslot, out, err, s)
+                   : launch_t<float, 128>(BH, n, k, w, idx, mcount, mdiv, slots, yslot, out, err, s);
   }
-  return d == 64 ? launch_t<__nv_bfloat16, 64>(BH, n, k, w, idx, mcount, slots, yslot, out, s)
-                 : launch_t<__nv_bfloat16, 128>(BH, n, k, w, idx, mcount, slots, yslot, out, s);
+  return d == 64 ? launch_t<__nv_bfloat16, 64>(BH, n, k, w, idx, mcount, mdiv, slots, yslot, out, err, s)
+                 : launch_t<__nv_bfloat16, 128>(BH, n, k, w, idx, mcount, mdiv, slots, yslot, out, err, s);
 }
 
 }  // namespace rt

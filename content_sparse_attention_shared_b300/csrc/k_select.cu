@@ -30,6 +30,9 @@
 // Rows whose boundary bin holds more than CAND_CAP candidates (many equal
 // scores), or too long to stage in shared memory, use an exact 32-bit
 // most-significant-digit radix select over order-preserving keys instead.
+// Rows of n <= 8192 scores (n a multiple of 4, w <= 256) take the per-thread
+// maximum bound kernel, longer rows with n a multiple of 4 the group-maximum
+// kernel; this histogram kernel serves the rest.
 #include "rt_internal.cuh"
 
 namespace rt {
@@ -154,7 +157,8 @@ __device__ void radix_select_row(const float* __restrict__ row, int n, int w, co
 
 __global__ void __launch_bounds__(THREADS)
 select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __restrict__ idx,
-                   int32_t* __restrict__ mcount, int32_t* __restrict__ slots, int staged) {
+                   int32_t* __restrict__ mcount, int32_t* __restrict__ slots, int staged,
+                   const unsigned int* __restrict__ err) {
   pdl_trigger();
   extern __shared__ __align__(16) uint16_t sbin[];  // [n] when staged
   __shared__ unsigned hist[NBINS];
@@ -171,6 +175,7 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
 
   if (!staged) {
     pdl_wait();
+    if (status_set(err)) return;
     radix_select_row(row, n, w, so, hist, wsum);
     return;
   }
@@ -178,6 +183,7 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
   for (int b = tid; b < NBINS; b += THREADS) hist[b] = 0u;
   if (tid == 0) s_ncand = 0;
   pdl_wait();
+  const bool failed = status_set(err);
   __syncthreads();
 
   // 1. bins + histogram: one vectorised read of the row
@@ -223,6 +229,7 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
       atomicAdd(&hist[b], 1u);
     }
   }
+  if (failed) return;  // uniform: only earlier kernels set the word
   __syncthreads();
 
   // 2. boundary bin: thread i owns bins [top - 8i - 7, top - 8i] (descending)
@@ -357,7 +364,7 @@ __device__ __forceinline__ unsigned long long cand_key(float x, int p) {
 __global__ void __launch_bounds__(THREADS, 7)
 select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
                          int32_t* __restrict__ idx, int32_t* __restrict__ mcount,
-                         int32_t* __restrict__ slots) {
+                         int32_t* __restrict__ slots, const unsigned int* __restrict__ err) {
   pdl_trigger();
   __shared__ unsigned hist[256];  // radix fallback
   __shared__ __align__(16) unsigned long long ckey[RCAP + 1];
@@ -377,6 +384,7 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
   kept[tid] = 0u;
   if (tid == 0) s_ncand = 0;
   pdl_wait();
+  const bool failed = status_set(err);
 
   auto load_chunks = [&](int i0, float4 (&v)[4]) {
 #pragma unroll
@@ -398,6 +406,7 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
     for (int u = 0; u < 4; ++u) m = fmaxf(m, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
   }
   const int mbin = w0 < n ? score_bin(m) : -1;
+  if (failed) return;  // uniform: only earlier kernels set the word
 
   // 2. b_L = the largest bin b with at least w thread maxima in bins >= b,
   //    by bisection over the bins with block-wide counts (no histogram, no
@@ -502,10 +511,201 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
   }
 }
 
+// ---------------------------------------------------------------------------
+// Long rows (n a multiple of 4, up to GROUP_N_MAX): group maxima.  The bound
+// of the kernel above, with groups of GSIZE consecutive scores in place of a
+// thread's scores, so that it stays tight for any n:
+//   1. one streaming read of the row (two float4 per group, four groups in
+//      flight per thread): the bin of every group's maximum goes to shared
+//      memory (u16) and into a 2048-bin histogram;
+//   2. b_L = the largest bin with at least w group maxima in bins >= b_L: the
+//      w groups holding the largest maxima own w distinct scores at least
+//      that large, so every kept score lies in a bin >= b_L (a block scan of
+//      the histogram from the top bin down);
+//   3. only the groups whose maximum reaches b_L are read again (from L2,
+//      right after the first pass); their scores of bin >= b_L become the
+//      candidates (typically a few more than w), packed as 64-bit keys (score
+//      key, complemented position), appended with one shared atomic per warp;
+//   4. a candidate is kept when fewer than w candidate keys exceed its own;
+//      kept positions go into a position bitmap;
+//   5. a block scan over the bitmap words (consecutive words per thread) puts
+//      them out in ascending order.
+// Rows where fewer than w groups exist or the bound leaves more than GCAP
+// candidates (many equal scores) use the exact radix select.
+// Shared memory: about n/4 + n/8 bytes + 16 KB, so several CTAs share an SM
+// and the first pass keeps enough loads in flight to stream at HBM speed.
+// ---------------------------------------------------------------------------
+constexpr int GSIZE = 8;
+constexpr int GCAP = 1024;
+constexpr int GROUP_N_MAX = 262144;
+
+inline size_t group_smem_bytes(int n) {
+  const size_t ng = (size_t)(n + GSIZE - 1) / GSIZE, nw = (size_t)(n + 31) / 32;
+  return ((ng * 2 + 15) & ~(size_t)15) + ((nw * 4 + 15) & ~(size_t)15) + (size_t)(GCAP + 1) * 8;
+}
+
+__global__ void __launch_bounds__(THREADS, 4)
+select_topw_group_kernel(const float* __restrict__ S, int n, int k, int w,
+                         int32_t* __restrict__ idx, int32_t* __restrict__ mcount,
+                         int32_t* __restrict__ slots, const unsigned int* __restrict__ err) {
+  pdl_trigger();
+  extern __shared__ __align__(16) uint8_t gsm[];
+  __shared__ unsigned hist[NBINS];
+  __shared__ int wsum[4 * WARPS];
+  __shared__ int s_bl, s_ncand;
+  const int NG = (n + GSIZE - 1) / GSIZE;
+  const int NW = (n + 31) / 32;
+  uint16_t* gbin = reinterpret_cast<uint16_t*>(gsm);                                   // [NG]
+  unsigned* kept = reinterpret_cast<unsigned*>(gsm + ((NG * 2 + 15) & ~15));           // [NW]
+  unsigned long long* ckey =
+      reinterpret_cast<unsigned long long*>(gsm + ((NG * 2 + 15) & ~15) + ((NW * 4 + 15) & ~15));
+
+  const int c = blockIdx.x;
+  const int bh = blockIdx.y;
+  const float* row = S + ((size_t)bh * k + c) * n;
+  const float4* row4 = reinterpret_cast<const float4*>(row);
+  const SelectOut so{idx + ((size_t)bh * k + c) * w, mcount, slots, bh, c, n, w};
+  const int tid = threadIdx.x, lane = tid & 31;
+
+  for (int i = tid; i < NW; i += THREADS) kept[i] = 0u;
+  for (int i = tid; i < NBINS; i += THREADS) hist[i] = 0u;
+  if (tid == 0) { s_ncand = 0; s_bl = -1; }
+  pdl_wait();
+  const bool failed = status_set(err);
+  __syncthreads();
+
+  // 1. bins of the group maxima
+  const int n4 = n >> 2;
+  const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  for (int g0 = tid; g0 < NG; g0 += 4 * THREADS) {
+    float4 v[4][2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * THREADS;
+      v[u][0] = (g < NG && 2 * g < n4) ? __ldcg(row4 + 2 * g) : ninf;
+      v[u][1] = (g < NG && 2 * g + 1 < n4) ? __ldcg(row4 + 2 * g + 1) : ninf;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * THREADS;
+      if (g < NG) {
+        const float m = fmaxf(fmaxf(fmaxf(v[u][0].x, v[u][0].y), fmaxf(v[u][0].z, v[u][0].w)),
+                              fmaxf(fmaxf(v[u][1].x, v[u][1].y), fmaxf(v[u][1].z, v[u][1].w)));
+        const int b = score_bin(m);
+        gbin[g] = (uint16_t)b;
+        atomicAdd(&hist[b], 1u);
+      }
+    }
+  }
+  if (failed) return;  // uniform: only earlier kernels set the word
+  __syncthreads();
+
+  // 2. b_L: thread i owns bins [top - 8i - 7, top - 8i] (descending)
+  {
+    const int hi_bin = NBINS - 1 - BINS_PER_THREAD * tid;
+    unsigned hb[BINS_PER_THREAD];
+    int lsum = 0;
+#pragma unroll
+    for (int q = 0; q < BINS_PER_THREAD; ++q) {
+      hb[q] = hist[hi_bin - q];
+      lsum += (int)hb[q];
+    }
+    int total;
+    const int excl = block_exclusive_scan<THREADS>(lsum, wsum, total);
+    if (excl < w && w <= excl + lsum) {
+      int cum = excl;
+#pragma unroll
+      for (int q = 0; q < BINS_PER_THREAD; ++q) {
+        if (cum < w && cum + (int)hb[q] >= w) s_bl = hi_bin - q;
+        cum += (int)hb[q];
+      }
+    }
+  }
+  __syncthreads();
+  const int bl = s_bl;
+  if (bl < 0) {  // fewer than w groups: exact radix path (uniform)
+    radix_select_row(row, n, w, so, hist, wsum);
+    return;
+  }
+
+  // 3. candidates from the groups whose maximum reaches b_L
+  {
+    const float pre = bl > 0 ? (float)bl * (1.0f / 1024.0f) - 1.0f - 1.0e-5f : -3.0e38f;
+    for (int g0 = 0; g0 < NG; g0 += THREADS) {
+      const int g = g0 + tid;
+      uint32_t cm = 0u;
+      float x[GSIZE];
+      if (g < NG && (int)gbin[g] >= bl) {
+        const float4 a = 2 * g < n4 ? __ldcg(row4 + 2 * g) : ninf;
+        const float4 b = 2 * g + 1 < n4 ? __ldcg(row4 + 2 * g + 1) : ninf;
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+#pragma unroll
+        for (int e = 0; e < GSIZE; ++e)
+          if (x[e] >= pre && score_bin(x[e]) >= bl) cm |= 1u << e;
+      }
+      const int cnt = __popc(cm);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+      int base = 0;
+      if (lane == 31 && wtot > 0) base = atomicAdd(&s_ncand, wtot);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      int slot = base + incl - cnt;
+      for (; cm != 0u; cm &= cm - 1u, ++slot) {
+        const int e = __ffs(cm) - 1;
+        if (slot < GCAP) ckey[slot] = cand_key(x[e], g * GSIZE + e);
+      }
+    }
+  }
+  __syncthreads();
+  const int nc = s_ncand;
+  if (nc > GCAP) {
+    radix_select_row(row, n, w, so, hist, wsum);  // uniform branch
+    return;
+  }
+  if (tid == 0) ckey[nc] = 0ull;  // pad to an even count (0 is below every key)
+  __syncthreads();
+
+  // 4. kept: fewer than w candidate keys above its own
+  const int nc2 = (nc + 1) & ~1;
+  for (int i = tid; i < nc; i += THREADS) {
+    const unsigned long long ki = ckey[i];
+    int rank = 0;
+    for (int j = 0; j < nc2; j += 2) {
+      const ulonglong2 kj = *reinterpret_cast<const ulonglong2*>(&ckey[j]);
+      rank += (kj.x > ki) + (kj.y > ki);
+    }
+    if (rank < w) {
+      const int p = (int)(0xFFFFFFFFu - (uint32_t)ki);
+      atomicOr(&kept[p >> 5], 1u << (p & 31));
+    }
+  }
+  __syncthreads();
+
+  // 5. ordered emission: thread tid takes words [tid*WPT, tid*WPT + WPT)
+  {
+    const int WPT = (NW + THREADS - 1) / THREADS;
+    const int q0 = tid * WPT;
+    int cnt = 0;
+    for (int q = q0; q < q0 + WPT && q < NW; ++q) cnt += __popc(kept[q]);
+    int total;
+    int o = block_exclusive_scan<THREADS>(cnt, wsum, total);
+    for (int q = q0; q < q0 + WPT && q < NW; ++q)
+      for (unsigned rem = kept[q]; rem != 0u; rem &= rem - 1u, ++o)
+        if (o < w) so.emit(o, q * 32 + __ffs(rem) - 1);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* idx,
-                          int32_t* mcount, int32_t* slots, cudaStream_t s) {
+                          int32_t* mcount, int32_t* slots, unsigned int* err, cudaStream_t s) {
+  const unsigned int* cerr = err;
   dim3 grid(k, BH);
   const int staged = n <= MAX_STAGED_BINS ? 1 : 0;
   // staged bins (u16, padded to 16 bytes) + two chunk masks per 32 positions
@@ -518,13 +718,23 @@ cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* 
   if (n <= BOUND_N_MAX && (n & 3) == 0 && w <= THREADS) {
     launch_begin(K_SELECT, s);
     e = launch_pdl(select_topw_bound_kernel, grid, dim3(THREADS), 0, s, S, n, k, w, idx, mcount,
-                   slots);
+                   slots, cerr);
+    launch_end(K_SELECT, s);
+    return e;
+  }
+  if (n <= GROUP_N_MAX && (n & 3) == 0) {
+    const size_t gsmem = group_smem_bytes(n);
+    e = set_smem_limit(reinterpret_cast<const void*>(select_topw_group_kernel), (int)gsmem);
+    if (e != cudaSuccess) return e;
+    launch_begin(K_SELECT, s);
+    e = launch_pdl(select_topw_group_kernel, grid, dim3(THREADS), gsmem, s, S, n, k, w, idx,
+                   mcount, slots, cerr);
     launch_end(K_SELECT, s);
     return e;
   }
   launch_begin(K_SELECT, s);
   e = launch_pdl(select_topw_kernel, grid, dim3(THREADS), smem, s, S, n, k, w, idx, mcount, slots,
-                 staged);
+                 staged, cerr);
   launch_end(K_SELECT, s);
   return e;
 }

@@ -50,6 +50,21 @@ void launch_end(int kind, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------
+// the device-side timeout test aid (rt_debug_inject_wait_timeout)
+// ---------------------------------------------------------------------------
+static std::atomic<unsigned> g_fault_kinds{0};
+static std::atomic<unsigned long long> g_fault_ns{0};
+
+uint64_t injected_limit_ns(int kind) {
+  const unsigned kinds = g_fault_kinds.load(std::memory_order_relaxed);
+  unsigned bit = 0;
+  if (kind == K_SCORE_TC) bit = RT_DEBUG_SCORE;
+  else if (kind == K_ATTN_TC) bit = RT_DEBUG_ATTENTION;
+  else if (kind == K_LOCAL_ATTN) bit = RT_DEBUG_LOCAL_ATTENTION;
+  return (kinds & bit) ? (uint64_t)g_fault_ns.load(std::memory_order_relaxed) : 0;
+}
+
+// ---------------------------------------------------------------------------
 // dynamic shared-memory limits, set once per (kernel, device)
 // ---------------------------------------------------------------------------
 static std::mutex g_attr_mu;
@@ -139,7 +154,7 @@ bool bf16_tensor_map_2d(const void* base, unsigned long long rows, unsigned cols
 static inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct FwdLayout {
-  size_t err, S, mcount, slots, idx, assign, yslot, prep, total;
+  size_t err, S, mcount, slots, idx, assign, yslot, prep, idx_k, mvis, total;
 };
 
 static FwdLayout fwd_layout(int B, int H, int n, int d, int k, int w) {
@@ -154,11 +169,15 @@ static FwdLayout fwd_layout(int B, int H, int n, int d, int k, int w) {
   L.assign = off; off += align256(BH * n * sizeof(int32_t));
   L.yslot = off; off += align256(BH * k * w * d * sizeof(float));
   L.prep = off; off += align256(score_prep_bytes(H, d, k));
+  L.idx_k = off; off += align256(BH * k * w * sizeof(int32_t));   // separate QK only
+  L.mvis = off; off += align256(BH * n * sizeof(int32_t));        // separate QK only
   L.total = off;
   return L;
 }
 
-static size_t ema_total(int B, int H, int n, int k) { return 256 + ema_workspace_bytes(B, H, n, k); }
+static size_t ema_total(int B, int H, int n, int d, int k, rt_dtype dt) {
+  return 256 + ema_workspace_bytes(B, H, n, d, k, dt);
+}
 
 }  // namespace rt
 
@@ -221,6 +240,16 @@ const char* rt_last_error_detail(void) { return t_err; }
 
 int64_t rt_launch_count(void) { return (int64_t)g_launches.load(); }
 
+rt_status rt_debug_inject_wait_timeout(unsigned kernels, unsigned long long limit_ns) {
+  if (kernels & ~(unsigned)(RT_DEBUG_SCORE | RT_DEBUG_ATTENTION | RT_DEBUG_LOCAL_ATTENTION))
+    return fail(RT_ERR_INVALID_ARG, "unknown kernel bits 0x%x", kernels);
+  if (kernels != 0 && (limit_ns == 0 || limit_ns > 1000000000ull))
+    return fail(RT_ERR_INVALID_ARG, "limit_ns must be in (0, 1e9]");
+  g_fault_ns.store(kernels ? limit_ns : 0ull);
+  g_fault_kinds.store(kernels);
+  return ok();
+}
+
 rt_status rt_profile_set(void* const* events, int n_pairs) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
   if (n_pairs < 0 || (n_pairs > 0 && events == nullptr))
@@ -242,7 +271,8 @@ int rt_profile_kernel_id(int i) {
 const char* rt_kernel_name(int id) {
   static const char* names[K_NUM_KINDS] = {
       "score_simt", "score_tc", "select_topw", "attention_simt", "attention_tc",
-      "scatter_average", "ema_topw", "ema_update", "centroid_prep", "local_attention"};
+      "scatter_average", "ema_topw", "ema_update", "centroid_prep", "local_attention",
+      "ema_bucket"};
   if (id < 0 || id >= K_NUM_KINDS) return "unknown";
   return names[id];
 }
@@ -250,7 +280,7 @@ const char* rt_kernel_name(int id) {
 size_t rt_workspace_bytes(int B, int H, int n, int d, int k, int w, rt_dtype dt) {
   if (check_shape(dt, B, H, n, d, k, w) != RT_OK) return 0;
   const size_t a = fwd_layout(B, H, n, d, k, w).total;
-  const size_t b = ema_total(B, H, n, k);
+  const size_t b = ema_total(B, H, n, d, k, dt);
   return a > b ? a : b;
 }
 
@@ -277,7 +307,88 @@ rt_status rt_route_assign(const void* qk, rt_dtype dt, int B, int H, int n, int 
   st = from_cuda(launch_score(qk, dt, B, H, n, d, centroids, k, S, assign, nullptr, prep, err, s),
                  "score kernel");
   if (st != RT_OK) return st;
-  st = from_cuda(launch_select(S, BH, n, k, w, idx, nullptr, nullptr, s), "select kernel");
+  st = from_cuda(launch_select(S, BH, n, k, w, idx, nullptr, nullptr, err, s), "select kernel");
+  if (st != RT_OK) return st;
+  return ok();
+}
+
+// The forward pass for both forms.  Shared QK (kp == q): score, select,
+// attention on the packed / key-block kernels, scatter.  Separate keys: the
+// queries and the keys are each scored and selected against the same
+// centroids, the key-block kernel attends between a cluster's queries and its
+// keys with the mask on original positions, and the scatter divides by each
+// position's count of memberships with a visible key.
+static rt_status forward(const void* q, const void* kp, const void* v, rt_dtype dt, int B, int H,
+                         int n, int d, const float* centroids, int kc, int w, int causal,
+                         float scale, void* out, int32_t* idx_out, int32_t* idx_k_out,
+                         int32_t* assign_out, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  rt_status st = check_shape(dt, B, H, n, d, kc, w);
+  if (st != RT_OK) return st;
+  if (!q || !kp || !v || !centroids || !out) return fail(RT_ERR_INVALID_ARG, "null tensor pointer");
+  if (causal != 0 && causal != 1) return fail(RT_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!std::isfinite(scale)) return fail(RT_ERR_INVALID_ARG, "scale is not finite");
+  if (!aligned16(q) || !aligned16(kp) || !aligned16(v) || !aligned16(centroids) ||
+      !aligned16(out) || (idx_out && !aligned16(idx_out)) ||
+      (idx_k_out && !aligned16(idx_k_out)) || (assign_out && !aligned16(assign_out)))
+    return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  const FwdLayout L = fwd_layout(B, H, n, d, kc, w);
+  if (!workspace || workspace_bytes < L.total)
+    return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, L.total);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (scale <= 0.0f) scale = 1.0f / sqrtf((float)d);
+  const bool separate = kp != q;
+
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  float* S = reinterpret_cast<float*>(ws + L.S);
+  int32_t* mcount = reinterpret_cast<int32_t*>(ws + L.mcount);
+  int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + L.idx);
+  float* yslot = reinterpret_cast<float*>(ws + L.yslot);
+  int32_t* slots = reinterpret_cast<int32_t*>(ws + L.slots);
+  unsigned int* err = reinterpret_cast<unsigned int*>(ws + L.err);
+  void* prep = score_prep_bytes(H, d, kc) ? static_cast<void*>(ws + L.prep) : nullptr;
+
+  st = from_cuda(launch_score(q, dt, B, H, n, d, centroids, kc, S, assign_out, mcount, prep, err, s),
+                 "score kernel");
+  if (st != RT_OK) return st;
+  st = from_cuda(launch_select(S, BH, n, kc, w, idx, mcount, slots, err, s), "select kernel");
+  if (st != RT_OK) return st;
+  int32_t* idx_k = nullptr;
+  int32_t* mvis = nullptr;
+  if (separate) {
+    idx_k = idx_k_out ? idx_k_out : reinterpret_cast<int32_t*>(ws + L.idx_k);
+    mvis = reinterpret_cast<int32_t*>(ws + L.mvis);
+    // the keys' routing; the score kernel zeroes mvis for the attention
+    st = from_cuda(launch_score(kp, dt, B, H, n, d, centroids, kc, S, nullptr, mvis, prep, err, s),
+                   "score kernel (keys)");
+    if (st != RT_OK) return st;
+    st = from_cuda(launch_select(S, BH, n, kc, w, idx_k, nullptr, nullptr, err, s),
+                   "select kernel (keys)");
+    if (st != RT_OK) return st;
+    if (attention_tc_supported(dt, d, w)) {
+      st = from_cuda(launch_attention_separate_tc(q, kp, v, BH, n, d, kc, w, causal, scale, idx,
+                                                  idx_k, mcount, mvis, out, yslot, err, s),
+                     "attention kernel");
+    } else {
+      st = from_cuda(launch_attention_simt(q, kp, v, dt, BH, n, d, kc, w, causal, scale, idx,
+                                           idx_k, mcount, mvis, out, yslot, err, s),
+                     "attention kernel");
+    }
+  } else if (attention_tc_supported(dt, d, w)) {
+    st = from_cuda(launch_attention_tc(q, v, BH, n, d, kc, w, causal, scale, idx, mcount, out,
+                                       yslot, err, s),
+                   "attention kernel");
+  } else {
+    st = from_cuda(launch_attention_simt(q, kp, v, dt, BH, n, d, kc, w, causal, scale, idx,
+                                         nullptr, mcount, nullptr, out, yslot, err, s),
+                   "attention kernel");
+  }
+  if (st != RT_OK) return st;
+  st = from_cuda(launch_scatter(dt, BH, n, d, kc, w, idx, mcount, mvis, slots, yslot, out, err, s),
+                 "scatter kernel");
   if (st != RT_OK) return st;
   return ok();
 }
@@ -287,52 +398,21 @@ rt_status rt_routing_attention(const void* q, const void* kp, const void* v, rt_
                                int causal, float scale, void* out, int32_t* idx_out,
                                int32_t* assign_out, void* workspace, size_t workspace_bytes,
                                void* stream) {
-  rt_status st = check_shape(dt, B, H, n, d, kc, w);
-  if (st != RT_OK) return st;
-  if (!q || !kp || !v || !centroids || !out) return fail(RT_ERR_INVALID_ARG, "null tensor pointer");
-  if (kp != q) return fail(RT_ERR_UNSUPPORTED, "separate keys: only shared QK (k == q) is routed");
-  if (causal != 0 && causal != 1) return fail(RT_ERR_INVALID_ARG, "causal must be 0 or 1");
-  if (!std::isfinite(scale)) return fail(RT_ERR_INVALID_ARG, "scale is not finite");
-  if (!aligned16(q) || !aligned16(v) || !aligned16(centroids) || !aligned16(out) ||
-      (idx_out && !aligned16(idx_out)) || (assign_out && !aligned16(assign_out)))
-    return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-  const FwdLayout L = fwd_layout(B, H, n, d, kc, w);
-  if (!workspace || workspace_bytes < L.total)
-    return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, L.total);
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  if (scale <= 0.0f) scale = 1.0f / sqrtf((float)d);
+  return forward(q, kp, v, dt, B, H, n, d, centroids, kc, w, causal, scale, out, idx_out,
+                 nullptr, assign_out, workspace, workspace_bytes, stream);
+}
 
-  char* ws = static_cast<char*>(workspace);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int BH = B * H;
-  float* S = reinterpret_cast<float*>(ws + L.S);
-  int32_t* mcount = reinterpret_cast<int32_t*>(ws + L.mcount);
-  int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + L.idx);
-  float* yslot = reinterpret_cast<float*>(ws + L.yslot);
-
-  unsigned int* err = reinterpret_cast<unsigned int*>(ws + L.err);
-  void* prep = score_prep_bytes(H, d, kc) ? static_cast<void*>(ws + L.prep) : nullptr;
-  st = from_cuda(launch_score(q, dt, B, H, n, d, centroids, kc, S, assign_out, mcount, prep, err, s),
-                 "score kernel");
-  if (st != RT_OK) return st;
-  int32_t* slots = reinterpret_cast<int32_t*>(ws + L.slots);
-  st = from_cuda(launch_select(S, BH, n, kc, w, idx, mcount, slots, s), "select kernel");
-  if (st != RT_OK) return st;
-  if (attention_tc_supported(dt, d, w)) {
-    st = from_cuda(launch_attention_tc(q, v, BH, n, d, kc, w, causal, scale, idx, mcount, out,
-                                       yslot, err, s),
-                   "attention kernel");
-  } else {
-    st = from_cuda(launch_attention_simt(q, kp, v, dt, BH, n, d, kc, w, causal, scale, idx,
-                                         mcount, out, yslot, s),
-                   "attention kernel");
-  }
-  if (st != RT_OK) return st;
-  st = from_cuda(launch_scatter(dt, BH, n, d, kc, w, idx, mcount, slots, yslot, out, s),
-                 "scatter kernel");
-  if (st != RT_OK) return st;
-  return ok();
+rt_status rt_routing_attention_separate(const void* q, const void* kp, const void* v, rt_dtype dt,
+                                        int B, int H, int n, int d, const float* centroids,
+                                        int kc, int w, int causal, float scale, void* out,
+                                        int32_t* idx_q_out, int32_t* idx_k_out,
+                                        int32_t* assign_out, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (q != nullptr && q == kp)
+    return fail(RT_ERR_INVALID_ARG, "separate keys: k must be a different tensor from q "
+                                    "(rt_routing_attention takes shared QK)");
+  return forward(q, kp, v, dt, B, H, n, d, centroids, kc, w, causal, scale, out, idx_q_out,
+                 idx_k_out, assign_out, workspace, workspace_bytes, stream);
 }
 
 rt_status rt_centroid_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
@@ -345,15 +425,55 @@ rt_status rt_centroid_ema(const void* qk, rt_dtype dt, int B, int H, int n, int 
   if (!aligned16(qk) || !aligned16(assign) || !aligned16(centroids))
     return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   if (k > 4096) return fail(RT_ERR_UNSUPPORTED, "k above 4096 for the centroid update");
-  const size_t need = ema_total(B, H, n, k);
+  const size_t need = ema_total(B, H, n, d, k, dt);
   if (!workspace || workspace_bytes < need)
     return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = from_cuda(launch_ema(qk, dt, B, H, n, d, assign, centroids, k, decay, ws + 256, s),
+  st = from_cuda(launch_ema(qk, dt, B, H, n, d, assign, centroids, k, decay, ws + 256,
+                            reinterpret_cast<unsigned int*>(ws), s),
                  "centroid update kernels");
+  if (st != RT_OK) return st;
+  return ok();
+}
+
+rt_status rt_centroid_ema_sums(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                               const int32_t* assign, int k, float* sums, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  rt_status st = check_shape(dt, B, H, n, d, k, 1);
+  if (st != RT_OK) return st;
+  if (!qk || !assign || !sums) return fail(RT_ERR_INVALID_ARG, "null qk/assign/sums");
+  if (!aligned16(qk) || !aligned16(assign) || !aligned16(sums))
+    return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (k > 4096) return fail(RT_ERR_UNSUPPORTED, "k above 4096 for the centroid update");
+  const size_t need = ema_total(B, H, n, d, k, dt);
+  if (!workspace || workspace_bytes < need)
+    return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  char* ws = static_cast<char*>(workspace);
+  st = from_cuda(launch_ema_sums(qk, dt, B, H, n, d, assign, k, sums, ws + 256,
+                                 reinterpret_cast<unsigned int*>(ws),
+                                 static_cast<cudaStream_t>(stream)),
+                 "centroid sum kernels");
+  if (st != RT_OK) return st;
+  return ok();
+}
+
+rt_status rt_centroid_ema_apply(const float* sums, int H, int d, float* centroids, int k,
+                                float decay, void* stream) {
+  if (H < 1 || k < 1) return fail(RT_ERR_INVALID_ARG, "H and k must be positive");
+  if (d != 64 && d != 128) return fail(RT_ERR_UNSUPPORTED, "head dimension d=%d (supported: 64, 128)", d);
+  if (!sums || !centroids) return fail(RT_ERR_INVALID_ARG, "null sums/centroids");
+  if (!(decay >= 0.0f && decay <= 1.0f)) return fail(RT_ERR_INVALID_ARG, "decay must be in [0, 1]");
+  if (!aligned16(centroids) || (reinterpret_cast<uintptr_t>(sums) & 3u) != 0)
+    return fail(RT_ERR_INVALID_ARG, "misaligned sums/centroids");
+  if ((long long)H * k > 0x7fffffffLL) return fail(RT_ERR_UNSUPPORTED, "H*k too large");
+  rt_status st = from_cuda(launch_ema_apply(sums, H, d, centroids, k, decay,
+                                            static_cast<cudaStream_t>(stream)),
+                           "centroid apply kernel");
   if (st != RT_OK) return st;
   return ok();
 }
@@ -368,12 +488,13 @@ rt_status rt_centroid_ema_topw(const void* qk, rt_dtype dt, int B, int H, int n,
   if (!aligned16(qk) || !aligned16(idx) || !aligned16(centroids))
     return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   if (k > 4096) return fail(RT_ERR_UNSUPPORTED, "k above 4096 for the centroid update");
-  const size_t need = ema_total(B, H, n, k);
+  const size_t need = ema_total(B, H, n, d, k, dt);
   if (!workspace || workspace_bytes < need)
     return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   st = from_cuda(launch_ema_topw(qk, dt, B, H, n, d, idx, w, centroids, k, decay,
+                                 static_cast<unsigned int*>(workspace),
                                  static_cast<cudaStream_t>(stream)),
                  "top-w centroid update kernel");
   if (st != RT_OK) return st;
@@ -416,8 +537,9 @@ rt_status rt_workspace_init(void* workspace, size_t workspace_bytes, void* strea
 }
 
 rt_status rt_check_device_status(void* workspace, size_t workspace_bytes, void* stream) {
-  if (!workspace || workspace_bytes < 256) return fail(RT_ERR_WORKSPACE, "no workspace");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!workspace && workspace_bytes == 0) return noalloc_check_status(s);
+  if (!workspace || workspace_bytes < 256) return fail(RT_ERR_WORKSPACE, "no workspace");
   unsigned int word = 0;
   cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);

@@ -27,13 +27,17 @@ enum KernelId {
   K_EMA_UPDATE = 7,
   K_CENTROID_PREP = 8,
   K_LOCAL_ATTN = 9,
-  K_NUM_KINDS = 10
+  K_EMA_BUCKET = 10,
+  K_NUM_KINDS = 11
 };
 
 // Error detail for the calling host thread (rt_last_error_detail) and the
 // shape checks shared by the entry points.
 rt_status record_error(rt_status s, const char* msg);
 rt_status validate_shape(rt_dtype dt, int B, int H, int n, int d, int k, int w);
+// Reads and clears the status word of rt_route_assign_noalloc in the current
+// context (synchronises `s`).
+rt_status noalloc_check_status(cudaStream_t s);
 
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
 // current device.  The attribute call is made only the first time a kernel
@@ -88,6 +92,70 @@ enum DeviceError : unsigned int {
   DEV_OK = 0,
   DEV_TIMEOUT = 1,
 };
+
+// Fail-stop: after its pdl_wait every kernel of a pass checks the device
+// status word and returns when it is set -- by an earlier kernel of the same
+// pass, or by an earlier pass on the same workspace that nobody has checked
+// since -- so no kernel computes on the partial results of one that gave up.
+// This form reads the word once per CTA and broadcasts it, for kernels whose
+// own CTAs may set it; it contains a block barrier, so every thread of the CTA
+// calls it, before any other barrier.
+__device__ __forceinline__ bool pass_failed(const unsigned int* err) {
+  __shared__ int s_failed;
+  if (threadIdx.x == 0) s_failed = (err != nullptr && __ldcg(err) != 0u) ? 1 : 0;
+  __syncthreads();
+  return s_failed != 0;
+}
+
+// The same check per thread, with no barrier, for kernels whose own CTAs never
+// set the word (so every thread sees the value its predecessors left): read
+// right after pdl_wait, tested once the kernel's first loads are in flight, so
+// it adds no round trip.
+__device__ __forceinline__ bool status_set(const unsigned int* err) {
+  return err != nullptr && __ldcg(err) != 0u;
+}
+
+// Test aid for the device-side timeout path (rt_debug_inject_wait_timeout):
+// with limit_ns > 0, thread 0 waits on an mbarrier that nothing arrives on,
+// bounded by limit_ns, before the kernel issues any asynchronous copy or MMA;
+// the wait runs out, the status word is set, and the caller returns -- with
+// nothing in flight.  Every thread of the CTA calls it (it contains block
+// barriers); returns true when the kernel must return.
+__device__ __forceinline__ bool injected_wait_timeout(uint64_t limit_ns, unsigned int* err) {
+  if (limit_ns == 0) return false;
+  __shared__ uint64_t fault_bar;
+  __shared__ int s_out;
+  if (threadIdx.x == 0) {
+    const uint32_t bar = static_cast<uint32_t>(__cvta_generic_to_shared(&fault_bar));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    bool done = false;
+    while (true) {
+      uint32_t ok;
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(ok)
+          : "r"(bar)
+          : "memory");
+      if (ok) { done = true; break; }
+      uint64_t t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > limit_ns) break;
+    }
+    if (!done && err != nullptr) atomicExch(err, (unsigned)DEV_TIMEOUT);
+    s_out = done ? 0 : 1;
+  }
+  __syncthreads();
+  return s_out != 0;
+}
+
+// Host side of the test aid: the limit to pass to a kernel of the given kind
+// (0 unless rt_debug_inject_wait_timeout selected that kind).
+uint64_t injected_limit_ns(int kind);
 
 // ---------------------------------------------------------------------------
 // small device helpers
@@ -155,7 +223,7 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 // (may be null), mcount: [BH,n] zeroed here when non-null.
 cudaError_t launch_score_simt(const void* qk, rt_dtype dt, int BH, int H, int n, int d,
                               const float* mu, int k, float* S, int32_t* a,
-                              int32_t* mcount, cudaStream_t s);
+                              int32_t* mcount, unsigned int* err, cudaStream_t s);
 
 // dispatcher: tcgen05 scoring for bf16 with k <= 256 (fp32-accurate via a
 // three-plane split of the centroids), the SIMT kernel otherwise.  prep: device
@@ -174,14 +242,18 @@ cudaError_t launch_score(const void* qk, rt_dtype dt, int B, int H, int n, int d
 // [BH, n, SLOTS_PER_ROW] (may be null; entry order is arbitrary).
 constexpr int SLOTS_PER_ROW = 8;
 cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* idx,
-                          int32_t* mcount, int32_t* slots, cudaStream_t s);
+                          int32_t* mcount, int32_t* slots, unsigned int* err, cudaStream_t s);
 
 // in-cluster attention.  Rows of positions with mcount == 1 go straight to
 // `out`; rows of positions in several clusters go to yslot [BH,k,w,d] fp32.
+// idx_k: the keys' own lists (separate queries and keys; null when queries
+// double as keys); mvis then counts every position's memberships with a
+// visible key (zeroed beforehand).
 cudaError_t launch_attention_simt(const void* q, const void* kk, const void* v, rt_dtype dt,
                                   int BH, int n, int d, int k, int w, int causal,
-                                  float scale, const int32_t* idx, const int32_t* mcount,
-                                  void* out, float* yslot, cudaStream_t s);
+                                  float scale, const int32_t* idx, const int32_t* idx_k,
+                                  const int32_t* mcount, int32_t* mvis, void* out, float* yslot,
+                                  unsigned int* err, cudaStream_t s);
 
 // the same on tcgen05 tensor cores (bf16 only): the pipelined kernel below
 // for w <= 128, the key-block kernel above that; err: device error word.
@@ -190,6 +262,15 @@ cudaError_t launch_attention_tc(const void* q, const void* v, int BH, int n, int
                                 int causal, float scale, const int32_t* idx,
                                 const int32_t* mcount, void* out, float* yslot,
                                 unsigned int* err, cudaStream_t s);
+
+// separate queries and keys on tcgen05 (bf16, any w): query rows from idx_q,
+// key/value rows from idx_k, causal on original positions; mvis (zeroed
+// beforehand) counts every position's memberships with a visible key.
+cudaError_t launch_attention_separate_tc(const void* q, const void* kk, const void* v, int BH,
+                                         int n, int d, int k, int w, int causal, float scale,
+                                         const int32_t* idx_q, const int32_t* idx_k,
+                                         const int32_t* mcount, int32_t* mvis, void* out,
+                                         float* yslot, unsigned int* err, cudaStream_t s);
 
 // local (sliding-window) causal attention, shared QK, bf16: every position
 // attends to the `window` positions ending at it; out [BH, n, d].
@@ -202,22 +283,33 @@ cudaError_t launch_attention_pipe(const void* q, const void* v, int BH, int n, i
                                   const int32_t* mcount, void* out, float* yslot,
                                   unsigned int* err, cudaStream_t s);
 
-// zero rows (mcount == 0) and the mean over clusters (mcount >= 2).
+// zero rows (mcount == 0) and the mean over clusters (mcount >= 2); mdiv
+// (may be null) replaces mcount as the divisor (0: zero row).
 cudaError_t launch_scatter(rt_dtype dt, int BH, int n, int d, int k, int w,
-                           const int32_t* idx, const int32_t* mcount, const int32_t* slots,
-                           const float* yslot, void* out, cudaStream_t s);
+                           const int32_t* idx, const int32_t* mcount, const int32_t* mdiv,
+                           const int32_t* slots, const float* yslot, void* out,
+                           unsigned int* err, cudaStream_t s);
 
-// centroid update: one CTA per (head, centroid) lists its rows, sums them
-// normalised in a fixed order, blends and renormalises (no workspace needed
-// beyond the status word: ema_workspace_bytes returns 0).
-size_t ema_workspace_bytes(int B, int H, int n, int k);
+// centroid update (argmax assignment), a segmented reduction: a bucketing
+// kernel sorts every chunk's rows by centroid, then one CTA per (head,
+// centroid) sums its rows.  ws: device scratch of
+// ema_workspace_bytes(B, H, n, d, k, dt) bytes.
+size_t ema_workspace_bytes(int B, int H, int n, int d, int k, rt_dtype dt);
 cudaError_t launch_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                        const int32_t* assign, float* mu, int k, float decay,
-                       void* ws, cudaStream_t s);
+                       void* ws, unsigned int* err, cudaStream_t s);
+// the same reduction stopped before the blend: sums [H][k][d+1] receives every
+// centroid's sum of normalised rows and (as a float) its count
+cudaError_t launch_ema_sums(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                            const int32_t* assign, int k, float* sums, void* ws,
+                            unsigned int* err, cudaStream_t s);
+// the blend from such sums (possibly added over shards of the batch)
+cudaError_t launch_ema_apply(const float* sums, int H, int d, float* mu, int k, float decay,
+                             cudaStream_t s);
 // the centroid step driven by the top-w lists idx [B,H,k,w] instead of an
 // assignment (entries outside [0, n) are skipped)
 cudaError_t launch_ema_topw(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                             const int32_t* idx, int w, float* mu, int k, float decay,
-                            cudaStream_t s);
+                            unsigned int* err, cudaStream_t s);
 
 }  // namespace rt

@@ -38,7 +38,9 @@
  *   - Errors found on the host (bad arguments, too-small workspace, a CUDA
  *     launch error) are returned immediately; nothing is launched then.
  *     A device-side error (a bounded wait that ran out) is recorded in the
- *     workspace and reported by rt_check_device_status().
+ *     workspace and reported by rt_check_device_status(); until that call
+ *     clears it, the kernels of every call on the workspace return without
+ *     computing.
  *   - Supported: d in {64, 128}; 1 <= w <= n; k >= 1; causal in {0, 1};
  *     dtype RT_F32 or RT_BF16 (Q, K, V and the output share it; centroids
  *     are always fp32).  Other values return RT_ERR_UNSUPPORTED or
@@ -92,8 +94,10 @@ rt_status rt_route_assign(const void* qk, rt_dtype dt, int B, int H, int n, int 
  * when causal=1), and the averaging scatter back to positions.
  * Source: §3 "Self-Attentive Auto-regressive Sequence Modeling" (softmax
  * attention, causal masking) and §4 (same-cluster query/key pairs only).
- *   q, k, v   [B,H,n,d]  dtype dt; shared QK: k must equal q (the same
- *                        pointer), otherwise RT_ERR_UNSUPPORTED
+ *   q, k, v   [B,H,n,d]  dtype dt; shared QK when k is the same pointer as q;
+ *                        a different k routes the keys separately (see
+ *                        rt_routing_attention_separate; idx_out then holds
+ *                        the queries' lists)
  *   centroids [H,kc,d]   fp32 (read only; the update is rt_centroid_ema)
  *   scale     logit scale; <= 0 selects 1/sqrt(d)
  *   out       [B,H,n,d]  dtype dt; every row is written (zero rows for
@@ -109,6 +113,33 @@ rt_status rt_routing_attention(const void* q, const void* k, const void* v, rt_d
                                void* out, int32_t* idx_out, int32_t* assign_out,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* Routing attention with separate queries and keys.
+ * Source: §4 "Routing attention with clustering" (queries and keys are
+ * routed to the same learned centroids; a query attends only to the keys of
+ * its own clusters), §3 (softmax attention, causal masking).  Read as: the
+ * queries and the keys are each normalised and scored against the centroids,
+ * and every centroid keeps its w best queries and, separately, its w best
+ * keys (ascending positions, ties to the lower position).  In cluster c each
+ * listed query attends with softmax to the cluster's listed keys (with
+ * causal=1 only to keys at positions not after its own).  A position's output
+ * is the mean over the clusters that listed it as a query AND gave it at
+ * least one visible key; a position with none gets a zero row.
+ *   q, k, v    [B,H,n,d] dtype dt; k must be a different tensor from q
+ *              (RT_ERR_INVALID_ARG otherwise; shared QK is
+ *              rt_routing_attention)
+ *   idx_q_out  [B,H,kc,w] out, may be NULL: the queries' lists
+ *   idx_k_out  [B,H,kc,w] out, may be NULL: the keys' lists
+ *   assign_out [B,H,n]    out, may be NULL: argmax centroid of every query
+ *   the rest as for rt_routing_attention (same workspace size).
+ * bf16: tcgen05 tensor cores (any w); fp32: CUDA cores. */
+rt_status rt_routing_attention_separate(const void* q, const void* k, const void* v,
+                                        rt_dtype dt, int B, int H, int n, int d,
+                                        const float* centroids, int kc, int w,
+                                        int causal, float scale, void* out,
+                                        int32_t* idx_q_out, int32_t* idx_k_out,
+                                        int32_t* assign_out, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
 /* One online spherical k-means step on the centroids, in place.
  * Source: §2 "Attention with Content-Based Sparsity" (centroids learned by
  * mini-batch spherical k-means), §4 (centroids shared across sequences,
@@ -120,13 +151,39 @@ rt_status rt_routing_attention(const void* q, const void* k, const void* v, rt_d
  *   assign    [B,H,n]    int32 in [0, k)
  *   centroids [H,k,d]    fp32, updated in place
  *   decay     in [0, 1]
- * Each centroid's rows are listed in a fixed order and summed in that order,
- * with no floating-point atomics: results are deterministic.  Needs a
- * workspace of at least rt_workspace_bytes(B, H, n, d, k, 1, dt) bytes (only
- * its device status word is used). */
+ * A segmented reduction: the rows are first sorted by assigned centroid
+ * chunk by chunk (integer counts only), then each centroid's rows are summed
+ * in that fixed order, with no floating-point atomics: results are
+ * deterministic.  Needs a workspace of at least
+ * rt_workspace_bytes(B, H, n, d, k, 1, dt) bytes (row ids and per-chunk
+ * counts live there). */
 rt_status rt_centroid_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                           const int32_t* assign, float* centroids, int k, float decay,
                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* The centroid step split for a batch sharded over several GPUs (one process
+ * per GPU, each holding some of the sequences).  The step's means run over
+ * every sequence of the batch (§4: centroids shared across sequences), so
+ * each shard computes its own sums, the shards' sums are added with one
+ * all-reduce (the caller's collective, e.g. NCCL), and every shard applies the
+ * same blend:
+ *   rt_centroid_ema_sums:  sums[h][c][0..d) = sum of r_t over this shard's
+ *                          rows with assign == c; sums[h][c][d] = their count
+ *                          (as a float, exact below 2^24);
+ *   (all-reduce sums over the shards: elementwise addition)
+ *   rt_centroid_ema_apply: for every (h, c) with count N > 0,
+ *                          mu_c <- normalise(decay*mu_c + (1-decay)*sum/N);
+ *                          other centroids are left bit-exact.
+ * With one shard the two calls give rt_centroid_ema's result (the sums are
+ * taken in the same fixed order).
+ *   sums      [H,k,d+1] fp32 (written by _sums; read by _apply)
+ *   the other arguments as for rt_centroid_ema; _sums needs the same
+ *   workspace, _apply none. */
+rt_status rt_centroid_ema_sums(const void* qk, rt_dtype dt, int B, int H, int n, int d,
+                               const int32_t* assign, int k, float* sums,
+                               void* workspace, size_t workspace_bytes, void* stream);
+rt_status rt_centroid_ema_apply(const float* sums, int H, int d, float* centroids, int k,
+                                float decay, void* stream);
 
 /* The same step driven by the top-w membership instead of the argmax
  * assignment: centroid c of head h moves toward the normalised rows its own
@@ -187,15 +244,23 @@ rt_status rt_workspace_init(void* workspace, size_t workspace_bytes, void* strea
  *
  * Same computation and outputs as rt_route_assign (no `scores` output), with
  * the fp32 score scratch [B,H,k,n] taken from a fixed array in device memory
- * that the library owns: at most RT_NOALLOC_MAX_SCORES elements (32 MiB),
- * held on every GPU that loads the library until the process exits.  Larger
+ * that the library owns: at most RT_NOALLOC_MAX_SCORES elements (32 MiB) per
+ * CUDA context that uses this call, held until the process exits.  Larger
  * B*H*k*n returns RT_ERR_UNSUPPORTED before anything is launched.
- *   - allocates nothing: no cudaMalloc/cudaFree, no allocating library call;
- *   - the first call on a device (with that device current) looks up the
- *     array's device address once; make that first call before any stream
- *     capture;
+ *   - allocates nothing itself: no cudaMalloc/cudaFree, no allocating
+ *     library call.  With lazy module loading (the CUDA default) the 32 MiB
+ *     are reserved by the driver when the first call in a context looks up
+ *     the array's address, so that first call may fail with RT_ERR_CUDA when
+ *     device memory is short: callers with a fixed memory budget should make
+ *     their first call at start-up;
+ *   - the first call in each context (with that context's device current)
+ *     looks the array's device address up once and caches it under the
+ *     context's unique id; make that first call before any stream capture;
  *   - every call shares the one array, so calls that overlap on the GPU
- *     (other streams, other host threads) race; serialise them.
+ *     (other streams, other host threads) race; serialise them;
+ *   - a device-side bounded wait that runs out is recorded in a status word
+ *     the library also keeps per context; rt_check_device_status(NULL, 0,
+ *     stream) reads and clears it.
  *   qk [B,H,n,d] dtype dt, centroids [H,k,d] fp32, idx [B,H,k,w] out,
  *   assign [B,H,n] out or NULL, stream as elsewhere. */
 #define RT_NOALLOC_MAX_SCORES (8u * 1024u * 1024u)
@@ -204,9 +269,31 @@ rt_status rt_route_assign_noalloc(const void* qk, rt_dtype dt, int B, int H, int
                                   int32_t* idx, int32_t* assign, void* stream);
 
 /* Synchronises `stream`, reads the device error word kept in `workspace`,
- * clears it, and returns RT_OK, RT_ERR_TIMEOUT or RT_ERR_CUDA.  Not for use
- * inside stream capture. */
+ * clears it, and returns RT_OK, RT_ERR_TIMEOUT or RT_ERR_CUDA.  While the
+ * word is set, every kernel of a later call on the same workspace returns at
+ * once without writing (fail-stop: nothing reads a partial result), so check
+ * the word after an error before reusing the workspace.  With
+ * workspace == NULL and workspace_bytes == 0 it reads (and clears) the status
+ * word of rt_route_assign_noalloc in the current context instead.  Not for
+ * use inside stream capture. */
 rt_status rt_check_device_status(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Test aid for the device-side timeout path; not for production use.  While
+ * `kernels` is non-zero, every later launch of the selected kernels begins
+ * with a wait, bounded by limit_ns (0 < limit_ns <= 1e9), on a barrier that
+ * nothing arrives on -- before the kernel issues any asynchronous copy or
+ * tensor-core operation -- so the wait runs out: the kernel sets the device
+ * status word (RT_ERR_TIMEOUT from rt_check_device_status) and returns with
+ * nothing in flight.  The later kernels of the same call find the word set
+ * and return at once (every kernel does, while the word is set), so the
+ * outputs of that call are left unwritten.  rt_debug_inject_wait_timeout(0, 0)
+ * turns it off; once rt_check_device_status has cleared the word, calls run
+ * normally again.  Process-wide setting.  RT_ERR_INVALID_ARG for unknown bits
+ * or a limit outside the range. */
+#define RT_DEBUG_SCORE 1u            /* the tensor-core score kernel            */
+#define RT_DEBUG_ATTENTION 2u        /* the tensor-core cluster-attention kernels */
+#define RT_DEBUG_LOCAL_ATTENTION 4u  /* the local-attention kernel               */
+rt_status rt_debug_inject_wait_timeout(unsigned kernels, unsigned long long limit_ns);
 
 /* Human-readable name of a status code (static string). */
 const char* rt_status_string(rt_status s);

@@ -24,6 +24,9 @@ Steps (per batch b and head h, with Q shared as K):
                  with a_t = c, over every sequence of the batch); unchanged if none
   a7' variant    the same step with the tokens of c's own top-w lists in place of
                  the argmax assignment (centroid_ema_topw)
+  a7 in halves   per-centroid sums and counts of a shard of the batch
+                 (centroid_sums), added over shards, then the blend
+                 (centroid_apply)
   local          the companion layer: causal attention of every position over the
                  `window` positions ending at it (local_attention)
   backward       gradients of a5..a6 with respect to the shared Q/K rows and V,
@@ -52,6 +55,8 @@ __all__ = [
     "routing_attention",
     "centroid_ema",
     "centroid_ema_topw",
+    "centroid_sums",
+    "centroid_apply",
     "local_attention",
     "routing_attention_head_backward",
     "routing_attention_head_separate",
@@ -287,6 +292,57 @@ def centroid_ema_topw(qk: np.ndarray, idx: np.ndarray, mu: np.ndarray, decay: fl
     return out
 
 
+def centroid_sums(qk: np.ndarray, assign: np.ndarray, k: int) -> np.ndarray:
+    """a7, first half: for every head h and centroid c, the sum of the
+    normalised rows r_t assigned to c over the sequences given, and how many
+    there are.  qk [B, H, n, d], assign [B, H, n] (entries outside [0, k) count
+    for no centroid).  Returns [H, k, d + 1]: the sum in [..., :d], the count
+    in [..., d].
+
+    Source: §4 "Routing attention with clustering" (centroids shared across
+    sequences), §2 (mini-batch k-means).  Reading: a batch split into shards
+    (one per GPU) gives each shard a part of every centroid's sum and count;
+    the parts add up to the whole batch's, so one all-reduce of these arrays
+    followed by centroid_apply is the step centroid_ema takes on the batch.
+    """
+    qk = np.asarray(qk, dtype=np.float64)
+    B, H, n, d = qk.shape
+    r = normalise_rows(qk)
+    a = np.asarray(assign)
+    out = np.zeros((H, k, d + 1))
+    for h in range(H):
+        rh = r[:, h].reshape(B * n, d)
+        ah = a[:, h].reshape(B * n)
+        for c in range(k):
+            sel = ah == c
+            out[h, c, :d] = rh[sel].sum(axis=0)
+            out[h, c, d] = sel.sum()
+    return out
+
+
+def centroid_apply(sums: np.ndarray, mu: np.ndarray, decay: float) -> np.ndarray:
+    """a7, second half: blend each centroid toward the mean sum / count and put
+    it back on the unit sphere; a centroid with count 0 is left as it was.
+    sums [H, k, d + 1] (as centroid_sums returns, possibly added over shards),
+    mu [H, k, d].  Returns the updated centroids (float64).
+
+    Source and readings as centroid_ema (§2, §4, §6 "Local vs Global").
+    """
+    sums = np.asarray(sums, dtype=np.float64)
+    mu = np.asarray(mu, dtype=np.float64)
+    d = mu.shape[-1]
+    out = mu.copy()
+    for h in range(mu.shape[0]):
+        for c in range(mu.shape[1]):
+            cnt = sums[h, c, d]
+            if cnt <= 0:
+                continue
+            blended = decay * mu[h, c] + (1.0 - decay) * sums[h, c, :d] / cnt
+            nrm = np.sqrt((blended * blended).sum())
+            out[h, c] = blended / nrm if nrm > 0 else blended
+    return out
+
+
 def local_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, window: int,
                     scale: float) -> np.ndarray:
     """Local (sliding-window) causal attention of one (batch, head).
@@ -349,7 +405,8 @@ def routing_attention_head_backward(q, v, idx, dO, causal: bool = True, scale=No
     return dq, dv
 
 
-def routing_attention_head_separate(q, k, v, mu, w: int, causal: bool = True, scale=None):
+def routing_attention_head_separate(q, k, v, mu, w: int, causal: bool = True, scale=None,
+                                    idx_q=None, idx_k=None):
     """Routing with separate queries and keys, for one (batch, head).
 
     Queries and keys are each normalised (a1), scored against the same
@@ -358,7 +415,8 @@ def routing_attention_head_separate(q, k, v, mu, w: int, causal: bool = True, sc
     the listed keys at positions not after its own (causal) with softmax
     (a5); a position's output is the mean over the clusters that listed it as
     a query and gave it at least one visible key, zero if none (a6).
-    Returns dict(O, idx_q, idx_k).
+    Returns dict(O, idx_q, idx_k).  ``idx_q`` / ``idx_k`` may be given to
+    evaluate a5..a6 on externally chosen lists (e.g. another implementation's).
 
     Source: §4 "Routing attention with clustering" (queries and keys routed to
     the same clusters; only same-cluster query/key pairs attend), §3.
@@ -371,8 +429,11 @@ def routing_attention_head_separate(q, k, v, mu, w: int, causal: bool = True, sc
     n, d = q.shape
     if scale is None or scale <= 0:
         scale = 1.0 / np.sqrt(d)
-    idx_q = top_w_per_centroid(centroid_scores(normalise_rows(q), mu), w)
-    idx_k = top_w_per_centroid(centroid_scores(normalise_rows(k), mu), w)
+    if idx_q is None:
+        idx_q = top_w_per_centroid(centroid_scores(normalise_rows(q), mu), w)
+    if idx_k is None:
+        idx_k = top_w_per_centroid(centroid_scores(normalise_rows(k), mu), w)
+    idx_q, idx_k = np.asarray(idx_q), np.asarray(idx_k)
     acc = np.zeros((n, d))
     cnt = np.zeros(n, dtype=np.int64)
     for c in range(idx_q.shape[0]):

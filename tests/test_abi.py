@@ -74,7 +74,9 @@ def _attn(lib, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(q=None), bnd.RT_ERR_INVALID_ARG),
-    (dict(k=FAKE + 4096), bnd.RT_ERR_UNSUPPORTED),          # separate keys
+    (dict(k=None), bnd.RT_ERR_INVALID_ARG),
+    (dict(k=FAKE + 4096, d=96), bnd.RT_ERR_UNSUPPORTED),   # separate keys, bad d
+    (dict(k=FAKE + 8), bnd.RT_ERR_INVALID_ARG),             # separate keys, misaligned
     (dict(d=96), bnd.RT_ERR_UNSUPPORTED),
     (dict(w=129), bnd.RT_ERR_INVALID_ARG),                   # w > n
     (dict(w=0), bnd.RT_ERR_INVALID_ARG),
@@ -124,6 +126,19 @@ def test_local_attention_validation(lib):
     assert call(q=None, k=None) == bnd.RT_ERR_INVALID_ARG
     assert call(wsb=8) == bnd.RT_ERR_WORKSPACE
     assert call(ws=FAKE + 16) == bnd.RT_ERR_INVALID_ARG   # workspace not 256-aligned
+    assert lib.rt_last_error_detail() != b""
+
+
+def test_separate_validation(lib):
+    def call(q=FAKE, k=FAKE + 4096, d=64, w=64, wsb=1 << 30, ws=FAKE):
+        return lib.rt_routing_attention_separate(q, k, FAKE, 1, 1, 1, 128, d, FAKE, 2, w, 1,
+                                                 ctypes.c_float(0.0), FAKE, None, None, None, ws,
+                                                 wsb, None)
+    assert call(k=FAKE) == bnd.RT_ERR_INVALID_ARG          # the same tensor: shared QK
+    assert call(d=96) == bnd.RT_ERR_UNSUPPORTED
+    assert call(w=129) == bnd.RT_ERR_INVALID_ARG
+    assert call(wsb=100) == bnd.RT_ERR_WORKSPACE
+    assert call(k=FAKE + 4100) == bnd.RT_ERR_INVALID_ARG   # misaligned keys
     assert lib.rt_last_error_detail() != b""
 
 

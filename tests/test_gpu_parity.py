@@ -242,10 +242,11 @@ def test_bad_arguments_raise_on_gpu():
     with pytest.raises(rt.RoutingAttentionError):
         rt.rt_routing_attention(q, q, q, mu, 16)
     q = torch.zeros((1, 1, 64, 64), dtype=torch.bfloat16, device="cuda")
-    k2 = q.clone()
     mu = torch.zeros((1, 4, 64), device="cuda")
     with pytest.raises(rt.RoutingAttentionError):
-        rt.rt_routing_attention(q, k2, q, mu, 16)
+        rt.rt_routing_attention(q, q, q, mu, 65)          # w > n
+    with pytest.raises(rt.RoutingAttentionError):
+        rt.rt_routing_attention_separate(q, q, q, mu, 16)  # keys must differ from queries
 
 
 # ---------------------------------------------------------------------------
@@ -330,3 +331,193 @@ def test_local_attention_full_size_sampled():
             want = orc.local_attention(q64[0, h, lo:t0 + 64], q64[0, h, lo:t0 + 64],
                                        v64[0, h, lo:t0 + 64], W, 1 / math.sqrt(d))[t0 - lo:]
             assert np.max(np.abs(got[0, h, t0:t0 + 64] - want)) <= ph.TOL_OUT["bf16"]
+
+
+# ---------------------------------------------------------------------------
+# the centroid step on assignments given directly (chunking edge cases)
+# ---------------------------------------------------------------------------
+
+EMA_CASES = [
+    # B, H, n, d, k, dtype, pattern
+    (2, 3, 3000, 64, 40, "bf16", "random"),     # several chunks per sequence, ragged tail
+    (1, 2, 2500, 128, 1500, "f32", "random"),   # k > 1024: 2048-position chunks, empty centroids
+    (3, 1, 5000, 128, 8, "bf16", "one"),        # one centroid takes all 15000 rows
+    (1, 1, 1, 64, 3, "bf16", "random"),         # a single row
+    (2, 2, 1100, 64, 16, "bf16", "invalid"),    # entries outside [0, k) are skipped
+]
+
+
+@pytest.mark.parametrize("case", EMA_CASES, ids=lambda c: "b{}h{}n{}d{}k{}{}{}".format(*c))
+def test_centroid_update_given_assignments(case):
+    B, H, n, d, k, dt, pattern = case
+    wl = make_random(B, H, n, d, min(k, n), 1, dtype=dt, seed=n + k)
+    q, _, _ = ph.to_device(wl)
+    rng = np.random.default_rng(n * 7 + k)
+    mu0 = rng.standard_normal((H, k, d))
+    mu0 = (mu0 / np.linalg.norm(mu0, axis=-1, keepdims=True)).astype(np.float32)
+    if pattern == "one":
+        a = np.zeros((B, H, n), dtype=np.int32)
+    else:
+        a = rng.integers(0, k, size=(B, H, n)).astype(np.int32)
+    if pattern == "invalid":
+        a[rng.random((B, H, n)) < 0.2] = -1
+        a[rng.random((B, H, n)) < 0.1] = k + 3
+    a_ref = np.where((a >= 0) & (a < k), a, -1)  # the oracle never matches -1
+    for decay in (0.0, 0.999):
+        mu = torch.from_numpy(mu0).cuda()
+        ws = rt.Workspace.for_shape(B, H, n, d, k, 1, q.dtype)
+        rt.rt_centroid_ema(q, torch.from_numpy(a).cuda(), mu, decay, workspace=ws)
+        torch.cuda.synchronize()
+        ws.check()
+        want = orc.centroid_ema(wl.q_f32().astype(np.float64), a_ref, mu0, decay)
+        got = mu.cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(got - want)) <= ph.TOL_EMA
+        for h in range(H):
+            hit = np.zeros(k, bool)
+            hit[np.unique(a_ref[:, h][a_ref[:, h] >= 0])] = True
+            assert np.array_equal(got[h, ~hit], mu0[h, ~hit].astype(np.float64))
+
+
+# ---------------------------------------------------------------------------
+# the centroid step in halves (per-shard sums, all-reduce, blend)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", [
+    (2, 8, 4096, 128, 128, "bf16"),
+    (2, 2, 1500, 64, 700, "f32"),
+], ids=lambda c: "b{}h{}n{}d{}k{}{}".format(*c))
+def test_centroid_sums_and_apply(case):
+    from content_sparse_attention_shared_b300 import sharded
+    B, H, n, d, k, dt = case
+    wl = make_random(B, H, n, d, k, 1, dtype=dt, seed=n + k)
+    q, _, mu = ph.to_device(wl)
+    a = rt.rt_route_assign(q, mu, 1)[1]
+    torch.cuda.synchronize()
+    a_np = a.cpu().numpy()
+    q64 = wl.q_f32().astype(np.float64)
+    # each sequence as a shard: sums against the oracle's
+    shard_sums = []
+    for b in range(B):
+        s = rt.rt_centroid_ema_sums(q[b:b + 1].contiguous(), a[b:b + 1].contiguous(), k)
+        torch.cuda.synchronize()
+        want = orc.centroid_sums(q64[b:b + 1], a_np[b:b + 1], k)
+        got = s.cpu().numpy().astype(np.float64)
+        assert np.array_equal(got[..., d], want[..., d])          # counts exact
+        cnt = np.maximum(want[..., d:], 1.0)
+        assert np.max(np.abs(got[..., :d] - want[..., :d]) / cnt) <= ph.TOL_EMA
+        shard_sums.append(s)
+    # "all-reduce" of the shards (elementwise sum), then the blend
+    for decay in (0.0, 0.999):
+        c = mu.clone()
+        rt.rt_centroid_ema_apply(shard_sums[0] + shard_sums[1], c, decay)
+        torch.cuda.synchronize()
+        want = orc.centroid_ema(q64, a_np, wl.centroids, decay)
+        assert np.max(np.abs(c.cpu().numpy() - want)) <= ph.TOL_EMA
+    # one shard holding the whole batch: the same bits as the one-call step
+    c1, c2 = mu.clone(), mu.clone()
+    rt.rt_centroid_ema(q, a, c1, 0.999)
+    sharded.sharded_centroid_ema(q, a, c2, 0.999)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
+
+
+# ---------------------------------------------------------------------------
+# separate queries and keys
+# ---------------------------------------------------------------------------
+
+def _run_separate(q, k, v, mu, w, causal=True):
+    B, H, n, d = q.shape
+    kc = mu.shape[1]
+    iq = torch.empty((B, H, kc, w), dtype=torch.int32, device="cuda")
+    ik = torch.empty((B, H, kc, w), dtype=torch.int32, device="cuda")
+    ws = rt.Workspace.for_shape(B, H, n, d, kc, w, q.dtype)
+    out = rt.rt_routing_attention_separate(q, k, v, mu, w, causal=causal, idx_q_out=iq,
+                                           idx_k_out=ik, workspace=ws)
+    torch.cuda.synchronize()
+    ws.check()
+    return out, iq.cpu().numpy(), ik.cpu().numpy()
+
+
+def _check_separate(q64, k64, v64, mu, out, iq, ik, w, causal, dtype):
+    B, H, n, d = q64.shape
+    got = ph.out_to_f64(out)
+    for b in range(B):
+        for h in range(H):
+            Sq = ph.oracle_scores(q64[b, h], mu[h])
+            Sk = ph.oracle_scores(k64[b, h], mu[h])
+            ph.check_index_lists(iq[b, h], Sq, w, n)
+            ph.check_index_lists(ik[b, h], Sk, w, n)
+            want = orc.routing_attention_head_separate(
+                q64[b, h], k64[b, h], v64[b, h], mu[h], w, causal=causal,
+                idx_q=iq[b, h], idx_k=ik[b, h])["O"]
+            assert np.max(np.abs(got[b, h] - want)) <= ph.TOL_OUT[dtype]
+            # positions with no membership that sees a key are exactly zero
+            assert np.all(got[b, h][np.all(want == 0.0, axis=1)] == 0.0)
+
+
+SEP_CASES = [
+    # B, H, n, d, k, w, dtype, causal
+    (1, 8, 4096, 64, 64, 64, "bf16", True),     # the n=4096 configuration's shape
+    (1, 8, 8192, 128, 128, 64, "bf16", True),   # the n=8192 configuration's shape
+    (2, 2, 777, 128, 24, 129, "bf16", True),    # ragged, two key blocks
+    (1, 2, 1000, 64, 9, 300, "bf16", False),    # three key blocks, non-causal
+    (1, 2, 300, 64, 5, 61, "f32", True),        # fp32 path
+    (2, 1, 200, 128, 4, 33, "f32", False),
+]
+
+
+@pytest.mark.parametrize("case", SEP_CASES, ids=lambda c: "b{}h{}n{}d{}k{}w{}{}{}".format(
+    c[0], c[1], c[2], c[3], c[4], c[5], c[6], "" if c[7] else "nc"))
+def test_separate_qk(case):
+    B, H, n, d, k, w, dt, causal = case
+    wq = make_random(B, H, n, d, k, w, dtype=dt, seed=n + 3 * k)
+    wk = make_random(B, H, n, d, k, w, dtype=dt, seed=n + 3 * k + 1)
+    q, v, mu = ph.to_device(wq)
+    kk, _, _ = ph.to_device(wk)
+    out, iq, ik = _run_separate(q, kk, v, mu, w, causal)
+    _check_separate(wq.q_f32().astype(np.float64), wk.q_f32().astype(np.float64),
+                    wq.v_f32().astype(np.float64), wq.centroids, out, iq, ik, w, causal, dt)
+
+
+@pytest.mark.parametrize("w", [8, 40])
+def test_separate_qk_queries_without_visible_keys(w):
+    # one centroid e: queries score high early, keys score high late.  With
+    # w = 8 every listed query (positions 0..7) precedes every listed key
+    # (32..39): all rows are zero.  With w = 40 the lists overlap and some
+    # queries see keys, others none.
+    n, d = 64, 64
+    rng = np.random.default_rng(5)
+    e = rng.standard_normal(d)
+    e -= e.mean()
+    e /= np.linalg.norm(e)
+    sign = np.where(np.arange(n) < 32, 1.0, -1.0)[:, None]
+    q = (sign * e)[None, None]
+    k = (-sign * e)[None, None]
+    v = rng.standard_normal((1, 1, n, d))
+    mu = e[None, None].astype(np.float32)
+    for dt, tdt in (("bf16", torch.bfloat16), ("f32", torch.float32)):
+        qt = torch.tensor(q, dtype=tdt, device="cuda")
+        kt = torch.tensor(k, dtype=tdt, device="cuda")
+        vt = torch.tensor(v, dtype=tdt, device="cuda")
+        out, iq, ik = _run_separate(qt, kt, vt, torch.tensor(mu, device="cuda"), w)
+        q64 = qt.double().cpu().numpy()
+        k64 = kt.double().cpu().numpy()
+        v64 = vt.double().cpu().numpy()
+        _check_separate(q64, k64, v64, mu, out, iq, ik, w, True, dt)
+        if w == 8:
+            assert iq[0, 0, 0].tolist() == list(range(8))
+            assert ik[0, 0, 0].tolist() == list(range(32, 40))
+            assert torch.all(out == 0)
+
+
+def test_separate_qk_with_equal_keys_matches_shared():
+    # keys equal to the queries (another tensor): the lists and the output of
+    # the shared-QK pass
+    wl = make_random(1, 2, 1000, 128, 12, 100, dtype="bf16", seed=9)
+    q, v, mu = ph.to_device(wl)
+    out, iq, ik = _run_separate(q, q.clone(), v, mu, wl.w)
+    idx = torch.empty((1, 2, 12, 100), dtype=torch.int32, device="cuda")
+    ref = rt.rt_routing_attention(q, q, v, mu, wl.w, idx_out=idx)
+    torch.cuda.synchronize()
+    assert np.array_equal(iq, idx.cpu().numpy()) and np.array_equal(ik, iq)
+    assert torch.max(torch.abs(out.float() - ref.float())).item() <= 2 * ph.TOL_OUT["bf16"]

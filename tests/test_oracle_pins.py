@@ -230,6 +230,54 @@ def check_ema_special_cases():
     np.testing.assert_allclose(np.linalg.norm(out[:2], axis=1), 1.0, atol=1e-12)
 
 
+def check_ema_in_halves():
+    """centroid_sums / centroid_apply: closed forms on the hand-built batch of
+    check_ema_special_cases, additivity over a split of the batch, and the two
+    halves together against the one-call step."""
+    rng = np.random.default_rng(22)
+    d, kc = 8, 3
+    e = _zero_mean_orthonormal(d, 3, rng)
+    mu = np.stack([e[0], e[1], e[2]])
+    ang = 0.4
+    t_plus = math.cos(ang) * e[0] + math.sin(ang) * e[1]
+    t_minus = math.cos(ang) * e[0] - math.sin(ang) * e[1]
+    x = np.zeros((2, 1, 3, d))
+    x[0, 0, 0] = 3 + 2 * t_plus       # normalises to t_plus
+    x[1, 0, 0] = -1 + 5 * t_minus     # t_minus
+    x[0, 0, 1] = 2 * e[1]             # e1
+    x[1, 0, 1] = 4 * e[1]             # e1
+    x[0, 0, 2] = 7 * t_plus           # t_plus
+    x[1, 0, 2] = 0.5 * t_minus        # t_minus
+    a = np.array([[[0, 1, 0]], [[0, 1, 0]]])
+    s_all = orc.centroid_sums(x, a, kc)
+    # centroid 0: 2 t_plus + 2 t_minus = 4 cos(ang) e0 over 4 rows; centroid 1:
+    # 2 e1 over 2 rows; centroid 2: nothing
+    np.testing.assert_allclose(s_all[0, 0, :d], 4 * math.cos(ang) * e[0], atol=1e-12)
+    np.testing.assert_allclose(s_all[0, 1, :d], 2 * e[1], atol=1e-12)
+    assert s_all[0, 0, d] == 4 and s_all[0, 1, d] == 2 and s_all[0, 2, d] == 0
+    assert np.all(s_all[0, 2, :d] == 0)
+    # additive over the two sequences
+    s0 = orc.centroid_sums(x[:1], a[:1], kc)
+    s1 = orc.centroid_sums(x[1:], a[1:], kc)
+    np.testing.assert_allclose(s0 + s1, s_all, atol=1e-12)
+    # the blend: decay 0 -> the mean direction; decay 1/2 between e2 and
+    # cos(ang) e0 (the mean, not the sum); an empty centroid untouched
+    np.testing.assert_allclose(orc.centroid_apply(s_all, mu[None], 0.0)[0][0], e[0], atol=1e-12)
+    mu2 = np.stack([e[2], e[1], e[0]])
+    got = orc.centroid_apply(s_all, mu2[None], 0.5)[0]
+    want = (e[2] + math.cos(ang) * e[0]) / math.sqrt(1 + math.cos(ang) ** 2)
+    np.testing.assert_allclose(got[0], want, atol=1e-12)
+    assert np.array_equal(got[2], mu2[2])
+    # random batches: sums over shards, applied, equal the one-call step
+    B, H, n = 4, 2, 9
+    xr = rng.standard_normal((B, H, n, d))
+    ar = rng.integers(0, kc, size=(B, H, n))
+    mur = orc.normalise_rows(rng.standard_normal((H, kc, d)))
+    parts = orc.centroid_sums(xr[:1], ar[:1], kc) + orc.centroid_sums(xr[1:], ar[1:], kc)
+    np.testing.assert_allclose(orc.centroid_apply(parts, mur, 0.7),
+                               orc.centroid_ema(xr, ar, mur, 0.7), atol=1e-12)
+
+
 def check_ema_topw_special_cases():
     rng = np.random.default_rng(21)
     d, kc = 8, 3
@@ -408,6 +456,7 @@ ALL_CHECKS = [
     check_top_w_exhaustive, check_top_w_invariants, check_full_attention_k1,
     check_k_copies_average, check_rows_sum_to_one, check_v_ones_and_coverage,
     check_w1_and_first_slot, check_ema_special_cases, check_ema_topw_special_cases,
+    check_ema_in_halves,
     check_local_attention, check_backward_autograd, check_backward_finite_difference,
     check_separate_routing,
 ]
@@ -554,6 +603,30 @@ def _mut_local_window_off_by_one(q, k, v, window, scale):
     return _ORIG_LOCAL(q, k, v, window + 1, scale)
 
 
+_ORIG_APPLY = orc.centroid_apply
+_ORIG_SUMS = orc.centroid_sums
+
+
+def _mut_apply_sum_not_mean(sums, mu, decay):
+    sums = np.array(sums, dtype=np.float64)
+    d = sums.shape[-1] - 1
+    sums[..., d] = np.where(sums[..., d] > 0, 1.0, 0.0)  # forgets the count
+    return _ORIG_APPLY(sums, mu, decay)
+
+
+def _mut_sums_raw_rows(qk, assign, k):
+    qk = np.asarray(qk, dtype=np.float64)
+    B, H, n, d = qk.shape
+    a = np.asarray(assign)
+    out = np.zeros((H, k, d + 1))
+    for h in range(H):
+        for c in range(k):
+            sel = a[:, h].reshape(-1) == c
+            out[h, c, :d] = qk[:, h].reshape(-1, d)[sel].sum(axis=0)  # not normalised
+            out[h, c, d] = sel.sum()
+    return out
+
+
 MUTANTS = [
     ("normalise_rows", _mut_no_centering),
     ("cluster_attention", _mut_mask_flipped),
@@ -567,6 +640,8 @@ MUTANTS = [
     ("local_attention", _mut_local_window_off_by_one),
     ("routing_attention_head_backward", _mut_backward_no_key_role),
     ("routing_attention_head_separate", _mut_separate_keys_follow_queries),
+    ("centroid_apply", _mut_apply_sum_not_mean),
+    ("centroid_sums", _mut_sums_raw_rows),
 ]
 
 

@@ -7,8 +7,11 @@ entry point takes its score scratch from a fixed array the library owns.  The
 test calls it through the C ABI, twice in a row (the array keeps the previous
 call's contents), and checks that its index lists and assignments equal those
 of rt_route_assign with a caller workspace -- bit-exact, the tolerance every
-index test here uses.  It also checks the size limit.  This file is collected
-last so that a failure here cannot hide another test's result.
+index test here uses.  The first case's lists are also checked against the
+fp64 oracle with the same rule the parity tests use, and after the calls the
+entry point's own device status word (read with rt_check_device_status(NULL,
+0, stream)) must be clear.  It also checks the size limit.  This file is
+collected last so that a failure here cannot hide another test's result.
 """
 
 import ctypes
@@ -16,6 +19,7 @@ import ctypes
 import numpy as np
 import pytest
 import torch
+
 
 from tests import parity_helpers as ph
 from workloads import make_random, make_workload
@@ -73,6 +77,18 @@ def test_noalloc_matches_workspace_path(lib, name, shape):
     assert _noalloc(lib, q, mu, wl.w, idx, None) == 0
     torch.cuda.synchronize()
     assert torch.equal(idx, idx_ref)
+    # the entry point's own device status word: no wait ran out
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.rt_check_device_status(None, 0, stream) == 0, lib.rt_last_error_detail()
+    if name == "c2":
+        # and the lists agree with the fp64 oracle (score-gap rule for swaps)
+        q64 = wl.q_f32().astype(np.float64)
+        got_idx, got_a = idx_ref.cpu().numpy(), a_ref.cpu().numpy()
+        for b in range(wl.B):
+            for h in range(wl.H):
+                S64 = ph.oracle_scores(q64[b, h], wl.centroids[h])
+                ph.check_index_lists(got_idx[b, h], S64, wl.w, wl.n)
+                ph.check_assign(got_a[b, h], S64)
 
 
 def test_noalloc_rejects_sizes_beyond_the_array(lib):
@@ -84,3 +100,30 @@ def test_noalloc_rejects_sizes_beyond_the_array(lib):
     assert st == 2  # RT_ERR_UNSUPPORTED
     assert b"exceed" in lib.rt_last_error_detail()
     assert torch.all(idx == 0)
+
+
+def test_noalloc_timeout_reported_on_its_own_status_word(lib):
+    # a bounded wait that runs out inside the entry point's score kernel (made
+    # to run out with the library's test aid, before the kernel issues any
+    # copy) is reported through the entry point's own status word, which
+    # rt_check_device_status(NULL, 0, stream) reads and clears; the next call
+    # is correct again
+    import content_sparse_attention_shared_b300 as rt
+    wl = make_workload("c2")
+    q, _, mu = ph.to_device(wl)
+    idx_ref, a_ref, _ = rt.rt_route_assign(q, mu, wl.w)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    idx = torch.full((wl.B, wl.H, wl.k, wl.w), -1, dtype=torch.int32, device="cuda")
+    assert lib.rt_debug_inject_wait_timeout(1, 1_000_000) == 0
+    try:
+        assert _noalloc(lib, q, mu, wl.w, idx, None) == 0
+        torch.cuda.synchronize()
+    finally:
+        lib.rt_debug_inject_wait_timeout(0, 0)
+    assert lib.rt_check_device_status(None, 0, stream) == 5  # RT_ERR_TIMEOUT
+    assert torch.all(idx == -1)                              # nothing after the score kernel ran
+    assert lib.rt_check_device_status(None, 0, stream) == 0  # cleared
+    a = torch.full((wl.B, wl.H, wl.n), -1, dtype=torch.int32, device="cuda")
+    assert _noalloc(lib, q, mu, wl.w, idx, a) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx_ref) and torch.equal(a, a_ref)
