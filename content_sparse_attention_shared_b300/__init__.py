@@ -13,13 +13,16 @@ from ._binding import (  # noqa: F401
     rt_centroid_ema_apply,
     rt_centroid_ema_sums,
     rt_centroid_ema_topw,
+    rt_debug_inject_wait_timeout,
     rt_launch_count,
     rt_local_attention,
+    rt_mixed_attention,
     rt_profile_kernel_name,
     rt_profile_set,
     rt_route_assign,
     rt_route_assign_noalloc,
     rt_routing_attention,
+    rt_routing_attention_backward,
     rt_routing_attention_separate,
     rt_workspace_bytes,
 )

@@ -31,6 +31,9 @@ SIGNATURES = {
     "rt_routing_attention_separate": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                _vp, _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp,
                                                _vp, _vp, _c_size, _vp]),
+    "rt_routing_attention_backward": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
+                                               _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp,
+                                               _c_size, _vp]),
     "rt_centroid_ema": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_int,
                                  _c_float, _vp, _c_size, _vp]),
     "rt_centroid_ema_topw": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int, _vp,
@@ -40,6 +43,9 @@ SIGNATURES = {
     "rt_centroid_ema_apply": (_c_int, [_vp, _c_int, _c_int, _vp, _c_int, _c_float, _vp]),
     "rt_local_attention": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                     _c_float, _vp, _vp, _c_size, _vp]),
+    "rt_mixed_attention": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                    _vp, _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp,
+                                    _c_size, _vp]),
     "rt_route_assign_noalloc": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_int,
                                          _c_int, _vp, _vp, _vp]),
     "rt_workspace_init": (_c_int, [_vp, _c_size, _vp]),
@@ -211,6 +217,25 @@ def rt_routing_attention_separate(q: torch.Tensor, k: torch.Tensor, v: torch.Ten
     return out
 
 
+def rt_routing_attention_backward(q: torch.Tensor, v: torch.Tensor, idx: torch.Tensor,
+                                  dout: torch.Tensor, causal: bool = True, scale: float = 0.0,
+                                  dq: Optional[torch.Tensor] = None,
+                                  dv: Optional[torch.Tensor] = None,
+                                  workspace: Optional[Workspace] = None, stream=None):
+    """Gradients (dq, dv), fp32, of the forward with routing held fixed."""
+    B, H, n, d = q.shape
+    kc, w = idx.shape[2], idx.shape[3]
+    if dq is None:
+        dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if dv is None:
+        dv = torch.empty(v.shape, dtype=torch.float32, device=v.device)
+    ws = _ws(workspace, B, H, n, d, kc, w, q.dtype, q.device)
+    _check(load_library().rt_routing_attention_backward(
+        _ptr(q), _ptr(v), _dtype_code(q), B, H, n, d, _ptr(idx), kc, w, 1 if causal else 0,
+        float(scale), _ptr(dout), _ptr(dq), _ptr(dv), ws.ptr, ws.nbytes, _stream(stream)))
+    return dq, dv
+
+
 def rt_centroid_ema(qk: torch.Tensor, assign: torch.Tensor, centroids: torch.Tensor, decay: float,
                     workspace: Optional[Workspace] = None, stream=None) -> torch.Tensor:
     B, H, n, d = qk.shape
@@ -279,6 +304,28 @@ def rt_debug_inject_wait_timeout(kernels: int, limit_ns: int) -> None:
     """Test aid: the selected kernels start with a bounded wait that runs out
     (0, 0 turns it off)."""
     _check(load_library().rt_debug_inject_wait_timeout(int(kernels), int(limit_ns)))
+
+
+def rt_mixed_attention(q: torch.Tensor, v: torch.Tensor, centroids: Optional[torch.Tensor],
+                       n_local: int, window: int, w: int, causal: bool = True,
+                       scale: float = 0.0, out: Optional[torch.Tensor] = None,
+                       idx_out: Optional[torch.Tensor] = None,
+                       assign_out: Optional[torch.Tensor] = None,
+                       workspace: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """Local attention on heads [0, n_local), routing attention on the rest."""
+    B, H, n, d = q.shape
+    Hr = H - n_local
+    kc = centroids.shape[1] if centroids is not None else 1
+    if out is None:
+        out = torch.empty_like(v)
+    if workspace is None:
+        nbytes = rt_workspace_bytes(1, Hr, n, d, kc, w, q.dtype) if Hr > 0 else 256
+        workspace = Workspace(nbytes, q.device)
+    _check(load_library().rt_mixed_attention(
+        _ptr(q), _ptr(v), _dtype_code(q), B, H, n, d, int(n_local), int(window), _ptr(centroids),
+        kc, w, 1 if causal else 0, float(scale), _ptr(out), _ptr(idx_out), _ptr(assign_out),
+        workspace.ptr, workspace.nbytes, _stream(stream)))
+    return out
 
 
 def rt_launch_count() -> int:

@@ -107,9 +107,9 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
   tc::tc_fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
   pdl_wait();  // the set-up above overlapped the previous kernel's tail
-  // a failed pass or the injected test timeout: no copy or MMA has been
-  // issued, so the CTA goes straight to the teardown (TMEM is given back)
-  const bool skip = pass_failed(err) || injected_wait_timeout(fault_ns, err);
+  // the injected test timeout: no copy or MMA has been issued, so the CTA goes
+  // straight to the teardown (TMEM is given back)
+  const bool skip = injected_wait_timeout(fault_ns, err);
 
   auto fail = [&](bool leader) {
     if (leader) atomicExch(err, (unsigned)DEV_TIMEOUT);

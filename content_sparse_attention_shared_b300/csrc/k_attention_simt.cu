@@ -53,11 +53,9 @@ attention_simt_kernel(const T* __restrict__ q, const T* __restrict__ kk, const T
                       int n, int k, int w, int causal, float scale,
                       const int32_t* __restrict__ idx, const int32_t* __restrict__ idx_k,
                       const int32_t* __restrict__ mcount, int32_t* __restrict__ mvis,
-                      T* __restrict__ out, float* __restrict__ yslot,
-                      const unsigned int* __restrict__ err) {
+                      T* __restrict__ out, float* __restrict__ yslot) {
   pdl_trigger();
   pdl_wait();
-  if (status_set(err)) return;  // uniform: only earlier kernels set the word
   extern __shared__ float smem[];
   constexpr int LDQ = D + 1;
   float* Qs = smem;              // [QB][D+1]
@@ -169,7 +167,7 @@ template <typename T, int D>
 cudaError_t launch_t(const void* q, const void* kk, const void* v, int BH, int n, int k, int w,
                      int causal, float scale, const int32_t* idx, const int32_t* idx_k,
                      const int32_t* mcount, int32_t* mvis, void* out, float* yslot,
-                     unsigned int* err, cudaStream_t s) {
+                     cudaStream_t s) {
   const size_t smem = ((size_t)(QB + KB) * (D + 1) + (size_t)KB * D) * sizeof(float);
   auto kern = idx_k != nullptr ? attention_simt_kernel<T, D, true> : attention_simt_kernel<T, D, false>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
@@ -178,8 +176,7 @@ cudaError_t launch_t(const void* q, const void* kk, const void* v, int BH, int n
   launch_begin(K_ATTN_SIMT, s);
   e = launch_pdl(kern, grid, dim3(THREADS), smem, s, static_cast<const T*>(q),
                  static_cast<const T*>(kk), static_cast<const T*>(v), n, k, w, causal, scale, idx,
-                 idx_k, mcount, mvis, static_cast<T*>(out), yslot,
-                 static_cast<const unsigned int*>(err));
+                 idx_k, mcount, mvis, static_cast<T*>(out), yslot);
   launch_end(K_ATTN_SIMT, s);
   return e;
 }
@@ -190,14 +187,14 @@ cudaError_t launch_attention_simt(const void* q, const void* kk, const void* v, 
                                   int BH, int n, int d, int k, int w, int causal,
                                   float scale, const int32_t* idx, const int32_t* idx_k,
                                   const int32_t* mcount, int32_t* mvis, void* out, float* yslot,
-                                  unsigned int* err, cudaStream_t s) {
+                                  cudaStream_t s) {
   if (dt == RT_F32) {
-    return d == 64 ? launch_t<float, 64>(q, kk, v, BH, n, k, w, causal, scale, idx, idx_k, mcount, mvis, out, yslot, err, s)
-                   : launch_t<float, 128>(q, kk, v, BH, n, k, w, causal, scale, idx, idx_k, mcount, mvis, out, yslot, err, s);
+    return d == 64 ? launch_t<float, 64>(q, kk, v, BH, n, k, w, causal, scale, idx, idx_k, mcount, mvis, out, yslot, s)
+                   : launch_t<float, 128>(q, kk, v, BH, n, k, w, causal, scale, idx, idx_k, mcount, mvis, out, yslot, s);
   }
   return d == 64
-             ? launch_t<__nv_bfloat16, 64>(q, kk, v, BH, n, k, w, causal, scale, idx, idx_k, mcount, mvis, out, yslot, err, s)
-             : launch_t<__nv_bfloat16, 128>(q, kk, v, BH, n, k, w, causal, scale, idx, idx_k, mcount, mvis, out, yslot, err, s);
+             ? launch_t<__nv_bfloat16, 64>(q, kk, v, BH, n, k, w, causal, scale, idx, idx_k, mcount, mvis, out, yslot, s)
+             : launch_t<__nv_bfloat16, 128>(q, kk, v, BH, n, k, w, causal, scale, idx, idx_k, mcount, mvis, out, yslot, s);
 }
 
 }  // namespace rt

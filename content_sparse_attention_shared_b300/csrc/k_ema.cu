@@ -209,8 +209,7 @@ constexpr int BUCKET_ROWS = 1024;  // positions per chunk for M = 1
 template <int M>
 __global__ void __launch_bounds__(BUCKET_THREADS)
 ema_bucket_kernel(const int32_t* __restrict__ assign, int H, int n, int k, int cps,
-                  int nchunks, int2* __restrict__ offcnt, int32_t* __restrict__ perm, int Bn,
-                  const unsigned int* __restrict__ err) {
+                  int nchunks, int2* __restrict__ offcnt, int32_t* __restrict__ perm, int Bn) {
   pdl_trigger();
   constexpr int G = 4 * M;  // groups of 32 positions per warp stripe
   constexpr int R = BUCKET_ROWS * M;
@@ -222,7 +221,6 @@ ema_bucket_kernel(const int32_t* __restrict__ assign, int H, int n, int k, int c
   const int t0 = (j - b * cps) * R;
   for (int i = tid; i < BUCKET_WARPS * k; i += BUCKET_THREADS) whist[i] = 0;
   pdl_wait();
-  const bool failed = status_set(err);
   const int32_t* arow = assign + ((size_t)b * H + h) * n;
   int a[G];
 #pragma unroll
@@ -231,7 +229,6 @@ ema_bucket_kernel(const int32_t* __restrict__ assign, int H, int n, int k, int c
     int c = t < n ? __ldcg(arow + t) : -1;
     a[e] = (c >= 0 && c < k) ? c : -1;
   }
-  if (failed) return;  // uniform: only earlier kernels set the word
   __syncthreads();  // counters cleared
   // rank of each row among the earlier rows of this warp's stripe with the
   // same centroid (groups in position order, lanes in position order)
@@ -287,7 +284,7 @@ __global__ void __launch_bounds__(THREADS2, 7)
 ema_segment_kernel(const T* __restrict__ qk, const int2* __restrict__ offcnt,
                    const int32_t* __restrict__ perm, int H, int n, int k, int cps, int R,
                    int nchunks, int Bn, float* __restrict__ mu, float decay,
-                   float* __restrict__ out, const unsigned int* __restrict__ err) {
+                   float* __restrict__ out) {
   pdl_trigger();
   __shared__ int rowlist[LIST];
   __shared__ int wsum[WARPS2];
@@ -296,7 +293,6 @@ ema_segment_kernel(const T* __restrict__ qk, const int2* __restrict__ offcnt,
   const int c = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x;
   pdl_wait();
-  const bool failed = status_set(err);
   const float old = (FINAL && tid < D) ? __ldcg(mu + ((size_t)h * k + c) * D + tid) : 0.0f;
 
   float acc[8];
@@ -317,7 +313,6 @@ ema_segment_kernel(const T* __restrict__ qk, const int2* __restrict__ offcnt,
       const int b = j / cps;
       base = (long long)b * n + (long long)(j - b * cps) * R + fc.x;
     }
-    if (failed) return;  // uniform: only earlier kernels set the word
     int total;
     const int ex = block_exclusive_scan<THREADS2>(fc.y, wsum, total);
     ex_s[tid] = ex;
@@ -355,8 +350,7 @@ ema_segment_kernel(const T* __restrict__ qk, const int2* __restrict__ offcnt,
 template <typename T, int D>
 __global__ void __launch_bounds__(THREADS2, 7)
 ema_topw_kernel(const T* __restrict__ qk, const int32_t* __restrict__ idx, int B, int H, int n,
-                int k, int w, float* __restrict__ mu, float decay,
-                const unsigned int* __restrict__ err) {
+                int k, int w, float* __restrict__ mu, float decay) {
   pdl_trigger();
   __shared__ int rowlist[LIST];
   __shared__ int wsum[WARPS2];
@@ -365,7 +359,6 @@ ema_topw_kernel(const T* __restrict__ qk, const int32_t* __restrict__ idx, int B
   const int c = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x;
   pdl_wait();
-  if (status_set(err)) return;  // uniform: only earlier kernels set the word
   const float old = (tid < D) ? __ldcg(mu + ((size_t)h * k + c) * D + tid) : 0.0f;
   float acc[8];
 #pragma unroll
@@ -416,11 +409,11 @@ ema_apply_kernel(const float* __restrict__ red, int k, float* __restrict__ mu, f
 
 template <typename T, int D>
 cudaError_t launch_topw(const void* qk, const int32_t* idx, int B, int H, int n, int k, int w,
-                        float* mu, float decay, unsigned int* err, cudaStream_t s) {
+                        float* mu, float decay, cudaStream_t s) {
   auto kern = ema_topw_kernel<T, D>;
   launch_begin(K_EMA_TOPW, s);
   cudaError_t e = launch_pdl(kern, dim3(k, H), dim3(THREADS2), 0, s, static_cast<const T*>(qk),
-                             idx, B, H, n, k, w, mu, decay, static_cast<const unsigned int*>(err));
+                             idx, B, H, n, k, w, mu, decay);
   launch_end(K_EMA_TOPW, s);
   return e;
 }
@@ -453,9 +446,7 @@ inline BucketPlan bucket_plan(int B, int H, int n, int k) {
 // count to out [H][k][D+1] and leave mu alone.
 template <typename T, int D, bool FINAL>
 cudaError_t launch_update(const void* qk, const int32_t* assign, int B, int H, int n, int k,
-                          float* mu, float decay, float* out, void* ws, unsigned int* err,
-                          cudaStream_t s) {
-  const unsigned int* cerr = err;
+                          float* mu, float decay, float* out, void* ws, cudaStream_t s) {
   cudaError_t e;
   const BucketPlan p = bucket_plan(B, H, n, k);
   int32_t* perm = static_cast<int32_t*>(ws);
@@ -467,14 +458,14 @@ cudaError_t launch_update(const void* qk, const int32_t* assign, int B, int H, i
   if (e != cudaSuccess) return e;
   launch_begin(K_EMA_BUCKET, s);
   e = launch_pdl(bucket, dim3(p.nchunks, H), dim3(BUCKET_THREADS), smem, s, assign, H, n, k,
-                 p.cps, p.nchunks, offcnt, perm, Bn, cerr);
+                 p.cps, p.nchunks, offcnt, perm, Bn);
   launch_end(K_EMA_BUCKET, s);
   if (e != cudaSuccess) return e;
   auto kern = ema_segment_kernel<T, D, FINAL>;
   launch_begin(K_EMA_UPDATE, s);
   e = launch_pdl(kern, dim3(k, H), dim3(THREADS2), 0, s, static_cast<const T*>(qk),
                  static_cast<const int2*>(offcnt), static_cast<const int32_t*>(perm), H, n, k,
-                 p.cps, p.R, p.nchunks, Bn, mu, decay, out, cerr);
+                 p.cps, p.R, p.nchunks, Bn, mu, decay, out);
   launch_end(K_EMA_UPDATE, s);
   return e;
 }
@@ -482,14 +473,14 @@ cudaError_t launch_update(const void* qk, const int32_t* assign, int B, int H, i
 template <bool FINAL>
 cudaError_t launch_update_any(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                               const int32_t* assign, float* mu, int k, float decay, float* out,
-                              void* ws, unsigned int* err, cudaStream_t s) {
+                              void* ws, cudaStream_t s) {
   if (dt == RT_F32) {
-    return d == 64 ? launch_update<float, 64, FINAL>(qk, assign, B, H, n, k, mu, decay, out, ws, err, s)
-                   : launch_update<float, 128, FINAL>(qk, assign, B, H, n, k, mu, decay, out, ws, err, s);
+    return d == 64 ? launch_update<float, 64, FINAL>(qk, assign, B, H, n, k, mu, decay, out, ws, s)
+                   : launch_update<float, 128, FINAL>(qk, assign, B, H, n, k, mu, decay, out, ws, s);
   }
   return d == 64
-             ? launch_update<__nv_bfloat16, 64, FINAL>(qk, assign, B, H, n, k, mu, decay, out, ws, err, s)
-             : launch_update<__nv_bfloat16, 128, FINAL>(qk, assign, B, H, n, k, mu, decay, out, ws, err, s);
+             ? launch_update<__nv_bfloat16, 64, FINAL>(qk, assign, B, H, n, k, mu, decay, out, ws, s)
+             : launch_update<__nv_bfloat16, 128, FINAL>(qk, assign, B, H, n, k, mu, decay, out, ws, s);
 }
 
 }  // namespace
@@ -501,14 +492,14 @@ size_t ema_workspace_bytes(int B, int H, int n, int /*d*/, int k, rt_dtype /*dt*
 
 cudaError_t launch_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                        const int32_t* assign, float* mu, int k, float decay, void* ws,
-                       unsigned int* err, cudaStream_t s) {
-  return launch_update_any<true>(qk, dt, B, H, n, d, assign, mu, k, decay, nullptr, ws, err, s);
+                       cudaStream_t s) {
+  return launch_update_any<true>(qk, dt, B, H, n, d, assign, mu, k, decay, nullptr, ws, s);
 }
 
 cudaError_t launch_ema_sums(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                             const int32_t* assign, int k, float* sums, void* ws,
-                            unsigned int* err, cudaStream_t s) {
-  return launch_update_any<false>(qk, dt, B, H, n, d, assign, nullptr, k, 0.0f, sums, ws, err, s);
+                            cudaStream_t s) {
+  return launch_update_any<false>(qk, dt, B, H, n, d, assign, nullptr, k, 0.0f, sums, ws, s);
 }
 
 cudaError_t launch_ema_apply(const float* sums, int H, int d, float* mu, int k, float decay,
@@ -522,13 +513,13 @@ cudaError_t launch_ema_apply(const float* sums, int H, int d, float* mu, int k, 
 
 cudaError_t launch_ema_topw(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                             const int32_t* idx, int w, float* mu, int k, float decay,
-                            unsigned int* err, cudaStream_t s) {
+                            cudaStream_t s) {
   if (dt == RT_F32) {
-    return d == 64 ? launch_topw<float, 64>(qk, idx, B, H, n, k, w, mu, decay, err, s)
-                   : launch_topw<float, 128>(qk, idx, B, H, n, k, w, mu, decay, err, s);
+    return d == 64 ? launch_topw<float, 64>(qk, idx, B, H, n, k, w, mu, decay, s)
+                   : launch_topw<float, 128>(qk, idx, B, H, n, k, w, mu, decay, s);
   }
-  return d == 64 ? launch_topw<__nv_bfloat16, 64>(qk, idx, B, H, n, k, w, mu, decay, err, s)
-                 : launch_topw<__nv_bfloat16, 128>(qk, idx, B, H, n, k, w, mu, decay, err, s);
+  return d == 64 ? launch_topw<__nv_bfloat16, 64>(qk, idx, B, H, n, k, w, mu, decay, s)
+                 : launch_topw<__nv_bfloat16, 128>(qk, idx, B, H, n, k, w, mu, decay, s);
 }
 
 }  // namespace rt

@@ -92,15 +92,18 @@ __device__ __forceinline__ void store8(T* dst, const float (&v)[8]) {
   }
 }
 
-template <typename T, int D>
+// SUM = false: the forward's averaging scatter (single-membership rows were
+// written by the attention kernel).  SUM = true: the backward's gather of
+// per-slot gradient rows -- every position with m >= 1 gets the plain sum of
+// its slot rows (fp32), m = 0 a zero row.
+template <typename T, int D, bool SUM>
 __global__ void __launch_bounds__(THREADS, 6)
 scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ idx,
                const int32_t* __restrict__ mcount, const int32_t* __restrict__ mdiv,
                const int32_t* __restrict__ slots, const float* __restrict__ yslot,
-               T* __restrict__ out, const unsigned int* __restrict__ err) {
+               T* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
-  const bool failed = status_set(err);
   constexpr int CH = D / 8;    // 8-feature chunks per row
   constexpr int PER = D / 32;  // contiguous features per lane on the warp-wide path
   const long long g = (long long)blockIdx.x * THREADS + threadIdx.x;
@@ -119,8 +122,6 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
     sa = __ldcg(sp);
     sb = __ldcg(sp + 1);
   }
-
-  if (failed) return;  // uniform: only earlier kernels set the word
 
   // rare: positions in more than SLOTS_PER_ROW clusters, one warp pass each
   unsigned slow = __ballot_sync(0xffffffffu, active && ch == 0 && m > SLOTS_PER_ROW);
@@ -160,11 +161,11 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
     const float fm = (float)mm;
     float o[PER];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) o[i] = mm > 0 ? acc[i] / fm : 0.0f;
+    for (int i = 0; i < PER; ++i) o[i] = SUM ? acc[i] : (mm > 0 ? acc[i] / fm : 0.0f);
     store_row<T, PER>(out + gt * D + lane * PER, o);
   }
 
-  if (!active || m == 1 || m > SLOTS_PER_ROW) return;
+  if (!active || (!SUM && m == 1) || m > SLOTS_PER_ROW) return;
   T* dst = out + r * D + ch * 8;
   float acc[8];
 #pragma unroll
@@ -204,37 +205,55 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
   }
   const float fm = (float)dv;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = dv > 0 ? acc[i] / fm : 0.0f;
+  for (int i = 0; i < 8; ++i) acc[i] = SUM ? acc[i] : (dv > 0 ? acc[i] / fm : 0.0f);
   store8<T>(dst, acc);
 }
 
 template <typename T, int D>
 cudaError_t launch_t(int BH, int n, int k, int w, const int32_t* idx, const int32_t* mcount,
                      const int32_t* mdiv, const int32_t* slots, const float* yslot, void* out,
-                     unsigned int* err, cudaStream_t s) {
+                     cudaStream_t s) {
   const long long rows = (long long)BH * n;
   const long long threads = rows * (D / 8);
   const long long blocks = (threads + THREADS - 1) / THREADS;
   launch_begin(K_SCATTER, s);
-  cudaError_t e = launch_pdl(scatter_kernel<T, D>, dim3((unsigned)blocks), dim3(THREADS), 0, s,
-                             rows, n, k, w, idx, mcount, mdiv, slots, yslot, static_cast<T*>(out),
-                             static_cast<const unsigned int*>(err));
+  cudaError_t e = launch_pdl(scatter_kernel<T, D, false>, dim3((unsigned)blocks), dim3(THREADS), 0, s,
+                             rows, n, k, w, idx, mcount, mdiv, slots, yslot, static_cast<T*>(out));
+  launch_end(K_SCATTER, s);
+  return e;
+}
+
+template <int D>
+cudaError_t launch_sum_t(int BH, int n, int k, int w, const int32_t* idx, const int32_t* mcount,
+                         const int32_t* slots, const float* yslot, float* out, cudaStream_t s) {
+  const long long rows = (long long)BH * n;
+  const long long blocks = (rows * (D / 8) + THREADS - 1) / THREADS;
+  launch_begin(K_SCATTER, s);
+  cudaError_t e = launch_pdl(scatter_kernel<float, D, true>, dim3((unsigned)blocks), dim3(THREADS),
+                             0, s, rows, n, k, w, idx, mcount,
+                             static_cast<const int32_t*>(nullptr), slots, yslot, out);
   launch_end(K_SCATTER, s);
   return e;
 }
 
 }  // namespace
 
+cudaError_t launch_gather_sum(int BH, int n, int d, int k, int w, const int32_t* idx,
+                              const int32_t* mcount, const int32_t* slots, const float* yslot,
+                              float* out, cudaStream_t s) {
+  return d == 64 ? launch_sum_t<64>(BH, n, k, w, idx, mcount, slots, yslot, out, s)
+                 : launch_sum_t<128>(BH, n, k, w, idx, mcount, slots, yslot, out, s);
+}
+
 cudaError_t launch_scatter(rt_dtype dt, int BH, int n, int d, int k, int w,
                            const int32_t* idx, const int32_t* mcount, const int32_t* mdiv,
-                           const int32_t* slots, const float* yslot, void* out,
-                           unsigned int* err, cudaStream_t s) {
+                           const int32_t* slots, const float* yslot, void* out, cudaStream_t s) {
   if (dt == RT_F32) {
-    return d == 64 ? launch_t<float, 64>(BH, n, k, w, idx, mcount, mdiv, slots, yslot, out, err, s)
-                   : launch_t<float, 128>(BH, n, k, w, idx, mcount, mdiv, slots, yslot, out, err, s);
+    return d == 64 ? launch_t<float, 64>(BH, n, k, w, idx, mcount, mdiv, slots, yslot, out, s)
+                   : launch_t<float, 128>(BH, n, k, w, idx, mcount, mdiv, slots, yslot, out, s);
   }
-  return d == 64 ? launch_t<__nv_bfloat16, 64>(BH, n, k, w, idx, mcount, mdiv, slots, yslot, out, err, s)
-                 : launch_t<__nv_bfloat16, 128>(BH, n, k, w, idx, mcount, mdiv, slots, yslot, out, err, s);
+  return d == 64 ? launch_t<__nv_bfloat16, 64>(BH, n, k, w, idx, mcount, mdiv, slots, yslot, out, s)
+                 : launch_t<__nv_bfloat16, 128>(BH, n, k, w, idx, mcount, mdiv, slots, yslot, out, s);
 }
 
 }  // namespace rt

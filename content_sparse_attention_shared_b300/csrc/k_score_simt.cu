@@ -26,10 +26,9 @@ template <typename T, int D>
 __global__ void __launch_bounds__(THREADS)
 score_simt_kernel(const T* __restrict__ qk, int H, int n, const float* __restrict__ mu,
                   int k, float* __restrict__ S, int32_t* __restrict__ assign,
-                  int32_t* __restrict__ mcount, const unsigned int* __restrict__ err) {
+                  int32_t* __restrict__ mcount) {
   pdl_trigger();
   pdl_wait();
-  if (status_set(err)) return;  // uniform: only earlier kernels set the word
   extern __shared__ float smem[];
   float* rT = smem;             // [D][PAD]
   float* muT = smem + D * PAD;  // [D][PAD]
@@ -140,7 +139,7 @@ score_simt_kernel(const T* __restrict__ qk, int H, int n, const float* __restric
 
 template <typename T, int D>
 cudaError_t launch_t(const void* qk, int BH, int H, int n, const float* mu, int k, float* S,
-                     int32_t* a, int32_t* mcount, unsigned int* err, cudaStream_t s) {
+                     int32_t* a, int32_t* mcount, cudaStream_t s) {
   const size_t smem = 2 * (size_t)D * PAD * sizeof(float);
   auto kern = score_simt_kernel<T, D>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
@@ -148,7 +147,7 @@ cudaError_t launch_t(const void* qk, int BH, int H, int n, const float* mu, int 
   dim3 grid((n + TOK - 1) / TOK, BH);
   launch_begin(K_SCORE_SIMT, s);
   e = launch_pdl(kern, grid, dim3(THREADS), smem, s, static_cast<const T*>(qk), H, n, mu, k, S, a,
-                 mcount, static_cast<const unsigned int*>(err));
+                 mcount);
   launch_end(K_SCORE_SIMT, s);
   return e;
 }
@@ -157,13 +156,13 @@ cudaError_t launch_t(const void* qk, int BH, int H, int n, const float* mu, int 
 
 cudaError_t launch_score_simt(const void* qk, rt_dtype dt, int BH, int H, int n, int d,
                               const float* mu, int k, float* S, int32_t* a,
-                              int32_t* mcount, unsigned int* err, cudaStream_t s) {
+                              int32_t* mcount, cudaStream_t s) {
   if (dt == RT_F32) {
-    return d == 64 ? launch_t<float, 64>(qk, BH, H, n, mu, k, S, a, mcount, err, s)
-                   : launch_t<float, 128>(qk, BH, H, n, mu, k, S, a, mcount, err, s);
+    return d == 64 ? launch_t<float, 64>(qk, BH, H, n, mu, k, S, a, mcount, s)
+                   : launch_t<float, 128>(qk, BH, H, n, mu, k, S, a, mcount, s);
   }
-  return d == 64 ? launch_t<__nv_bfloat16, 64>(qk, BH, H, n, mu, k, S, a, mcount, err, s)
-                 : launch_t<__nv_bfloat16, 128>(qk, BH, H, n, mu, k, S, a, mcount, err, s);
+  return d == 64 ? launch_t<__nv_bfloat16, 64>(qk, BH, H, n, mu, k, S, a, mcount, s)
+                 : launch_t<__nv_bfloat16, 128>(qk, BH, H, n, mu, k, S, a, mcount, s);
 }
 
 }  // namespace rt

@@ -110,11 +110,9 @@ __device__ __forceinline__ void split_store8(uint8_t* planes, size_t plane_bytes
 // fixed shuffle order.
 template <int D>
 __global__ void __launch_bounds__(256)
-centroid_prep_kernel(const float* __restrict__ mu, int k, int kpad, uint8_t* __restrict__ image,
-                     const unsigned int* __restrict__ err) {
+centroid_prep_kernel(const float* __restrict__ mu, int k, int kpad, uint8_t* __restrict__ image) {
   pdl_trigger();
   pdl_wait();
-  if (status_set(err)) return;  // uniform: only earlier kernels set the word
   const int h = blockIdx.y, c0 = blockIdx.x * 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const size_t plane_bytes = (size_t)kpad * D * 2;
@@ -209,9 +207,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
     tc::fence_mbar_init();
   }
   pdl_wait();  // every global access below comes after the previous kernel
-  // nothing is in flight and no TMEM is held yet: a failed pass or the
-  // injected test timeout returns here
-  if (pass_failed(err) || injected_wait_timeout(fault_ns, err)) return;
+  // the injected test timeout returns here: nothing is in flight and no TMEM
+  // is held yet
+  if (injected_wait_timeout(fault_ns, err)) return;
   if (tid == 0) {
     if (PREP) {
       // the head's centroid image, in bulk copies of at most 32 KiB
@@ -550,7 +548,7 @@ cudaError_t launch_t(const ScoreCfg& c, const void* qk, int B, int H, int n, con
   if (prep != nullptr) {
     launch_begin(K_CENTROID_PREP, s);
     e = launch_pdl(centroid_prep_kernel<D>, dim3((c.kpad + 31) / 32, H), dim3(256), 0, s, mu, k,
-                   c.kpad, static_cast<uint8_t*>(prep), static_cast<const unsigned int*>(err));
+                   c.kpad, static_cast<uint8_t*>(prep));
     launch_end(K_CENTROID_PREP, s);
     if (e != cudaSuccess) return e;
   }
@@ -591,7 +589,7 @@ cudaError_t launch_score(const void* qk, rt_dtype dt, int B, int H, int n, int d
     return d == 64 ? launch_t<64>(c, qk, B, H, n, mu, k, S, a, mcount, prep, err, s)
                    : launch_t<128>(c, qk, B, H, n, mu, k, S, a, mcount, prep, err, s);
   }
-  return launch_score_simt(qk, dt, B * H, H, n, d, mu, k, S, a, mcount, err, s);
+  return launch_score_simt(qk, dt, B * H, H, n, d, mu, k, S, a, mcount, s);
 }
 
 }  // namespace rt

@@ -157,8 +157,7 @@ __device__ void radix_select_row(const float* __restrict__ row, int n, int w, co
 
 __global__ void __launch_bounds__(THREADS)
 select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __restrict__ idx,
-                   int32_t* __restrict__ mcount, int32_t* __restrict__ slots, int staged,
-                   const unsigned int* __restrict__ err) {
+                   int32_t* __restrict__ mcount, int32_t* __restrict__ slots, int staged) {
   pdl_trigger();
   extern __shared__ __align__(16) uint16_t sbin[];  // [n] when staged
   __shared__ unsigned hist[NBINS];
@@ -175,7 +174,6 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
 
   if (!staged) {
     pdl_wait();
-    if (status_set(err)) return;
     radix_select_row(row, n, w, so, hist, wsum);
     return;
   }
@@ -183,7 +181,6 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
   for (int b = tid; b < NBINS; b += THREADS) hist[b] = 0u;
   if (tid == 0) s_ncand = 0;
   pdl_wait();
-  const bool failed = status_set(err);
   __syncthreads();
 
   // 1. bins + histogram: one vectorised read of the row
@@ -229,7 +226,6 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
       atomicAdd(&hist[b], 1u);
     }
   }
-  if (failed) return;  // uniform: only earlier kernels set the word
   __syncthreads();
 
   // 2. boundary bin: thread i owns bins [top - 8i - 7, top - 8i] (descending)
@@ -364,7 +360,7 @@ __device__ __forceinline__ unsigned long long cand_key(float x, int p) {
 __global__ void __launch_bounds__(THREADS, 7)
 select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
                          int32_t* __restrict__ idx, int32_t* __restrict__ mcount,
-                         int32_t* __restrict__ slots, const unsigned int* __restrict__ err) {
+                         int32_t* __restrict__ slots) {
   pdl_trigger();
   __shared__ unsigned hist[256];  // radix fallback
   __shared__ __align__(16) unsigned long long ckey[RCAP + 1];
@@ -384,7 +380,6 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
   kept[tid] = 0u;
   if (tid == 0) s_ncand = 0;
   pdl_wait();
-  const bool failed = status_set(err);
 
   auto load_chunks = [&](int i0, float4 (&v)[4]) {
 #pragma unroll
@@ -406,7 +401,6 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
     for (int u = 0; u < 4; ++u) m = fmaxf(m, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
   }
   const int mbin = w0 < n ? score_bin(m) : -1;
-  if (failed) return;  // uniform: only earlier kernels set the word
 
   // 2. b_L = the largest bin b with at least w thread maxima in bins >= b,
   //    by bisection over the bins with block-wide counts (no histogram, no
@@ -517,7 +511,10 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
 // thread's scores, so that it stays tight for any n:
 //   1. one streaming read of the row (two float4 per group, four groups in
 //      flight per thread): the bin of every group's maximum goes to shared
-//      memory (u16) and into a 2048-bin histogram;
+//      memory (u16); the bins at or above the smallest thread maximum (a
+//      lower bound on the w-th largest group maximum when w <= 256) are
+//      counted in a 2048-bin histogram, one shared atomic per distinct bin of
+//      a warp;
 //   2. b_L = the largest bin with at least w group maxima in bins >= b_L: the
 //      w groups holding the largest maxima own w distinct scores at least
 //      that large, so every kept score lies in a bin >= b_L (a block scan of
@@ -547,7 +544,7 @@ inline size_t group_smem_bytes(int n) {
 __global__ void __launch_bounds__(THREADS, 4)
 select_topw_group_kernel(const float* __restrict__ S, int n, int k, int w,
                          int32_t* __restrict__ idx, int32_t* __restrict__ mcount,
-                         int32_t* __restrict__ slots, const unsigned int* __restrict__ err) {
+                         int32_t* __restrict__ slots) {
   pdl_trigger();
   extern __shared__ __align__(16) uint8_t gsm[];
   __shared__ unsigned hist[NBINS];
@@ -571,12 +568,12 @@ select_topw_group_kernel(const float* __restrict__ S, int n, int k, int w,
   for (int i = tid; i < NBINS; i += THREADS) hist[i] = 0u;
   if (tid == 0) { s_ncand = 0; s_bl = -1; }
   pdl_wait();
-  const bool failed = status_set(err);
   __syncthreads();
 
-  // 1. bins of the group maxima
+  // 1. bins of the group maxima (and this thread's largest group maximum)
   const int n4 = n >> 2;
   const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  float tmax = -INFINITY;
   for (int g0 = tid; g0 < NG; g0 += 4 * THREADS) {
     float4 v[4][2];
 #pragma unroll
@@ -591,13 +588,37 @@ select_topw_group_kernel(const float* __restrict__ S, int n, int k, int w,
       if (g < NG) {
         const float m = fmaxf(fmaxf(fmaxf(v[u][0].x, v[u][0].y), fmaxf(v[u][0].z, v[u][0].w)),
                               fmaxf(fmaxf(v[u][1].x, v[u][1].y), fmaxf(v[u][1].z, v[u][1].w)));
-        const int b = score_bin(m);
-        gbin[g] = (uint16_t)b;
-        atomicAdd(&hist[b], 1u);
+        gbin[g] = (uint16_t)score_bin(m);
+        tmax = fmaxf(tmax, m);
       }
     }
   }
-  if (failed) return;  // uniform: only earlier kernels set the word
+  // Prefilter: when every thread owns a group and w <= THREADS, the smallest
+  // thread maximum T0 is at most the w-th largest group maximum (the THREADS
+  // threads own THREADS distinct groups with maxima >= T0), so b_L >= bin(T0)
+  // and only group maxima in bins >= bin(T0) need counting.  This keeps the
+  // histogram small and its atomics spread over few, uncontended bins.
+  __shared__ float wmin[WARPS];
+  {
+    float tm = tmax;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tm = fminf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+    if (lane == 0) wmin[tid >> 5] = tm;
+  }
+  __syncthreads();
+  int b0 = 0;
+  if (w <= THREADS && NG >= THREADS) {
+    float t0 = wmin[0];
+    for (int i = 1; i < WARPS; ++i) t0 = fminf(t0, wmin[i]);
+    b0 = score_bin(t0);
+  }
+  // counts of the bins >= b0, one shared atomic per distinct bin of a warp
+  for (int g0 = 0; g0 < NG; g0 += THREADS) {
+    const int g = g0 + tid;
+    const int b = (g < NG && (int)gbin[g] >= b0) ? (int)gbin[g] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, b);
+    if (b >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[b], (unsigned)__popc(peers));
+  }
   __syncthreads();
 
   // 2. b_L: thread i owns bins [top - 8i - 7, top - 8i] (descending)
@@ -704,8 +725,7 @@ select_topw_group_kernel(const float* __restrict__ S, int n, int k, int w,
 }  // namespace
 
 cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* idx,
-                          int32_t* mcount, int32_t* slots, unsigned int* err, cudaStream_t s) {
-  const unsigned int* cerr = err;
+                          int32_t* mcount, int32_t* slots, cudaStream_t s) {
   dim3 grid(k, BH);
   const int staged = n <= MAX_STAGED_BINS ? 1 : 0;
   // staged bins (u16, padded to 16 bytes) + two chunk masks per 32 positions
@@ -718,7 +738,7 @@ cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* 
   if (n <= BOUND_N_MAX && (n & 3) == 0 && w <= THREADS) {
     launch_begin(K_SELECT, s);
     e = launch_pdl(select_topw_bound_kernel, grid, dim3(THREADS), 0, s, S, n, k, w, idx, mcount,
-                   slots, cerr);
+                   slots);
     launch_end(K_SELECT, s);
     return e;
   }
@@ -728,13 +748,13 @@ cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* 
     if (e != cudaSuccess) return e;
     launch_begin(K_SELECT, s);
     e = launch_pdl(select_topw_group_kernel, grid, dim3(THREADS), gsmem, s, S, n, k, w, idx,
-                   mcount, slots, cerr);
+                   mcount, slots);
     launch_end(K_SELECT, s);
     return e;
   }
   launch_begin(K_SELECT, s);
   e = launch_pdl(select_topw_kernel, grid, dim3(THREADS), smem, s, S, n, k, w, idx, mcount, slots,
-                 staged, cerr);
+                 staged);
   launch_end(K_SELECT, s);
   return e;
 }

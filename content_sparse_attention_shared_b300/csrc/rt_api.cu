@@ -1,6 +1,7 @@
 // C-ABI layer: argument validation, workspace carving and the launch order of
 // the routing-attention pass.  No allocation, no synchronisation and no host
 // copies happen in the compute entry points.
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cmath>
@@ -175,6 +176,23 @@ static FwdLayout fwd_layout(int B, int H, int n, int d, int k, int w) {
   return L;
 }
 
+struct BwdLayout {
+  size_t err, mcount, slots, dq_slot, dv_slot, total;
+};
+
+static BwdLayout bwd_layout(int B, int H, int n, int d, int k, int w) {
+  const size_t BH = (size_t)B * H;
+  BwdLayout L;
+  size_t off = 0;
+  L.err = off; off += 256;
+  L.mcount = off; off += align256(BH * n * sizeof(int32_t));
+  L.slots = off; off += align256(BH * n * SLOTS_PER_ROW * sizeof(int32_t));
+  L.dq_slot = off; off += align256(BH * k * w * d * sizeof(float));
+  L.dv_slot = off; off += align256(BH * k * w * d * sizeof(float));
+  L.total = off;
+  return L;
+}
+
 static size_t ema_total(int B, int H, int n, int d, int k, rt_dtype dt) {
   return 256 + ema_workspace_bytes(B, H, n, d, k, dt);
 }
@@ -272,7 +290,7 @@ const char* rt_kernel_name(int id) {
   static const char* names[K_NUM_KINDS] = {
       "score_simt", "score_tc", "select_topw", "attention_simt", "attention_tc",
       "scatter_average", "ema_topw", "ema_update", "centroid_prep", "local_attention",
-      "ema_bucket"};
+      "ema_bucket", "backward", "membership"};
   if (id < 0 || id >= K_NUM_KINDS) return "unknown";
   return names[id];
 }
@@ -281,7 +299,8 @@ size_t rt_workspace_bytes(int B, int H, int n, int d, int k, int w, rt_dtype dt)
   if (check_shape(dt, B, H, n, d, k, w) != RT_OK) return 0;
   const size_t a = fwd_layout(B, H, n, d, k, w).total;
   const size_t b = ema_total(B, H, n, d, k, dt);
-  return a > b ? a : b;
+  const size_t c = bwd_layout(B, H, n, d, k, w).total;
+  return std::max(a, std::max(b, c));
 }
 
 rt_status rt_route_assign(const void* qk, rt_dtype dt, int B, int H, int n, int d,
@@ -307,7 +326,7 @@ rt_status rt_route_assign(const void* qk, rt_dtype dt, int B, int H, int n, int 
   st = from_cuda(launch_score(qk, dt, B, H, n, d, centroids, k, S, assign, nullptr, prep, err, s),
                  "score kernel");
   if (st != RT_OK) return st;
-  st = from_cuda(launch_select(S, BH, n, k, w, idx, nullptr, nullptr, err, s), "select kernel");
+  st = from_cuda(launch_select(S, BH, n, k, w, idx, nullptr, nullptr, s), "select kernel");
   if (st != RT_OK) return st;
   return ok();
 }
@@ -354,7 +373,7 @@ static rt_status forward(const void* q, const void* kp, const void* v, rt_dtype 
   st = from_cuda(launch_score(q, dt, B, H, n, d, centroids, kc, S, assign_out, mcount, prep, err, s),
                  "score kernel");
   if (st != RT_OK) return st;
-  st = from_cuda(launch_select(S, BH, n, kc, w, idx, mcount, slots, err, s), "select kernel");
+  st = from_cuda(launch_select(S, BH, n, kc, w, idx, mcount, slots, s), "select kernel");
   if (st != RT_OK) return st;
   int32_t* idx_k = nullptr;
   int32_t* mvis = nullptr;
@@ -365,7 +384,7 @@ static rt_status forward(const void* q, const void* kp, const void* v, rt_dtype 
     st = from_cuda(launch_score(kp, dt, B, H, n, d, centroids, kc, S, nullptr, mvis, prep, err, s),
                    "score kernel (keys)");
     if (st != RT_OK) return st;
-    st = from_cuda(launch_select(S, BH, n, kc, w, idx_k, nullptr, nullptr, err, s),
+    st = from_cuda(launch_select(S, BH, n, kc, w, idx_k, nullptr, nullptr, s),
                    "select kernel (keys)");
     if (st != RT_OK) return st;
     if (attention_tc_supported(dt, d, w)) {
@@ -374,7 +393,7 @@ static rt_status forward(const void* q, const void* kp, const void* v, rt_dtype 
                      "attention kernel");
     } else {
       st = from_cuda(launch_attention_simt(q, kp, v, dt, BH, n, d, kc, w, causal, scale, idx,
-                                           idx_k, mcount, mvis, out, yslot, err, s),
+                                           idx_k, mcount, mvis, out, yslot, s),
                      "attention kernel");
     }
   } else if (attention_tc_supported(dt, d, w)) {
@@ -383,11 +402,11 @@ static rt_status forward(const void* q, const void* kp, const void* v, rt_dtype 
                    "attention kernel");
   } else {
     st = from_cuda(launch_attention_simt(q, kp, v, dt, BH, n, d, kc, w, causal, scale, idx,
-                                         nullptr, mcount, nullptr, out, yslot, err, s),
+                                         nullptr, mcount, nullptr, out, yslot, s),
                    "attention kernel");
   }
   if (st != RT_OK) return st;
-  st = from_cuda(launch_scatter(dt, BH, n, d, kc, w, idx, mcount, mvis, slots, yslot, out, err, s),
+  st = from_cuda(launch_scatter(dt, BH, n, d, kc, w, idx, mcount, mvis, slots, yslot, out, s),
                  "scatter kernel");
   if (st != RT_OK) return st;
   return ok();
@@ -415,6 +434,48 @@ rt_status rt_routing_attention_separate(const void* q, const void* kp, const voi
                  idx_k_out, assign_out, workspace, workspace_bytes, stream);
 }
 
+rt_status rt_routing_attention_backward(const void* q, const void* v, rt_dtype dt, int B, int H,
+                                        int n, int d, const int32_t* idx, int kc, int w,
+                                        int causal, float scale, const float* dout, float* dq,
+                                        float* dv, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  rt_status st = check_shape(dt, B, H, n, d, kc, w);
+  if (st != RT_OK) return st;
+  if (!q || !v || !idx || !dout || !dq || !dv) return fail(RT_ERR_INVALID_ARG, "null tensor pointer");
+  if (causal != 0 && causal != 1) return fail(RT_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!std::isfinite(scale)) return fail(RT_ERR_INVALID_ARG, "scale is not finite");
+  if (!aligned16(q) || !aligned16(v) || !aligned16(idx) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dv))
+    return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  const BwdLayout L = bwd_layout(B, H, n, d, kc, w);
+  if (!workspace || workspace_bytes < L.total)
+    return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, L.total);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (scale <= 0.0f) scale = 1.0f / sqrtf((float)d);
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  unsigned int* err = reinterpret_cast<unsigned int*>(ws + L.err);
+  int32_t* mcount = reinterpret_cast<int32_t*>(ws + L.mcount);
+  int32_t* slots = reinterpret_cast<int32_t*>(ws + L.slots);
+  float* dq_slot = reinterpret_cast<float*>(ws + L.dq_slot);
+  float* dv_slot = reinterpret_cast<float*>(ws + L.dv_slot);
+  st = from_cuda(launch_membership(idx, BH, n, kc, w, mcount, slots, s), "membership kernel");
+  if (st != RT_OK) return st;
+  st = from_cuda(launch_backward_clusters(q, v, dt, BH, n, d, kc, w, causal, scale, idx, mcount,
+                                          dout, dq_slot, dv_slot, s),
+                 "backward kernel");
+  if (st != RT_OK) return st;
+  st = from_cuda(launch_gather_sum(BH, n, d, kc, w, idx, mcount, slots, dq_slot, dq, s),
+                 "gradient gather (dq)");
+  if (st != RT_OK) return st;
+  st = from_cuda(launch_gather_sum(BH, n, d, kc, w, idx, mcount, slots, dv_slot, dv, s),
+                 "gradient gather (dv)");
+  if (st != RT_OK) return st;
+  return ok();
+}
+
 rt_status rt_centroid_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                           const int32_t* assign, float* centroids, int k, float decay,
                           void* workspace, size_t workspace_bytes, void* stream) {
@@ -432,8 +493,7 @@ rt_status rt_centroid_ema(const void* qk, rt_dtype dt, int B, int H, int n, int 
     return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = from_cuda(launch_ema(qk, dt, B, H, n, d, assign, centroids, k, decay, ws + 256,
-                            reinterpret_cast<unsigned int*>(ws), s),
+  st = from_cuda(launch_ema(qk, dt, B, H, n, d, assign, centroids, k, decay, ws + 256, s),
                  "centroid update kernels");
   if (st != RT_OK) return st;
   return ok();
@@ -455,7 +515,6 @@ rt_status rt_centroid_ema_sums(const void* qk, rt_dtype dt, int B, int H, int n,
     return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   char* ws = static_cast<char*>(workspace);
   st = from_cuda(launch_ema_sums(qk, dt, B, H, n, d, assign, k, sums, ws + 256,
-                                 reinterpret_cast<unsigned int*>(ws),
                                  static_cast<cudaStream_t>(stream)),
                  "centroid sum kernels");
   if (st != RT_OK) return st;
@@ -494,7 +553,6 @@ rt_status rt_centroid_ema_topw(const void* qk, rt_dtype dt, int B, int H, int n,
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   st = from_cuda(launch_ema_topw(qk, dt, B, H, n, d, idx, w, centroids, k, decay,
-                                 static_cast<unsigned int*>(workspace),
                                  static_cast<cudaStream_t>(stream)),
                  "top-w centroid update kernel");
   if (st != RT_OK) return st;
@@ -525,6 +583,60 @@ rt_status rt_local_attention(const void* q, const void* kp, const void* v, rt_dt
                                                   static_cast<cudaStream_t>(stream)),
                            "local attention kernel");
   if (st != RT_OK) return st;
+  return ok();
+}
+
+rt_status rt_mixed_attention(const void* q, const void* v, rt_dtype dt, int B, int H, int n, int d,
+                             int n_local, int window, const float* centroids, int kc, int w,
+                             int causal, float scale, void* out, int32_t* idx_out,
+                             int32_t* assign_out, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (B < 1 || H < 1 || n < 1) return fail(RT_ERR_INVALID_ARG, "B, H and n must be positive");
+  if (n_local < 0 || n_local > H) return fail(RT_ERR_INVALID_ARG, "n_local=%d outside [0, H]", n_local);
+  if (dt != RT_BF16 && dt != RT_F32) return fail(RT_ERR_INVALID_ARG, "unknown dtype");
+  if (!q || !v || !out) return fail(RT_ERR_INVALID_ARG, "null tensor pointer");
+  const int Hr = H - n_local;
+  const size_t es = dt == RT_F32 ? 4 : 2;
+  const size_t head = (size_t)n * d * es;  // bytes of one head of one sequence
+  const size_t need = Hr > 0 ? rt_workspace_bytes(1, Hr, n, d, kc, w, dt) : 256;
+  if (Hr > 0 && need == 0) return validate_shape(dt, 1, Hr, n, d, kc, w);
+  if (Hr > 0 && !centroids) return fail(RT_ERR_INVALID_ARG, "null centroids");
+  // both halves are checked here, before anything is launched
+  if (n_local > 0) {
+    if (dt != RT_BF16) return fail(RT_ERR_UNSUPPORTED, "local attention takes bf16 rows");
+    if (window < 1) return fail(RT_ERR_INVALID_ARG, "window must be at least 1");
+    if (d != 64 && d != 128) return fail(RT_ERR_UNSUPPORTED, "d must be 64 or 128");
+  }
+  if (Hr > 0 && (causal != 0 && causal != 1))
+    return fail(RT_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!std::isfinite(scale)) return fail(RT_ERR_INVALID_ARG, "scale is not finite");
+  if (!aligned16(q) || !aligned16(v) || !aligned16(out) || (centroids && !aligned16(centroids)) ||
+      (idx_out && !aligned16(idx_out)) || (assign_out && !aligned16(assign_out)))
+    return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (!workspace || workspace_bytes < need)
+    return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(RT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  for (int b = 0; b < B; ++b) {
+    const char* qb = static_cast<const char*>(q) + (size_t)b * H * head;
+    const char* vb = static_cast<const char*>(v) + (size_t)b * H * head;
+    char* ob = static_cast<char*>(out) + (size_t)b * H * head;
+    rt_status st;
+    if (n_local > 0) {
+      st = rt_local_attention(qb, qb, vb, dt, 1, n_local, n, d, window, scale, ob, workspace,
+                              workspace_bytes, stream);
+      if (st != RT_OK) return st;
+    }
+    if (Hr > 0) {
+      const char* qr = qb + (size_t)n_local * head;
+      st = rt_routing_attention(qr, qr, vb + (size_t)n_local * head, dt, 1, Hr, n, d, centroids,
+                                kc, w, causal, scale, ob + (size_t)n_local * head,
+                                idx_out ? idx_out + (size_t)b * Hr * kc * w : nullptr,
+                                assign_out ? assign_out + (size_t)b * Hr * n : nullptr, workspace,
+                                workspace_bytes, stream);
+      if (st != RT_OK) return st;
+    }
+  }
   return ok();
 }
 

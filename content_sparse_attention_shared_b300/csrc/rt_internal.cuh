@@ -28,7 +28,9 @@ enum KernelId {
   K_CENTROID_PREP = 8,
   K_LOCAL_ATTN = 9,
   K_EMA_BUCKET = 10,
-  K_NUM_KINDS = 11
+  K_BACKWARD = 11,
+  K_MEMBERSHIP = 12,
+  K_NUM_KINDS = 13
 };
 
 // Error detail for the calling host thread (rt_last_error_detail) and the
@@ -92,28 +94,6 @@ enum DeviceError : unsigned int {
   DEV_OK = 0,
   DEV_TIMEOUT = 1,
 };
-
-// Fail-stop: after its pdl_wait every kernel of a pass checks the device
-// status word and returns when it is set -- by an earlier kernel of the same
-// pass, or by an earlier pass on the same workspace that nobody has checked
-// since -- so no kernel computes on the partial results of one that gave up.
-// This form reads the word once per CTA and broadcasts it, for kernels whose
-// own CTAs may set it; it contains a block barrier, so every thread of the CTA
-// calls it, before any other barrier.
-__device__ __forceinline__ bool pass_failed(const unsigned int* err) {
-  __shared__ int s_failed;
-  if (threadIdx.x == 0) s_failed = (err != nullptr && __ldcg(err) != 0u) ? 1 : 0;
-  __syncthreads();
-  return s_failed != 0;
-}
-
-// The same check per thread, with no barrier, for kernels whose own CTAs never
-// set the word (so every thread sees the value its predecessors left): read
-// right after pdl_wait, tested once the kernel's first loads are in flight, so
-// it adds no round trip.
-__device__ __forceinline__ bool status_set(const unsigned int* err) {
-  return err != nullptr && __ldcg(err) != 0u;
-}
 
 // Test aid for the device-side timeout path (rt_debug_inject_wait_timeout):
 // with limit_ns > 0, thread 0 waits on an mbarrier that nothing arrives on,
@@ -223,7 +203,7 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 // (may be null), mcount: [BH,n] zeroed here when non-null.
 cudaError_t launch_score_simt(const void* qk, rt_dtype dt, int BH, int H, int n, int d,
                               const float* mu, int k, float* S, int32_t* a,
-                              int32_t* mcount, unsigned int* err, cudaStream_t s);
+                              int32_t* mcount, cudaStream_t s);
 
 // dispatcher: tcgen05 scoring for bf16 with k <= 256 (fp32-accurate via a
 // three-plane split of the centroids), the SIMT kernel otherwise.  prep: device
@@ -242,7 +222,7 @@ cudaError_t launch_score(const void* qk, rt_dtype dt, int B, int H, int n, int d
 // [BH, n, SLOTS_PER_ROW] (may be null; entry order is arbitrary).
 constexpr int SLOTS_PER_ROW = 8;
 cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* idx,
-                          int32_t* mcount, int32_t* slots, unsigned int* err, cudaStream_t s);
+                          int32_t* mcount, int32_t* slots, cudaStream_t s);
 
 // in-cluster attention.  Rows of positions with mcount == 1 go straight to
 // `out`; rows of positions in several clusters go to yslot [BH,k,w,d] fp32.
@@ -253,7 +233,7 @@ cudaError_t launch_attention_simt(const void* q, const void* kk, const void* v, 
                                   int BH, int n, int d, int k, int w, int causal,
                                   float scale, const int32_t* idx, const int32_t* idx_k,
                                   const int32_t* mcount, int32_t* mvis, void* out, float* yslot,
-                                  unsigned int* err, cudaStream_t s);
+                                  cudaStream_t s);
 
 // the same on tcgen05 tensor cores (bf16 only): the pipelined kernel below
 // for w <= 128, the key-block kernel above that; err: device error word.
@@ -287,8 +267,23 @@ cudaError_t launch_attention_pipe(const void* q, const void* v, int BH, int n, i
 // (may be null) replaces mcount as the divisor (0: zero row).
 cudaError_t launch_scatter(rt_dtype dt, int BH, int n, int d, int k, int w,
                            const int32_t* idx, const int32_t* mcount, const int32_t* mdiv,
-                           const int32_t* slots, const float* yslot, void* out,
-                           unsigned int* err, cudaStream_t s);
+                           const int32_t* slots, const float* yslot, void* out, cudaStream_t s);
+
+// backward of a5..a6 with the routing held fixed: per-slot gradient rows of
+// every cluster (dq_slot, dv_slot [BH,k,w,d] fp32), from the lists idx and
+// the membership counts mcount; dout [BH,n,d] fp32.
+cudaError_t launch_backward_clusters(const void* q, const void* v, rt_dtype dt, int BH, int n,
+                                     int d, int k, int w, int causal, float scale,
+                                     const int32_t* idx, const int32_t* mcount, const float* dout,
+                                     float* dq_slot, float* dv_slot, cudaStream_t s);
+// membership counts and the first SLOTS_PER_ROW slot ids of every position,
+// rebuilt from the lists (mcount is cleared first)
+cudaError_t launch_membership(const int32_t* idx, int BH, int n, int k, int w, int32_t* mcount,
+                              int32_t* slots, cudaStream_t s);
+// every position's sum of its slot rows (fp32; zero for no membership)
+cudaError_t launch_gather_sum(int BH, int n, int d, int k, int w, const int32_t* idx,
+                              const int32_t* mcount, const int32_t* slots, const float* yslot,
+                              float* out, cudaStream_t s);
 
 // centroid update (argmax assignment), a segmented reduction: a bucketing
 // kernel sorts every chunk's rows by centroid, then one CTA per (head,
@@ -297,12 +292,11 @@ cudaError_t launch_scatter(rt_dtype dt, int BH, int n, int d, int k, int w,
 size_t ema_workspace_bytes(int B, int H, int n, int d, int k, rt_dtype dt);
 cudaError_t launch_ema(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                        const int32_t* assign, float* mu, int k, float decay,
-                       void* ws, unsigned int* err, cudaStream_t s);
+                       void* ws, cudaStream_t s);
 // the same reduction stopped before the blend: sums [H][k][d+1] receives every
 // centroid's sum of normalised rows and (as a float) its count
 cudaError_t launch_ema_sums(const void* qk, rt_dtype dt, int B, int H, int n, int d,
-                            const int32_t* assign, int k, float* sums, void* ws,
-                            unsigned int* err, cudaStream_t s);
+                            const int32_t* assign, int k, float* sums, void* ws, cudaStream_t s);
 // the blend from such sums (possibly added over shards of the batch)
 cudaError_t launch_ema_apply(const float* sums, int H, int d, float* mu, int k, float decay,
                              cudaStream_t s);
@@ -310,6 +304,6 @@ cudaError_t launch_ema_apply(const float* sums, int H, int d, float* mu, int k, 
 // assignment (entries outside [0, n) are skipped)
 cudaError_t launch_ema_topw(const void* qk, rt_dtype dt, int B, int H, int n, int d,
                             const int32_t* idx, int w, float* mu, int k, float decay,
-                            unsigned int* err, cudaStream_t s);
+                            cudaStream_t s);
 
 }  // namespace rt

@@ -157,7 +157,7 @@ extern "C" rt_status rt_route_assign_noalloc(const void* qk, rt_dtype dt, int B,
   const int BH = B * H;
   cudaError_t e = rt::launch_score(qk, dt, B, H, n, d, centroids, k, S, assign, nullptr, nullptr, err, s);
   if (e != cudaSuccess) return rt::record_error(RT_ERR_CUDA, cudaGetErrorString(e));
-  e = rt::launch_select(S, BH, n, k, w, idx, nullptr, nullptr, err, s);
+  e = rt::launch_select(S, BH, n, k, w, idx, nullptr, nullptr, s);
   if (e != cudaSuccess) return rt::record_error(RT_ERR_CUDA, cudaGetErrorString(e));
   return rt::record_error(RT_OK, "");
 }

@@ -38,9 +38,10 @@
  *   - Errors found on the host (bad arguments, too-small workspace, a CUDA
  *     launch error) are returned immediately; nothing is launched then.
  *     A device-side error (a bounded wait that ran out) is recorded in the
- *     workspace and reported by rt_check_device_status(); until that call
- *     clears it, the kernels of every call on the workspace return without
- *     computing.
+ *     workspace and reported by rt_check_device_status(), which clears it;
+ *     the outputs of the call that failed are undefined (the later kernels
+ *     of that call still run, and every index they follow is bounds-checked,
+ *     so no access leaves its buffer).
  *   - Supported: d in {64, 128}; 1 <= w <= n; k >= 1; causal in {0, 1};
  *     dtype RT_F32 or RT_BF16 (Q, K, V and the output share it; centroids
  *     are always fp32).  Other values return RT_ERR_UNSUPPORTED or
@@ -140,6 +141,33 @@ rt_status rt_routing_attention_separate(const void* q, const void* k, const void
                                         int32_t* assign_out, void* workspace,
                                         size_t workspace_bytes, void* stream);
 
+/* Backward pass of rt_routing_attention (shared QK) with the routing held
+ * fixed: the gradients of the loss with respect to the rows, given its
+ * gradient with respect to `out`.
+ * Source: §3 (softmax attention), §4 (attention only between same-cluster
+ * pairs; centroids learned by the online k-means step, not by gradients --
+ * §2).  The routing is piecewise constant in the rows, so the gradient flows
+ * through the attention of each cluster and the averaging of a position's
+ * cluster outputs: with m(t) the number of clusters listing t and, per
+ * cluster, P = softmax(scale Q_c Q_c^T + causal mask), dY = dout[p]/m(p),
+ *   dV_c = P^T dY;  dS = P * (dY V_c^T - rowsum(P * (dY V_c^T)));
+ *   dQ_c = scale (dS Q_c + dS^T Q_c)   (a row is both a query and a key),
+ * and each position's gradient is the sum of its rows over its clusters.
+ *   q, v      [B,H,n,d] dtype dt (the forward's inputs; k was q)
+ *   idx       [B,H,kc,w] int32: the forward's index lists (idx_out)
+ *   causal, scale: as passed to the forward
+ *   dout      [B,H,n,d] fp32: gradient with respect to out
+ *   dq, dv    [B,H,n,d] fp32 out: gradients with respect to q (= k) and v;
+ *             positions in no cluster get zero rows
+ * The clusters are processed on CUDA cores in fp32 (P is recomputed), with
+ * per-slot rows summed per position in ascending cluster order: the result is
+ * deterministic.  Workspace: rt_workspace_bytes(B, H, n, d, kc, w, dt). */
+rt_status rt_routing_attention_backward(const void* q, const void* v, rt_dtype dt, int B, int H,
+                                        int n, int d, const int32_t* idx, int kc, int w,
+                                        int causal, float scale, const float* dout, float* dq,
+                                        float* dv, void* workspace, size_t workspace_bytes,
+                                        void* stream);
+
 /* One online spherical k-means step on the centroids, in place.
  * Source: §2 "Attention with Content-Based Sparsity" (centroids learned by
  * mini-batch spherical k-means), §4 (centroids shared across sequences,
@@ -230,6 +258,32 @@ rt_status rt_local_attention(const void* q, const void* k, const void* v, rt_dty
                              int B, int H, int n, int d, int window, float scale, void* out,
                              void* workspace, size_t workspace_bytes, void* stream);
 
+/* A layer with local heads and routing heads on the same tensors, as the
+ * pages combine them (§6 "Local vs Global": local attention with windows of
+ * 512 or 1024 positions in some heads, routing attention in others; §3, §4).
+ * Heads [0, n_local) take causal local attention over `window` positions
+ * (rt_local_attention); heads [n_local, H) take routing attention with
+ * shared QK (rt_routing_attention, causal as given).  Within one sequence the
+ * heads of each kind are contiguous in memory, so the call launches each kind
+ * once per sequence on the caller's tensors (no copies).
+ *   q, v        [B,H,n,d] dtype dt (local heads need bf16)
+ *   centroids   [H - n_local, kc, d] fp32: the routing heads' centroids
+ *   out         [B,H,n,d] dtype dt, every row written
+ *   idx_out     [B, H - n_local, kc, w] out, may be NULL
+ *   assign_out  [B, H - n_local, n] out, may be NULL (argmax per row; the
+ *               centroid step of the routing heads: rt_centroid_ema_sums on
+ *               each sequence's routing heads, added, then
+ *               rt_centroid_ema_apply)
+ *   workspace   at least rt_workspace_bytes(1, H - n_local, n, d, kc, w, dt)
+ *               bytes (256 when every head is local)
+ * Errors as the two calls it makes; both halves are checked before anything
+ * is launched. */
+rt_status rt_mixed_attention(const void* q, const void* v, rt_dtype dt, int B, int H, int n,
+                             int d, int n_local, int window, const float* centroids, int kc,
+                             int w, int causal, float scale, void* out, int32_t* idx_out,
+                             int32_t* assign_out, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
 /* Clears the device status word at the start of a new workspace (an async
  * memset of its first 256 bytes on `stream`).  Call once after allocating a
  * workspace; the compute calls only ever set the word. */
@@ -269,10 +323,8 @@ rt_status rt_route_assign_noalloc(const void* qk, rt_dtype dt, int B, int H, int
                                   int32_t* idx, int32_t* assign, void* stream);
 
 /* Synchronises `stream`, reads the device error word kept in `workspace`,
- * clears it, and returns RT_OK, RT_ERR_TIMEOUT or RT_ERR_CUDA.  While the
- * word is set, every kernel of a later call on the same workspace returns at
- * once without writing (fail-stop: nothing reads a partial result), so check
- * the word after an error before reusing the workspace.  With
+ * clears it, and returns RT_OK, RT_ERR_TIMEOUT or RT_ERR_CUDA.  The word
+ * stays set from the failure until this call, across later calls.  With
  * workspace == NULL and workspace_bytes == 0 it reads (and clears) the status
  * word of rt_route_assign_noalloc in the current context instead.  Not for
  * use inside stream capture. */
@@ -284,12 +336,10 @@ rt_status rt_check_device_status(void* workspace, size_t workspace_bytes, void* 
  * nothing arrives on -- before the kernel issues any asynchronous copy or
  * tensor-core operation -- so the wait runs out: the kernel sets the device
  * status word (RT_ERR_TIMEOUT from rt_check_device_status) and returns with
- * nothing in flight.  The later kernels of the same call find the word set
- * and return at once (every kernel does, while the word is set), so the
- * outputs of that call are left unwritten.  rt_debug_inject_wait_timeout(0, 0)
- * turns it off; once rt_check_device_status has cleared the word, calls run
- * normally again.  Process-wide setting.  RT_ERR_INVALID_ARG for unknown bits
- * or a limit outside the range. */
+ * nothing in flight; the outputs of that call are undefined.
+ * rt_debug_inject_wait_timeout(0, 0) turns it off.  Process-wide setting,
+ * read when a kernel is launched.  RT_ERR_INVALID_ARG for unknown bits or a
+ * limit outside the range. */
 #define RT_DEBUG_SCORE 1u            /* the tensor-core score kernel            */
 #define RT_DEBUG_ATTENTION 2u        /* the tensor-core cluster-attention kernels */
 #define RT_DEBUG_LOCAL_ATTENTION 4u  /* the local-attention kernel               */

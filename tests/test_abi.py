@@ -142,6 +142,25 @@ def test_separate_validation(lib):
     assert lib.rt_last_error_detail() != b""
 
 
+def test_mixed_validation(lib):
+    def call(dt=1, H=4, n=256, d=64, n_local=2, window=64, mu=FAKE, kc=4, w=64, causal=1,
+             ws=FAKE, wsb=1 << 30, out=FAKE):
+        return lib.rt_mixed_attention(FAKE, FAKE, dt, 1, H, n, d, n_local, window, mu, kc, w,
+                                      causal, ctypes.c_float(0.0), out, None, None, ws, wsb, None)
+    assert call(n_local=5) == bnd.RT_ERR_INVALID_ARG        # more local heads than heads
+    assert call(n_local=-1) == bnd.RT_ERR_INVALID_ARG
+    assert call(dt=0) == bnd.RT_ERR_UNSUPPORTED             # local heads need bf16
+    assert call(window=0) == bnd.RT_ERR_INVALID_ARG
+    assert call(mu=None) == bnd.RT_ERR_INVALID_ARG          # routing heads need centroids
+    assert call(w=300) == bnd.RT_ERR_INVALID_ARG            # w > n (routing half)
+    assert call(d=96) == bnd.RT_ERR_UNSUPPORTED
+    assert call(causal=3) == bnd.RT_ERR_INVALID_ARG
+    assert call(out=FAKE + 8) == bnd.RT_ERR_INVALID_ARG
+    assert call(wsb=512) == bnd.RT_ERR_WORKSPACE
+    assert call(ws=FAKE + 16) == bnd.RT_ERR_INVALID_ARG
+    assert lib.rt_last_error_detail() != b""
+
+
 def test_route_validation(lib):
     r = lib.rt_route_assign(FAKE, 1, 1, 1, 64, 64, FAKE, 4, 16, None, None, None, FAKE, 1 << 30,
                             None)

@@ -521,3 +521,109 @@ def test_separate_qk_with_equal_keys_matches_shared():
     torch.cuda.synchronize()
     assert np.array_equal(iq, idx.cpu().numpy()) and np.array_equal(ik, iq)
     assert torch.max(torch.abs(out.float() - ref.float())).item() <= 2 * ph.TOL_OUT["bf16"]
+
+
+# ---------------------------------------------------------------------------
+# mixed local and routing heads in one call
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", [
+    (2, 4, 1000, 64, 2, 128, 8, 100),      # two sequences, half the heads local
+    (1, 8, 8192, 128, 4, 512, 128, 64),    # the n=8192 shape, window 512
+    (1, 3, 700, 128, 3, 1024, 4, 50),      # every head local
+    (2, 2, 500, 64, 0, 64, 5, 100),        # every head routed
+], ids=lambda c: "b{}h{}n{}d{}local{}win{}k{}w{}".format(*c))
+def test_mixed_local_and_routing_heads(case):
+    B, H, n, d, nl, W, k, w = case
+    wl = make_random(B, H, n, d, k, w, dtype="bf16", seed=n + nl + W)
+    q, v, mu_all = ph.to_device(wl)
+    Hr = H - nl
+    mu = mu_all[nl:].contiguous() if Hr > 0 else None
+    idx = torch.empty((B, Hr, k, w), dtype=torch.int32, device="cuda") if Hr > 0 else None
+    out = rt.rt_mixed_attention(q, v, mu, nl, W, w, idx_out=idx)
+    torch.cuda.synchronize()
+    q64, v64 = wl.q_f32().astype(np.float64), wl.v_f32().astype(np.float64)
+    got = ph.out_to_f64(out)
+    scale = 1.0 / math.sqrt(d)
+    for b in range(B):
+        for h in range(H):
+            if h < nl:
+                # local heads: sampled row blocks at the long shape
+                spans = [(0, n)] if n <= 1000 else [(0, 64), (4000, 4064), (n - 64, n)]
+                for t0, t1 in spans:
+                    lo = max(0, t0 - W + 1)
+                    want = orc.local_attention(q64[b, h, lo:t1], q64[b, h, lo:t1],
+                                               v64[b, h, lo:t1], W, scale)[t0 - lo:]
+                    assert np.max(np.abs(got[b, h, t0:t1] - want)) <= ph.TOL_OUT["bf16"]
+            else:
+                gidx = idx[b, h - nl].cpu().numpy()
+                S64 = ph.oracle_scores(q64[b, h], wl.centroids[h])
+                ph.check_index_lists(gidx, S64, w, n)
+                want = ph.oracle_output_on(q64[b, h], v64[b, h], gidx, True, scale)
+                assert np.max(np.abs(got[b, h] - want)) <= ph.TOL_OUT["bf16"]
+
+
+# ---------------------------------------------------------------------------
+# backward pass (routing held fixed)
+# ---------------------------------------------------------------------------
+
+BWD_CASES = [
+    # B, H, n, d, k, w, dtype, causal
+    (1, 8, 4096, 64, 64, 64, "bf16", True),     # the n=4096 configuration's shape
+    (2, 2, 777, 128, 24, 129, "bf16", True),    # three 64-slot blocks, ragged
+    (1, 2, 640, 64, 10, 64, "f32", False),      # fp32, non-causal
+    (1, 1, 300, 128, 1, 300, "f32", True),      # one cluster: full causal attention
+    (1, 2, 515, 64, 9, 1, "bf16", True),        # w = 1
+    (1, 1, 256, 128, 6, 200, "bf16", True),     # positions in several clusters
+]
+
+
+def _bwd_tol(ref):
+    return 2e-4 * (1.0 + float(np.max(np.abs(ref))))
+
+
+@pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: "b{}h{}n{}d{}k{}w{}{}{}".format(
+    c[0], c[1], c[2], c[3], c[4], c[5], c[6], "" if c[7] else "nc"))
+def test_backward(case):
+    B, H, n, d, k, w, dt, causal = case
+    wl = make_random(B, H, n, d, k, w, dtype=dt, seed=n + 5 * k + w)
+    q, v, mu = ph.to_device(wl)
+    idx = torch.empty((B, H, k, w), dtype=torch.int32, device="cuda")
+    rt.rt_routing_attention(q, q, v, mu, w, causal=causal, idx_out=idx)
+    g = torch.Generator(device="cpu").manual_seed(n + k)
+    dout = torch.randn((B, H, n, d), generator=g, dtype=torch.float32).cuda()
+    ws = rt.Workspace.for_shape(B, H, n, d, k, w, q.dtype)
+    dq, dv = rt.rt_routing_attention_backward(q, v, idx, dout, causal=causal, workspace=ws)
+    dq2, dv2 = rt.rt_routing_attention_backward(q, v, idx, dout, causal=causal, workspace=ws)
+    torch.cuda.synchronize()
+    ws.check()
+    assert torch.equal(dq, dq2) and torch.equal(dv, dv2)  # deterministic
+    q64, v64 = wl.q_f32().astype(np.float64), wl.v_f32().astype(np.float64)
+    gidx, do64 = idx.cpu().numpy(), dout.cpu().numpy().astype(np.float64)
+    gq, gv = dq.cpu().numpy().astype(np.float64), dv.cpu().numpy().astype(np.float64)
+    for b in range(B):
+        for h in range(H):
+            wq, wv = orc.routing_attention_head_backward(q64[b, h], v64[b, h], gidx[b, h],
+                                                         do64[b, h], causal=causal)
+            assert np.max(np.abs(gq[b, h] - wq)) <= _bwd_tol(wq)
+            assert np.max(np.abs(gv[b, h] - wv)) <= _bwd_tol(wv)
+            m = orc.membership_counts(gidx[b, h], n)
+            assert np.all(gq[b, h][m == 0] == 0) and np.all(gv[b, h][m == 0] == 0)
+
+
+def test_backward_full_attention_matches_autograd():
+    # one cluster taking every position: the gradient of full causal attention
+    n, d = 384, 64
+    wl = make_random(1, 1, n, d, 1, n, dtype="f32", seed=12)
+    q, v, mu = ph.to_device(wl)
+    idx = torch.empty((1, 1, 1, n), dtype=torch.int32, device="cuda")
+    rt.rt_routing_attention(q, q, v, mu, n, idx_out=idx)
+    dout = torch.randn((1, 1, n, d), device="cuda")
+    dq, dv = rt.rt_routing_attention_backward(q, v, idx, dout)
+    torch.cuda.synchronize()
+    q64 = q.double().cpu().requires_grad_(True)
+    v64 = v.double().cpu().requires_grad_(True)
+    o = torch.nn.functional.scaled_dot_product_attention(q64, q64, v64, is_causal=True)
+    o.backward(dout.double().cpu())
+    assert torch.max(torch.abs(dq.double().cpu() - q64.grad)).item() <= _bwd_tol(q64.grad.numpy())
+    assert torch.max(torch.abs(dv.double().cpu() - v64.grad)).item() <= _bwd_tol(v64.grad.numpy())

@@ -1,16 +1,16 @@
 """The device-side timeout path, exercised without a GPU fault.
 
 Every mbarrier wait in the tensor-core kernels is bounded; when one runs out
-the kernel sets the device status word, gives back what it holds and returns,
-and every later kernel finds the word set and returns too.  This test makes a
-wait run out on purpose with the library's test aid
-(rt_debug_inject_wait_timeout): the selected kernels begin with a bounded
-wait (1 ms) on a barrier that nothing arrives on, before they issue any copy
-or tensor-core operation, so nothing is in flight when they give up.  It then
-checks that the call returned, that rt_check_device_status reports
-RT_ERR_TIMEOUT (and clears the word), that the outputs of the failed call were
-left alone where the fail-stop rule says so, and that the next call is
-correct again.
+the kernel sets the device status word, gives back what it holds and returns.
+The later kernels of the call still run on what they find (every index they
+follow is bounds-checked), so the call's outputs are undefined but no access
+leaves its buffer.  This test makes a wait run out on purpose with the
+library's test aid (rt_debug_inject_wait_timeout): the selected kernels begin
+with a bounded wait (1 ms) on a barrier that nothing arrives on, before they
+issue any copy or tensor-core operation, so nothing is in flight when they
+give up.  It then checks that the call returned, that rt_check_device_status
+reports RT_ERR_TIMEOUT (and clears the word; it stays set until then), and
+that the next call is correct again.
 """
 
 import ctypes
@@ -65,13 +65,8 @@ def test_forward_timeout_reported_and_recoverable(kernels, cid):
     finally:
         rt.rt_debug_inject_wait_timeout(0, 0)
     _expect_timeout(ws)
-    if kernels == bnd.RT_DEBUG_SCORE:
-        # nothing after the score kernel ran: lists and output untouched
-        assert torch.all(idx == -5) and torch.all(out == 7.0)
-    else:
-        # routing ran; the attention gave up and the scatter did nothing
-        assert torch.equal(idx, ref_idx)
-    # fail-stop holds until the word is checked: nothing ran in between, and
+    if kernels == bnd.RT_DEBUG_ATTENTION:
+        assert torch.equal(idx, ref_idx)  # routing ran before the attention gave up
     # the next call computes the same result as before the failure
     out2 = rt.rt_routing_attention(q, q, v, mu, wl.w, workspace=ws)
     torch.cuda.synchronize()
@@ -79,29 +74,26 @@ def test_forward_timeout_reported_and_recoverable(kernels, cid):
     assert torch.equal(out2, ref)
 
 
-def test_failed_pass_stops_later_calls_until_checked():
+def test_status_word_stays_set_until_checked():
+    # calls after a failure, before the check, return normally; the word stays
+    # set, and every later call's result is right again once it is cleared
     wl = make_random(1, 2, 1000, 128, 8, 100, dtype="bf16", seed=3)
     q, v, mu = ph.to_device(wl)
     ws = rt.Workspace.for_shape(wl.B, wl.H, wl.n, wl.d, wl.k, wl.w, q.dtype)
+    ref = rt.rt_routing_attention(q, q, v, mu, wl.w, workspace=ws).clone()
     rt.rt_debug_inject_wait_timeout(bnd.RT_DEBUG_SCORE, LIMIT_NS)
     try:
         rt.rt_routing_attention(q, q, v, mu, wl.w, workspace=ws)
     finally:
         rt.rt_debug_inject_wait_timeout(0, 0)
-    # a second call on the same workspace before the check: every kernel
-    # finds the word set and writes nothing
-    out = torch.full_like(v, 3.0)
-    mu2 = mu.clone()
-    a = torch.zeros((1, 2, 1000), dtype=torch.int32, device="cuda")
-    rt.rt_routing_attention(q, q, v, mu, wl.w, out=out, workspace=ws)
-    rt.rt_centroid_ema(q, a, mu2, 0.0, workspace=ws)
+    out = rt.rt_routing_attention(q, q, v, mu, wl.w, workspace=ws)
     torch.cuda.synchronize()
-    assert torch.all(out == 3.0) and torch.equal(mu2, mu)
-    _expect_timeout(ws)
-    rt.rt_routing_attention(q, q, v, mu, wl.w, out=out, workspace=ws)
+    assert torch.equal(out, ref)  # this call itself ran normally
+    _expect_timeout(ws)           # ... but the earlier failure is still reported
+    out = rt.rt_routing_attention(q, q, v, mu, wl.w, workspace=ws)
     torch.cuda.synchronize()
     ws.check()
-    assert not torch.all(out == 3.0)
+    assert torch.equal(out, ref)
 
 
 def test_local_attention_timeout():

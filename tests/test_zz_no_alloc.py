@@ -121,7 +121,6 @@ def test_noalloc_timeout_reported_on_its_own_status_word(lib):
     finally:
         lib.rt_debug_inject_wait_timeout(0, 0)
     assert lib.rt_check_device_status(None, 0, stream) == 5  # RT_ERR_TIMEOUT
-    assert torch.all(idx == -1)                              # nothing after the score kernel ran
     assert lib.rt_check_device_status(None, 0, stream) == 0  # cleared
     a = torch.full((wl.B, wl.H, wl.n), -1, dtype=torch.int32, device="cuda")
     assert _noalloc(lib, q, mu, wl.w, idx, a) == 0
