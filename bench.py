@@ -502,7 +502,7 @@ class Measured:
     """Device measurements of one workload (the library's tensors stay on the
     GPU until close())."""
 
-    def __init__(self, wl, dev):
+    def __init__(self, wl, dev, fused=False):
         import numpy as np
         import torch
 
@@ -522,6 +522,7 @@ class Measured:
         self.assign = torch.empty((wl.B, wl.H, wl.n), dtype=torch.int32, device=dev)
         self.ws = rt.Workspace.for_shape(wl.B, wl.H, wl.n, wl.d, wl.k, wl.w, self.q.dtype, dev)
         self.rt = rt
+        self.fused = fused
 
     def step(self, qq=None, vv=None):
         # launches go to torch's current stream (the capture stream while a
@@ -529,6 +530,12 @@ class Measured:
         rt, wl = self.rt, self.wl
         qq = self.q if qq is None else qq
         vv = self.v if vv is None else vv
+        if wl.ema and self.fused:
+            # the training-step call: the centroid update overlaps the forward's tail
+            rt.rt_routing_attention_step(qq, vv, self.mu, wl.w, wl.decay, causal=True,
+                                         out=self.out, idx_out=self.idx, assign_out=self.assign,
+                                         workspace=self.ws)
+            return
         rt.rt_routing_attention(qq, qq, vv, self.mu, wl.w, causal=True, out=self.out,
                                 idx_out=self.idx, assign_out=self.assign, workspace=self.ws)
         if wl.ema:
@@ -725,7 +732,7 @@ def run_ours(args, wl_id, wl):
                                      getattr(props, "pci_device_id", 0))
 
     # ---- the headline workload ------------------------------------------
-    m = Measured(wl, dev)
+    m = Measured(wl, dev, fused=args.fused_step)
     m.capture(args.warmup)
     clk = ClockSampler(local, pci)
     t_ms = m.timed(args.steps, flush, stream, world, clocks=clk, soak_ms=args.soak_ms)
@@ -746,7 +753,7 @@ def run_ours(args, wl_id, wl):
             if cid == wl_id:
                 ct, ck = t_ms, kern
             else:
-                cm = Measured(cw, dev)
+                cm = Measured(cw, dev, fused=args.fused_step)
                 cm.capture(args.warmup)
                 ct = cm.timed(csteps, flush, stream, world)
                 ck = cm.kernel_times(csteps, flush)
@@ -803,6 +810,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="measure the headline workload only (no `configs` map)")
+    ap.add_argument("--fused-step", action="store_true",
+                    help="time the step as one rt_routing_attention_step call")
     ap.add_argument("--soak-ms", type=float, default=300.0,
                     help="untimed replays right before the timed region, for the clock record")
     args = ap.parse_args()

@@ -24,5 +24,6 @@ from ._binding import (  # noqa: F401
     rt_routing_attention,
     rt_routing_attention_backward,
     rt_routing_attention_separate,
+    rt_routing_attention_step,
     rt_workspace_bytes,
 )

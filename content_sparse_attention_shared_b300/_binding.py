@@ -28,6 +28,9 @@ SIGNATURES = {
     "rt_routing_attention": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                       _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp, _c_size,
                                       _vp]),
+    "rt_routing_attention_step": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
+                                           _c_int, _c_int, _c_int, _c_float, _c_float, _vp, _vp, _vp,
+                                           _vp, _c_size, _vp]),
     "rt_routing_attention_separate": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                _vp, _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp,
                                                _vp, _vp, _c_size, _vp]),
@@ -194,6 +197,25 @@ def rt_routing_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, H, n, d, _ptr(centroids), kc, w,
         1 if causal else 0, float(scale), _ptr(out), _ptr(idx_out), _ptr(assign_out), ws.ptr,
         ws.nbytes, _stream(stream)))
+    return out
+
+
+def rt_routing_attention_step(q: torch.Tensor, v: torch.Tensor, centroids: torch.Tensor, w: int,
+                              decay: float, causal: bool = True, scale: float = 0.0,
+                              out: Optional[torch.Tensor] = None,
+                              idx_out: Optional[torch.Tensor] = None,
+                              assign_out: Optional[torch.Tensor] = None,
+                              workspace: Optional[Workspace] = None, stream=None) -> torch.Tensor:
+    """Forward pass, then the centroid step on the same rows (centroids in place)."""
+    B, H, n, d = q.shape
+    kc = centroids.shape[1]
+    if out is None:
+        out = torch.empty_like(v)
+    ws = _ws(workspace, B, H, n, d, kc, w, q.dtype, q.device)
+    _check(load_library().rt_routing_attention_step(
+        _ptr(q), _ptr(v), _dtype_code(q), B, H, n, d, _ptr(centroids), kc, w, 1 if causal else 0,
+        float(scale), float(decay), _ptr(out), _ptr(idx_out), _ptr(assign_out), ws.ptr, ws.nbytes,
+        _stream(stream)))
     return out
 
 

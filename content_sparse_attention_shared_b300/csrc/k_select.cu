@@ -65,6 +65,43 @@ struct SelectOut {
         slots[((size_t)bh * n + t) * SLOTS_PER_ROW + prev] = c * w + o;
     }
   }
+  // Emits the positions of the set bits of `word` (bit b = position base + b,
+  // ascending) to output slots o, o + 1, ...; returns the next slot.  The
+  // membership atomics of up to NB positions are issued together, so a
+  // thread with several kept positions waits for one round trip, not one
+  // per position.
+  template <int NB = 8>
+  __device__ __forceinline__ int emit_word(int o, unsigned word, int base) const {
+    while (word != 0u) {
+      int p[NB], prev[NB];
+      int cnt = 0;
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        p[i] = 0;
+        prev[i] = SLOTS_PER_ROW;
+        if (word != 0u) {
+          p[i] = base + __ffs(word) - 1;
+          word &= word - 1u;
+          cnt = i + 1;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        if (i < cnt && o + i < w) {
+          out[o + i] = p[i];
+          if (mcount != nullptr) prev[i] = atomicAdd(&mcount[(size_t)bh * n + p[i]], 1);
+        }
+      }
+      if (slots != nullptr) {
+#pragma unroll
+        for (int i = 0; i < NB; ++i)
+          if (i < cnt && o + i < w && (unsigned)prev[i] < (unsigned)SLOTS_PER_ROW)
+            slots[((size_t)bh * n + p[i]) * SLOTS_PER_ROW + prev[i]] = c * w + o + i;
+      }
+      o += cnt;
+    }
+    return o;
+  }
 };
 
 // Exact fallback: 32-bit MSD radix select on order-preserving keys, reading
@@ -316,14 +353,7 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
     const unsigned km = (q < nq) ? hmask[q] : 0u;
     int total;
     const int ex = block_exclusive_scan<THREADS>(__popc(km), wsum, total);
-    unsigned rem = km;
-    int o = carry + ex;
-    while (rem) {
-      const int b = __ffs(rem) - 1;
-      rem &= rem - 1;
-      if (o < w) so.emit(o, q * 32 + b);
-      ++o;
-    }
+    so.emit_word(carry + ex, km, q * 32);
     carry += total;
   }
 }
@@ -499,9 +529,8 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
   {
     const unsigned km = kept[tid];
     int total;
-    int o = block_exclusive_scan<THREADS>(__popc(km), wsum, total);
-    for (unsigned rem = km; rem != 0u; rem &= rem - 1u, ++o)
-      if (o < w) so.emit(o, tid * 32 + __ffs(rem) - 1);
+    const int o = block_exclusive_scan<THREADS>(__popc(km), wsum, total);
+    so.emit_word<4>(o, km, tid * 32);
   }
 }
 
@@ -520,11 +549,14 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
 //      that large, so every kept score lies in a bin >= b_L (a block scan of
 //      the histogram from the top bin down);
 //   3. only the groups whose maximum reaches b_L are read again (from L2,
-//      right after the first pass); their scores of bin >= b_L become the
+//      right after the first pass): they are listed first, then read one per
+//      thread with every load in flight; their scores of bin >= b_L become the
 //      candidates (typically a few more than w), packed as 64-bit keys (score
 //      key, complemented position), appended with one shared atomic per warp;
 //   4. a candidate is kept when fewer than w candidate keys exceed its own;
-//      kept positions go into a position bitmap;
+//      when fewer than w scores lie above the boundary bin (the usual case)
+//      those are all kept and only the boundary bin's few candidates are
+//      ranked, among themselves; kept positions go into a position bitmap;
 //   5. a block scan over the bitmap words (consecutive words per thread) puts
 //      them out in ascending order.
 // Rows where fewer than w groups exist or the bound leaves more than GCAP
@@ -538,7 +570,8 @@ constexpr int GROUP_N_MAX = 262144;
 
 inline size_t group_smem_bytes(int n) {
   const size_t ng = (size_t)(n + GSIZE - 1) / GSIZE, nw = (size_t)(n + 31) / 32;
-  return ((ng * 2 + 15) & ~(size_t)15) + ((nw * 4 + 15) & ~(size_t)15) + (size_t)(GCAP + 1) * 8;
+  return ((ng * 2 + 15) & ~(size_t)15) + ((nw * 4 + 15) & ~(size_t)15) + (size_t)(GCAP + 1) * 8 +
+         (size_t)GCAP * 4;
 }
 
 __global__ void __launch_bounds__(THREADS, 4)
@@ -549,13 +582,14 @@ select_topw_group_kernel(const float* __restrict__ S, int n, int k, int w,
   extern __shared__ __align__(16) uint8_t gsm[];
   __shared__ unsigned hist[NBINS];
   __shared__ int wsum[4 * WARPS];
-  __shared__ int s_bl, s_ncand;
+  __shared__ int s_bl, s_ncand, s_nq, s_nq2;
   const int NG = (n + GSIZE - 1) / GSIZE;
   const int NW = (n + 31) / 32;
   uint16_t* gbin = reinterpret_cast<uint16_t*>(gsm);                                   // [NG]
   unsigned* kept = reinterpret_cast<unsigned*>(gsm + ((NG * 2 + 15) & ~15));           // [NW]
   unsigned long long* ckey =
       reinterpret_cast<unsigned long long*>(gsm + ((NG * 2 + 15) & ~15) + ((NW * 4 + 15) & ~15));
+  int* qlist = reinterpret_cast<int*>(ckey + GCAP + 1);  // [GCAP] qualifying groups
 
   const int c = blockIdx.x;
   const int bh = blockIdx.y;
@@ -566,7 +600,7 @@ select_topw_group_kernel(const float* __restrict__ S, int n, int k, int w,
 
   for (int i = tid; i < NW; i += THREADS) kept[i] = 0u;
   for (int i = tid; i < NBINS; i += THREADS) hist[i] = 0u;
-  if (tid == 0) { s_ncand = 0; s_bl = -1; }
+  if (tid == 0) { s_ncand = 0; s_nq = 0; s_nq2 = 0; s_bl = -1; }
   pdl_wait();
   __syncthreads();
 
@@ -649,61 +683,114 @@ select_topw_group_kernel(const float* __restrict__ S, int n, int k, int w,
     return;
   }
 
-  // 3. candidates from the groups whose maximum reaches b_L
+  // 3. candidates from the groups whose maximum reaches b_L: first the list of
+  //    those groups (shared memory only), then one group per thread, every
+  //    load in flight at once
+  for (int g0 = 0; g0 < NG; g0 += THREADS) {
+    const int g = g0 + tid;
+    const bool ok = g < NG && (int)gbin[g] >= bl;
+    const unsigned bal = __ballot_sync(0xffffffffu, ok);
+    int base = 0;
+    if (lane == 0 && bal != 0u) base = atomicAdd(&s_nq, __popc(bal));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int slot = base + __popc(bal & ((1u << lane) - 1u));
+    if (ok && slot < GCAP) qlist[slot] = g;
+  }
+  __syncthreads();
+  const int nq = s_nq;
+  if (nq > GCAP) {  // many groups in the boundary bin: exact radix path (uniform)
+    radix_select_row(row, n, w, so, hist, wsum);
+    return;
+  }
+  // candidates above the boundary bin fill ckey from the front (nA), those in
+  // it from the back (nE)
   {
     const float pre = bl > 0 ? (float)bl * (1.0f / 1024.0f) - 1.0f - 1.0e-5f : -3.0e38f;
-    for (int g0 = 0; g0 < NG; g0 += THREADS) {
-      const int g = g0 + tid;
-      uint32_t cm = 0u;
+    for (int i0 = 0; i0 < nq; i0 += THREADS) {
+      const int i = i0 + tid;
+      uint32_t ca = 0u, ce = 0u;  // above the boundary bin / in it
       float x[GSIZE];
-      if (g < NG && (int)gbin[g] >= bl) {
+      int g = 0;
+      if (i < nq) {
+        g = qlist[i];
         const float4 a = 2 * g < n4 ? __ldcg(row4 + 2 * g) : ninf;
         const float4 b = 2 * g + 1 < n4 ? __ldcg(row4 + 2 * g + 1) : ninf;
         x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
         x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 #pragma unroll
-        for (int e = 0; e < GSIZE; ++e)
-          if (x[e] >= pre && score_bin(x[e]) >= bl) cm |= 1u << e;
+        for (int e = 0; e < GSIZE; ++e) {
+          if (x[e] >= pre) {
+            const int sb = score_bin(x[e]);
+            if (sb > bl) ca |= 1u << e;
+            else if (sb == bl) ce |= 1u << e;
+          }
+        }
       }
-      const int cnt = __popc(cm);
-      int incl = cnt;
+      int sa, se;
+      {
+        const int cnt = __popc(ca) | (__popc(ce) << 16);  // both counts in one scan
+        int incl = cnt;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+        int baseA = 0, baseE = 0;
+        if (lane == 31) {
+          if (wtot & 0xffff) baseA = atomicAdd(&s_ncand, wtot & 0xffff);
+          if (wtot >> 16) baseE = atomicAdd(&s_nq2, wtot >> 16);
+        }
+        baseA = __shfl_sync(0xffffffffu, baseA, 31);
+        baseE = __shfl_sync(0xffffffffu, baseE, 31);
+        const int ex = incl - cnt;
+        sa = baseA + (ex & 0xffff);
+        se = baseE + (ex >> 16);
       }
-      const int wtot = __shfl_sync(0xffffffffu, incl, 31);
-      int base = 0;
-      if (lane == 31 && wtot > 0) base = atomicAdd(&s_ncand, wtot);
-      base = __shfl_sync(0xffffffffu, base, 31);
-      int slot = base + incl - cnt;
-      for (; cm != 0u; cm &= cm - 1u, ++slot) {
-        const int e = __ffs(cm) - 1;
-        if (slot < GCAP) ckey[slot] = cand_key(x[e], g * GSIZE + e);
+#pragma unroll
+      for (int e = 0; e < GSIZE; ++e) {
+        if ((ca >> e) & 1u) {
+          if (sa < GCAP) ckey[sa] = cand_key(x[e], g * GSIZE + e);
+          ++sa;
+        } else if ((ce >> e) & 1u) {
+          if (se < GCAP) ckey[GCAP - 1 - se] = cand_key(x[e], g * GSIZE + e);
+          ++se;
+        }
       }
     }
   }
   __syncthreads();
-  const int nc = s_ncand;
-  if (nc > GCAP) {
+  const int nA = s_ncand, nE = s_nq2;
+  if (nA + nE > GCAP) {
     radix_select_row(row, n, w, so, hist, wsum);  // uniform branch
     return;
   }
-  if (tid == 0) ckey[nc] = 0ull;  // pad to an even count (0 is below every key)
-  __syncthreads();
 
-  // 4. kept: fewer than w candidate keys above its own
-  const int nc2 = (nc + 1) & ~1;
-  for (int i = tid; i < nc; i += THREADS) {
-    const unsigned long long ki = ckey[i];
-    int rank = 0;
-    for (int j = 0; j < nc2; j += 2) {
-      const ulonglong2 kj = *reinterpret_cast<const ulonglong2*>(&ckey[j]);
-      rank += (kj.x > ki) + (kj.y > ki);
+  // 4. kept: fewer than w candidate keys above its own.  Usually fewer than w
+  //    scores lie above the boundary bin: those are all kept, and only the
+  //    boundary bin's candidates are ranked, among themselves, for the
+  //    remaining w - nA places.  Otherwise every candidate is ranked.
+  {
+    const unsigned long long* cE = ckey + (GCAP - nE);
+    const bool above_all = nA < w;
+    if (above_all) {
+      for (int i = tid; i < nA; i += THREADS) {
+        const int p = (int)(0xFFFFFFFFu - (uint32_t)ckey[i]);
+        atomicOr(&kept[p >> 5], 1u << (p & 31));
+      }
     }
-    if (rank < w) {
-      const int p = (int)(0xFFFFFFFFu - (uint32_t)ki);
-      atomicOr(&kept[p >> 5], 1u << (p & 31));
+    const int need = above_all ? w - nA : w;
+    const int total = above_all ? nE : nA + nE;
+    for (int i = tid; i < total; i += THREADS) {
+      const unsigned long long ki = (above_all || i >= nA) ? cE[above_all ? i : i - nA] : ckey[i];
+      int rank = 0;
+      for (int j = 0; j < nE; ++j) rank += cE[j] > ki;
+      if (!above_all)
+        for (int j = 0; j < nA; ++j) rank += ckey[j] > ki;
+      if (rank < need) {
+        const int p = (int)(0xFFFFFFFFu - (uint32_t)ki);
+        atomicOr(&kept[p >> 5], 1u << (p & 31));
+      }
     }
   }
   __syncthreads();
@@ -716,9 +803,7 @@ select_topw_group_kernel(const float* __restrict__ S, int n, int k, int w,
     for (int q = q0; q < q0 + WPT && q < NW; ++q) cnt += __popc(kept[q]);
     int total;
     int o = block_exclusive_scan<THREADS>(cnt, wsum, total);
-    for (int q = q0; q < q0 + WPT && q < NW; ++q)
-      for (unsigned rem = kept[q]; rem != 0u; rem &= rem - 1u, ++o)
-        if (o < w) so.emit(o, q * 32 + __ffs(rem) - 1);
+    for (int q = q0; q < q0 + WPT && q < NW; ++q) o = so.emit_word(o, kept[q], q * 32);
   }
 }
 

@@ -14,6 +14,10 @@
 
 #include "rt_internal.cuh"
 
+#ifndef RT_STEP_FORK_AFTER_SCORE
+#define RT_STEP_FORK_AFTER_SCORE 0
+#endif
+
 namespace rt {
 
 // ---------------------------------------------------------------------------
@@ -82,6 +86,33 @@ cudaError_t set_smem_limit(const void* func, int bytes) {
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) g_attr_set[key] = bytes;
   return e;
+}
+
+// ---------------------------------------------------------------------------
+// the side stream of the training step (one per device, created on first use)
+// ---------------------------------------------------------------------------
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+static std::mutex g_side_mu;  // held from the fork to the join of a step
+static std::map<int, SideStream> g_side;
+
+static cudaError_t side_stream(SideStream* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  auto it = g_side.find(dev);
+  if (it == g_side.end()) {
+    SideStream ss;
+    e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+    it = g_side.emplace(dev, ss).first;
+  }
+  *out = it->second;
+  return cudaSuccess;
 }
 
 // ---------------------------------------------------------------------------
@@ -155,10 +186,10 @@ bool bf16_tensor_map_2d(const void* base, unsigned long long rows, unsigned cols
 static inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct FwdLayout {
-  size_t err, S, mcount, slots, idx, assign, yslot, prep, idx_k, mvis, total;
+  size_t err, S, mcount, slots, idx, assign, yslot, prep, idx_k, mvis, ema, total;
 };
 
-static FwdLayout fwd_layout(int B, int H, int n, int d, int k, int w) {
+static FwdLayout fwd_layout(int B, int H, int n, int d, int k, int w, rt_dtype dt) {
   const size_t BH = (size_t)B * H;
   FwdLayout L;
   size_t off = 0;
@@ -172,6 +203,7 @@ static FwdLayout fwd_layout(int B, int H, int n, int d, int k, int w) {
   L.prep = off; off += align256(score_prep_bytes(H, d, k));
   L.idx_k = off; off += align256(BH * k * w * sizeof(int32_t));   // separate QK only
   L.mvis = off; off += align256(BH * n * sizeof(int32_t));        // separate QK only
+  L.ema = off; off += align256(ema_workspace_bytes(B, H, n, d, k, dt));  // the training step
   L.total = off;
   return L;
 }
@@ -297,7 +329,7 @@ const char* rt_kernel_name(int id) {
 
 size_t rt_workspace_bytes(int B, int H, int n, int d, int k, int w, rt_dtype dt) {
   if (check_shape(dt, B, H, n, d, k, w) != RT_OK) return 0;
-  const size_t a = fwd_layout(B, H, n, d, k, w).total;
+  const size_t a = fwd_layout(B, H, n, d, k, w, dt).total;
   const size_t b = ema_total(B, H, n, d, k, dt);
   const size_t c = bwd_layout(B, H, n, d, k, w).total;
   return std::max(a, std::max(b, c));
@@ -312,7 +344,7 @@ rt_status rt_route_assign(const void* qk, rt_dtype dt, int B, int H, int n, int 
   if (!aligned16(qk) || !aligned16(centroids) || !aligned16(idx) ||
       (assign && !aligned16(assign)) || (scores && !aligned16(scores)))
     return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-  const FwdLayout L = fwd_layout(B, H, n, d, k, w);
+  const FwdLayout L = fwd_layout(B, H, n, d, k, w, dt);
   if (!workspace || workspace_bytes < L.total)
     return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, L.total);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -337,11 +369,23 @@ rt_status rt_route_assign(const void* qk, rt_dtype dt, int B, int H, int n, int 
 // centroids, the key-block kernel attends between a cluster's queries and its
 // keys with the mask on original positions, and the scatter divides by each
 // position's count of memberships with a visible key.
+// The centroid step a training step adds to the forward pass (mu == nullptr:
+// none).  It needs only the argmax assignment, so it is forked onto the side
+// stream once the assignment exists and joined back at the end of the pass.
+struct StepEma {
+  float* mu = nullptr;
+  float decay = 0.0f;
+};
+// where the side stream forks: after the score kernel (the centroid step runs
+// beside select, attention and scatter) or after the attention kernel (beside
+// the scatter only, leaving every SM to the persistent attention kernel)
+constexpr bool kForkAfterScore = RT_STEP_FORK_AFTER_SCORE;
+
 static rt_status forward(const void* q, const void* kp, const void* v, rt_dtype dt, int B, int H,
                          int n, int d, const float* centroids, int kc, int w, int causal,
                          float scale, void* out, int32_t* idx_out, int32_t* idx_k_out,
                          int32_t* assign_out, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+                         void* stream, const StepEma& ema = StepEma()) {
   rt_status st = check_shape(dt, B, H, n, d, kc, w);
   if (st != RT_OK) return st;
   if (!q || !kp || !v || !centroids || !out) return fail(RT_ERR_INVALID_ARG, "null tensor pointer");
@@ -351,7 +395,7 @@ static rt_status forward(const void* q, const void* kp, const void* v, rt_dtype 
       !aligned16(out) || (idx_out && !aligned16(idx_out)) ||
       (idx_k_out && !aligned16(idx_k_out)) || (assign_out && !aligned16(assign_out)))
     return fail(RT_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-  const FwdLayout L = fwd_layout(B, H, n, d, kc, w);
+  const FwdLayout L = fwd_layout(B, H, n, d, kc, w, dt);
   if (!workspace || workspace_bytes < L.total)
     return fail(RT_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, L.total);
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -370,9 +414,31 @@ static rt_status forward(const void* q, const void* kp, const void* v, rt_dtype 
   unsigned int* err = reinterpret_cast<unsigned int*>(ws + L.err);
   void* prep = score_prep_bytes(H, d, kc) ? static_cast<void*>(ws + L.prep) : nullptr;
 
-  st = from_cuda(launch_score(q, dt, B, H, n, d, centroids, kc, S, assign_out, mcount, prep, err, s),
+  int32_t* assign = assign_out;
+  if (ema.mu != nullptr && assign == nullptr) assign = reinterpret_cast<int32_t*>(ws + L.assign);
+  std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
+  SideStream side;
+  if (ema.mu != nullptr) {
+    side_lock.lock();
+    st = from_cuda(side_stream(&side), "creating the side stream");
+    if (st != RT_OK) return st;
+  }
+  auto fork_ema = [&]() -> rt_status {
+    cudaError_t e = cudaEventRecord(side.fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side.s, side.fork, 0);
+    if (e == cudaSuccess)
+      e = launch_ema(q, dt, B, H, n, d, assign, ema.mu, kc, ema.decay, ws + L.ema, side.s);
+    if (e == cudaSuccess) e = cudaEventRecord(side.join, side.s);
+    return from_cuda(e, "centroid update (side stream)");
+  };
+
+  st = from_cuda(launch_score(q, dt, B, H, n, d, centroids, kc, S, assign, mcount, prep, err, s),
                  "score kernel");
   if (st != RT_OK) return st;
+  if (ema.mu != nullptr && kForkAfterScore) {
+    st = fork_ema();
+    if (st != RT_OK) return st;
+  }
   st = from_cuda(launch_select(S, BH, n, kc, w, idx, mcount, slots, s), "select kernel");
   if (st != RT_OK) return st;
   int32_t* idx_k = nullptr;
@@ -406,9 +472,17 @@ static rt_status forward(const void* q, const void* kp, const void* v, rt_dtype 
                    "attention kernel");
   }
   if (st != RT_OK) return st;
+  if (ema.mu != nullptr && !kForkAfterScore) {
+    st = fork_ema();
+    if (st != RT_OK) return st;
+  }
   st = from_cuda(launch_scatter(dt, BH, n, d, kc, w, idx, mcount, mvis, slots, yslot, out, s),
                  "scatter kernel");
   if (st != RT_OK) return st;
+  if (ema.mu != nullptr) {
+    st = from_cuda(cudaStreamWaitEvent(s, side.join, 0), "joining the side stream");
+    if (st != RT_OK) return st;
+  }
   return ok();
 }
 
@@ -419,6 +493,21 @@ rt_status rt_routing_attention(const void* q, const void* kp, const void* v, rt_
                                void* stream) {
   return forward(q, kp, v, dt, B, H, n, d, centroids, kc, w, causal, scale, out, idx_out,
                  nullptr, assign_out, workspace, workspace_bytes, stream);
+}
+
+rt_status rt_routing_attention_step(const void* q, const void* v, rt_dtype dt, int B, int H,
+                                    int n, int d, float* centroids, int kc, int w, int causal,
+                                    float scale, float decay, void* out, int32_t* idx_out,
+                                    int32_t* assign_out, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  if (!(decay >= 0.0f && decay <= 1.0f)) return fail(RT_ERR_INVALID_ARG, "decay must be in [0, 1]");
+  if (kc > 4096) return fail(RT_ERR_UNSUPPORTED, "k above 4096 for the centroid update");
+  if (!centroids) return fail(RT_ERR_INVALID_ARG, "null centroids");
+  StepEma ema;
+  ema.mu = centroids;
+  ema.decay = decay;
+  return forward(q, q, v, dt, B, H, n, d, centroids, kc, w, causal, scale, out, idx_out, nullptr,
+                 assign_out, workspace, workspace_bytes, stream, ema);
 }
 
 rt_status rt_routing_attention_separate(const void* q, const void* kp, const void* v, rt_dtype dt,

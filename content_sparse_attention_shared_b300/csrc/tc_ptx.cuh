@@ -171,19 +171,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t 
   return d;
 }
 
-// TMA gather of four rows (row0..row3) of a 2-D tensor map whose box is
-// {box_cols, 1}, starting at column x, into consecutive box rows at smem_dst
-// (128-byte aligned), completing on `bar`.
-__device__ __forceinline__ void tma_gather4(void* smem_dst, const void* map, int x, int row0,
-                                            int row1, int row2, int row3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(row0), "r"(row1), "r"(row2), "r"(row3),
-      "r"(smem_u32(bar))
-      : "memory");
-}
-
 // Instruction descriptor for kind::f16 with fp32 accumulation.
 //   ab_bf16: operands are bf16 (else fp16); a_mn / b_mn: operand is MN-major.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool ab_bf16, bool a_mn,

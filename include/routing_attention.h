@@ -114,6 +114,29 @@ rt_status rt_routing_attention(const void* q, const void* k, const void* v, rt_d
                                void* out, int32_t* idx_out, int32_t* assign_out,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* One training step of the layer: the forward pass of rt_routing_attention
+ * (shared QK) followed by the centroid step of rt_centroid_ema on the same
+ * rows and the assignment the forward computed -- the routing uses the
+ * centroids as they were, then they move.  Source: §4 "Routing attention with
+ * clustering" (centroids learned online while the layer runs), §2.
+ * The centroid step needs only the assignment, so it runs on a second stream
+ * the library owns (one per device, created by the first call; make that
+ * call before any stream capture), forked from `stream` once the assignment
+ * exists and joined back before the call's last operation: the caller sees
+ * one stream, and the step captures into a CUDA graph as a fork and a join.
+ * Calls from several host threads are serialised around the fork.
+ *   q, v        [B,H,n,d] dtype dt (queries double as keys)
+ *   centroids   [H,kc,d] fp32, read by the routing, then updated in place
+ *   decay       in [0, 1]
+ *   out, idx_out, assign_out, causal, scale: as rt_routing_attention
+ *   workspace   rt_workspace_bytes(B, H, n, d, kc, w, dt) bytes
+ * Results equal rt_routing_attention followed by rt_centroid_ema. */
+rt_status rt_routing_attention_step(const void* q, const void* v, rt_dtype dt, int B, int H,
+                                    int n, int d, float* centroids, int kc, int w, int causal,
+                                    float scale, float decay, void* out, int32_t* idx_out,
+                                    int32_t* assign_out, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
 /* Routing attention with separate queries and keys.
  * Source: §4 "Routing attention with clustering" (queries and keys are
  * routed to the same learned centroids; a query attends only to the keys of

@@ -161,6 +161,19 @@ def test_mixed_validation(lib):
     assert lib.rt_last_error_detail() != b""
 
 
+def test_step_validation(lib):
+    def call(decay=0.5, kc=4, w=64, mu=FAKE, wsb=1 << 30):
+        return lib.rt_routing_attention_step(FAKE, FAKE, 1, 1, 1, 128, 64, mu, kc, w, 1,
+                                             ctypes.c_float(0.0), ctypes.c_float(decay), FAKE,
+                                             None, None, FAKE, wsb, None)
+    assert call(decay=1.5) == bnd.RT_ERR_INVALID_ARG
+    assert call(mu=None) == bnd.RT_ERR_INVALID_ARG
+    assert call(kc=5000) == bnd.RT_ERR_UNSUPPORTED
+    assert call(w=129) == bnd.RT_ERR_INVALID_ARG
+    assert call(wsb=100) == bnd.RT_ERR_WORKSPACE
+    assert lib.rt_last_error_detail() != b""
+
+
 def test_route_validation(lib):
     r = lib.rt_route_assign(FAKE, 1, 1, 1, 64, 64, FAKE, 4, 16, None, None, None, FAKE, 1 << 30,
                             None)

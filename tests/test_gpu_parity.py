@@ -627,3 +627,50 @@ def test_backward_full_attention_matches_autograd():
     o.backward(dout.double().cpu())
     assert torch.max(torch.abs(dq.double().cpu() - q64.grad)).item() <= _bwd_tol(q64.grad.numpy())
     assert torch.max(torch.abs(dv.double().cpu() - v64.grad)).item() <= _bwd_tol(v64.grad.numpy())
+
+
+# ---------------------------------------------------------------------------
+# the training-step call (forward, then the centroid step on a forked stream)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cid", ["c1", "c3", "c5"])
+def test_training_step_equals_two_calls(cid):
+    wl = make_workload(cid)
+    q, v, mu = ph.to_device(wl)
+    B, H, n, d, k, w = wl.B, wl.H, wl.n, wl.d, wl.k, wl.w
+    ws = rt.Workspace.for_shape(B, H, n, d, k, w, q.dtype)
+    idx1 = torch.empty((B, H, k, w), dtype=torch.int32, device="cuda")
+    a1 = torch.empty((B, H, n), dtype=torch.int32, device="cuda")
+    mu1 = mu.clone()
+    out1 = rt.rt_routing_attention(q, q, v, mu1, w, idx_out=idx1, assign_out=a1, workspace=ws)
+    rt.rt_centroid_ema(q, a1, mu1, wl.decay, workspace=ws)
+    idx2 = torch.empty_like(idx1)
+    a2 = torch.empty_like(a1)
+    mu2 = mu.clone()
+    out2 = rt.rt_routing_attention_step(q, v, mu2, w, wl.decay, idx_out=idx2, assign_out=a2,
+                                        workspace=ws)
+    torch.cuda.synchronize()
+    ws.check()
+    assert torch.equal(out1, out2) and torch.equal(idx1, idx2) and torch.equal(a1, a2)
+    assert torch.equal(mu1, mu2)
+    # and inside a captured graph, replayed twice (the centroids move each time)
+    mu3 = mu.clone()
+    out3 = torch.empty_like(out1)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        rt.rt_routing_attention_step(q, v, mu3.clone(), w, wl.decay, out=out3, workspace=ws)
+    side.synchronize()
+    with torch.cuda.graph(g, stream=side):
+        rt.rt_routing_attention_step(q, v, mu3, w, wl.decay, out=out3, workspace=ws)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out3, out1) and torch.equal(mu3, mu1)
+    g.replay()
+    torch.cuda.synchronize()
+    mu4 = mu1.clone()
+    out4 = rt.rt_routing_attention(q, q, v, mu1, w, assign_out=a1, workspace=ws)
+    rt.rt_centroid_ema(q, a1, mu4, wl.decay, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out3, out4) and torch.equal(mu3, mu4)
