@@ -8,8 +8,8 @@
 // lower triangle in slot order (diagonal included).  Queries double as keys
 // (shared QK).
 //
-// This kernel serves clusters wider than one 128-row tile (w > 128; narrower
-// clusters go to the pipelined kernel in k_attention_pipe.cu), routing with
+// This kernel serves clusters wider than two 128-row tiles (w > 256; narrower
+// clusters go to k_attention_pipe.cu and k_attention_pair.cu), routing with
 // separate queries and keys (any w; queries and keys of a cluster come from
 // their own lists, the mask compares original positions), and local
 // attention.  Work unit: a
@@ -498,6 +498,8 @@ cudaError_t launch_attention_tc(const void* q, const void* v, int BH, int n, int
                                 unsigned int* err, cudaStream_t s) {
   if (w <= ROWS)
     return launch_attention_pipe(q, v, BH, n, d, k, w, causal, scale, idx, mcount, out, yslot, err, s);
+  if (w <= 2 * ROWS)
+    return launch_attention_pair(q, v, BH, n, d, k, w, causal, scale, idx, mcount, out, yslot, err, s);
   return d == 64 ? launch_t<64>(q, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, err, s)
                  : launch_t<128>(q, v, BH, n, k, w, causal, scale, idx, mcount, out, yslot, err, s);
 }

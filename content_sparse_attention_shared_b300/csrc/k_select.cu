@@ -369,14 +369,15 @@ select_topw_kernel(const float* __restrict__ S, int n, int k, int w, int32_t* __
 // the bin b_L of that maximum; b_L is found by bisection over the bins with
 // block-wide counts (no histogram).  Only threads whose maximum reaches b_L
 // read their scores again; the scores of bin >= b_L (typically a few more than
-// w) become candidates, appended with one shared-memory atomic per warp and
-// packed as 64-bit keys (score key, complemented position)
-// so that one integer compare orders them by (score desc, position asc).  A
-// candidate is kept when fewer than w keys exceed its own; kept positions are
-// set in a position bitmap, and a block-wide scan over the bitmap words puts
-// them out in ascending order.  Rows where the bound leaves more than RCAP
-// candidates (many equal scores), or with fewer than w non-empty threads, use
-// the exact radix select.
+// w) become candidates, each taking a slot with a shared-memory atomic, packed
+// as 64-bit keys (score key, complemented position) so that one integer
+// compare orders them by (score desc, position asc).  A candidate is kept when
+// fewer than w keys exceed its own; when fewer than w candidates lie above the
+// boundary bin (the usual case) those are all kept and only the boundary bin's
+// few candidates are ranked.  Kept positions are set in a position bitmap, and
+// a block-wide scan over the bitmap words puts them out in ascending order.
+// Rows where the bound leaves more than RCAP candidates (many equal scores), or
+// with fewer than w non-empty threads, use the exact radix select.
 // ---------------------------------------------------------------------------
 constexpr int CHUNKS_MAX = 8;  // 128-position chunks per warp
 constexpr int BOUND_N_MAX = THREADS * 4 * CHUNKS_MAX;
@@ -393,10 +394,10 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
                          int32_t* __restrict__ slots) {
   pdl_trigger();
   __shared__ unsigned hist[256];  // radix fallback
-  __shared__ __align__(16) unsigned long long ckey[RCAP + 1];
+  __shared__ __align__(16) unsigned long long ckey[RCAP];
   __shared__ unsigned kept[THREADS];  // position bitmap, 32 positions per word
   __shared__ int wsum[4 * WARPS];
-  __shared__ int s_ncand;
+  __shared__ int s_ncand, s_nedge;
 
   const int c = blockIdx.x;
   const int bh = blockIdx.y;
@@ -408,7 +409,7 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
   const int w0 = warp * seg + 4 * (tid & 31);                     // first position of this thread
 
   kept[tid] = 0u;
-  if (tid == 0) s_ncand = 0;
+  if (tid == 0) { s_ncand = 0; s_nedge = 0; }
   pdl_wait();
 
   auto load_chunks = [&](int i0, float4 (&v)[4]) {
@@ -453,14 +454,13 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
   // 3. candidates: scores of bin >= b_L, read again only by the threads whose
   //    maximum qualifies.  A float compare against a value a little below the
   //    bin's lower edge filters first; the bin itself is only computed for
-  //    the few scores that pass.  One shared-memory atomic per warp reserves
-  //    the warp's candidate slots.
+  //    the few scores that pass.  A candidate above the boundary bin takes a
+  //    slot from the front of ckey, one in it a slot from the back (shared
+  //    atomics; the ranking below does not depend on the slot order).
   {
     const bool mine = bl >= 0 && mbin >= bl;
     // (finite for bin 0, so that the -inf padding past n never qualifies)
     const float pre = bl > 0 ? (float)bl * (1.0f / 1024.0f) - 1.0f - 1.0e-5f : -3.0e38f;
-    uint32_t cmask = 0u;
-    float x0 = 0.0f, x1 = 0.0f;  // the first two candidate scores (usually all of them)
     if (mine) {
 #pragma unroll
       for (int i0 = 0; i0 < CHUNKS_MAX; i0 += 4) {
@@ -471,55 +471,56 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
           const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            if (e4[e] >= pre && score_bin(e4[e]) >= bl) {
-              if (cmask == 0u) x0 = e4[e];
-              else if ((cmask & (cmask - 1u)) == 0u) x1 = e4[e];
-              cmask |= 1u << (4 * (i0 + u) + e);
+            if (e4[e] >= pre) {
+              const int sb = score_bin(e4[e]);
+              if (sb >= bl) {
+                const int p = w0 + 128 * (i0 + u) + e;
+                if (sb > bl) {
+                  const int slot = atomicAdd(&s_ncand, 1);
+                  if (slot < RCAP) ckey[slot] = cand_key(e4[e], p);
+                } else {
+                  const int slot = atomicAdd(&s_nedge, 1);
+                  if (slot < RCAP) ckey[RCAP - 1 - slot] = cand_key(e4[e], p);
+                }
+              }
             }
           }
         }
       }
     }
-    const int cnt = __popc(cmask);
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if ((tid & 31) >= o) incl += y;
-    }
-    const int wtot = __shfl_sync(0xffffffffu, incl, 31);
-    int base = 0;
-    if ((tid & 31) == 31 && wtot > 0) base = atomicAdd(&s_ncand, wtot);
-    base = __shfl_sync(0xffffffffu, base, 31);
-    int slot = base + incl - cnt;
-    for (int j = 0; cmask != 0u; cmask &= cmask - 1u, ++slot, ++j) {
-      const int bit = __ffs(cmask) - 1;
-      const int p = w0 + 128 * (bit >> 2) + (bit & 3);
-      const float x = j == 0 ? x0 : j == 1 ? x1 : __ldcg(row + p);
-      if (slot < RCAP) ckey[slot] = cand_key(x, p);
-    }
   }
   __syncthreads();
-  const int nc = s_ncand;
-  if (bl < 0 || nc > RCAP) {
+  const int nA = s_ncand, nE = s_nedge;
+  if (bl < 0 || nA + nE > RCAP) {
     radix_select_row(row, n, w, so, hist, wsum);  // uniform branch
     return;
   }
-  if (tid == 0) ckey[nc] = 0ull;  // pad to an even count (0 is below every key)
-  __syncthreads();
 
-  // 4. kept: fewer than w candidate keys above its own
-  const int nc2 = (nc + 1) & ~1;
-  for (int i = tid; i < nc; i += THREADS) {
-    const unsigned long long ki = ckey[i];
-    int rank = 0;
-    for (int j = 0; j < nc2; j += 2) {
-      const ulonglong2 kj = *reinterpret_cast<const ulonglong2*>(&ckey[j]);
-      rank += (kj.x > ki) + (kj.y > ki);
+  // 4. kept: fewer than w candidate keys above its own.  Usually fewer than w
+  //    scores lie above the boundary bin: those are all kept, and only the
+  //    boundary bin's candidates are ranked, among themselves, for the
+  //    remaining w - nA places.  Otherwise every candidate is ranked.
+  {
+    const unsigned long long* cE = ckey + (RCAP - nE);
+    const bool above_all = nA < w;
+    if (above_all) {
+      for (int i = tid; i < nA; i += THREADS) {
+        const int p = (int)(0xFFFFFFFFu - (uint32_t)ckey[i]);
+        atomicOr(&kept[p >> 5], 1u << (p & 31));
+      }
     }
-    if (rank < w) {
-      const int p = (int)(0xFFFFFFFFu - (uint32_t)ki);
-      atomicOr(&kept[p >> 5], 1u << (p & 31));
+    const int need = above_all ? w - nA : w;
+    const int total = above_all ? nE : nA + nE;
+    for (int i = tid; i < total; i += THREADS) {
+      const unsigned long long ki = (above_all || i >= nA) ? cE[above_all ? i : i - nA] : ckey[i];
+      int rank = 0;
+      for (int j = 0; j < nE; ++j) rank += cE[j] > ki;
+      if (!above_all)
+        for (int j = 0; j < nA; ++j) rank += ckey[j] > ki;
+      if (rank < need) {
+        const int p = (int)(0xFFFFFFFFu - (uint32_t)ki);
+        atomicOr(&kept[p >> 5], 1u << (p & 31));
+      }
     }
   }
   __syncthreads();

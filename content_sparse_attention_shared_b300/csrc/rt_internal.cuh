@@ -235,8 +235,9 @@ cudaError_t launch_attention_simt(const void* q, const void* kk, const void* v, 
                                   const int32_t* mcount, int32_t* mvis, void* out, float* yslot,
                                   cudaStream_t s);
 
-// the same on tcgen05 tensor cores (bf16 only): the pipelined kernel below
-// for w <= 128, the key-block kernel above that; err: device error word.
+// the same on tcgen05 tensor cores (bf16 only): the pipelined kernel for
+// w <= 128, the two-tile kernel for w <= 256, the key-block kernel above
+// that; err: device error word.
 bool attention_tc_supported(rt_dtype dt, int d, int w);
 cudaError_t launch_attention_tc(const void* q, const void* v, int BH, int n, int d, int k, int w,
                                 int causal, float scale, const int32_t* idx,
@@ -256,6 +257,13 @@ cudaError_t launch_attention_separate_tc(const void* q, const void* kk, const vo
 // attends to the `window` positions ending at it; out [BH, n, d].
 cudaError_t launch_local_attention(const void* q, const void* v, int BH, int n, int d, int window,
                                    float scale, void* out, unsigned int* err, cudaStream_t s);
+
+// clusters of 128 < w <= 256 (two row tiles): one CTA per cluster, both
+// tiles' scores in TMEM at once (bf16 only).
+cudaError_t launch_attention_pair(const void* q, const void* v, int BH, int n, int d, int k,
+                                  int w, int causal, float scale, const int32_t* idx,
+                                  const int32_t* mcount, void* out, float* yslot,
+                                  unsigned int* err, cudaStream_t s);
 
 // the same, persistent and pipelined, for w <= 128 (bf16 only).
 cudaError_t launch_attention_pipe(const void* q, const void* v, int BH, int n, int d, int k,

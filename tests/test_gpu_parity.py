@@ -171,6 +171,9 @@ SWEEP = [
     (1, 1, 600, 64, 2, 300, "bf16", False),     # several key blocks, non-causal
     (1, 2, 1024, 128, 8, 128, "bf16", False),   # one cluster per tile, non-causal
     (2, 1, 1500, 64, 5, 384, "bf16", True),     # three key blocks, causal
+    (1, 2, 700, 64, 5, 200, "bf16", False),     # two row tiles in one CTA, non-causal
+    (2, 1, 500, 128, 3, 256, "bf16", True),     # two full row tiles
+    (1, 1, 300, 64, 2, 150, "bf16", True),      # two row tiles, d = 64
 ]
 
 
