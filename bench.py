@@ -65,13 +65,24 @@ def _peaks():
 # and read once, index lists, per-slot output rows.
 # ---------------------------------------------------------------------------
 
+def select_uses_group_bins(wl):
+    """Whether the score kernel writes group bins and the select reads those
+    instead of whole score rows (rows of n >= 32768, n a multiple of 4)."""
+    return 32768 <= wl.n <= 262144 and wl.n % 4 == 0
+
+
 def kernel_work(name, wl):
     s = 2 if wl.dtype == "bf16" else 4
     BH, n, d, k, w = wl.B * wl.H, wl.n, wl.d, wl.k, wl.w
+    gbins = BH * k * ((n + 7) // 8) * 2 if select_uses_group_bins(wl) else 0
     if name in ("score_simt", "score_tc"):
-        byts = BH * n * d * s + BH * k * n * 4 + BH * n * 4 * 2
+        byts = BH * n * d * s + BH * k * n * 4 + BH * n * 4 * 2 + gbins
         return dict(bytes=byts, flops=2.0 * BH * n * k * d)
     if name == "select_topw":
+        if gbins:
+            # the group bins, the w groups (8 scores each) that must be read
+            # again at least, index lists and membership counts
+            return dict(bytes=gbins + BH * k * w * 8 * 4 + BH * k * w * 4 * 2, flops=0.0)
         return dict(bytes=BH * k * n * 4 + BH * k * w * 4 * 2, flops=0.0)
     if name in ("attention_simt", "attention_tc"):
         # gathered Q(=K) and V rows, per-slot output rows, index lists
@@ -149,7 +160,8 @@ KERNEL_SOURCES = {
     "score_simt": ["k_score_simt.cu"], "score_tc": ["k_score_tc.cu", "tc_ptx.cuh"],
     "centroid_prep": ["k_score_tc.cu"], "select_topw": ["k_select.cu"],
     "attention_simt": ["k_attention_simt.cu"],
-    "attention_tc": ["k_attention_tc.cu", "k_attention_pipe.cu", "attn_common.cuh", "tc_ptx.cuh"],
+    "attention_tc": ["k_attention_tc.cu", "k_attention_pipe.cu", "k_attention_pair.cu",
+                     "attn_common.cuh", "tc_ptx.cuh"],
     "scatter_average": ["k_scatter.cu"], "ema_update": ["k_ema.cu"], "ema_bucket": ["k_ema.cu"],
 }
 
@@ -606,7 +618,19 @@ class Measured:
     def kernel_times(self, steps, flush):
         """Per-kernel device times: eager steps behind a sleep kernel, so the
         host has every launch queued before the GPU reaches it and the launch
-        hook's events bracket device time only."""
+        hook's events bracket device time only.  The steps take the sequential
+        form (forward, then the centroid update on the same stream), so no
+        kernel's bracket includes time spent waiting for SMs that another
+        stream holds."""
+        import torch
+        rt = self.rt
+        fused, self.fused = self.fused, False
+        try:
+            return self._kernel_times(steps, flush)
+        finally:
+            self.fused = fused
+
+    def _kernel_times(self, steps, flush):
         import torch
         rt = self.rt
         prof_steps = min(steps, 50)
@@ -780,7 +804,9 @@ def run_ours(args, wl_id, wl):
         "timing": {"l2": "flushed before every timed step (256 MiB write)",
                    "graph": "the step captured once as a CUDA graph, replayed per step",
                    "kernel_times": "eager steps behind a sleep kernel, CUDA events around each "
-                                   "launch (includes a few us of launch gap per kernel)"},
+                                   "launch (includes a few us of launch gap per kernel); the "
+                                   "centroid update runs after the forward on one stream, so "
+                                   "each kernel is timed alone"},
         "tflops": tflops, "tflops_causal": causal_flops(wl) * world / (t_ms * 1e-3) / 1e12,
         "tflops_frac_bf16": tflops / peaks["bf16_tflops"],
         "roofline": roofline_for(kern, wl, peaks),

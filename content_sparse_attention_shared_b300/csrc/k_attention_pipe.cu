@@ -17,17 +17,23 @@
 //               operand of S and the MN-major operand of O), and mark a stage
 //               full once their copies have landed;
 //   warp 12     issues the MMAs: S = Q Q^T into the TMEM accumulator of the
-//               tile's group, then O = P V into the same columns;
+//               tile's group, then O = P V into the same columns and, with
+//               the same P against a column of ones, P's row sums (the sums
+//               of exactly the bf16 weights the O MMA used, in fp32);
 //   warps 4-7,  two softmax/epilogue groups taking alternate tiles: softmax of
 //   warps 8-11  their rows from TMEM (only the 16-column chunks holding a valid
-//               key of some row of the warp), P (bf16) into the stage's Q
-//               space, then the O rows, staged in the stage's shared memory and
-//               written row-contiguously: bf16 to `out` for a position in one
-//               cluster, fp32 to its slot row in `yslot` otherwise.
+//               key of some row of the warp; chunks every row of the warp sees
+//               in full skip the mask), P (bf16) into the stage's Q space, then
+//               the O rows divided by their sums, staged in the stage's shared
+//               memory as 128-byte-swizzled boxes: one bulk tensor store per 32
+//               features writes all of the tile's slot rows to `yslot` (fp32),
+//               while the warps copy the rows of positions in exactly one
+//               cluster to `out` (bf16) themselves.
 // So the gathers of the next tiles overlap the softmax, MMAs and stores of
 // the current ones, and every SM stays busy until the last tile.  Every
 // mbarrier wait is bounded; a wait that runs out sets the device error word
-// and the CTA winds down.
+// and the CTA winds down (the four warps of an epilogue group agree on it at
+// one barrier per tile, so none is left waiting there).
 #include "attn_common.cuh"
 
 namespace rt {
@@ -45,8 +51,11 @@ struct PipeSmem {
   static constexpr int XB = QB > PB ? QB : PB;
   static constexpr int STAGE = XB + QB;       // + V tile; also holds the fp32 O rows
   static constexpr int NS = D == 128 ? 3 : 4;
-  static constexpr int BYTES = NS * STAGE;
+  // B operand of the row-sum MMA: 16 x 128 keys of bf16, row 0 all ones
+  static constexpr int ONES_OFF = NS * STAGE;
+  static constexpr int BYTES = ONES_OFF + 16 * ROWS * 2;
   static_assert(STAGE >= ROWS * D * 4, "a stage must hold the fp32 output rows");
+  static_assert(STAGE % 1024 == 0, "bulk-store boxes start on 1024-byte boundaries");
 };
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -55,10 +64,25 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __device__ __forceinline__ void producer_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");  // warps 0-3 only
 }
+// Barrier `id` over the 128 threads of one epilogue group, returning whether
+// v held in all of them.
+__device__ __forceinline__ bool group_all(int id, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id)
+      : "memory");
+  return r != 0u;
+}
 
 template <int D>
 __global__ void __launch_bounds__(PTHREADS, 1)
-attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int n, int k, int w,
+attention_pipe_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __restrict__ q,
+                      const bf16* __restrict__ v, int n, int k, int w,
                       int g, int tiles_per_bh, int ntiles, int causal, float scale_log2,
                       const int32_t* __restrict__ idx, const int32_t* __restrict__ mcount,
                       bf16* __restrict__ out, float* __restrict__ yslot,
@@ -72,9 +96,7 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
   __shared__ uint64_t sfull_bar[2], pfull_bar[2], ofull_bar[2], tfree_bar[2];
   __shared__ int pos_s[NS][ROWS];    // member position per tile row (-1: padding)
   __shared__ int m_s[NS][ROWS];      // its membership count
-  __shared__ int cl_s[NS][ROWS];     // its cluster
   __shared__ int bh_s[NS];           // the tile's batch*head
-  __shared__ unsigned long long dst_s[2][ROWS];  // per group: output row address | kind
   __shared__ uint32_t tmem_base_sh;
   __shared__ int stop_flag, prod_abort;
 
@@ -84,8 +106,19 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
   const int T = (ntiles > first) ? (ntiles - first + stride - 1) / stride : 0;  // my tiles
 
   if (warp == MMA_WARP) {
-    tc::tmem_alloc(&tmem_base_sh, 256);
+    // accumulators: columns [128a, 128a + 128) for group a (S, then O), the
+    // row sums of P at 256 + 16a
+    tc::tmem_alloc(&tmem_base_sh, 512);
     tc::tmem_relinquish();
+    // the ones operand: 16 rows (n) x 128 keys, K-major core matrices of
+    // 8 rows x 16 bytes; core matrix (n/8, key/8) at ((n/8)*16 + key/8)*128, so
+    // lane L writes core matrix L, whose first row is n = 0 for L < 16
+    uint4* o4 = reinterpret_cast<uint4*>(sm + L::ONES_OFF + lane * 128);
+    const uint32_t one2 = lane < 16 ? 0x3F803F80u : 0u;  // two bf16 1.0
+    o4[0] = make_uint4(one2, one2, one2, one2);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) o4[i] = make_uint4(0u, 0u, 0u, 0u);
+    tc::fence_proxy_async_smem();
   }
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -122,10 +155,10 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
     // ======================= producers (128 threads) =======================
     const int r = tid;  // tile row
     // the row's position and membership count for tile `tile`
-    auto load_meta = [&](int tile, int& p, int& m, int& cluster) {
+    auto load_meta = [&](int tile, int& p, int& m) {
       const int bh = tile / tiles_per_bh, lt = tile - bh * tiles_per_bh;
       const int ci = r / w;
-      cluster = lt * g + ci;
+      const int cluster = lt * g + ci;
       p = -1;
       m = 0;
       if (ci < g && cluster < k) {
@@ -134,8 +167,8 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
         else m = __ldcg(mcount + (size_t)bh * n + p);
       }
     };
-    int np = -1, nm = 0, ncl = 0;
-    if (T > 0) load_meta(first, np, nm, ncl);
+    int np = -1, nm = 0;
+    if (T > 0) load_meta(first, np, nm);
     for (int i = 0; i < T; ++i) {
       const int tile = first + i * stride;
       const int s = i % NS;
@@ -150,7 +183,6 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
       const int bh = tile / tiles_per_bh;
       pos_s[s][r] = np;
       m_s[s][r] = nm;
-      cl_s[s][r] = ncl;
       if (r == 0) bh_s[s] = bh;
       producer_sync();  // the stage's positions are visible to the four warps
       const bf16* q_bh = q + (size_t)bh * n * D;
@@ -159,7 +191,7 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
       gather_sw128<D>(st, q_bh, pos_s[s], warp, 4);
       gather_sw128<D>(st + L::XB, v_bh, pos_s[s], warp, 4);
       cp_async_commit();
-      if (i + 1 < T) load_meta(tile + stride, np, nm, ncl);  // next tile, while copies fly
+      if (i + 1 < T) load_meta(tile + stride, np, nm);  // next tile, while copies fly
       cp_async_wait_all();           // this thread's copies have landed
       tc::fence_proxy_async_smem();  // ... and are visible to the MMA
       mbar_arrive(&full_bar[s]);     // the stage is full once all 128 arrived
@@ -169,6 +201,8 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
     if (lane == 0) {
       constexpr uint32_t IDESC_S = tc::idesc_f16(ROWS, ROWS, true, false, false);
       constexpr uint32_t IDESC_O = tc::idesc_f16(ROWS, D, true, false, true);
+      constexpr uint32_t IDESC_L = tc::idesc_f16(ROWS, 16, true, false, false);
+      const uint32_t ones = tc::smem_u32(sm + L::ONES_OFF);
       // S(j) needs tile j's rows and a free accumulator; O(j) needs P(j).
       // Whichever is ready is issued, so O(j) never waits behind the data
       // of tile j + 1.
@@ -202,6 +236,9 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
           const uint64_t ad = tc::smem_desc_noswizzle(pa + kk * 256, 128, 2048);
           const uint64_t bd = tc::smem_desc_sw128_mn(va + kk * 2048, ROWS * 128, 1024);
           tc::mma_f16_ss(tmem + a * 128, ad, bd, IDESC_O, kk > 0 ? 1u : 0u);
+          // the row sums of the same bf16 P: P times a column of ones
+          const uint64_t od = tc::smem_desc_noswizzle(ones + kk * 256, 128, 2048);
+          tc::mma_f16_ss(tmem + 256 + a * 16, ad, od, IDESC_L, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(&ofull_bar[a]);
       };
@@ -232,11 +269,12 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
     const int grp = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int r = 32 * quad + lane;  // tile row == TMEM lane
-    const uint32_t t_row = tmem + grp * 128 + ((uint32_t)(32 * quad) << 16);
+    const uint32_t lanes = (uint32_t)(32 * quad) << 16;
+    const uint32_t t_row = tmem + grp * 128 + lanes;
+    const uint32_t t_sum = tmem + 256 + grp * 16 + lanes;  // the row sums of P
     const int ci = r / w;
     const int row_lo = ci * w, row_hi = row_lo + w;
-    constexpr int CPR = D / 4;     // 16-byte fp32 chunks per output row
-    constexpr int RPI = 32 / CPR;  // rows per warp instruction in the copy-out
+    const bool leader = quad == 0 && lane == 0;  // issues the group's bulk stores
     for (int j = grp; j < T; j += 2) {
       const int s = j % NS;
       const uint32_t use_s = (uint32_t)(j / NS), use_a = (uint32_t)(j >> 1);
@@ -246,155 +284,206 @@ attention_pipe_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
                 tc::mbar_wait_bounded(&full_bar[s], use_s & 1u, WAIT_LIMIT_NS) &&
                 !*(volatile int*)&stop_flag;
       ok = __all_sync(0xffffffffu, ok);
-      if (!ok) { fail(lane == 0); break; }
-      tc::tc_fence_after_sync();
-      const int my_pos = pos_s[s][r];
-      const bool row_valid = my_pos >= 0;
       uint8_t* st = sm + (size_t)s * L::STAGE;
-
-      // ---- softmax of this row over its cluster's keys ---------------------
-      int jmin = row_lo, jmax = causal ? r + 1 : row_hi;
-      if (!row_valid || jmax <= jmin) { jmin = ROWS; jmax = 0; }
-      const int wlo = __reduce_min_sync(0xffffffffu, jmin);
-      const int whi = __reduce_max_sync(0xffffffffu, jmax);
-      const int ch_lo = (whi > wlo) ? (wlo >> 4) : 0;
-      const int ch_hi = (whi > wlo) ? ((whi + 15) >> 4) : 0;
-      // TMEM is read two 16-column chunks per wait
-      float mrow = -INFINITY;
-      for (int ch = ch_lo; ch < ch_hi; ch += 2) {
-        uint32_t rr[2][16];
-        tc::tmem_ld16(t_row + ch * 16, rr[0]);
-        if (ch + 1 < ch_hi) tc::tmem_ld16(t_row + (ch + 1) * 16, rr[1]);
-        tc::tmem_ld_wait();
+      const int my_pos = ok ? pos_s[s][r] : -1;
+      const bool row_valid = my_pos >= 0;
+      if (ok) {
+        tc::tc_fence_after_sync();
+        // ---- softmax of this row over its cluster's keys -------------------
+        int jmin = row_lo, jmax = causal ? r + 1 : row_hi;
+        if (!row_valid || jmax <= jmin) { jmin = ROWS; jmax = 0; }
+        const int wlo = __reduce_min_sync(0xffffffffu, jmin);
+        const int whi = __reduce_max_sync(0xffffffffu, jmax);
+        // [flo, fhi): columns every valid row of the warp sees (no mask there;
+        // an invalid row's values are never stored)
+        const int flo = __reduce_max_sync(0xffffffffu, row_valid ? jmin : 0);
+        const int fhi = __reduce_min_sync(0xffffffffu, row_valid ? jmax : ROWS);
+        const int ch_lo = (whi > wlo) ? (wlo >> 4) : 0;
+        const int ch_hi = (whi > wlo) ? ((whi + 15) >> 4) : 0;
+        auto full_chunk = [&](int ch) { return ch * 16 >= flo && ch * 16 + 16 <= fhi; };
+        // TMEM is read two 16-column chunks per wait
+        float mrow = -INFINITY;
+        for (int ch = ch_lo; ch < ch_hi; ch += 2) {
+          uint32_t rr[2][16];
+          tc::tmem_ld16(t_row + ch * 16, rr[0]);
+          if (ch + 1 < ch_hi) tc::tmem_ld16(t_row + (ch + 1) * 16, rr[1]);
+          tc::tmem_ld_wait();
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          if (ch + hh >= ch_hi) break;
+          for (int hh = 0; hh < 2; ++hh) {
+            const int c = ch + hh;
+            if (c >= ch_hi) break;
+            if (full_chunk(c)) {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int col = (ch + hh) * 16 + jj;
-            if (col >= jmin && col < jmax) mrow = fmaxf(mrow, __uint_as_float(rr[hh][jj]));
+              for (int jj = 0; jj < 16; ++jj) mrow = fmaxf(mrow, __uint_as_float(rr[hh][jj]));
+            } else {
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) {
+                const int col = c * 16 + jj;
+                if (col >= jmin && col < jmax) mrow = fmaxf(mrow, __uint_as_float(rr[hh][jj]));
+              }
+            }
           }
         }
-      }
-      const float mscaled = (mrow == -INFINITY) ? 0.0f : mrow * scale_log2;
-      float lsum = 0.0f;
-      const uint32_t prow = tc::smem_u32(st) + (r >> 3) * 2048 + (r & 7) * 16;
-      auto store_chunk = [&](int ch, const uint32_t (&pk)[8]) {
+        const float neg_m = (mrow == -INFINITY) ? 0.0f : -mrow * scale_log2;
+        const uint32_t prow = tc::smem_u32(st) + (r >> 3) * 2048 + (r & 7) * 16;
+        auto store_chunk = [&](int ch, const uint32_t (&pk)[8]) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t addr = prow + (2 * ch + h) * 128;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * h]),
-                       "r"(pk[4 * h + 1]), "r"(pk[4 * h + 2]), "r"(pk[4 * h + 3])
-                       : "memory");
-        }
-      };
-      {
-        const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-#pragma unroll 1
-        for (int ch = 0; ch < ROWS / 16; ++ch)
-          if (ch < ch_lo || ch >= ch_hi) store_chunk(ch, zero);
-      }
-#pragma unroll 1
-      for (int ch = ch_lo; ch < ch_hi; ch += 2) {
-        uint32_t rr[2][16];
-        tc::tmem_ld16(t_row + ch * 16, rr[0]);
-        if (ch + 1 < ch_hi) tc::tmem_ld16(t_row + (ch + 1) * 16, rr[1]);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          if (ch + hh >= ch_hi) break;
-          uint32_t pk[8];
-#pragma unroll
-          for (int jj = 0; jj < 16; jj += 2) {
-            const int col = (ch + hh) * 16 + jj;
-            const bool ok0 = col >= jmin && col < jmax;
-            const bool ok1 = col + 1 >= jmin && col + 1 < jmax;
-            const float e0 = ok0 ? exp2f(__uint_as_float(rr[hh][jj]) * scale_log2 - mscaled) : 0.0f;
-            const float e1 = ok1 ? exp2f(__uint_as_float(rr[hh][jj + 1]) * scale_log2 - mscaled) : 0.0f;
-            const uint32_t pp = pack_bf16(e0, e1);
-            pk[jj >> 1] = pp;
-            lsum += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xffff0000u);
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t addr = prow + (2 * ch + h) * 128;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * h]),
+                         "r"(pk[4 * h + 1]), "r"(pk[4 * h + 2]), "r"(pk[4 * h + 3])
+                         : "memory");
           }
-          store_chunk(ch + hh, pk);
+        };
+        {
+          const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll 1
+          for (int ch = 0; ch < ROWS / 16; ++ch)
+            if (ch < ch_lo || ch >= ch_hi) store_chunk(ch, zero);
         }
-      }
-      tc::fence_proxy_async_smem();  // P (generic writes) before the MMA reads it
-      tc::tc_fence_before_sync();    // S reads done before O overwrites the columns
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&pfull_bar[grp]);
+        // P = 2^(S*scale*log2e - max), bf16; its row sums come from the O MMA
+#pragma unroll 1
+        for (int ch = ch_lo; ch < ch_hi; ch += 2) {
+          uint32_t rr[2][16];
+          tc::tmem_ld16(t_row + ch * 16, rr[0]);
+          if (ch + 1 < ch_hi) tc::tmem_ld16(t_row + (ch + 1) * 16, rr[1]);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int c = ch + hh;
+            if (c >= ch_hi) break;
+            uint32_t pk[8];
+            if (full_chunk(c)) {
+#pragma unroll
+              for (int jj = 0; jj < 16; jj += 2) {
+                const float e0 = tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj]), scale_log2, neg_m));
+                const float e1 = tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj + 1]), scale_log2, neg_m));
+                pk[jj >> 1] = pack_bf16(e0, e1);
+              }
+            } else {
+#pragma unroll
+              for (int jj = 0; jj < 16; jj += 2) {
+                const int col = c * 16 + jj;
+                const bool ok0 = col >= jmin && col < jmax;
+                const bool ok1 = col + 1 >= jmin && col + 1 < jmax;
+                const float e0 =
+                    ok0 ? tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj]), scale_log2, neg_m)) : 0.0f;
+                const float e1 =
+                    ok1 ? tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj + 1]), scale_log2, neg_m)) : 0.0f;
+                pk[jj >> 1] = pack_bf16(e0, e1);
+              }
+            }
+            store_chunk(c, pk);
+          }
+        }
+        tc::fence_proxy_async_smem();  // P (generic writes) before the MMA reads it
+        tc::tc_fence_before_sync();    // S reads done before O overwrites the columns
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pfull_bar[grp]);
 
-      // ---- O rows: TMEM -> fp32 staging (the stage's shared memory) ---------
-      ok = tc::mbar_wait_bounded(&ofull_bar[grp], use_a & 1u, WAIT_LIMIT_NS) &&
-           !*(volatile int*)&stop_flag;
-      ok = __all_sync(0xffffffffu, ok);
+        ok = tc::mbar_wait_bounded(&ofull_bar[grp], use_a & 1u, WAIT_LIMIT_NS) &&
+             !*(volatile int*)&stop_flag;
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        // ---- O rows / row sum: TMEM -> fp32 staging over the stage ---------
+        // Layout of a bulk-store box: D/32 segments of [128 rows][128 bytes],
+        // 16-byte chunk q of row r at (q ^ (r % 8)) (128-byte swizzle).
+        tc::tc_fence_after_sync();
+        uint32_t lraw;
+        tc::tmem_ld1(t_sum, lraw);
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t rr[2][16];
+          tc::tmem_ld16(t_row + c0, rr[0]);
+          tc::tmem_ld16(t_row + c0 + 16, rr[1]);
+          tc::tmem_ld_wait();
+          const float lsum = __uint_as_float(lraw);
+          const float inv_l = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const int chunk = c0 / 4 + q4;
+            const uint32_t* x = &rr[q4 >> 2][4 * (q4 & 3)];
+            *reinterpret_cast<float4*>(st + (chunk >> 3) * (ROWS * 128) + r * 128 +
+                                       (((chunk & 7) ^ (r & 7)) << 4)) =
+                make_float4(__uint_as_float(x[0]) * inv_l, __uint_as_float(x[1]) * inv_l,
+                            __uint_as_float(x[2]) * inv_l, __uint_as_float(x[3]) * inv_l);
+          }
+        }
+        tc::tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tfree_bar[grp]);  // the accumulator may be reused
+        tc::fence_proxy_async_smem();  // the staged rows, before the bulk store reads them
+      }
+      // the four warps of the group decide together (each reaches this barrier
+      // once per tile, whatever happened above)
+      ok = group_all(2 + grp, ok);
       if (!ok) { fail(lane == 0); break; }
-      tc::tc_fence_after_sync();
-      float4* stage = reinterpret_cast<float4*>(st);
-      const float inv_l = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        uint32_t rr[16];
-        tc::tmem_ld16(t_row + c0, rr);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int chunk = c0 / 4 + q4;
-          stage[r * CPR + (chunk ^ (r & 7))] =
-              make_float4(__uint_as_float(rr[4 * q4]) * inv_l, __uint_as_float(rr[4 * q4 + 1]) * inv_l,
-                          __uint_as_float(rr[4 * q4 + 2]) * inv_l,
-                          __uint_as_float(rr[4 * q4 + 3]) * inv_l);
-        }
-      }
-      tc::tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tfree_bar[grp]);  // the accumulator may be reused
 
-      // ---- copy-out: each warp writes its own 32 rows, row-contiguously -----
-      // The owner of a row publishes where the row goes (bf16 into `out`,
-      // fp32 into its slot row of `yslot`, or nowhere for padding); then the
-      // warp copies row after row, every lane moving 16 bytes of it.
-      {
-        const int bh = bh_s[s];
-        const int my_m = m_s[s][r];
-        const int my_cl = cl_s[s][r];
-        void* dst = nullptr;
-        int kind = 0;  // 0 none, 1 bf16 out, 2 fp32 slot row
-        if (row_valid) {
-          if (my_m == 1) {
-            dst = out + ((size_t)bh * n + my_pos) * D;
-            kind = 1;
-          } else {
-            dst = yslot + (((size_t)bh * k + my_cl) * w + (r - ci * w)) * D;
-            kind = 2;
-          }
-        }
-        dst_s[grp][r] = reinterpret_cast<unsigned long long>(dst) | (unsigned long long)kind;
+      // ---- copy-out ----------------------------------------------------------
+      // Every slot row of the tile's clusters goes to `yslot` (fp32) with one
+      // bulk tensor store per 32 features (rows past the head's k*w clusters
+      // are clipped by the tensor map); rows of positions in exactly one
+      // cluster also go straight to `out` as bf16, a warp per row.
+      const int tile = first + j * stride;
+      const int bh = bh_s[s];
+      if (leader) {
+        const int y0 = (tile - bh * tiles_per_bh) * g * w;
+#pragma unroll
+        for (int sg = 0; sg < D / 32; ++sg)
+          tc::tma_store_3d(&ymap, st + sg * (ROWS * 128), sg * 32, y0, bh);
+        tc::bulk_commit();
       }
-      __syncwarp();
-      const int chn = lane % CPR;
-#pragma unroll 4
-      for (int it = 0; it < 32 / RPI; ++it) {
-        const int row = 32 * quad + it * RPI + lane / CPR;
-        const unsigned long long dk = dst_s[grp][row];
-        const float4 val = stage[row * CPR + (chn ^ (row & 7))];
-        const int kind = (int)(dk & 3u);
-        if (kind == 1) {
+      unsigned single = __ballot_sync(0xffffffffu, row_valid && m_s[s][r] == 1);
+      bf16* out_bh = out + (size_t)bh * n * D;
+      if constexpr (D == 128) {
+        while (single) {
+          const int i = __ffs(single) - 1;
+          single &= single - 1;
+          const int row = 32 * quad + i;
+          const int p = __shfl_sync(0xffffffffu, my_pos, i);
+          const float4 val = *reinterpret_cast<const float4*>(
+              st + (lane >> 3) * (ROWS * 128) + row * 128 + (((lane & 7) ^ (row & 7)) << 4));
           uint2 u;
           u.x = pack_bf16(val.x, val.y);
           u.y = pack_bf16(val.z, val.w);
-          reinterpret_cast<uint2*>(dk & ~3ull)[chn] = u;
-        } else if (kind == 2) {
-          reinterpret_cast<float4*>(dk & ~3ull)[chn] = val;
+          reinterpret_cast<uint2*>(out_bh + (size_t)p * D)[lane] = u;
+        }
+      } else {  // D == 64: 16 chunks a row, two rows a pass
+        const int half = lane >> 4, c = lane & 15;
+        while (single) {
+          const int i0 = __ffs(single) - 1;
+          single &= single - 1;
+          int i1 = -1;
+          if (single) {
+            i1 = __ffs(single) - 1;
+            single &= single - 1;
+          }
+          const int p0 = __shfl_sync(0xffffffffu, my_pos, i0);
+          const int p1 = __shfl_sync(0xffffffffu, my_pos, i1 < 0 ? i0 : i1);
+          const int i = half ? i1 : i0;
+          if (i >= 0) {
+            const int row = 32 * quad + i;
+            const int p = half ? p1 : p0;
+            const float4 val = *reinterpret_cast<const float4*>(
+                st + (c >> 3) * (ROWS * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+            uint2 u;
+            u.x = pack_bf16(val.x, val.y);
+            u.y = pack_bf16(val.z, val.w);
+            reinterpret_cast<uint2*>(out_bh + (size_t)p * D)[c] = u;
+          }
         }
       }
+      if (leader) tc::bulk_wait_read_all();  // the bulk stores have read the stage
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);  // the stage may be refilled
     }
+    if (leader) tc::bulk_wait_all();  // this CTA's bulk stores are complete
   }
 
   tc::tc_fence_before_sync();
   __syncthreads();
-  if (warp == MMA_WARP) tc::tmem_dealloc(tmem, 256);
+  if (warp == MMA_WARP) tc::tmem_dealloc(tmem, 512);
 }
 
 template <int D>
@@ -414,8 +503,13 @@ cudaError_t launch_pipe(const void* q, const void* v, int BH, int n, int k, int 
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = (int)(ntiles < sms ? ntiles : sms);
   const float scale_log2 = scale * 1.4426950408889634f;
+  // yslot as [BH][k*w slot rows][D] fp32; a box is one tile's g*w rows
+  CUtensorMap ymap;
+  if (!f32_tensor_map_3d(yslot, D, (unsigned long long)k * w, (unsigned)BH, (unsigned)(g * w),
+                         &ymap))
+    return cudaErrorInvalidValue;
   launch_begin(K_ATTN_TC, s);
-  e = launch_pdl(kern, dim3(grid), dim3(PTHREADS), smem, s, static_cast<const bf16*>(q),
+  e = launch_pdl(kern, dim3(grid), dim3(PTHREADS), smem, s, ymap, static_cast<const bf16*>(q),
                  static_cast<const bf16*>(v), n, k, w, g, tiles_per_bh, (int)ntiles, causal,
                  scale_log2, idx, mcount, static_cast<bf16*>(out), yslot, err,
                  injected_limit_ns(K_ATTN_TC));

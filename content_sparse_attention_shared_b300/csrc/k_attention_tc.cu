@@ -489,7 +489,7 @@ cudaError_t launch_attention_separate_tc(const void* q, const void* kk, const vo
 }
 
 bool attention_tc_supported(rt_dtype dt, int d, int w) {
-  return dt == RT_BF16 && (d == 64 || d == 128) && w >= 1;
+  return dt == RT_BF16 && (d == 64 || d == 128) && w >= 1 && tensor_maps_available();
 }
 
 cudaError_t launch_attention_tc(const void* q, const void* v, int BH, int n, int d, int k, int w,

@@ -11,7 +11,9 @@
 // staged transposed in shared memory; each thread accumulates a 4x4 block of
 // scores over the head dimension in a fixed order, so a score is the same
 // fp32 value in every call.  Scores are written centroid-major [BH,k,n] so
-// that a warp stores 16 consecutive positions per centroid.
+// that a warp stores 16 consecutive positions per centroid, optionally with
+// the group bins of the select kernel (the 8 positions of a group are 8 lanes
+// of a warp, reduced by shuffles).
 #include "rt_internal.cuh"
 
 namespace rt {
@@ -26,7 +28,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(THREADS)
 score_simt_kernel(const T* __restrict__ qk, int H, int n, const float* __restrict__ mu,
                   int k, float* __restrict__ S, int32_t* __restrict__ assign,
-                  int32_t* __restrict__ mcount) {
+                  int32_t* __restrict__ mcount, uint16_t* __restrict__ gbins, int gstride) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ float smem[];
@@ -114,6 +116,25 @@ score_simt_kernel(const T* __restrict__ qk, int H, int n, const float* __restric
         }
       }
     }
+    if (gbins != nullptr) {
+      // group bins: the lanes tx = 8m .. 8m+7 of a half-warp hold one group of
+      // 8 positions; its 16 (i, jj) columns are reduced in two rounds of 8
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float m[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int i = 2 * r + (q >> 2), jj = q & 3;
+          m[q] = (t0 + tx + 16 * i < n) ? acc[i][jj] : -INFINITY;
+        }
+        const float gm = octet_column_max(m, lane);
+        const int q = lane & 7, i = 2 * r + (q >> 2), jj = q & 3;
+        const int c = c0 + ty + 16 * jj;
+        const int g = (t0 + 16 * i) / GROUP_SIZE + (tx >> 3);
+        if (c < k && g * GROUP_SIZE < n)
+          gbins[((size_t)bh * k + c) * gstride + g] = (uint16_t)score_bin(gm);
+      }
+    }
   }
 
   if (assign != nullptr) {
@@ -139,7 +160,7 @@ score_simt_kernel(const T* __restrict__ qk, int H, int n, const float* __restric
 
 template <typename T, int D>
 cudaError_t launch_t(const void* qk, int BH, int H, int n, const float* mu, int k, float* S,
-                     int32_t* a, int32_t* mcount, cudaStream_t s) {
+                     int32_t* a, int32_t* mcount, uint16_t* gbins, cudaStream_t s) {
   const size_t smem = 2 * (size_t)D * PAD * sizeof(float);
   auto kern = score_simt_kernel<T, D>;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
@@ -147,7 +168,7 @@ cudaError_t launch_t(const void* qk, int BH, int H, int n, const float* mu, int 
   dim3 grid((n + TOK - 1) / TOK, BH);
   launch_begin(K_SCORE_SIMT, s);
   e = launch_pdl(kern, grid, dim3(THREADS), smem, s, static_cast<const T*>(qk), H, n, mu, k, S, a,
-                 mcount);
+                 mcount, S != nullptr ? gbins : nullptr, gbin_stride(n));
   launch_end(K_SCORE_SIMT, s);
   return e;
 }
@@ -156,13 +177,13 @@ cudaError_t launch_t(const void* qk, int BH, int H, int n, const float* mu, int 
 
 cudaError_t launch_score_simt(const void* qk, rt_dtype dt, int BH, int H, int n, int d,
                               const float* mu, int k, float* S, int32_t* a,
-                              int32_t* mcount, cudaStream_t s) {
+                              int32_t* mcount, uint16_t* gbins, cudaStream_t s) {
   if (dt == RT_F32) {
-    return d == 64 ? launch_t<float, 64>(qk, BH, H, n, mu, k, S, a, mcount, s)
-                   : launch_t<float, 128>(qk, BH, H, n, mu, k, S, a, mcount, s);
+    return d == 64 ? launch_t<float, 64>(qk, BH, H, n, mu, k, S, a, mcount, gbins, s)
+                   : launch_t<float, 128>(qk, BH, H, n, mu, k, S, a, mcount, gbins, s);
   }
-  return d == 64 ? launch_t<__nv_bfloat16, 64>(qk, BH, H, n, mu, k, S, a, mcount, s)
-                 : launch_t<__nv_bfloat16, 128>(qk, BH, H, n, mu, k, S, a, mcount, s);
+  return d == 64 ? launch_t<__nv_bfloat16, 64>(qk, BH, H, n, mu, k, S, a, mcount, gbins, s)
+                 : launch_t<__nv_bfloat16, 128>(qk, BH, H, n, mu, k, S, a, mcount, gbins, s);
 }
 
 }  // namespace rt

@@ -25,7 +25,11 @@
 // take alternate tiles: each reads its rows' statistics (mean, centred norm)
 // from the staged tile in shared memory while the MMA runs, then the scores
 // from TMEM, writes them centroid-major [BH,k,n] with coalesced stores and
-// takes the argmax.  Every mbarrier wait is bounded; a wait that runs out
+// takes the argmax.  With the scores it can write the group bins of the
+// select kernel (the bin of the largest score of every 8 consecutive
+// positions per centroid): a tile row is a lane, so a group is a lane octet,
+// and a shuffle reduce-scatter leaves each lane one centroid's group maximum
+// per 8 columns.  Every mbarrier wait is bounded; a wait that runs out
 // sets the device error word and the CTA stops.
 #include "rt_internal.cuh"
 #include "tc_ptx.cuh"
@@ -170,7 +174,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
                 const float* __restrict__ mu, const uint8_t* __restrict__ image, int k, int kpad,
                 int acc_cols, int stages, int ctas_per_head, float* __restrict__ S,
                 int32_t* __restrict__ assign, int32_t* __restrict__ mcount,
-                unsigned int* __restrict__ err, uint64_t fault_ns) {
+                uint16_t* __restrict__ gbins, int gstride, unsigned int* __restrict__ err,
+                uint64_t fault_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -449,6 +454,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
       int best_c = 0;
       const float nmean = -mean;
       float* sp = (S != nullptr && valid) ? S + (size_t)bh * k * n + t : nullptr;
+      // group bins: the lane octet holding positions 8m..8m+7 of this tile
+      // reduces each centroid's column, and lane 8m+j writes centroid j's bin
+      const int gi = tb * (ROWS / GROUP_SIZE) + (row >> 3);
+      uint16_t* gp = (gbins != nullptr && gi * GROUP_SIZE < n)
+                         ? gbins + (size_t)bh * k * gstride + gi + (size_t)(lane & 7) * gstride
+                         : nullptr;
       const uint32_t tacc = tmem + grp * acc_cols + lane_base;
       for (int c0 = 0; c0 < kpad; c0 += 32) {
         uint32_t r[2][16];
@@ -471,6 +482,18 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
           if (zero_row) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) sc[j] = 0.0f;
+          }
+          if (gbins != nullptr) {  // warp-uniform: the shuffles need every lane
+#pragma unroll
+            for (int hv = 0; hv < 2; ++hv) {
+              float m[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) m[j] = valid ? sc[8 * hv + j] : -INFINITY;
+              const float gm = octet_column_max(m, lane);
+              const int cg = cb + 8 * hv + (lane & 7);
+              if (gp != nullptr && cg < k)
+                gp[(size_t)(cb + 8 * hv) * gstride] = (uint16_t)score_bin(gm);
+            }
           }
           if (cb + 16 <= k) {
 #pragma unroll
@@ -540,7 +563,7 @@ bool plan(int d, int k, ScoreCfg& c) {
 
 template <int D>
 cudaError_t launch_t(const ScoreCfg& c, const void* qk, int B, int H, int n, const float* mu,
-                     int k, float* S, int32_t* a, int32_t* mcount, void* prep,
+                     int k, float* S, int32_t* a, int32_t* mcount, uint16_t* gbins, void* prep,
                      unsigned int* err, cudaStream_t s) {
   CUtensorMap map;
   if (!q_tensor_map(qk, (unsigned long long)B * H * n, D, &map)) return cudaErrorInvalidValue;
@@ -562,7 +585,8 @@ cudaError_t launch_t(const ScoreCfg& c, const void* qk, int B, int H, int n, con
   launch_begin(K_SCORE_TC, s);
   e = launch_pdl(kern, dim3(cph, H), dim3(THREADS), c.smem, s, map, B, H, n, mu,
                  static_cast<const uint8_t*>(prep), k, c.kpad, c.acc_cols, c.stages, cph, S, a,
-                 mcount, err, injected_limit_ns(K_SCORE_TC));
+                 mcount, S != nullptr ? gbins : nullptr, gbin_stride(n), err,
+                 injected_limit_ns(K_SCORE_TC));
   launch_end(K_SCORE_TC, s);
   return e;
 }
@@ -581,15 +605,15 @@ size_t score_prep_bytes(int H, int d, int k) {
 }
 
 cudaError_t launch_score(const void* qk, rt_dtype dt, int B, int H, int n, int d, const float* mu,
-                         int k, float* S, int32_t* a, int32_t* mcount, void* prep,
-                         unsigned int* err, cudaStream_t s) {
+                         int k, float* S, int32_t* a, int32_t* mcount, uint16_t* gbins,
+                         void* prep, unsigned int* err, cudaStream_t s) {
   ScoreCfg c;
   if (dt == RT_BF16 && (d == 64 || d == 128) && plan(d, k, c) && tensor_maps_available() &&
       (reinterpret_cast<uintptr_t>(qk) & 15u) == 0) {
-    return d == 64 ? launch_t<64>(c, qk, B, H, n, mu, k, S, a, mcount, prep, err, s)
-                   : launch_t<128>(c, qk, B, H, n, mu, k, S, a, mcount, prep, err, s);
+    return d == 64 ? launch_t<64>(c, qk, B, H, n, mu, k, S, a, mcount, gbins, prep, err, s)
+                   : launch_t<128>(c, qk, B, H, n, mu, k, S, a, mcount, gbins, prep, err, s);
   }
-  return launch_score_simt(qk, dt, B * H, H, n, d, mu, k, S, a, mcount, s);
+  return launch_score_simt(qk, dt, B * H, H, n, d, mu, k, S, a, mcount, gbins, s);
 }
 
 }  // namespace rt

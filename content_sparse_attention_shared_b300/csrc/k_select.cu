@@ -40,17 +40,10 @@ namespace {
 
 constexpr int THREADS = 256;
 constexpr int WARPS = THREADS / 32;
-constexpr int NBINS = 2048;
+constexpr int NBINS = SCORE_BINS;  // score_bin: [-1, 1] -> [0, 2047], non-decreasing
 constexpr int BINS_PER_THREAD = NBINS / THREADS;
 constexpr int CAND_CAP = 1024;
 constexpr int MAX_STAGED_BINS = 80 * 1024;  // u16 bins staged in shared memory
-
-__device__ __forceinline__ int score_bin(float s) {
-  // non-decreasing in s; [-1, 1] -> [0, 2047] (NaN -> 0)
-  float f = (s + 1.0f) * 1024.0f;
-  f = fminf(fmaxf(f, 0.0f), (float)(NBINS - 1));
-  return (int)f;
-}
 
 struct SelectOut {
   int32_t* out;
@@ -565,7 +558,7 @@ select_topw_bound_kernel(const float* __restrict__ S, int n, int k, int w,
 // Shared memory: about n/4 + n/8 bytes + 16 KB, so several CTAs share an SM
 // and the first pass keeps enough loads in flight to stream at HBM speed.
 // ---------------------------------------------------------------------------
-constexpr int GSIZE = 8;
+constexpr int GSIZE = GROUP_SIZE;
 constexpr int GCAP = 1024;
 constexpr int GROUP_N_MAX = 262144;
 
@@ -575,9 +568,10 @@ inline size_t group_smem_bytes(int n) {
          (size_t)GCAP * 4;
 }
 
+template <bool FROM_GBINS>
 __global__ void __launch_bounds__(THREADS, 4)
-select_topw_group_kernel(const float* __restrict__ S, int n, int k, int w,
-                         int32_t* __restrict__ idx, int32_t* __restrict__ mcount,
+select_topw_group_kernel(const float* __restrict__ S, const uint16_t* __restrict__ gbins, int n,
+                         int k, int w, int32_t* __restrict__ idx, int32_t* __restrict__ mcount,
                          int32_t* __restrict__ slots) {
   pdl_trigger();
   extern __shared__ __align__(16) uint8_t gsm[];
@@ -605,47 +599,92 @@ select_topw_group_kernel(const float* __restrict__ S, int n, int k, int w,
   pdl_wait();
   __syncthreads();
 
-  // 1. bins of the group maxima (and this thread's largest group maximum)
   const int n4 = n >> 2;
   const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-  float tmax = -INFINITY;
-  for (int g0 = tid; g0 < NG; g0 += 4 * THREADS) {
-    float4 v[4][2];
+  int b0 = 0;
+  if constexpr (FROM_GBINS) {
+    // 1. the group bins the score kernel wrote: 8 groups per 16-byte load,
+    //    copied to shared memory (the padding past NG comes along, unused);
+    //    a thread's largest bin feeds the prefilter below
+    const uint4* src = reinterpret_cast<const uint4*>(gbins + ((size_t)bh * k + c) * gbin_stride(n));
+    uint4* dst = reinterpret_cast<uint4*>(gbin);
+    const int NV = (NG + 7) / 8;
+    int tb = -1;
+    for (int v0 = tid; v0 < NV; v0 += 4 * THREADS) {
+      uint4 v[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int g = g0 + u * THREADS;
-      v[u][0] = (g < NG && 2 * g < n4) ? __ldcg(row4 + 2 * g) : ninf;
-      v[u][1] = (g < NG && 2 * g + 1 < n4) ? __ldcg(row4 + 2 * g + 1) : ninf;
-    }
+      for (int u = 0; u < 4; ++u) {
+        const int i = v0 + u * THREADS;
+        v[u] = i < NV ? __ldcg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int g = g0 + u * THREADS;
-      if (g < NG) {
-        const float m = fmaxf(fmaxf(fmaxf(v[u][0].x, v[u][0].y), fmaxf(v[u][0].z, v[u][0].w)),
-                              fmaxf(fmaxf(v[u][1].x, v[u][1].y), fmaxf(v[u][1].z, v[u][1].w)));
-        gbin[g] = (uint16_t)score_bin(m);
-        tmax = fmaxf(tmax, m);
+      for (int u = 0; u < 4; ++u) {
+        const int i = v0 + u * THREADS;
+        if (i < NV) {
+          dst[i] = v[u];
+          const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (8 * i + e < NG) tb = max(tb, (int)((wv[e >> 1] >> (16 * (e & 1))) & 0xffffu));
+        }
       }
     }
-  }
-  // Prefilter: when every thread owns a group and w <= THREADS, the smallest
-  // thread maximum T0 is at most the w-th largest group maximum (the THREADS
-  // threads own THREADS distinct groups with maxima >= T0), so b_L >= bin(T0)
-  // and only group maxima in bins >= bin(T0) need counting.  This keeps the
-  // histogram small and its atomics spread over few, uncontended bins.
-  __shared__ float wmin[WARPS];
-  {
-    float tm = tmax;
+    // Prefilter: the min(THREADS, NV) threads that own groups own distinct
+    // groups, each one of bin >= the smallest thread maximum b0; with w no
+    // more than them, b_L >= b0, and only bins >= b0 need counting.
+    __shared__ int wmin_b[WARPS];
+    {
+      int tm = tb >= 0 ? tb : NBINS;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tm = fminf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
-    if (lane == 0) wmin[tid >> 5] = tm;
-  }
-  __syncthreads();
-  int b0 = 0;
-  if (w <= THREADS && NG >= THREADS) {
-    float t0 = wmin[0];
-    for (int i = 1; i < WARPS; ++i) t0 = fminf(t0, wmin[i]);
-    b0 = score_bin(t0);
+      for (int o = 16; o > 0; o >>= 1) tm = min(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+      if (lane == 0) wmin_b[tid >> 5] = tm;
+    }
+    __syncthreads();
+    if (w <= min(THREADS, NV)) {
+      int t0 = wmin_b[0];
+      for (int i = 1; i < WARPS; ++i) t0 = min(t0, wmin_b[i]);
+      b0 = t0;
+    }
+  } else {
+    // 1. bins of the group maxima (and this thread's largest group maximum)
+    float tmax = -INFINITY;
+    for (int g0 = tid; g0 < NG; g0 += 4 * THREADS) {
+      float4 v[4][2];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int g = g0 + u * THREADS;
+        v[u][0] = (g < NG && 2 * g < n4) ? __ldcg(row4 + 2 * g) : ninf;
+        v[u][1] = (g < NG && 2 * g + 1 < n4) ? __ldcg(row4 + 2 * g + 1) : ninf;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int g = g0 + u * THREADS;
+        if (g < NG) {
+          const float m = fmaxf(fmaxf(fmaxf(v[u][0].x, v[u][0].y), fmaxf(v[u][0].z, v[u][0].w)),
+                                fmaxf(fmaxf(v[u][1].x, v[u][1].y), fmaxf(v[u][1].z, v[u][1].w)));
+          gbin[g] = (uint16_t)score_bin(m);
+          tmax = fmaxf(tmax, m);
+        }
+      }
+    }
+    // Prefilter: when every thread owns a group and w <= THREADS, the smallest
+    // thread maximum T0 is at most the w-th largest group maximum (the THREADS
+    // threads own THREADS distinct groups with maxima >= T0), so b_L >= bin(T0)
+    // and only group maxima in bins >= bin(T0) need counting.  This keeps the
+    // histogram small and its atomics spread over few, uncontended bins.
+    __shared__ float wmin[WARPS];
+    {
+      float tm = tmax;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) tm = fminf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+      if (lane == 0) wmin[tid >> 5] = tm;
+    }
+    __syncthreads();
+    if (w <= THREADS && NG >= THREADS) {
+      float t0 = wmin[0];
+      for (int i = 1; i < WARPS; ++i) t0 = fminf(t0, wmin[i]);
+      b0 = score_bin(t0);
+    }
   }
   // counts of the bins >= b0, one shared atomic per distinct bin of a warp
   for (int g0 = 0; g0 < NG; g0 += THREADS) {
@@ -810,8 +849,18 @@ select_topw_group_kernel(const float* __restrict__ S, int n, int k, int w,
 
 }  // namespace
 
-cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* idx,
-                          int32_t* mcount, int32_t* slots, cudaStream_t s) {
+// Group bins from the score epilogue cost that kernel a shuffle reduction per
+// 8 columns; they pay only where the select would otherwise stream long rows:
+// measured on B300, n = 65536 (256 KiB rows) gains about 75 us a forward at
+// H = 8, k = 256, while n = 8192 and n = 12288 lose 8 and 15 us.
+constexpr int GROUP_BINS_MIN_N = 32768;
+
+bool select_wants_group_bins(int n) {
+  return n >= GROUP_BINS_MIN_N && n <= GROUP_N_MAX && (n & 3) == 0;
+}
+
+cudaError_t launch_select(const float* S, const uint16_t* gbins, int BH, int n, int k, int w,
+                          int32_t* idx, int32_t* mcount, int32_t* slots, cudaStream_t s) {
   dim3 grid(k, BH);
   const int staged = n <= MAX_STAGED_BINS ? 1 : 0;
   // staged bins (u16, padded to 16 bytes) + two chunk masks per 32 positions
@@ -821,6 +870,16 @@ cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* 
   const size_t smem = staged ? stage_bytes(n) : 0;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(select_topw_kernel), (int)stage_bytes(MAX_STAGED_BINS));
   if (e != cudaSuccess) return e;
+  if (gbins != nullptr && n <= GROUP_N_MAX && (n & 3) == 0) {
+    const size_t gsmem = group_smem_bytes(n);
+    e = set_smem_limit(reinterpret_cast<const void*>(select_topw_group_kernel<true>), (int)gsmem);
+    if (e != cudaSuccess) return e;
+    launch_begin(K_SELECT, s);
+    e = launch_pdl(select_topw_group_kernel<true>, grid, dim3(THREADS), gsmem, s, S, gbins, n, k,
+                   w, idx, mcount, slots);
+    launch_end(K_SELECT, s);
+    return e;
+  }
   if (n <= BOUND_N_MAX && (n & 3) == 0 && w <= THREADS) {
     launch_begin(K_SELECT, s);
     e = launch_pdl(select_topw_bound_kernel, grid, dim3(THREADS), 0, s, S, n, k, w, idx, mcount,
@@ -830,11 +889,11 @@ cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* 
   }
   if (n <= GROUP_N_MAX && (n & 3) == 0) {
     const size_t gsmem = group_smem_bytes(n);
-    e = set_smem_limit(reinterpret_cast<const void*>(select_topw_group_kernel), (int)gsmem);
+    e = set_smem_limit(reinterpret_cast<const void*>(select_topw_group_kernel<false>), (int)gsmem);
     if (e != cudaSuccess) return e;
     launch_begin(K_SELECT, s);
-    e = launch_pdl(select_topw_group_kernel, grid, dim3(THREADS), gsmem, s, S, n, k, w, idx,
-                   mcount, slots);
+    e = launch_pdl(select_topw_group_kernel<false>, grid, dim3(THREADS), gsmem, s, S, nullptr, n,
+                   k, w, idx, mcount, slots);
     launch_end(K_SELECT, s);
     return e;
   }

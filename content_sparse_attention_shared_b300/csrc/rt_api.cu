@@ -176,13 +176,53 @@ bool bf16_tensor_map_2d(const void* base, unsigned long long rows, unsigned cols
   return true;
 }
 
+bool f32_tensor_map_3d(const void* base, unsigned cols, unsigned long long rows,
+                       unsigned batches, unsigned box_rows, CUtensorMap* out) {
+  struct Entry {
+    const void* ptr;
+    unsigned long long rows;
+    unsigned cols, batches, box_rows;
+    CUtensorMap map;
+  };
+  constexpr int N = 16;
+  static std::mutex mu;
+  static Entry cache[N];
+  static int used = 0, next = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].ptr == base && cache[i].rows == rows && cache[i].cols == cols &&
+          cache[i].batches == batches && cache[i].box_rows == box_rows) {
+        *out = cache[i].map;
+        return true;
+      }
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || cols % 32 != 0 || box_rows < 1 || box_rows > 256) return false;
+  CUtensorMap map;
+  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batches};
+  const cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)cols * 4 * rows};
+  const cuuint32_t box[3] = {32u, (cuuint32_t)box_rows, 1u};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  cache[next] = Entry{base, rows, cols, batches, box_rows, map};
+  next = (next + 1) % N;
+  if (used < N) ++used;
+  *out = map;
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 // workspace layout
 // ---------------------------------------------------------------------------
 static inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct FwdLayout {
-  size_t err, S, mcount, slots, idx, assign, yslot, prep, idx_k, mvis, ema, total;
+  size_t err, S, gbins, mcount, slots, idx, assign, yslot, prep, idx_k, mvis, ema, total;
 };
 
 static FwdLayout fwd_layout(int B, int H, int n, int d, int k, int w, rt_dtype dt) {
@@ -191,6 +231,8 @@ static FwdLayout fwd_layout(int B, int H, int n, int d, int k, int w, rt_dtype d
   size_t off = 0;
   L.err = off; off += 256;
   L.S = off; off += align256(BH * k * n * sizeof(float));
+  L.gbins = off;
+  if (select_wants_group_bins(n)) off += align256(BH * k * (size_t)gbin_stride(n) * sizeof(uint16_t));
   L.mcount = off; off += align256(BH * n * sizeof(int32_t));
   L.slots = off; off += align256(BH * n * SLOTS_PER_ROW * sizeof(int32_t));
   L.idx = off; off += align256(BH * k * w * sizeof(int32_t));
@@ -351,10 +393,13 @@ rt_status rt_route_assign(const void* qk, rt_dtype dt, int B, int H, int n, int 
   float* S = scores ? scores : reinterpret_cast<float*>(ws + L.S);
   unsigned int* err = reinterpret_cast<unsigned int*>(ws + L.err);
   void* prep = score_prep_bytes(H, d, k) ? static_cast<void*>(ws + L.prep) : nullptr;
-  st = from_cuda(launch_score(qk, dt, B, H, n, d, centroids, k, S, assign, nullptr, prep, err, s),
-                 "score kernel");
+  uint16_t* gbins =
+      select_wants_group_bins(n) ? reinterpret_cast<uint16_t*>(ws + L.gbins) : nullptr;
+  st = from_cuda(
+      launch_score(qk, dt, B, H, n, d, centroids, k, S, assign, nullptr, gbins, prep, err, s),
+      "score kernel");
   if (st != RT_OK) return st;
-  st = from_cuda(launch_select(S, BH, n, k, w, idx, nullptr, nullptr, s), "select kernel");
+  st = from_cuda(launch_select(S, gbins, BH, n, k, w, idx, nullptr, nullptr, s), "select kernel");
   if (st != RT_OK) return st;
   return ok();
 }
@@ -427,14 +472,17 @@ static rt_status forward(const void* q, const void* kp, const void* v, rt_dtype 
     return from_cuda(e, "centroid update (side stream)");
   };
 
-  st = from_cuda(launch_score(q, dt, B, H, n, d, centroids, kc, S, assign, mcount, prep, err, s),
-                 "score kernel");
+  uint16_t* gbins =
+      select_wants_group_bins(n) ? reinterpret_cast<uint16_t*>(ws + L.gbins) : nullptr;
+  st = from_cuda(
+      launch_score(q, dt, B, H, n, d, centroids, kc, S, assign, mcount, gbins, prep, err, s),
+      "score kernel");
   if (st != RT_OK) return st;
   if (ema.mu != nullptr) {
     st = fork_ema();
     if (st != RT_OK) return st;
   }
-  st = from_cuda(launch_select(S, BH, n, kc, w, idx, mcount, slots, s), "select kernel");
+  st = from_cuda(launch_select(S, gbins, BH, n, kc, w, idx, mcount, slots, s), "select kernel");
   if (st != RT_OK) return st;
   int32_t* idx_k = nullptr;
   int32_t* mvis = nullptr;
@@ -442,10 +490,11 @@ static rt_status forward(const void* q, const void* kp, const void* v, rt_dtype 
     idx_k = idx_k_out ? idx_k_out : reinterpret_cast<int32_t*>(ws + L.idx_k);
     mvis = reinterpret_cast<int32_t*>(ws + L.mvis);
     // the keys' routing; the score kernel zeroes mvis for the attention
-    st = from_cuda(launch_score(kp, dt, B, H, n, d, centroids, kc, S, nullptr, mvis, prep, err, s),
-                   "score kernel (keys)");
+    st = from_cuda(
+        launch_score(kp, dt, B, H, n, d, centroids, kc, S, nullptr, mvis, gbins, prep, err, s),
+        "score kernel (keys)");
     if (st != RT_OK) return st;
-    st = from_cuda(launch_select(S, BH, n, kc, w, idx_k, nullptr, nullptr, s),
+    st = from_cuda(launch_select(S, gbins, BH, n, kc, w, idx_k, nullptr, nullptr, s),
                    "select kernel (keys)");
     if (st != RT_OK) return st;
     if (attention_tc_supported(dt, d, w)) {

@@ -54,6 +54,11 @@ cudaError_t set_smem_limit(const void* func, int bytes);
 bool tensor_maps_available();
 bool bf16_tensor_map_2d(const void* base, unsigned long long rows, unsigned cols,
                         unsigned box_cols, unsigned box_rows, CUtensorMap* out);
+// 3-D tensor map of fp32 rows [batches][rows][cols] (cols contiguous, a
+// multiple of 32) with boxes of 32 columns x box_rows rows x 1 batch and
+// 128-byte swizzle, for bulk stores of staged row tiles (cached the same way).
+bool f32_tensor_map_3d(const void* base, unsigned cols, unsigned long long rows,
+                       unsigned batches, unsigned box_rows, CUtensorMap* out);
 
 // Programmatic dependent launch: every kernel of the library is launched with
 // programmatic stream serialization allowed, tells the runtime at its start
@@ -196,14 +201,63 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 }
 
 // ---------------------------------------------------------------------------
+// group bins: a by-product of the score kernels for the select kernel
+// ---------------------------------------------------------------------------
+// Scores are cosines of unit vectors, so they lie in [-1, 1].  A score's bin is
+// its interval in a partition of [-1, 1] into SCORE_BINS equal parts (clamped;
+// non-decreasing in the score, so every score of a higher bin is strictly
+// larger; NaN -> 0).  For every run of GROUP_SIZE consecutive positions of a
+// (batch*head, centroid) row the score kernels can also write the bin of the
+// run's largest score ("group bin") to gbins [BH, k, gbin_stride(n)] u16; the
+// entries past ceil(n / GROUP_SIZE) of a row are padding and never written.
+// Since the bin is monotone, a group's bin is the largest bin of its members.
+constexpr int SCORE_BINS = 2048;
+constexpr int GROUP_SIZE = 8;
+
+__host__ __device__ inline int gbin_stride(int n) {
+  const int ng = (n + GROUP_SIZE - 1) / GROUP_SIZE;
+  return (ng + 7) & ~7;  // rows start on 16-byte boundaries
+}
+
+__device__ __forceinline__ int score_bin(float s) {
+  float f = (s + 1.0f) * (0.5f * SCORE_BINS);
+  f = fminf(fmaxf(f, 0.0f), (float)(SCORE_BINS - 1));
+  return (int)f;
+}
+
+// Column maxima over the 8 lanes of each aligned lane octet (lanes 8m..8m+7):
+// v holds a lane's value for 8 columns; lane l returns the maximum over its
+// octet of column (l & 7).  A reduce-scatter in three exchange steps (4, 2,
+// then 1 value per lane), 7 shuffles for 8 columns.  Every lane of the warp
+// must call it.
+__device__ __forceinline__ float octet_column_max(const float (&v)[8], int lane) {
+  const bool b2 = (lane & 4) != 0, b1 = (lane & 2) != 0, b0 = (lane & 1) != 0;
+  float u[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float keep = b2 ? v[j + 4] : v[j], give = b2 ? v[j] : v[j + 4];
+    u[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, 4));
+  }
+  float u2[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float keep = b1 ? u[j + 2] : u[j], give = b1 ? u[j] : u[j + 2];
+    u2[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, 2));
+  }
+  const float keep = b0 ? u2[1] : u2[0], give = b0 ? u2[0] : u2[1];
+  return fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, 1));
+}
+
+// ---------------------------------------------------------------------------
 // launchers (one per kernel family); all asynchronous on `s`
 // ---------------------------------------------------------------------------
 
 // normalise + score + argmax.  S: [BH,k,n] fp32 (may be null), a: [BH,n]
-// (may be null), mcount: [BH,n] zeroed here when non-null.
+// (may be null), mcount: [BH,n] zeroed here when non-null, gbins: the group
+// bins [BH,k,gbin_stride(n)] (may be null; written only with S).
 cudaError_t launch_score_simt(const void* qk, rt_dtype dt, int BH, int H, int n, int d,
                               const float* mu, int k, float* S, int32_t* a,
-                              int32_t* mcount, cudaStream_t s);
+                              int32_t* mcount, uint16_t* gbins, cudaStream_t s);
 
 // dispatcher: tcgen05 scoring for bf16 with k <= 256 (fp32-accurate via a
 // three-plane split of the centroids), the SIMT kernel otherwise.  prep: device
@@ -213,16 +267,23 @@ cudaError_t launch_score_simt(const void* qk, rt_dtype dt, int BH, int H, int n,
 bool score_tc_supported(rt_dtype dt, int d, int k);
 size_t score_prep_bytes(int H, int d, int k);
 cudaError_t launch_score(const void* qk, rt_dtype dt, int B, int H, int n, int d, const float* mu,
-                         int k, float* S, int32_t* a, int32_t* mcount, void* prep,
-                         unsigned int* err, cudaStream_t s);
+                         int k, float* S, int32_t* a, int32_t* mcount, uint16_t* gbins,
+                         void* prep, unsigned int* err, cudaStream_t s);
 
 // top-w per centroid in ascending position order; counts memberships into
 // mcount (atomic integer increments; may be null) and records up to
 // SLOTS_PER_ROW global slot ids (c*w + slot) per position in `slots`
-// [BH, n, SLOTS_PER_ROW] (may be null; entry order is arbitrary).
+// [BH, n, SLOTS_PER_ROW] (may be null; entry order is arbitrary).  gbins:
+// the group bins the score kernel wrote with S (may be null: the select then
+// derives everything from S).
 constexpr int SLOTS_PER_ROW = 8;
-cudaError_t launch_select(const float* S, int BH, int n, int k, int w, int32_t* idx,
-                          int32_t* mcount, int32_t* slots, cudaStream_t s);
+
+// Whether the forward asks the score kernel for group bins: only for rows long
+// enough that streaming them costs the select more than the bins cost the
+// score epilogue.
+bool select_wants_group_bins(int n);
+cudaError_t launch_select(const float* S, const uint16_t* gbins, int BH, int n, int k, int w,
+                          int32_t* idx, int32_t* mcount, int32_t* slots, cudaStream_t s);
 
 // in-cluster attention.  Rows of positions with mcount == 1 go straight to
 // `out`; rows of positions in several clusters go to yslot [BH,k,w,d] fp32.

@@ -155,9 +155,10 @@ extern "C" rt_status rt_route_assign_noalloc(const void* qk, rt_dtype dt, int B,
   unsigned int* err = static_cast<unsigned int*>(addrs.status);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int BH = B * H;
-  cudaError_t e = rt::launch_score(qk, dt, B, H, n, d, centroids, k, S, assign, nullptr, nullptr, err, s);
+  cudaError_t e =
+      rt::launch_score(qk, dt, B, H, n, d, centroids, k, S, assign, nullptr, nullptr, nullptr, err, s);
   if (e != cudaSuccess) return rt::record_error(RT_ERR_CUDA, cudaGetErrorString(e));
-  e = rt::launch_select(S, BH, n, k, w, idx, nullptr, nullptr, s);
+  e = rt::launch_select(S, nullptr, BH, n, k, w, idx, nullptr, nullptr, s);
   if (e != cudaSuccess) return rt::record_error(RT_ERR_CUDA, cudaGetErrorString(e));
   return rt::record_error(RT_OK, "");
 }

@@ -174,6 +174,9 @@ SWEEP = [
     (1, 2, 700, 64, 5, 200, "bf16", False),     # two row tiles in one CTA, non-causal
     (2, 1, 500, 128, 3, 256, "bf16", True),     # two full row tiles
     (1, 1, 300, 64, 2, 150, "bf16", True),      # two row tiles, d = 64
+    (1, 1, 33004, 64, 6, 256, "bf16", True),    # long rows: select from group bins, last group ragged
+    (1, 2, 32772, 128, 3, 200, "f32", True),    # the same through the fp32 score kernel
+    (1, 1, 32771, 64, 4, 100, "bf16", True),    # long rows with n % 4 != 0: no group bins
 ]
 
 
