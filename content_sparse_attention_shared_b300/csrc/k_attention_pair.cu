@@ -17,9 +17,12 @@
 // rows, warps 4-7 tile 1's (the TMEM lane quadrant of warp w is w % 4), one
 // thread per row: the row's maximum, exp2 of the visible columns, P (bf16)
 // into shared memory (tile 1's over Q, which S no longer needs), then O = P V
-// into the score columns, the O rows staged in shared memory as fp32 and
-// written row-contiguously: bf16 to `out` for a position in one cluster, fp32
-// to its slot row of `yslot` otherwise.  Every mbarrier wait is bounded; one
+// into the score columns together with P's row sums (the same P against a
+// column of ones), the O rows divided by their sums and staged over Q and V as
+// 128-byte-swizzled boxes: one bulk tensor store per 32 features writes the
+// cluster's slot rows to `yslot` (fp32), while the warps copy the rows of
+// positions in exactly one cluster to `out` (bf16).  Chunks of 16 keys that
+// every row of a warp sees skip the mask.  Every mbarrier wait is bounded; one
 // that runs out sets the device status word, waits (bounded again) for the
 // CTA's own MMAs, gives back TMEM and returns.
 #include "attn_common.cuh"
@@ -42,8 +45,11 @@ struct PairSmem {
   static constexpr int P0_OFF = QB + VB;
   // tile 1's P goes over Q once the scores are done when it fits there
   static constexpr int P1_OFF = QB >= PB ? Q_OFF : P0_OFF + PB;
-  static constexpr int BYTES = (QB >= PB ? P0_OFF + PB : P1_OFF + PB);
+  // B operand of the row-sum MMA: 16 x 256 keys of bf16, row 0 all ones
+  static constexpr int ONES_OFF = (QB >= PB ? P0_OFF + PB : P1_OFF + PB);
+  static constexpr int BYTES = ONES_OFF + 16 * NR * 2;
   static_assert(QB + VB >= NR * D * 4, "the output staging fits over Q and V");
+  static_assert(ONES_OFF % 1024 == 0, "aligned operand");
 };
 
 // Gather NR rows (positions pos[r], -1 = zero row) of D bf16 into the
@@ -69,7 +75,8 @@ __device__ __forceinline__ void gather_rows_sw128(uint8_t* dst, const bf16* __re
 
 template <int D>
 __global__ void __launch_bounds__(PR_THREADS, 1)
-attention_pair_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, int n, int k, int w,
+attention_pair_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __restrict__ q,
+                      const bf16* __restrict__ v, int n, int k, int w,
                       int causal, float scale_log2, const int32_t* __restrict__ idx,
                       const int32_t* __restrict__ mcount, bf16* __restrict__ out,
                       float* __restrict__ yslot, unsigned int* __restrict__ err,
@@ -108,6 +115,16 @@ attention_pair_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
   if (warp == 0) {
     tc::tmem_alloc(&tmem_base_sh, 512);
     tc::tmem_relinquish();
+  }
+  if (tid < 64) {
+    // the ones operand: 16 rows (n) x 256 keys, K-major core matrices of 8 rows
+    // x 16 bytes, core matrix (n/8, key/8) at ((n/8)*32 + key/8)*128: thread i
+    // writes core matrix i, whose first row is n = 0 for i < 32
+    uint4* o4 = reinterpret_cast<uint4*>(sm + L::ONES_OFF + tid * 128);
+    const uint32_t one2 = tid < 32 ? 0x3F803F80u : 0u;  // two bf16 1.0
+    o4[0] = make_uint4(one2, one2, one2, one2);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) o4[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
   gather_rows_sw128<D>(sm + L::Q_OFF, q_bh, pos_s);
@@ -164,6 +181,9 @@ attention_pair_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
   if (!row_valid) jmax = 0;
   const int whi = __reduce_max_sync(0xffffffffu, jmax);
   const int ch_hi = (whi + 15) >> 4;
+  // keys every valid row of the warp sees: those chunks need no mask (an
+  // invalid row's values are never stored)
+  const int fhi = __reduce_min_sync(0xffffffffu, row_valid ? jmax : NR);
   float mrow = -INFINITY;
   for (int ch = 0; ch < ch_hi; ch += 2) {
     uint32_t rr[2][16];
@@ -172,16 +192,19 @@ attention_pair_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
     tc::tmem_ld_wait();
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      if (ch + hh >= ch_hi) break;
+      const int c = ch + hh;
+      if (c >= ch_hi) break;
+      if (c * 16 + 16 <= fhi) {
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const int col = (ch + hh) * 16 + jj;
-        if (col < jmax) mrow = fmaxf(mrow, __uint_as_float(rr[hh][jj]));
+        for (int jj = 0; jj < 16; ++jj) mrow = fmaxf(mrow, __uint_as_float(rr[hh][jj]));
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+          if (c * 16 + jj < jmax) mrow = fmaxf(mrow, __uint_as_float(rr[hh][jj]));
       }
     }
   }
-  const float mscaled = (mrow == -INFINITY) ? 0.0f : mrow * scale_log2;
-  float lsum = 0.0f;
+  const float neg_m = (mrow == -INFINITY) ? 0.0f : -mrow * scale_log2;
   // P row: K-major core matrices, element (r, key) at (r/8)*(kt*16) +
   // (key/8)*128 + (r%8)*16 + (key%8)*2
   uint8_t* pt = sm + (t == 0 ? L::P0_OFF : L::P1_OFF);
@@ -200,6 +223,7 @@ attention_pair_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
 #pragma unroll 1
     for (int ch = ch_hi; ch < kt / 16; ++ch) store_chunk(ch, zero);
   }
+  // P = 2^(S*scale*log2e - max), bf16; its row sums come from the O MMA
 #pragma unroll 1
   for (int ch = 0; ch < ch_hi; ch += 2) {
     uint32_t rr[2][16];
@@ -208,18 +232,29 @@ attention_pair_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
     tc::tmem_ld_wait();
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      if (ch + hh >= ch_hi) break;
+      const int c = ch + hh;
+      if (c >= ch_hi) break;
       uint32_t pk[8];
+      if (c * 16 + 16 <= fhi) {
 #pragma unroll
-      for (int jj = 0; jj < 16; jj += 2) {
-        const int col = (ch + hh) * 16 + jj;
-        const float e0 = col < jmax ? exp2f(__uint_as_float(rr[hh][jj]) * scale_log2 - mscaled) : 0.0f;
-        const float e1 = col + 1 < jmax ? exp2f(__uint_as_float(rr[hh][jj + 1]) * scale_log2 - mscaled) : 0.0f;
-        const uint32_t pp = pack_bf16(e0, e1);
-        pk[jj >> 1] = pp;
-        lsum += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xffff0000u);
+        for (int jj = 0; jj < 16; jj += 2) {
+          const float e0 = tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj]), scale_log2, neg_m));
+          const float e1 = tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj + 1]), scale_log2, neg_m));
+          pk[jj >> 1] = pack_bf16(e0, e1);
+        }
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 16; jj += 2) {
+          const int col = c * 16 + jj;
+          const float e0 =
+              col < jmax ? tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj]), scale_log2, neg_m)) : 0.0f;
+          const float e1 =
+              col + 1 < jmax ? tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj + 1]), scale_log2, neg_m))
+                             : 0.0f;
+          pk[jj >> 1] = pack_bf16(e0, e1);
+        }
       }
-      store_chunk(ch + hh, pk);
+      store_chunk(c, pk);
     }
   }
   tc::fence_proxy_async_smem();  // P (generic writes) before the MMA reads it
@@ -227,10 +262,13 @@ attention_pair_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
   __syncthreads();
   tc::tc_fence_after_sync();
 
-  // ---- O = P V into the score columns ---------------------------------------
+  // ---- O = P V into the score columns, and the row sums of the same bf16 P
+  //      (P times a column of ones) just after them -----------------------------
   if (tid == 0) {
     const uint32_t va = tc::smem_u32(sm + L::V_OFF);
+    const uint32_t ones = tc::smem_u32(sm + L::ONES_OFF);
     const uint32_t idesc_o = tc::idesc_f16(ROWS, D, true, false, true);
+    const uint32_t idesc_l = tc::idesc_f16(ROWS, 16, true, false, false);
 #pragma unroll
     for (int tt = 0; tt < 2; ++tt) {
       const int ktt = tt == 0 ? n0 : NR;
@@ -239,6 +277,8 @@ attention_pair_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
         const uint64_t ad = tc::smem_desc_noswizzle(pa + kk * 256, 128, ktt * 16);
         const uint64_t bd = tc::smem_desc_sw128_mn(va + kk * 2048, NR * 128, 1024);
         tc::mma_f16_ss(tmem + tt * 256, ad, bd, idesc_o, kk > 0 ? 1u : 0u);
+        const uint64_t od = tc::smem_desc_noswizzle(ones + kk * 256, 128, NR * 16);
+        tc::mma_f16_ss(tmem + tt * 256 + D, ad, od, idesc_l, kk > 0 ? 1u : 0u);
       }
     }
     tc::mma_commit(&bar_o);
@@ -255,44 +295,86 @@ attention_pair_kernel(const bf16* __restrict__ q, const bf16* __restrict__ v, in
   }
   tc::tc_fence_after_sync();
 
-  // ---- O rows: TMEM -> fp32 staging over Q and V (free now) -> global -------
-  constexpr int CPR = D / 4;     // 16-byte fp32 chunks per row
-  constexpr int RPI = 32 / CPR;  // rows per warp instruction in the copy-out
-  float4* stage = reinterpret_cast<float4*>(sm);
-  const float inv_l = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+  // ---- O rows divided by their sums: TMEM -> fp32 staging over Q and V (free
+  //      now) as bulk-store boxes: D/32 segments of [256 rows][128 bytes],
+  //      16-byte chunk q of row s at (q ^ (s % 8)) (128-byte swizzle) ----------
+  uint32_t lraw;
+  tc::tmem_ld1(t_row + D, lraw);
 #pragma unroll
-  for (int c0 = 0; c0 < D; c0 += 16) {
-    uint32_t rr[16];
-    tc::tmem_ld16(t_row + c0, rr);
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t rr[2][16];
+    tc::tmem_ld16(t_row + c0, rr[0]);
+    tc::tmem_ld16(t_row + c0 + 16, rr[1]);
     tc::tmem_ld_wait();
+    const float lsum = __uint_as_float(lraw);
+    const float inv_l = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < 8; ++q4) {
       const int chunk = c0 / 4 + q4;
-      stage[slot * CPR + (chunk ^ (slot & 7))] =
-          make_float4(__uint_as_float(rr[4 * q4]) * inv_l, __uint_as_float(rr[4 * q4 + 1]) * inv_l,
-                      __uint_as_float(rr[4 * q4 + 2]) * inv_l,
-                      __uint_as_float(rr[4 * q4 + 3]) * inv_l);
+      const uint32_t* x = &rr[q4 >> 2][4 * (q4 & 3)];
+      *reinterpret_cast<float4*>(sm + (chunk >> 3) * (NR * 128) + slot * 128 +
+                                 (((chunk & 7) ^ (slot & 7)) << 4)) =
+          make_float4(__uint_as_float(x[0]) * inv_l, __uint_as_float(x[1]) * inv_l,
+                      __uint_as_float(x[2]) * inv_l, __uint_as_float(x[3]) * inv_l);
     }
   }
   tc::tc_fence_before_sync();
+  tc::fence_proxy_async_smem();  // the staged rows, before the bulk store reads them
   __syncthreads();
-  // each warp writes 32 slots, row-contiguously
-  const int chn = lane % CPR;
-#pragma unroll 4
-  for (int it = 0; it < 32 / RPI; ++it) {
-    const int s = warp * 32 + it * RPI + lane / CPR;
-    const int p = pos_s[s];
-    if (s >= w || p < 0) continue;
-    const float4 val = stage[s * CPR + (chn ^ (s & 7))];
-    if (m_s[s] == 1) {
-      uint2 u;
-      u.x = pack_bf16(val.x, val.y);
-      u.y = pack_bf16(val.z, val.w);
-      reinterpret_cast<uint2*>(out + ((size_t)bh * n + p) * D)[chn] = u;
-    } else {
-      reinterpret_cast<float4*>(yslot + (((size_t)bh * k + c) * w + s) * D)[chn] = val;
+  // every slot row of the cluster to `yslot` (fp32), one bulk tensor store per
+  // 32 features; rows of positions in exactly one cluster also straight to
+  // `out` as bf16, a warp per row
+  if (tid == 0) {
+#pragma unroll
+    for (int sg = 0; sg < D / 32; ++sg)
+      tc::tma_store_3d(&ymap, sm + sg * (NR * 128), sg * 32, c * w, bh);
+    tc::bulk_commit();
+  }
+  {
+    const int my_s = warp * 32 + lane;
+    const int my_p = pos_s[my_s];
+    unsigned single = __ballot_sync(0xffffffffu, my_s < w && my_p >= 0 && m_s[my_s] == 1);
+    bf16* out_bh = out + (size_t)bh * n * D;
+    if constexpr (D == 128) {
+      while (single) {
+        const int i = __ffs(single) - 1;
+        single &= single - 1;
+        const int row = warp * 32 + i;
+        const int p = __shfl_sync(0xffffffffu, my_p, i);
+        const float4 val = *reinterpret_cast<const float4*>(
+            sm + (lane >> 3) * (NR * 128) + row * 128 + (((lane & 7) ^ (row & 7)) << 4));
+        uint2 u;
+        u.x = pack_bf16(val.x, val.y);
+        u.y = pack_bf16(val.z, val.w);
+        reinterpret_cast<uint2*>(out_bh + (size_t)p * D)[lane] = u;
+      }
+    } else {  // D == 64: 16 chunks a row, two rows a pass
+      const int half = lane >> 4, cc = lane & 15;
+      while (single) {
+        const int i0 = __ffs(single) - 1;
+        single &= single - 1;
+        int i1 = -1;
+        if (single) {
+          i1 = __ffs(single) - 1;
+          single &= single - 1;
+        }
+        const int p0 = __shfl_sync(0xffffffffu, my_p, i0);
+        const int p1 = __shfl_sync(0xffffffffu, my_p, i1 < 0 ? i0 : i1);
+        const int i = half ? i1 : i0;
+        if (i >= 0) {
+          const int row = warp * 32 + i;
+          const int p = half ? p1 : p0;
+          const float4 val = *reinterpret_cast<const float4*>(
+              sm + (cc >> 3) * (NR * 128) + row * 128 + (((cc & 7) ^ (row & 7)) << 4));
+          uint2 u;
+          u.x = pack_bf16(val.x, val.y);
+          u.y = pack_bf16(val.z, val.w);
+          reinterpret_cast<uint2*>(out_bh + (size_t)p * D)[cc] = u;
+        }
+      }
     }
   }
+  if (tid == 0) tc::bulk_wait_all();  // the bulk stores have read the rows and landed
   tc::tc_fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
@@ -307,8 +389,12 @@ cudaError_t launch_pair_t(const void* q, const void* v, int BH, int n, int k, in
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   const float scale_log2 = scale * 1.4426950408889634f;
+  // yslot as [BH][k*w slot rows][D] fp32; a box is one cluster's w rows
+  CUtensorMap ymap;
+  if (!f32_tensor_map_3d(yslot, D, (unsigned long long)k * w, (unsigned)BH, (unsigned)w, &ymap))
+    return cudaErrorInvalidValue;
   launch_begin(K_ATTN_TC, s);
-  e = launch_pdl(kern, dim3(k, BH), dim3(PR_THREADS), smem, s, static_cast<const bf16*>(q),
+  e = launch_pdl(kern, dim3(k, BH), dim3(PR_THREADS), smem, s, ymap, static_cast<const bf16*>(q),
                  static_cast<const bf16*>(v), n, k, w, causal, scale_log2, idx, mcount,
                  static_cast<bf16*>(out), yslot, err, injected_limit_ns(K_ATTN_TC));
   launch_end(K_ATTN_TC, s);
