@@ -1,7 +1,7 @@
 """Routing-attention benchmark (one JSON line on stdout, rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload c3] [--no-configs] [--no-cpu-baseline]
+                    [--workload c3] [--no-configs] [--no-cpu-baseline] [--sequential-step]
 
 A step is one pass of the whole hot path over one batch of synthetic input:
 routing (normalise, score, argmax, top-w per centroid, position sort),
@@ -9,8 +9,11 @@ in-cluster causal attention, the averaging scatter and, where the workload
 has one, the centroid update.  The headline workload is the n=8192, H=8,
 d=128 configuration (mix128_bf16_b1h8_n8192_d128_k128_w64).
 
-ours:       CUDA library; device time with CUDA events per step (K replays of
-            the step captured as one CUDA graph), L2 flushed (256 MiB write)
+ours:       CUDA library; the step is one rt_routing_attention_step call (the
+            forward, with the centroid update on a side stream from the end
+            of the score kernel; --sequential-step: rt_routing_attention then
+            rt_centroid_ema); device time with CUDA events per step (K replays
+            of the step captured as one CUDA graph), L2 flushed (256 MiB write)
             before every timed step; e2e = the same step through the public
             API with pinned-host inputs copied in and the output copied out
             inside the timed region; per-kernel times from the library's launch
@@ -756,7 +759,7 @@ def run_ours(args, wl_id, wl):
                                      getattr(props, "pci_device_id", 0))
 
     # ---- the headline workload ------------------------------------------
-    m = Measured(wl, dev, fused=args.fused_step)
+    m = Measured(wl, dev, fused=not args.sequential_step)
     m.capture(args.warmup)
     clk = ClockSampler(local, pci)
     t_ms = m.timed(args.steps, flush, stream, world, clocks=clk, soak_ms=args.soak_ms)
@@ -777,7 +780,7 @@ def run_ours(args, wl_id, wl):
             if cid == wl_id:
                 ct, ck = t_ms, kern
             else:
-                cm = Measured(cw, dev, fused=args.fused_step)
+                cm = Measured(cw, dev, fused=not args.sequential_step)
                 cm.capture(args.warmup)
                 ct = cm.timed(csteps, flush, stream, world)
                 ck = cm.kernel_times(csteps, flush)
@@ -801,7 +804,10 @@ def run_ours(args, wl_id, wl):
         "warmup": args.warmup, "ms_per_step": t_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": base_config(wl),
-        "timing": {"l2": "flushed before every timed step (256 MiB write)",
+        "timing": {"step_call": ("rt_routing_attention + rt_centroid_ema, one stream"
+                                 if args.sequential_step or not wl.ema else
+                                 "rt_routing_attention_step (centroid update on a side stream)"),
+                   "l2": "flushed before every timed step (256 MiB write)",
                    "graph": "the step captured once as a CUDA graph, replayed per step",
                    "kernel_times": "eager steps behind a sleep kernel, CUDA events around each "
                                    "launch (includes a few us of launch gap per kernel); the "
@@ -836,8 +842,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="measure the headline workload only (no `configs` map)")
-    ap.add_argument("--fused-step", action="store_true",
-                    help="time the step as one rt_routing_attention_step call")
+    ap.add_argument("--sequential-step", action="store_true",
+                    help="time the step as rt_routing_attention then rt_centroid_ema on one "
+                         "stream (default: one rt_routing_attention_step call, which runs the "
+                         "centroid update on a side stream beside the forward's tail)")
     ap.add_argument("--soak-ms", type=float, default=300.0,
                     help="untimed replays right before the timed region, for the clock record")
     args = ap.parse_args()
