@@ -16,9 +16,9 @@
 // softmax sees its whole row: no online rescaling.  Warps 0-3 take tile 0's
 // rows, warps 4-7 tile 1's (the TMEM lane quadrant of warp w is w % 4), one
 // thread per row: the row's maximum, exp2 of the visible columns, P (bf16)
-// into shared memory (tile 1's over Q, which S no longer needs), then O = P V
-// into the score columns together with P's row sums (the same P against a
-// column of ones), the O rows divided by their sums and staged over Q and V as
+// into shared memory (tile 1's over Q, which S no longer needs) with the row
+// sums of exactly those bf16 weights, then O = P V into the score columns, the
+// O rows divided by their sums and staged over Q and V as
 // 128-byte-swizzled boxes: one bulk tensor store per 32 features writes the
 // cluster's slot rows to `yslot` (fp32), while the warps copy the rows of
 // positions in exactly one cluster to `out` (bf16).  Chunks of 16 keys that
@@ -45,11 +45,8 @@ struct PairSmem {
   static constexpr int P0_OFF = QB + VB;
   // tile 1's P goes over Q once the scores are done when it fits there
   static constexpr int P1_OFF = QB >= PB ? Q_OFF : P0_OFF + PB;
-  // B operand of the row-sum MMA: 16 x 256 keys of bf16, row 0 all ones
-  static constexpr int ONES_OFF = (QB >= PB ? P0_OFF + PB : P1_OFF + PB);
-  static constexpr int BYTES = ONES_OFF + 16 * NR * 2;
+  static constexpr int BYTES = (QB >= PB ? P0_OFF + PB : P1_OFF + PB);
   static_assert(QB + VB >= NR * D * 4, "the output staging fits over Q and V");
-  static_assert(ONES_OFF % 1024 == 0, "aligned operand");
 };
 
 // Gather NR rows (positions pos[r], -1 = zero row) of D bf16 into the
@@ -115,16 +112,6 @@ attention_pair_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
   if (warp == 0) {
     tc::tmem_alloc(&tmem_base_sh, 512);
     tc::tmem_relinquish();
-  }
-  if (tid < 64) {
-    // the ones operand: 16 rows (n) x 256 keys, K-major core matrices of 8 rows
-    // x 16 bytes, core matrix (n/8, key/8) at ((n/8)*32 + key/8)*128: thread i
-    // writes core matrix i, whose first row is n = 0 for i < 32
-    uint4* o4 = reinterpret_cast<uint4*>(sm + L::ONES_OFF + tid * 128);
-    const uint32_t one2 = tid < 32 ? 0x3F803F80u : 0u;  // two bf16 1.0
-    o4[0] = make_uint4(one2, one2, one2, one2);
-#pragma unroll
-    for (int i = 1; i < 8; ++i) o4[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
   gather_rows_sw128<D>(sm + L::Q_OFF, q_bh, pos_s);
@@ -205,6 +192,7 @@ attention_pair_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
     }
   }
   const float neg_m = (mrow == -INFINITY) ? 0.0f : -mrow * scale_log2;
+  float lsum = 0.0f;  // the sum of this row's bf16 weights
   // P row: K-major core matrices, element (r, key) at (r/8)*(kt*16) +
   // (key/8)*128 + (r%8)*16 + (key%8)*2
   uint8_t* pt = sm + (t == 0 ? L::P0_OFF : L::P1_OFF);
@@ -223,7 +211,7 @@ attention_pair_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
 #pragma unroll 1
     for (int ch = ch_hi; ch < kt / 16; ++ch) store_chunk(ch, zero);
   }
-  // P = 2^(S*scale*log2e - max), bf16; its row sums come from the O MMA
+  // P = 2^(S*scale*log2e - max), bf16, and the sum of those bf16 values
 #pragma unroll 1
   for (int ch = 0; ch < ch_hi; ch += 2) {
     uint32_t rr[2][16];
@@ -241,6 +229,7 @@ attention_pair_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
           const float e0 = tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj]), scale_log2, neg_m));
           const float e1 = tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj + 1]), scale_log2, neg_m));
           pk[jj >> 1] = pack_bf16(e0, e1);
+          lsum += __uint_as_float(pk[jj >> 1] << 16) + __uint_as_float(pk[jj >> 1] & 0xffff0000u);
         }
       } else {
 #pragma unroll
@@ -252,6 +241,7 @@ attention_pair_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
               col + 1 < jmax ? tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj + 1]), scale_log2, neg_m))
                              : 0.0f;
           pk[jj >> 1] = pack_bf16(e0, e1);
+          lsum += __uint_as_float(pk[jj >> 1] << 16) + __uint_as_float(pk[jj >> 1] & 0xffff0000u);
         }
       }
       store_chunk(c, pk);
@@ -262,13 +252,10 @@ attention_pair_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
   __syncthreads();
   tc::tc_fence_after_sync();
 
-  // ---- O = P V into the score columns, and the row sums of the same bf16 P
-  //      (P times a column of ones) just after them -----------------------------
+  // ---- O = P V into the score columns -----------------------------------------
   if (tid == 0) {
     const uint32_t va = tc::smem_u32(sm + L::V_OFF);
-    const uint32_t ones = tc::smem_u32(sm + L::ONES_OFF);
     const uint32_t idesc_o = tc::idesc_f16(ROWS, D, true, false, true);
-    const uint32_t idesc_l = tc::idesc_f16(ROWS, 16, true, false, false);
 #pragma unroll
     for (int tt = 0; tt < 2; ++tt) {
       const int ktt = tt == 0 ? n0 : NR;
@@ -277,8 +264,6 @@ attention_pair_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
         const uint64_t ad = tc::smem_desc_noswizzle(pa + kk * 256, 128, ktt * 16);
         const uint64_t bd = tc::smem_desc_sw128_mn(va + kk * 2048, NR * 128, 1024);
         tc::mma_f16_ss(tmem + tt * 256, ad, bd, idesc_o, kk > 0 ? 1u : 0u);
-        const uint64_t od = tc::smem_desc_noswizzle(ones + kk * 256, 128, NR * 16);
-        tc::mma_f16_ss(tmem + tt * 256 + D, ad, od, idesc_l, kk > 0 ? 1u : 0u);
       }
     }
     tc::mma_commit(&bar_o);
@@ -298,16 +283,13 @@ attention_pair_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
   // ---- O rows divided by their sums: TMEM -> fp32 staging over Q and V (free
   //      now) as bulk-store boxes: D/32 segments of [256 rows][128 bytes],
   //      16-byte chunk q of row s at (q ^ (s % 8)) (128-byte swizzle) ----------
-  uint32_t lraw;
-  tc::tmem_ld1(t_row + D, lraw);
+  const float inv_l = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
 #pragma unroll
   for (int c0 = 0; c0 < D; c0 += 32) {
     uint32_t rr[2][16];
     tc::tmem_ld16(t_row + c0, rr[0]);
     tc::tmem_ld16(t_row + c0 + 16, rr[1]);
     tc::tmem_ld_wait();
-    const float lsum = __uint_as_float(lraw);
-    const float inv_l = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
 #pragma unroll
     for (int q4 = 0; q4 < 8; ++q4) {
       const int chunk = c0 / 4 + q4;

@@ -17,14 +17,13 @@
 //               operand of S and the MN-major operand of O), and mark a stage
 //               full once their copies have landed;
 //   warp 12     issues the MMAs: S = Q Q^T into the TMEM accumulator of the
-//               tile's group, then O = P V into the same columns and, with
-//               the same P against a column of ones, P's row sums (the sums
-//               of exactly the bf16 weights the O MMA used, in fp32);
+//               tile's group, then O = P V into the same columns;
 //   warps 4-7,  two softmax/epilogue groups taking alternate tiles: softmax of
 //   warps 8-11  their rows from TMEM (only the 16-column chunks holding a valid
 //               key of some row of the warp; chunks every row of the warp sees
-//               in full skip the mask), P (bf16) into the stage's Q space, then
-//               the O rows divided by their sums, staged in the stage's shared
+//               in full skip the mask), P (bf16) into the stage's Q space with
+//               the row sums of exactly those bf16 weights, then the O rows
+//               divided by their sums, staged in the stage's shared
 //               memory as 128-byte-swizzled boxes: one bulk tensor store per 32
 //               features writes all of the tile's slot rows to `yslot` (fp32),
 //               while the warps copy the rows of positions in exactly one
@@ -51,9 +50,7 @@ struct PipeSmem {
   static constexpr int XB = QB > PB ? QB : PB;
   static constexpr int STAGE = XB + QB;       // + V tile; also holds the fp32 O rows
   static constexpr int NS = D == 128 ? 3 : 4;
-  // B operand of the row-sum MMA: 16 x 128 keys of bf16, row 0 all ones
-  static constexpr int ONES_OFF = NS * STAGE;
-  static constexpr int BYTES = ONES_OFF + 16 * ROWS * 2;
+  static constexpr int BYTES = NS * STAGE;
   static_assert(STAGE >= ROWS * D * 4, "a stage must hold the fp32 output rows");
   static_assert(STAGE % 1024 == 0, "bulk-store boxes start on 1024-byte boundaries");
 };
@@ -106,19 +103,9 @@ attention_pipe_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
   const int T = (ntiles > first) ? (ntiles - first + stride - 1) / stride : 0;  // my tiles
 
   if (warp == MMA_WARP) {
-    // accumulators: columns [128a, 128a + 128) for group a (S, then O), the
-    // row sums of P at 256 + 16a
-    tc::tmem_alloc(&tmem_base_sh, 512);
+    // accumulators: columns [128a, 128a + 128) for group a (S, then O)
+    tc::tmem_alloc(&tmem_base_sh, 256);
     tc::tmem_relinquish();
-    // the ones operand: 16 rows (n) x 128 keys, K-major core matrices of
-    // 8 rows x 16 bytes; core matrix (n/8, key/8) at ((n/8)*16 + key/8)*128, so
-    // lane L writes core matrix L, whose first row is n = 0 for L < 16
-    uint4* o4 = reinterpret_cast<uint4*>(sm + L::ONES_OFF + lane * 128);
-    const uint32_t one2 = lane < 16 ? 0x3F803F80u : 0u;  // two bf16 1.0
-    o4[0] = make_uint4(one2, one2, one2, one2);
-#pragma unroll
-    for (int i = 1; i < 8; ++i) o4[i] = make_uint4(0u, 0u, 0u, 0u);
-    tc::fence_proxy_async_smem();
   }
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -201,8 +188,6 @@ attention_pipe_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
     if (lane == 0) {
       constexpr uint32_t IDESC_S = tc::idesc_f16(ROWS, ROWS, true, false, false);
       constexpr uint32_t IDESC_O = tc::idesc_f16(ROWS, D, true, false, true);
-      constexpr uint32_t IDESC_L = tc::idesc_f16(ROWS, 16, true, false, false);
-      const uint32_t ones = tc::smem_u32(sm + L::ONES_OFF);
       // S(j) needs tile j's rows and a free accumulator; O(j) needs P(j).
       // Whichever is ready is issued, so O(j) never waits behind the data
       // of tile j + 1.
@@ -236,9 +221,6 @@ attention_pipe_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
           const uint64_t ad = tc::smem_desc_noswizzle(pa + kk * 256, 128, 2048);
           const uint64_t bd = tc::smem_desc_sw128_mn(va + kk * 2048, ROWS * 128, 1024);
           tc::mma_f16_ss(tmem + a * 128, ad, bd, IDESC_O, kk > 0 ? 1u : 0u);
-          // the row sums of the same bf16 P: P times a column of ones
-          const uint64_t od = tc::smem_desc_noswizzle(ones + kk * 256, 128, 2048);
-          tc::mma_f16_ss(tmem + 256 + a * 16, ad, od, IDESC_L, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(&ofull_bar[a]);
       };
@@ -271,10 +253,10 @@ attention_pipe_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
     const int r = 32 * quad + lane;  // tile row == TMEM lane
     const uint32_t lanes = (uint32_t)(32 * quad) << 16;
     const uint32_t t_row = tmem + grp * 128 + lanes;
-    const uint32_t t_sum = tmem + 256 + grp * 16 + lanes;  // the row sums of P
     const int ci = r / w;
     const int row_lo = ci * w, row_hi = row_lo + w;
     const bool leader = quad == 0 && lane == 0;  // issues the group's bulk stores
+    float lsum = 0.0f;  // the row sum of this tile's bf16 weights
     for (int j = grp; j < T; j += 2) {
       const int s = j % NS;
       const uint32_t use_s = (uint32_t)(j / NS), use_a = (uint32_t)(j >> 1);
@@ -325,6 +307,7 @@ attention_pipe_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
           }
         }
         const float neg_m = (mrow == -INFINITY) ? 0.0f : -mrow * scale_log2;
+        lsum = 0.0f;
         const uint32_t prow = tc::smem_u32(st) + (r >> 3) * 2048 + (r & 7) * 16;
         auto store_chunk = [&](int ch, const uint32_t (&pk)[8]) {
 #pragma unroll
@@ -341,7 +324,7 @@ attention_pipe_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
           for (int ch = 0; ch < ROWS / 16; ++ch)
             if (ch < ch_lo || ch >= ch_hi) store_chunk(ch, zero);
         }
-        // P = 2^(S*scale*log2e - max), bf16; its row sums come from the O MMA
+        // P = 2^(S*scale*log2e - max), bf16, and the sum of those bf16 values
 #pragma unroll 1
         for (int ch = ch_lo; ch < ch_hi; ch += 2) {
           uint32_t rr[2][16];
@@ -359,6 +342,7 @@ attention_pipe_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
                 const float e0 = tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj]), scale_log2, neg_m));
                 const float e1 = tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj + 1]), scale_log2, neg_m));
                 pk[jj >> 1] = pack_bf16(e0, e1);
+                lsum += __uint_as_float(pk[jj >> 1] << 16) + __uint_as_float(pk[jj >> 1] & 0xffff0000u);
               }
             } else {
 #pragma unroll
@@ -371,6 +355,7 @@ attention_pipe_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
                 const float e1 =
                     ok1 ? tc::exp2_approx(fmaf(__uint_as_float(rr[hh][jj + 1]), scale_log2, neg_m)) : 0.0f;
                 pk[jj >> 1] = pack_bf16(e0, e1);
+                lsum += __uint_as_float(pk[jj >> 1] << 16) + __uint_as_float(pk[jj >> 1] & 0xffff0000u);
               }
             }
             store_chunk(c, pk);
@@ -386,20 +371,17 @@ attention_pipe_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
         ok = __all_sync(0xffffffffu, ok);
       }
       if (ok) {
-        // ---- O rows / row sum: TMEM -> fp32 staging over the stage ---------
+        // ---- O rows / row sum -> fp32 staging over the stage ----------------
         // Layout of a bulk-store box: D/32 segments of [128 rows][128 bytes],
         // 16-byte chunk q of row r at (q ^ (r % 8)) (128-byte swizzle).
         tc::tc_fence_after_sync();
-        uint32_t lraw;
-        tc::tmem_ld1(t_sum, lraw);
+        const float inv_l = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t rr[2][16];
           tc::tmem_ld16(t_row + c0, rr[0]);
           tc::tmem_ld16(t_row + c0 + 16, rr[1]);
           tc::tmem_ld_wait();
-          const float lsum = __uint_as_float(lraw);
-          const float inv_l = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             const int chunk = c0 / 4 + q4;
@@ -483,7 +465,7 @@ attention_pipe_kernel(const __grid_constant__ CUtensorMap ymap, const bf16* __re
 
   tc::tc_fence_before_sync();
   __syncthreads();
-  if (warp == MMA_WARP) tc::tmem_dealloc(tmem, 512);
+  if (warp == MMA_WARP) tc::tmem_dealloc(tmem, 256);
 }
 
 template <int D>
