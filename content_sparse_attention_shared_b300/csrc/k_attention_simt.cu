@@ -9,13 +9,14 @@
 // mask on original positions is the lower triangle in slot order, diagonal
 // included.
 //
-// One CTA takes 64 query slots of one cluster and walks the cluster's key
-// slots in blocks of 64 with an online (running max / running sum) softmax.
+// One CTA takes 64 query slots of one cluster (16 when the problem has too
+// few clusters to fill the GPU that way) and walks the cluster's key slots in
+// blocks of 64 with an online (running max / running sum) softmax.
 // With SEP (separate queries and keys) the key and value rows come from the
 // keys' own lists (idx_k) and the causal mask compares original positions; a
 // query with no visible key gets a zero row and is not counted in mvis.
-// Gathered K and V rows are staged in shared memory as fp32; each warp owns 8
-// query rows.  The epilogue writes a row straight to the output when the
+// Gathered K and V rows are staged in shared memory as fp32; each warp owns
+// 8 (or 2) query rows.  The epilogue writes a row straight to the output when the
 // position belongs to exactly one cluster, else to the per-slot buffer that
 // the scatter kernel averages.
 #include "rt_internal.cuh"
@@ -23,10 +24,8 @@
 namespace rt {
 namespace {
 
-constexpr int QB = 64;
 constexpr int KB = 64;
 constexpr int THREADS = 256;
-constexpr int ROWS_PER_WARP = QB / (THREADS / 32);
 
 template <typename T, int D>
 __device__ __forceinline__ void load_rows(float* dst, int ld, const T* __restrict__ src,
@@ -47,7 +46,7 @@ __device__ __forceinline__ void load_rows(float* dst, int ld, const T* __restric
   }
 }
 
-template <typename T, int D, bool SEP>
+template <typename T, int D, bool SEP, int QB>
 __global__ void __launch_bounds__(THREADS)
 attention_simt_kernel(const T* __restrict__ q, const T* __restrict__ kk, const T* __restrict__ v,
                       int n, int k, int w, int causal, float scale,
@@ -56,6 +55,7 @@ attention_simt_kernel(const T* __restrict__ q, const T* __restrict__ kk, const T
                       T* __restrict__ out, float* __restrict__ yslot) {
   pdl_trigger();
   pdl_wait();
+  constexpr int ROWS_PER_WARP = QB / (THREADS / 32);
   extern __shared__ float smem[];
   constexpr int LDQ = D + 1;
   float* Qs = smem;              // [QB][D+1]
@@ -168,8 +168,16 @@ cudaError_t launch_t(const void* q, const void* kk, const void* v, int BH, int n
                      int causal, float scale, const int32_t* idx, const int32_t* idx_k,
                      const int32_t* mcount, int32_t* mvis, void* out, float* yslot,
                      cudaStream_t s) {
+  // 64 query rows a CTA, or 16 when that would leave most SMs idle
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const bool small = (long long)((w + 63) / 64) * k * BH < 2LL * sms;
+  const int QB = small ? 16 : 64;
   const size_t smem = ((size_t)(QB + KB) * (D + 1) + (size_t)KB * D) * sizeof(float);
-  auto kern = idx_k != nullptr ? attention_simt_kernel<T, D, true> : attention_simt_kernel<T, D, false>;
+  auto kern = idx_k != nullptr
+                  ? (small ? attention_simt_kernel<T, D, true, 16> : attention_simt_kernel<T, D, true, 64>)
+                  : (small ? attention_simt_kernel<T, D, false, 16> : attention_simt_kernel<T, D, false, 64>);
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((w + QB - 1) / QB, k, BH);

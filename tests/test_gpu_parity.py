@@ -177,6 +177,7 @@ SWEEP = [
     (1, 1, 33004, 64, 6, 256, "bf16", True),    # long rows: select from group bins, last group ragged
     (1, 2, 32772, 128, 3, 200, "f32", True),    # the same through the fp32 score kernel
     (1, 1, 32771, 64, 4, 100, "bf16", True),    # long rows with n % 4 != 0: no group bins
+    (1, 8, 4096, 64, 64, 64, "f32", True),      # fp32 with enough clusters for 64-row query blocks
 ]
 
 
