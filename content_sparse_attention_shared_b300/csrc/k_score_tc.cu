@@ -461,6 +461,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
                          ? gbins + (size_t)bh * k * gstride + gi + (size_t)(lane & 7) * gstride
                          : nullptr;
       const uint32_t tacc = tmem + grp * acc_cols + lane_base;
+      const bool tile_full = (tb + 1) * ROWS <= n;  // the same for the whole tile
       for (int c0 = 0; c0 < kpad; c0 += 32) {
         uint32_t r[2][16];
         tc::tmem_ld16(tacc + c0, r[0]);
@@ -479,16 +480,14 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
             sc[4 * q4 + 2] = fmaf(nmean, su.z, __uint_as_float(r[hh][4 * q4 + 2])) * inv;
             sc[4 * q4 + 3] = fmaf(nmean, su.w, __uint_as_float(r[hh][4 * q4 + 3])) * inv;
           }
-          if (zero_row) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) sc[j] = 0.0f;
-          }
+          // (a row with a zero centred norm has inv = 0, so its scores are 0)
           if (gbins != nullptr) {  // warp-uniform: the shuffles need every lane
 #pragma unroll
             for (int hv = 0; hv < 2; ++hv) {
               float m[8];
 #pragma unroll
-              for (int j = 0; j < 8; ++j) m[j] = valid ? sc[8 * hv + j] : -INFINITY;
+              for (int j = 0; j < 8; ++j)
+                m[j] = (tile_full || valid) ? sc[8 * hv + j] : -INFINITY;
               const float gm = octet_column_max(m, lane);
               const int cg = cb + 8 * hv + (lane & 7);
               if (gp != nullptr && cg < k)
