@@ -95,6 +95,46 @@ struct SelectOut {
     }
     return o;
   }
+  // The same over the words [q0, q1) of a position bitmap (word q: positions
+  // 32q..32q+31): the kept positions of all the words are batched together,
+  // so a thread owning several words waits for one round trip, not one per
+  // non-empty word.
+  template <int NB = 8>
+  __device__ __forceinline__ int emit_words(int o, const unsigned* words, int q0, int q1) const {
+    int q = q0;
+    unsigned word = q < q1 ? words[q] : 0u;
+    while (true) {
+      int p[NB], prev[NB];
+      int cnt = 0;
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        p[i] = 0;
+        prev[i] = SLOTS_PER_ROW;
+        while (word == 0u && q + 1 < q1) word = words[++q];
+        if (word != 0u) {
+          p[i] = q * 32 + __ffs(word) - 1;
+          word &= word - 1u;
+          cnt = i + 1;
+        }
+      }
+      if (cnt == 0) break;
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        if (i < cnt && o + i < w) {
+          out[o + i] = p[i];
+          if (mcount != nullptr) prev[i] = atomicAdd(&mcount[(size_t)bh * n + p[i]], 1);
+        }
+      }
+      if (slots != nullptr) {
+#pragma unroll
+        for (int i = 0; i < NB; ++i)
+          if (i < cnt && o + i < w && (unsigned)prev[i] < (unsigned)SLOTS_PER_ROW)
+            slots[((size_t)bh * n + p[i]) * SLOTS_PER_ROW + prev[i]] = c * w + o + i;
+      }
+      o += cnt;
+    }
+    return o;
+  }
 };
 
 // Exact fallback: 32-bit MSD radix select on order-preserving keys, reading
@@ -690,8 +730,10 @@ select_topw_group_kernel(const float* __restrict__ S, const uint16_t* __restrict
   for (int g0 = 0; g0 < NG; g0 += THREADS) {
     const int g = g0 + tid;
     const int b = (g < NG && (int)gbin[g] >= b0) ? (int)gbin[g] : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, b);
-    if (b >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[b], (unsigned)__popc(peers));
+    if (__any_sync(0xffffffffu, b >= 0)) {  // (most warps hold no bin >= b0)
+      const unsigned peers = __match_any_sync(0xffffffffu, b);
+      if (b >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[b], (unsigned)__popc(peers));
+    }
   }
   __syncthreads();
 
@@ -724,17 +766,27 @@ select_topw_group_kernel(const float* __restrict__ S, const uint16_t* __restrict
   }
 
   // 3. candidates from the groups whose maximum reaches b_L: first the list of
-  //    those groups (shared memory only), then one group per thread, every
-  //    load in flight at once
-  for (int g0 = 0; g0 < NG; g0 += THREADS) {
-    const int g = g0 + tid;
-    const bool ok = g < NG && (int)gbin[g] >= bl;
-    const unsigned bal = __ballot_sync(0xffffffffu, ok);
+  //    those groups (shared memory only: each warp counts its groups with
+  //    ballots, reserves its range with one atomic, then writes them), then
+  //    two groups per thread, every load in flight at once
+  {
+    const unsigned lt = (1u << lane) - 1u;
+    int wcount = 0;
+    for (int g0 = 0; g0 < NG; g0 += THREADS) {
+      const int g = g0 + tid;
+      wcount += __popc(__ballot_sync(0xffffffffu, g < NG && (int)gbin[g] >= bl));
+    }
     int base = 0;
-    if (lane == 0 && bal != 0u) base = atomicAdd(&s_nq, __popc(bal));
+    if (lane == 0 && wcount != 0) base = atomicAdd(&s_nq, wcount);
     base = __shfl_sync(0xffffffffu, base, 0);
-    const int slot = base + __popc(bal & ((1u << lane) - 1u));
-    if (ok && slot < GCAP) qlist[slot] = g;
+    for (int g0 = 0; g0 < NG; g0 += THREADS) {
+      const int g = g0 + tid;
+      const bool ok = g < NG && (int)gbin[g] >= bl;
+      const unsigned bal = __ballot_sync(0xffffffffu, ok);
+      const int slot = base + __popc(bal & lt);
+      if (ok && slot < GCAP) qlist[slot] = g;
+      base += __popc(bal);
+    }
   }
   __syncthreads();
   const int nq = s_nq;
@@ -745,30 +797,45 @@ select_topw_group_kernel(const float* __restrict__ S, const uint16_t* __restrict
   // candidates above the boundary bin fill ckey from the front (nA), those in
   // it from the back (nE)
   {
+    // groups a thread loads at once: two on the long rows that come with
+    // precomputed group bins, one on the shorter rows below them
+    constexpr int GPT = FROM_GBINS ? 2 : 1;
     const float pre = bl > 0 ? (float)bl * (1.0f / 1024.0f) - 1.0f - 1.0e-5f : -3.0e38f;
-    for (int i0 = 0; i0 < nq; i0 += THREADS) {
-      const int i = i0 + tid;
-      uint32_t ca = 0u, ce = 0u;  // above the boundary bin / in it
-      float x[GSIZE];
-      int g = 0;
-      if (i < nq) {
-        g = qlist[i];
-        const float4 a = 2 * g < n4 ? __ldcg(row4 + 2 * g) : ninf;
-        const float4 b = 2 * g + 1 < n4 ? __ldcg(row4 + 2 * g + 1) : ninf;
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    for (int i0 = 0; i0 < nq; i0 += GPT * THREADS) {
+      uint32_t ca[GPT], ce[GPT];  // above the boundary bin / in it
+      float x[GPT][GSIZE];
+      int g[GPT];
+#pragma unroll
+      for (int u = 0; u < GPT; ++u) {
+        ca[u] = 0u;
+        ce[u] = 0u;
+        g[u] = 0;
+        const int i = i0 + u * THREADS + tid;
+        float4 a = ninf, b = ninf;
+        if (i < nq) {
+          g[u] = qlist[i];
+          if (2 * g[u] < n4) a = __ldcg(row4 + 2 * g[u]);
+          if (2 * g[u] + 1 < n4) b = __ldcg(row4 + 2 * g[u] + 1);
+        }
+        x[u][0] = a.x; x[u][1] = a.y; x[u][2] = a.z; x[u][3] = a.w;
+        x[u][4] = b.x; x[u][5] = b.y; x[u][6] = b.z; x[u][7] = b.w;
+      }
+#pragma unroll
+      for (int u = 0; u < GPT; ++u) {
 #pragma unroll
         for (int e = 0; e < GSIZE; ++e) {
-          if (x[e] >= pre) {
-            const int sb = score_bin(x[e]);
-            if (sb > bl) ca |= 1u << e;
-            else if (sb == bl) ce |= 1u << e;
+          if (x[u][e] >= pre) {
+            const int sb = score_bin(x[u][e]);
+            if (sb > bl) ca[u] |= 1u << e;
+            else if (sb == bl) ce[u] |= 1u << e;
           }
         }
       }
       int sa, se;
       {
-        const int cnt = __popc(ca) | (__popc(ce) << 16);  // both counts in one scan
+        int cnt = 0;  // both counts in one scan
+#pragma unroll
+        for (int u = 0; u < GPT; ++u) cnt += __popc(ca[u]) | (__popc(ce[u]) << 16);
         int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -788,13 +855,16 @@ select_topw_group_kernel(const float* __restrict__ S, const uint16_t* __restrict
         se = baseE + (ex >> 16);
       }
 #pragma unroll
-      for (int e = 0; e < GSIZE; ++e) {
-        if ((ca >> e) & 1u) {
-          if (sa < GCAP) ckey[sa] = cand_key(x[e], g * GSIZE + e);
-          ++sa;
-        } else if ((ce >> e) & 1u) {
-          if (se < GCAP) ckey[GCAP - 1 - se] = cand_key(x[e], g * GSIZE + e);
-          ++se;
+      for (int u = 0; u < GPT; ++u) {
+#pragma unroll
+        for (int e = 0; e < GSIZE; ++e) {
+          if ((ca[u] >> e) & 1u) {
+            if (sa < GCAP) ckey[sa] = cand_key(x[u][e], g[u] * GSIZE + e);
+            ++sa;
+          } else if ((ce[u] >> e) & 1u) {
+            if (se < GCAP) ckey[GCAP - 1 - se] = cand_key(x[u][e], g[u] * GSIZE + e);
+            ++se;
+          }
         }
       }
     }
@@ -842,8 +912,8 @@ select_topw_group_kernel(const float* __restrict__ S, const uint16_t* __restrict
     int cnt = 0;
     for (int q = q0; q < q0 + WPT && q < NW; ++q) cnt += __popc(kept[q]);
     int total;
-    int o = block_exclusive_scan<THREADS>(cnt, wsum, total);
-    for (int q = q0; q < q0 + WPT && q < NW; ++q) o = so.emit_word(o, kept[q], q * 32);
+    const int o = block_exclusive_scan<THREADS>(cnt, wsum, total);
+    so.emit_words(o, kept, q0, min(q0 + WPT, NW));
   }
 }
 

@@ -178,6 +178,7 @@ SWEEP = [
     (1, 2, 32772, 128, 3, 200, "f32", True),    # the same through the fp32 score kernel
     (1, 1, 32771, 64, 4, 100, "bf16", True),    # long rows with n % 4 != 0: no group bins
     (1, 8, 4096, 64, 64, 64, "f32", True),      # fp32 with enough clusters for 64-row query blocks
+    (1, 2, 10004, 64, 7, 200, "bf16", True),    # select rows of 8192 < n <= 16384, ragged segments
 ]
 
 
