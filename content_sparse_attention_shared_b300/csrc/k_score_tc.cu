@@ -39,7 +39,8 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 constexpr int ROWS = 128;
-constexpr int THREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 two epilogue groups
+// warp 0 TMA, warp 1 MMA, then NG epilogue groups of four warps
+__host__ __device__ constexpr int score_threads(int ng) { return 64 + 128 * ng; }
 constexpr uint64_t WAIT_LIMIT_NS = 200ull * 1000 * 1000;
 constexpr int MAX_SMEM = 232448;  // 227 KiB opt-in per block
 constexpr int BOX_K = 64;         // elements per 128-byte swizzled row
@@ -168,8 +169,8 @@ centroid_prep_kernel(const float* __restrict__ mu, int k, int kpad, uint8_t* __r
   }
 }
 
-template <int D, bool PREP>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int D, bool PREP, int NG>
+__global__ void __launch_bounds__(score_threads(NG), 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
                 const float* __restrict__ mu, const uint8_t* __restrict__ image, int k, int kpad,
                 int acc_cols, int stages, int ctas_per_head, float* __restrict__ S,
@@ -186,7 +187,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
   uint8_t* Bs = As + (size_t)stages * A_BYTES;       // 3 planes x [kpad x D] K-major
   float* sumu = reinterpret_cast<float*>(Bs + 3 * (size_t)plane_bytes);  // [kpad]
 
-  __shared__ uint64_t full_bar[4], empty_bar[4], accf_bar[2], acce_bar[2], prep_bar;
+  constexpr int THREADS = score_threads(NG);
+  __shared__ uint64_t full_bar[4], empty_bar[4], accf_bar[NG], acce_bar[NG], prep_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int stop_flag;
 
@@ -203,7 +205,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
       tc::mbar_init(&full_bar[i], 1);
       tc::mbar_init(&empty_bar[i], 4);  // the 4 warps of the epilogue group that read the tile
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NG; ++i) {
       tc::mbar_init(&accf_bar[i], 1);
       tc::mbar_init(&acce_bar[i], 4);
     }
@@ -296,7 +298,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
     }
   }
   if (warp == 1) {
-    tc::tmem_alloc(&tmem_base_sh, 2 * acc_cols);
+    tc::tmem_alloc(&tmem_base_sh, NG * acc_cols);
     tc::tmem_relinquish();
   }
   tc::fence_proxy_async_smem();  // planes written by threads, read by the MMA
@@ -340,8 +342,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
       for (int tile = first; tile < ntiles; tile += stride, ++i) {
         const int s = i % stages;
         const uint32_t use = (uint32_t)(i / stages);
-        const int ab = i & 1;
-        const uint32_t ause = (uint32_t)(i >> 1);
+        const int ab = i % NG;
+        const uint32_t ause = (uint32_t)(i / NG);
         if (!tc::mbar_wait_bounded(&full_bar[s], use & 1u, WAIT_LIMIT_NS) ||
             !tc::mbar_wait_bounded(&acce_bar[ab], (ause & 1u) ^ 1u, WAIT_LIMIT_NS) ||
             *(volatile int*)&stop_flag) {
@@ -369,7 +371,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
     }
   } else {
     // ===================== epilogue groups (warps 2-5, 6-9) ==================
-    const int grp = (warp - 2) >> 2;         // takes tiles i with i % 2 == grp
+    const int grp = (warp - 2) >> 2;         // takes tiles i with i % NG == grp
     const int quad = warp & 3;               // TMEM lane quadrant this warp may read
     const int row = 32 * quad + lane;        // tile row == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
@@ -383,19 +385,26 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
       }
     }
     int i = grp;
-    for (int tile = first + grp * stride; tile < ntiles; tile += 2 * stride, i += 2) {
+    for (int tile = first + grp * stride; tile < ntiles; tile += NG * stride, i += NG) {
       const int s = i % stages;
       const uint32_t use = (uint32_t)(i / stages);
-      const uint32_t ause = (uint32_t)(i >> 1);
+      const uint32_t ause = (uint32_t)(i / NG);
       const int b = tile / tiles_per_bh, tb = tile - b * tiles_per_bh;
       const int bh = b * H + h;
       const int t = tb * ROWS + row;
       const bool valid = t < n;
-      // Wait for this tile's MMA; the tile's TMA phase is then complete too
-      // (the MMA waited for it) and cannot advance before this group releases
-      // the stage, so the full-barrier wait below returns at once and only
-      // orders the staged bytes for this thread.
-      bool ok = tc::mbar_wait_bounded(&accf_bar[grp], ause & 1u, WAIT_LIMIT_NS) &&
+      // The row statistics need only the staged tile.  When the stage's
+      // previous use was this group's own tile (NG divides the stage count),
+      // the group waits for the TMA alone, computes them while the MMA runs
+      // and waits for the MMA afterwards: the full barrier cannot be a phase
+      // behind or ahead, since the stage is refilled only after this group
+      // releases it, which follows the MMA's completion.  Otherwise it waits
+      // for the MMA first, which implies the tile's TMA phase (the MMA waited
+      // for it); that phase cannot advance before this group releases the
+      // stage, so the full-barrier wait returns at once and only orders the
+      // staged bytes for this thread.
+      const bool early = stages % NG == 0;
+      bool ok = (early || tc::mbar_wait_bounded(&accf_bar[grp], ause & 1u, WAIT_LIMIT_NS)) &&
                 tc::mbar_wait_bounded(&full_bar[s], use & 1u, WAIT_LIMIT_NS) &&
                 !*(volatile int*)&stop_flag;
       ok = __all_sync(0xffffffffu, ok);  // warp-uniform: tcgen05.ld below is collective
@@ -404,52 +413,74 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
         stop_flag = 1;
         break;
       }
-      tc::tc_fence_after_sync();
       // row statistics from the staged tile: mean and centred norm
       float mean = 0.0f, inv = 0.0f;
       bool zero_row = true;
       {
-        // two passes over the row in shared memory (sum, then centred squares)
+        // two passes over the row in shared memory (sum, then centred
+        // squares), QB 16-byte chunks in flight (all of them when the
+        // registers allow), four partial sums each
         const uint8_t* arow = As + (size_t)s * A_BYTES + row * 128;
-        float sx = 0.0f;
+        auto chunk = [&](int q) {  // chunk q: features 8q..8q+7
+          return *reinterpret_cast<const uint4*>(arow + (q >> 3) * (ROWS * 128) +
+                                                 (((q & 7) ^ (row & 7)) << 4));
+        };
+        constexpr int QB = NG == 2 ? D / 8 : 8;
+        float p4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 1
+        for (int q0 = 0; q0 < D / 8; q0 += QB) {
+          uint4 v[QB];
 #pragma unroll
-        for (int kb = 0; kb < KB; ++kb) {
+          for (int u = 0; u < QB; ++u) v[u] = chunk(q0 + u);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 v = *reinterpret_cast<const uint4*>(arow + kb * (ROWS * 128) +
-                                                            ((j ^ (row & 7)) << 4));
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+          for (int u = 0; u < QB; ++u) {
+            const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&w4[e]);
-              sx += __low2float(p2);
-              sx += __high2float(p2);
+              p4[e] += __low2float(p2);
+              p4[e] += __high2float(p2);
             }
           }
         }
-        mean = sx / (float)D;
-        float sxx = 0.0f;
+        mean = ((p4[0] + p4[1]) + (p4[2] + p4[3])) / (float)D;
+        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 1
+        for (int q0 = 0; q0 < D / 8; q0 += QB) {
+          uint4 v[QB];
 #pragma unroll
-        for (int kb = 0; kb < KB; ++kb) {
+          for (int u = 0; u < QB; ++u) v[u] = chunk(q0 + u);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 v = *reinterpret_cast<const uint4*>(arow + kb * (ROWS * 128) +
-                                                            ((j ^ (row & 7)) << 4));
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+          for (int u = 0; u < QB; ++u) {
+            const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&w4[e]);
               const float a = __low2float(p2) - mean, bq = __high2float(p2) - mean;
-              sxx = fmaf(a, a, sxx);
-              sxx = fmaf(bq, bq, sxx);
+              s4[e] = fmaf(a, a, s4[e]);
+              s4[e] = fmaf(bq, bq, s4[e]);
             }
           }
         }
+        const float sxx = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         zero_row = !(sxx > 0.0f);
         inv = zero_row ? 0.0f : 1.0f / sqrtf(sxx);
       }
+      if (early) {
+        bool okm = tc::mbar_wait_bounded(&accf_bar[grp], ause & 1u, WAIT_LIMIT_NS) &&
+                   !*(volatile int*)&stop_flag;
+        okm = __all_sync(0xffffffffu, okm);
+        if (!okm) {
+          if (lane == 0) set_timeout(err);
+          stop_flag = 1;
+          break;
+        }
+      }
+      // stage free: rows read and the MMA done (the MMA reads the stage too,
+      // so it is released only after the accumulator barrier)
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[s]);  // stage free: MMA done, rows read
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+      tc::tc_fence_after_sync();
       float best = -INFINITY;
       int best_c = 0;
       const float nmean = -mean;
@@ -495,14 +526,31 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
             }
           }
           if (cb + 16 <= k) {
+            // argmax of the 16 columns as a pairwise tree (the left one wins
+            // ties, so each node holds the first maximum of its range), then
+            // against the running best: five dependent steps, not sixteen
+            float tv[8];
+            int ti[8];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (sc[j] > best) { best = sc[j]; best_c = cb + j; }
+            for (int j = 0; j < 8; ++j) {
+              const bool right = sc[2 * j + 1] > sc[2 * j];
+              tv[j] = right ? sc[2 * j + 1] : sc[2 * j];
+              ti[j] = 2 * j + (right ? 1 : 0);
             }
-            if (sp != nullptr) {
-              float* p = sp + (size_t)cb * n;
 #pragma unroll
-              for (int j = 0; j < 16; ++j) { *p = sc[j]; p += n; }
+            for (int span = 4; span >= 1; span >>= 1) {
+#pragma unroll
+              for (int j = 0; j < span; ++j) {
+                const bool right = tv[2 * j + 1] > tv[2 * j];
+                tv[j] = right ? tv[2 * j + 1] : tv[2 * j];
+                ti[j] = right ? ti[2 * j + 1] : ti[2 * j];
+              }
+            }
+            if (tv[0] > best) { best = tv[0]; best_c = cb + ti[0]; }
+            if (sp != nullptr) {
+              // (column offsets are the same for the whole warp)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) sp[(size_t)(cb + j) * n] = sc[j];
             }
           } else {
 #pragma unroll
@@ -527,7 +575,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
 
   tc::tc_fence_before_sync();
   __syncthreads();
-  if (warp == 1) tc::tmem_dealloc(tmem, 2 * acc_cols);
+  if (warp == 1) tc::tmem_dealloc(tmem, NG * acc_cols);
 }
 
 // ---------------------------------------------------------------------------
@@ -574,7 +622,11 @@ cudaError_t launch_t(const ScoreCfg& c, const void* qk, int B, int H, int n, con
     launch_end(K_CENTROID_PREP, s);
     if (e != cudaSuccess) return e;
   }
-  auto kern = prep != nullptr ? score_tc_kernel<D, true> : score_tc_kernel<D, false>;
+  // four epilogue groups (four tiles in flight) when four accumulators fit
+  // in the 512 TMEM columns, else two
+  const int ng = 4 * c.acc_cols <= 512 ? 4 : 2;
+  auto kern = prep != nullptr ? (ng == 4 ? score_tc_kernel<D, true, 4> : score_tc_kernel<D, true, 2>)
+                              : (ng == 4 ? score_tc_kernel<D, false, 4> : score_tc_kernel<D, false, 2>);
   e = set_smem_limit(reinterpret_cast<const void*>(kern), (int)c.smem);
   if (e != cudaSuccess) return e;
   const int tiles_per_head = B * ((n + ROWS - 1) / ROWS);
@@ -582,7 +634,7 @@ cudaError_t launch_t(const ScoreCfg& c, const void* qk, int B, int H, int n, con
   if (cph < 1) cph = 1;
   if (cph > tiles_per_head) cph = tiles_per_head;
   launch_begin(K_SCORE_TC, s);
-  e = launch_pdl(kern, dim3(cph, H), dim3(THREADS), c.smem, s, map, B, H, n, mu,
+  e = launch_pdl(kern, dim3(cph, H), dim3(score_threads(ng)), c.smem, s, map, B, H, n, mu,
                  static_cast<const uint8_t*>(prep), k, c.kpad, c.acc_cols, c.stages, cph, S, a,
                  mcount, S != nullptr ? gbins : nullptr, gbin_stride(n), err,
                  injected_limit_ns(K_SCORE_TC));
