@@ -16,10 +16,13 @@ ours:       CUDA library; the step is one rt_routing_attention_step call (the
             of the step captured as one CUDA graph), L2 flushed (256 MiB write)
             before every timed step; e2e = the same step through the public
             API with pinned-host inputs copied in and the output copied out
-            inside the timed region; per-kernel times from the library's launch
-            hook.  At one GPU the line also carries `configs`: the same
-            measurements (fewer steps) on every one of the five workloads, each
-            with the oracle timed on one core and on all host cores.
+            inside the timed region (copies in, compute and copies out
+            overlapped across consecutive steps, as a serving loop runs them,
+            with double-buffered device inputs and outputs); per-kernel times
+            from the library's launch hook.  At one GPU the line also carries
+            `configs`: the same measurements (fewer steps) on every one of the
+            five workloads, each with the oracle timed on one core and on all
+            host cores.
 reference:  the fp64 CPU oracle on the host cores: every step runs all heads
             of the workload, one head per worker process (spawned, one BLAS
             thread each, as many workers as heads or cores), and is timed as
@@ -539,19 +542,20 @@ class Measured:
         self.rt = rt
         self.fused = fused
 
-    def step(self, qq=None, vv=None):
+    def step(self, qq=None, vv=None, oo=None):
         # launches go to torch's current stream (the capture stream while a
         # CUDA graph is being recorded)
         rt, wl = self.rt, self.wl
         qq = self.q if qq is None else qq
         vv = self.v if vv is None else vv
+        oo = self.out if oo is None else oo
         if wl.ema and self.fused:
             # the training-step call: the centroid update overlaps the forward's tail
             rt.rt_routing_attention_step(qq, vv, self.mu, wl.w, wl.decay, causal=True,
-                                         out=self.out, idx_out=self.idx, assign_out=self.assign,
+                                         out=oo, idx_out=self.idx, assign_out=self.assign,
                                          workspace=self.ws)
             return
-        rt.rt_routing_attention(qq, qq, vv, self.mu, wl.w, causal=True, out=self.out,
+        rt.rt_routing_attention(qq, qq, vv, self.mu, wl.w, causal=True, out=oo,
                                 idx_out=self.idx, assign_out=self.assign, workspace=self.ws)
         if wl.ema:
             rt.rt_centroid_ema(qq, self.assign, self.mu, wl.decay, workspace=self.ws)
@@ -663,28 +667,58 @@ class Measured:
         return kern
 
     def e2e(self, steps, flush, stream, world):
-        """The same step through the public API from pinned host buffers: Q and
-        V copied in and the output copied out inside the timed region."""
+        """The same step through the public API from pinned host buffers, run
+        the way a serving loop runs it: every step's Q and V are copied in on
+        a copy stream, the step (L2 flush, then the library call) runs on the
+        compute stream once they have landed, and its output is copied out on
+        a second copy stream.  Two sets of device buffers let the next step's
+        inputs come in while this step computes and the previous output goes
+        out (host-to-device and device-to-host copies use separate copy
+        engines and PCIe directions).  The timed region runs from the first
+        step's first copy in to the last step's copy out, so it holds every
+        step's copies; the time per step is that span / steps."""
         import torch
         import torch.distributed as dist
-        out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
+        dev = self.dev
+        h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        qb = [self.q, torch.empty_like(self.q)]
+        vb = [self.v, torch.empty_like(self.v)]
+        ob = [self.out, torch.empty_like(self.out)]
+        out_h = [torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory() for _ in range(2)]
+        ev = lambda: torch.cuda.Event(enable_timing=False)
+        landed = [ev() for _ in range(steps)]
+        computed = [ev() for _ in range(steps)]
+        drained = [ev() for _ in range(steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
+        t0.record(stream)
+        h2d_s.wait_stream(stream)
         for i in range(steps):
+            j = i % 2
+            with torch.cuda.stream(h2d_s):
+                if i >= 2:
+                    h2d_s.wait_event(computed[i - 2])  # the step that read this buffer is done
+                qb[j].copy_(self.q_h, non_blocking=True)
+                vb[j].copy_(self.v_h, non_blocking=True)
+                landed[i].record(h2d_s)
+            stream.wait_event(landed[i])
+            if i >= 2:
+                stream.wait_event(drained[i - 2])  # this output buffer has been read out
             flush.zero_()
-            ev[i][0].record(stream)
-            self.q.copy_(self.q_h, non_blocking=True)
-            self.v.copy_(self.v_h, non_blocking=True)
-            self.step()
-            out_h.copy_(self.out, non_blocking=True)
-            ev[i][1].record(stream)
+            self.step(qb[j], vb[j], ob[j])
+            computed[i].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(computed[i])
+                out_h[j].copy_(ob[j], non_blocking=True)
+                drained[i].record(d2h_s)
+        stream.wait_event(drained[steps - 1])
+        t1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = slowest_rank_ms(statistics.mean(a.elapsed_time(b) for a, b in ev), self.dev)
+        e2e_ms = slowest_rank_ms(t0.elapsed_time(t1) / steps, dev)
         h2d = (self.q_h.numel() * self.q_h.element_size() + self.v_h.numel() * self.v_h.element_size())
-        d2h = out_h.numel() * out_h.element_size()
+        d2h = out_h[0].numel() * out_h[0].element_size()
         return e2e_ms, h2d, d2h
 
     def close(self):

@@ -179,6 +179,8 @@ SWEEP = [
     (1, 1, 32771, 64, 4, 100, "bf16", True),    # long rows with n % 4 != 0: no group bins
     (1, 8, 4096, 64, 64, 64, "f32", True),      # fp32 with enough clusters for 64-row query blocks
     (1, 2, 10004, 64, 7, 200, "bf16", True),    # select rows of 8192 < n <= 16384, ragged segments
+    (1, 2, 2000, 128, 200, 16, "bf16", True),   # 128 < k <= 256: column halves, ragged upper half and tile
+    (2, 1, 777, 64, 144, 8, "bf16", True),      # the same with d = 64, one 16-column upper half, two sequences
 ]
 
 
