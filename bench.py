@@ -623,13 +623,13 @@ class Measured:
         return t_ms
 
     def kernel_times(self, steps, flush):
-        """Per-kernel device times: eager steps behind a sleep kernel, so the
-        host has every launch queued before the GPU reaches it and the launch
-        hook's events bracket device time only.  The steps take the sequential
-        form (forward, then the centroid update on the same stream), so no
-        kernel's bracket includes time spent waiting for SMs that another
-        stream holds."""
-        import torch
+        """Per-kernel device times: one step in its sequential form (forward,
+        then the centroid update on the same stream, so no kernel's bracket
+        includes time spent waiting for SMs that another stream holds) is
+        captured as a CUDA graph with the library's launch hook on, which puts
+        a CUDA-event record node just before and just after every kernel; the
+        graph is replayed, L2 flushed before each replay, and each kernel's
+        time is the mean over the replays of its event pair's elapsed time."""
         rt = self.rt
         fused, self.fused = self.fused, False
         try:
@@ -641,20 +641,33 @@ class Measured:
         import torch
         rt = self.rt
         prof_steps = min(steps, 50)
-        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(self.launches_per_step * prof_steps)]
+        self.step()  # the sequential form once, eagerly, before its capture
         torch.cuda.synchronize()
+        n0 = rt.rt_launch_count()
+        self.step()
+        torch.cuda.synchronize()
+        per_step = rt.rt_launch_count() - n0
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(per_step)]
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(self.dev)
+        cap.wait_stream(torch.cuda.current_stream(self.dev))
         rt.rt_profile_set(pairs)
+        try:
+            with torch.cuda.graph(graph, stream=cap):
+                self.step()
+            names = [rt.rt_profile_kernel_name(i) for i in range(len(pairs))]
+        finally:
+            rt.rt_profile_set([])
+        torch.cuda.synchronize()
+        per_kind = {}
         for _ in range(prof_steps):
             flush.zero_()
-            torch.cuda._sleep(400000)  # about 0.2 ms at 2 GHz
-            self.step()
-        torch.cuda.synchronize()
-        names = [rt.rt_profile_kernel_name(i) for i in range(len(pairs))]
-        rt.rt_profile_set([])
-        per_kind = {}
-        for i, (a, b) in enumerate(pairs):
-            per_kind.setdefault(names[i], []).append(a.elapsed_time(b))
+            graph.replay()
+            torch.cuda.synchronize()
+            for i, (a, b) in enumerate(pairs):
+                per_kind.setdefault(names[i], []).append(a.elapsed_time(b))
+        del graph
         kern = {k2: {"launches": len(v2), "avg_us": 1e3 * statistics.mean(v2),
                      "total_ms": sum(v2)} for k2, v2 in per_kind.items()}
         total = sum(x["total_ms"] for x in kern.values())
@@ -843,10 +856,15 @@ def run_ours(args, wl_id, wl):
                                  "rt_routing_attention_step (centroid update on a side stream)"),
                    "l2": "flushed before every timed step (256 MiB write)",
                    "graph": "the step captured once as a CUDA graph, replayed per step",
-                   "kernel_times": "eager steps behind a sleep kernel, CUDA events around each "
-                                   "launch (includes a few us of launch gap per kernel); the "
-                                   "centroid update runs after the forward on one stream, so "
-                                   "each kernel is timed alone"},
+                   "kernel_times": "one step captured as a CUDA graph with a CUDA-event "
+                                   "record node before and after every kernel, replayed with "
+                                   "L2 flushed before each replay (a kernel's bracket includes "
+                                   "its launch latency inside the graph); the centroid update "
+                                   "runs after the forward on one stream, so each kernel is "
+                                   "timed alone"},
+        "e2e_schedule": ("copies in, compute and copies out overlapped across consecutive steps "
+                         "(double-buffered device inputs and outputs); the timed span runs "
+                         "from the first step's first copy in to the last step's copy out"),
         "tflops": tflops, "tflops_causal": causal_flops(wl) * world / (t_ms * 1e-3) / 1e12,
         "tflops_frac_bf16": tflops / peaks["bf16_tflops"],
         "roofline": roofline_for(kern, wl, peaks),

@@ -27,6 +27,20 @@ static int g_prof_pairs = 0;
 static int g_prof_next = 0;
 static thread_local int t_prof_slot = -1;
 
+// A timing event around a launch.  Under stream capture it becomes an event
+// record node of the graph (recorded at every replay) rather than a
+// capture-time dependency, so a captured step can be timed kernel by kernel.
+static cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &st) != cudaSuccess) {
+    cudaGetLastError();
+    st = cudaStreamCaptureStatusNone;
+  }
+  return st == cudaStreamCaptureStatusActive
+             ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+             : cudaEventRecord(ev, s);
+}
+
 void launch_begin(int kind, cudaStream_t s) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   t_prof_slot = -1;
@@ -34,7 +48,7 @@ void launch_begin(int kind, cudaStream_t s) {
   if (g_prof_next < g_prof_pairs) {
     t_prof_slot = g_prof_next++;
     g_prof_kinds[t_prof_slot] = kind;
-    if (cudaEventRecord(g_prof_events[2 * t_prof_slot], s) != cudaSuccess) {
+    if (record_timing_event(g_prof_events[2 * t_prof_slot], s) != cudaSuccess) {
       cudaGetLastError();  // a bad timing event must not fail the launch
       g_prof_kinds[t_prof_slot] = -1;
     }
@@ -45,7 +59,8 @@ void launch_end(int kind, cudaStream_t s) {
   (void)kind;
   if (t_prof_slot < 0) return;
   std::lock_guard<std::mutex> lk(g_prof_mu);
-  if (t_prof_slot < g_prof_pairs && cudaEventRecord(g_prof_events[2 * t_prof_slot + 1], s) != cudaSuccess)
+  if (t_prof_slot < g_prof_pairs &&
+      record_timing_event(g_prof_events[2 * t_prof_slot + 1], s) != cudaSuccess)
     cudaGetLastError();
   t_prof_slot = -1;
 }

@@ -383,7 +383,9 @@ int64_t rt_launch_count(void);
  * library launches after this call (i < n_pairs) records events[2i] just
  * before and events[2i+1] just after itself on its stream.  `events` are
  * cudaEvent_t handles created by the caller with timing enabled; the array
- * is copied.  rt_profile_set(NULL, 0) switches the hook off. */
+ * is copied.  On a stream that is being captured into a CUDA graph the
+ * events are recorded as external event nodes, so each replay records them.
+ * rt_profile_set(NULL, 0) switches the hook off. */
 rt_status rt_profile_set(void* const* events, int n_pairs);
 
 /* Kernel-kind id of the i-th launch recorded since rt_profile_set (or -1),
