@@ -726,13 +726,17 @@ select_topw_group_kernel(const float* __restrict__ S, const uint16_t* __restrict
       b0 = score_bin(t0);
     }
   }
-  // counts of the bins >= b0, one shared atomic per distinct bin of a warp
-  for (int g0 = 0; g0 < NG; g0 += THREADS) {
-    const int g = g0 + tid;
-    const int b = (g < NG && (int)gbin[g] >= b0) ? (int)gbin[g] : -1;
-    if (__any_sync(0xffffffffu, b >= 0)) {  // (most warps hold no bin >= b0)
-      const unsigned peers = __match_any_sync(0xffffffffu, b);
-      if (b >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[b], (unsigned)__popc(peers));
+  // counts of the bins >= b0: two bins per 32-bit shared load, a shared
+  // atomic for each bin at or above b0 (few of them, spread over many bins;
+  // a bin outside the histogram, which only an unfinished score kernel
+  // could leave, is not counted)
+  {
+    const uint32_t* gb2 = reinterpret_cast<const uint32_t*>(gbin);
+    for (int v = tid; 2 * v < NG; v += THREADS) {
+      const uint32_t pr = gb2[v];
+      const int lo = (int)(pr & 0xffffu), hi = (int)(pr >> 16);
+      if (lo >= b0 && lo < NBINS) atomicAdd(&hist[lo], 1u);
+      if (2 * v + 1 < NG && hi >= b0 && hi < NBINS) atomicAdd(&hist[hi], 1u);
     }
   }
   __syncthreads();
