@@ -181,6 +181,7 @@ SWEEP = [
     (1, 2, 10004, 64, 7, 200, "bf16", True),    # select rows of 8192 < n <= 16384, ragged segments
     (1, 2, 2000, 128, 200, 16, "bf16", True),   # 128 < k <= 256: column halves, ragged upper half and tile
     (2, 1, 777, 64, 144, 8, "bf16", True),      # the same with d = 64, one 16-column upper half, two sequences
+    (1, 8, 16384, 64, 256, 64, "bf16", True),   # k = 256 on rows past 8192 without group bins (134 MB of S)
 ]
 
 
