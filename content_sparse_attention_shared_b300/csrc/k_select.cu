@@ -602,14 +602,20 @@ constexpr int GSIZE = GROUP_SIZE;
 constexpr int GCAP = 1024;
 constexpr int GROUP_N_MAX = 262144;
 
-inline size_t group_smem_bytes(int n) {
+// Shared memory: the group bins [NG] (u16), whose space the position bitmap
+// [NW] takes over once the qualifying groups are listed, then the candidate
+// keys and the qualifying-group list.
+inline size_t group_region0_bytes(int n) {
   const size_t ng = (size_t)(n + GSIZE - 1) / GSIZE, nw = (size_t)(n + 31) / 32;
-  return ((ng * 2 + 15) & ~(size_t)15) + ((nw * 4 + 15) & ~(size_t)15) + (size_t)(GCAP + 1) * 8 +
-         (size_t)GCAP * 4;
+  return std::max((ng * 2 + 15) & ~(size_t)15, (nw * 4 + 15) & ~(size_t)15);
+}
+inline size_t group_smem_bytes(int n) {
+  return group_region0_bytes(n) + (size_t)(GCAP + 1) * 8 + (size_t)GCAP * 4;
 }
 
+// (5 CTAs an SM: about 37 KB of shared memory each at n = 65536)
 template <bool FROM_GBINS>
-__global__ void __launch_bounds__(THREADS, 4)
+__global__ void __launch_bounds__(THREADS, 5)
 select_topw_group_kernel(const float* __restrict__ S, const uint16_t* __restrict__ gbins, int n,
                          int k, int w, int32_t* __restrict__ idx, int32_t* __restrict__ mcount,
                          int32_t* __restrict__ slots) {
@@ -620,10 +626,10 @@ select_topw_group_kernel(const float* __restrict__ S, const uint16_t* __restrict
   __shared__ int s_bl, s_ncand, s_nq, s_nq2;
   const int NG = (n + GSIZE - 1) / GSIZE;
   const int NW = (n + 31) / 32;
-  uint16_t* gbin = reinterpret_cast<uint16_t*>(gsm);                                   // [NG]
-  unsigned* kept = reinterpret_cast<unsigned*>(gsm + ((NG * 2 + 15) & ~15));           // [NW]
-  unsigned long long* ckey =
-      reinterpret_cast<unsigned long long*>(gsm + ((NG * 2 + 15) & ~15) + ((NW * 4 + 15) & ~15));
+  const int R0 = max((NG * 2 + 15) & ~15, (NW * 4 + 15) & ~15);
+  uint16_t* gbin = reinterpret_cast<uint16_t*>(gsm);  // [NG], until the groups are listed
+  unsigned* kept = reinterpret_cast<unsigned*>(gsm);  // [NW], after that
+  unsigned long long* ckey = reinterpret_cast<unsigned long long*>(gsm + R0);
   int* qlist = reinterpret_cast<int*>(ckey + GCAP + 1);  // [GCAP] qualifying groups
 
   const int c = blockIdx.x;
@@ -633,7 +639,6 @@ select_topw_group_kernel(const float* __restrict__ S, const uint16_t* __restrict
   const SelectOut so{idx + ((size_t)bh * k + c) * w, mcount, slots, bh, c, n, w};
   const int tid = threadIdx.x, lane = tid & 31;
 
-  for (int i = tid; i < NW; i += THREADS) kept[i] = 0u;
   for (int i = tid; i < NBINS; i += THREADS) hist[i] = 0u;
   if (tid == 0) { s_ncand = 0; s_nq = 0; s_nq2 = 0; s_bl = -1; }
   pdl_wait();
@@ -798,6 +803,9 @@ select_topw_group_kernel(const float* __restrict__ S, const uint16_t* __restrict
     radix_select_row(row, n, w, so, hist, wsum);
     return;
   }
+  // the group bins are read no more: their space becomes the position bitmap
+  // (cleared here, first written after the barrier that ends the candidates)
+  for (int i = tid; i < NW; i += THREADS) kept[i] = 0u;
   // candidates above the boundary bin fill ckey from the front (nA), those in
   // it from the back (nE)
   {
