@@ -182,13 +182,15 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
   sort8(ids);
   const long long bh = r / n;
   const float* ybase = yslot + (size_t)bh * k * w * D + ch * 8;
-  // slot rows summed in ascending cluster order, four loads in flight at a time
+  // slot rows summed in ascending cluster order, two rows in flight at a time
+  // (four would not fit the 40 registers that six CTAs an SM leave, and
+  // spilling them, or fewer CTAs, measured slower)
 #pragma unroll
-  for (int i0 = 0; i0 < 8; i0 += 4) {
+  for (int i0 = 0; i0 < 8; i0 += 2) {
     if (i0 >= m) break;
-    float4 y[4][2];
+    float4 y[2][2];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 2; ++u) {
       if (i0 + u < m && ids[i0 + u] != 0x7fffffff) {
         const float4* p = reinterpret_cast<const float4*>(ybase + (size_t)ids[i0 + u] * D);
         y[u][0] = __ldcg(p);
@@ -196,7 +198,7 @@ scatter_kernel(long long BHn, int n, int k, int w, const int32_t* __restrict__ i
       }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 2; ++u) {
       if (i0 + u < m && ids[i0 + u] != 0x7fffffff) {
         acc[0] += y[u][0].x; acc[1] += y[u][0].y; acc[2] += y[u][0].z; acc[3] += y[u][0].w;
         acc[4] += y[u][1].x; acc[5] += y[u][1].y; acc[6] += y[u][1].z; acc[7] += y[u][1].w;
