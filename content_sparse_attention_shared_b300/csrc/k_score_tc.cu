@@ -21,11 +21,12 @@
 // matrices, written 16 bytes per thread, conflict-free); warp 0 streams
 // 128-row tiles of Q with TMA (2-D tensor map, 64-element x 128-row boxes,
 // 128-byte swizzle) into a ring of stages, warp 1 issues the MMAs into one of
-// two TMEM accumulators, and two epilogue warpgroups (warps 2-5 and 6-9)
-// take alternate tiles: each reads its rows' statistics (mean, centred norm)
-// from the staged tile in shared memory while the MMA runs, then the scores
-// from TMEM, writes them centroid-major [BH,k,n] with coalesced stores and
-// takes the argmax.  With the scores it can write the group bins of the
+// NG TMEM accumulators, and NG epilogue warpgroups (warps 2-5, 6-9, ...; NG =
+// 4 when four accumulators fit in TMEM, else 2) take the tiles in turn: each
+// reads its rows' statistics (mean, centred norm) from the staged tile in
+// shared memory (while the MMA runs, when the group owns its stage), then
+// the scores from TMEM, writes them centroid-major [BH,k,n] with coalesced
+// stores and takes the argmax.  With the scores it can write the group bins of the
 // select kernel (the bin of the largest score of every 8 consecutive
 // positions per centroid): a tile row is a lane, so a group is a lane octet,
 // and a shuffle reduce-scatter leaves each lane one centroid's group maximum
@@ -380,7 +381,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap qmap, int B, int H, int n,
       }
     }
   } else {
-    // ===================== epilogue groups (warps 2-5, 6-9) ==================
+    // ===================== epilogue groups (warps 2 .. 4 NG + 1) =============
     const int grp = (warp - 2) >> 2;         // takes tiles i with i % NG == grp
     const int quad = warp & 3;               // TMEM lane quadrant this warp may read
     const int row = 32 * quad + lane;        // tile row == TMEM lane
